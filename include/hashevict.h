@@ -1,0 +1,148 @@
+/*
+ * hashevict.h — C ABI of the B300 HashEvict decode-step library (libhashevict.so).
+ *
+ * The operation ("HashEvict: A Pre-Attention KV Cache Eviction Strategy using
+ * Locality-Sensitive Hashing", arXiv 2412.16187; abstract and the technical
+ * framework of the method section, steps 1-5):
+ *   per decode step and per (batch, KV head),
+ *   1-2. project the current query heads and the current key onto a shared
+ *        Gaussian matrix W[head_dim][bits] and binarise by sign into `bits`-bit codes;
+ *   3.   score every cached key by the Hamming distance between its stored code
+ *        and the query codes (summed over the G = heads / kv_heads query heads
+ *        of the KV group);
+ *   4.   evict the most dissimilar cached token (largest distance; ties go to
+ *        the lowest slot) before any attention is computed;
+ *   5.   write the current token's key, value and code into the evicted slot;
+ *   then attend: out = softmax(q K^T / sqrt(head_dim)) V over the retained
+ *   cache (which now holds the current token), as every decode step does
+ *   (TTKV page, introduction).
+ *   While fewer than `budget` tokens are cached the current token is appended
+ *   to the next free slot instead (no scoring).
+ *
+ * Conventions for every entry point:
+ *   - Return 0 (HE_OK) on success, a negative HE_E* code on failure; nothing
+ *     aborts.  he_strerror() names a code.  A CUDA error seen by the library is
+ *     returned as HE_ECUDA and remembered: the handle then refuses further work.
+ *   - Element type: HE_DTYPE_BF16 (bf16 bit patterns, 2 bytes) or HE_DTYPE_FP32.
+ *     q, k, v, K, V and W all use the handle's element type.  Outputs are fp32.
+ *   - "device" pointers are CUDA device memory of the device current when the
+ *     handle was created; "host" pointers are host memory.  Every pointer must
+ *     be 16-byte aligned.  Caller-owned buffers stay owned by the caller.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls that
+ *     take a stream are asynchronous on it; calls that take host buffers
+ *     synchronise the handle's last-used stream first.
+ *   - A handle is not thread-safe; use one handle per layer and per thread.
+ */
+#ifndef HASHEVICT_H
+#define HASHEVICT_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define HE_OK 0
+#define HE_EINVAL (-1)      /* bad configuration, size, pointer or alignment */
+#define HE_ENOTFILLED (-2)  /* he_step before he_fill */
+#define HE_ECUDA (-3)       /* a CUDA call failed (sticky for the handle) */
+#define HE_ENOMEM (-4)      /* device allocation failed */
+#define HE_EDEVICE (-5)     /* a kernel reported an internal error (wait gave up) */
+
+#define HE_DTYPE_BF16 0
+#define HE_DTYPE_FP32 1
+
+/* Handle configuration.  Supported: head_dim in {64, 128};
+ * G = heads / kv_heads in {1, 2, 4, 8}; bits in {8, 16, 32, 64};
+ * 1 <= budget <= 2^24; batch * kv_heads <= 2^16; dtype HE_DTYPE_*. */
+typedef struct {
+  int32_t batch;
+  int32_t heads;     /* query heads */
+  int32_t kv_heads;  /* key/value heads; heads % kv_heads == 0 */
+  int32_t head_dim;  /* D */
+  int32_t bits;      /* code length b (projection width) */
+  int32_t budget;    /* cache slots per (batch, KV head) */
+  int32_t dtype;     /* HE_DTYPE_BF16 or HE_DTYPE_FP32 */
+  int32_t reserved;  /* must be 0 */
+  uint64_t seed;     /* draws W; one handle (and one seed) per layer */
+} he_cfg;
+
+typedef struct he_ctx* he_handle;
+
+/* Creates a handle on the current CUDA device and allocates, in device memory
+ * owned by the handle: the cache K, V [batch][kv_heads][budget][head_dim], the
+ * codes [batch][kv_heads][budget] (bits/8-byte words), W [head_dim][bits] drawn
+ * from cfg->seed (see he_get_projection) and the step's scratch.
+ * Errors: HE_EINVAL (cfg or out NULL, unsupported sizes), HE_ENOMEM, HE_ECUDA. */
+int he_create(const he_cfg* cfg, he_handle* out);
+
+/* Fills the cache with n <= budget prompt tokens and codes their keys
+ * (method steps 1-2 applied to the cached keys).  K, V: device
+ * [batch][kv_heads][n][head_dim].  n = 0 empties the cache (K, V may be NULL).
+ * Errors: HE_EINVAL (NULL handle, n out of range, NULL or misaligned K/V), HE_ECUDA. */
+int he_fill(he_handle h, const void* K, const void* V, int32_t n, void* stream);
+
+/* One decode step (method steps 1-5, then attention), one kernel launch.
+ * q: device [batch][heads][head_dim]; k, v: device [batch][kv_heads][head_dim];
+ * out: device fp32 [batch][heads][head_dim].  Updates the cache in place.
+ * Errors: HE_EINVAL (NULL handle or pointer, misalignment), HE_ENOTFILLED, HE_ECUDA. */
+int he_step(he_handle h, const void* q, const void* k, const void* v, float* out, void* stream);
+
+/* he_step on HOST buffers (same shapes): copies q, k, v to handle-owned device
+ * staging buffers, runs the step, copies out back and synchronises `stream`.
+ * Returns when out is written.  Errors: as he_step. */
+int he_step_host(he_handle h, const void* q, const void* k, const void* v, float* out,
+                 void* stream);
+
+/* Frees everything the handle owns.  NULL-safe.  Synchronises the device. */
+int he_destroy(he_handle h);
+
+/* Slots written by the last step, host [batch][kv_heads]: the evicted slot, or
+ * -1 when the token was appended to a cache not yet full.  Synchronises.
+ * Also returns HE_EDEVICE if a kernel of this handle reported an internal error. */
+int he_last_evicted(he_handle h, int32_t* host_slots);
+
+/* Snapshot of the cache into host buffers (any may be NULL):
+ * K, V [batch][kv_heads][budget][head_dim] (element type), codes
+ * [batch][kv_heads][budget] (bits/8-byte words), occupancy (one int).  Synchronises. */
+int he_read_state(he_handle h, void* K, void* V, void* codes, int32_t* occupancy);
+
+/* The projection matrix W [head_dim][bits] (element type), host.  W[d][j] is a
+ * counter-based N(0,1) draw: st = SplitMix64(seed ^ 0x48455F50524F4A57); for
+ * element e = d*bits + j, three SplitMix64(st + 3e + r) give twelve 16-bit
+ * integers u; W = (sum u - 393210) / 65536, rounded to bf16 (nearest-even) for
+ * bf16 handles.  Synchronises. */
+int he_get_projection(he_handle h, void* host_W);
+
+/* Codes of n vectors (method steps 1-2): x device [n][head_dim] (element type),
+ * codes device [n] words of bits/8 bytes.  bit j = (sum_d x[d] W[d][j] > 0),
+ * the sum in fp32, fused multiply-add, d = 0..head_dim-1 in order from +0.
+ * Errors: HE_EINVAL, HE_ECUDA. */
+int he_codes(he_handle h, const void* x, int32_t n, void* codes, void* stream);
+
+/* Group-summed Hamming distances of every resident slot to the step's query
+ * (method step 3) without changing the cache: q device [batch][heads][head_dim],
+ * dist device int32 [batch][kv_heads][budget] (slots >= occupancy get 0).
+ * Errors: HE_EINVAL, HE_ENOTFILLED, HE_ECUDA. */
+int he_scores(he_handle h, const void* q, int32_t* dist, void* stream);
+
+/* Number of resident tokens (host-side state; no synchronisation). */
+int he_occupancy(he_handle h, int32_t* occupancy);
+
+/* Algorithmic HBM bytes of one full-cache step (read of retained K, V and codes,
+ * write of the overwritten slot, q/k/v in, out, W) — the roofline numerator. */
+int he_step_bytes(he_handle h, uint64_t* bytes);
+
+/* Launch shape of the step kernel for the current occupancy: CTAs, CTAs per SM,
+ * cache tiles (32 slots each) and pipeline stages. */
+int he_launch_info(he_handle h, int32_t* ctas, int32_t* ctas_per_sm, int32_t* tiles,
+                   int32_t* stages);
+
+/* Human-readable name of a return code. */
+const char* he_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HASHEVICT_H */

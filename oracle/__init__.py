@@ -1,0 +1,195 @@
+"""CPU oracle of the HashEvict decode step — TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg
+may import this package.  The product path (``lsh_pre_attention_decode_b300``)
+never does: it shares no code with the oracle.
+
+The arithmetic lives in ``hashevict_oracle.c`` (plain C, compiled with gcc,
+``-ffp-contract=off`` so that only the fused multiply-adds the code spells out
+are fused).  This module only marshals numpy arrays:
+
+* bf16 tensors are ``numpy.uint16`` arrays of bf16 bit patterns (dtype code 0),
+* fp32 tensors are ``numpy.float32`` arrays (dtype code 1),
+* codes are ``numpy.uint64`` (bit j of the code = bit j of the word).
+
+Method: "HashEvict: A Pre-Attention KV Cache Eviction Strategy using
+Locality-Sensitive Hashing" (arXiv 2412.16187), abstract and technical
+framework steps 1-5; attention over the retained cache per the TTKV page's
+introduction (each decode step attends the whole cache).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "hashevict_oracle.c")
+LIB = os.path.join(HERE, "libhashevict_oracle.so")
+
+_i32 = ctypes.c_int32
+_u64 = ctypes.c_uint64
+_vp = ctypes.c_void_p
+
+
+def build(out: str = LIB, mutant: int = 0) -> str:
+    """Compile the oracle with gcc.  ``mutant`` > 0 plants one known mistake
+    (see the ORACLE_MUTANT blocks in the C file); only the pin tests use that."""
+    src_m = os.path.getmtime(SRC)
+    if os.path.exists(out) and os.path.getmtime(out) >= src_m and mutant == 0:
+        return out
+    cmd = ["gcc", "-O2", "-std=c11", "-Wall", "-ffp-contract=off", "-fPIC", "-shared",
+           f"-DORACLE_MUTANT={int(mutant)}", "-o", out, SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+def _dtype_code(a: np.ndarray) -> int:
+    if a.dtype == np.uint16:
+        return 0
+    if a.dtype == np.float32:
+        return 1
+    raise TypeError(f"oracle tensors are uint16 (bf16 bits) or float32, got {a.dtype}")
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(_vp)
+
+
+@dataclass
+class UnitState:
+    """Cache of one (batch, KV head) unit: K, V [budget][D], codes [budget]."""
+    W: np.ndarray
+    bits: int
+    budget: int
+    K: np.ndarray
+    V: np.ndarray
+    codes: np.ndarray
+    occupancy: int
+
+
+class Oracle:
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        lib.orc_projection.argtypes = [_u64, _i32, _i32, _i32, _vp]
+        lib.orc_projection.restype = None
+        lib.orc_code.argtypes = [_vp, _i32, _i32, _vp, _i32]
+        lib.orc_code.restype = _u64
+        lib.orc_code_many.argtypes = [_vp, _i32, _i32, _i32, _vp, _i32, _vp]
+        lib.orc_code_many.restype = None
+        lib.orc_group_distance.argtypes = [_vp, _i32, _u64]
+        lib.orc_group_distance.restype = _i32
+        lib.orc_most_dissimilar.argtypes = [_vp, _i32]
+        lib.orc_most_dissimilar.restype = _i32
+        lib.orc_attend.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp]
+        lib.orc_attend.restype = None
+        lib.orc_unit_fill.argtypes = [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _i32, _vp, _vp,
+                                      _vp, _vp]
+        lib.orc_unit_fill.restype = None
+        lib.orc_unit_stream.argtypes = [_vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp,
+                                        _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+        lib.orc_unit_stream.restype = None
+        self.lib = lib
+
+    # -- steps 1-2 -----------------------------------------------------------
+    def projection(self, seed: int, head_dim: int, bits: int, dtype: str) -> np.ndarray:
+        """W[head_dim][bits], drawn from ``seed`` (bf16 bits or fp32)."""
+        W = np.empty((head_dim, bits), np.uint16 if dtype == "bf16" else np.float32)
+        self.lib.orc_projection(seed, head_dim, bits, _dtype_code(W), _ptr(W))
+        return W
+
+    def code(self, x: np.ndarray, W: np.ndarray) -> np.ndarray:
+        """Codes of the rows of x [n][D] (or one vector [D]) -> uint64 [n]."""
+        x2 = np.ascontiguousarray(x.reshape(-1, x.shape[-1]))
+        Wc = np.ascontiguousarray(W)
+        if _dtype_code(x2) != _dtype_code(Wc):
+            raise TypeError("x and W must have the same element type")
+        out = np.empty(x2.shape[0], np.uint64)
+        self.lib.orc_code_many(_ptr(x2), x2.shape[0], _dtype_code(x2), x2.shape[1], _ptr(Wc),
+                               Wc.shape[1], _ptr(out))
+        return out
+
+    # -- steps 3-4 -----------------------------------------------------------
+    def group_distance(self, code_q: np.ndarray, code_slot: int) -> int:
+        cq = np.ascontiguousarray(code_q, np.uint64)
+        return int(self.lib.orc_group_distance(_ptr(cq), cq.size, int(code_slot)))
+
+    def most_dissimilar(self, dist: np.ndarray) -> int:
+        d = np.ascontiguousarray(dist, np.int32)
+        return int(self.lib.orc_most_dissimilar(_ptr(d), d.size))
+
+    # -- attention -----------------------------------------------------------
+    def attend(self, q: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
+        """fp64 softmax(q K^T / sqrt(D)) V for q [G][D], K, V [n][D]."""
+        q2 = np.ascontiguousarray(q.reshape(-1, q.shape[-1]))
+        K2 = np.ascontiguousarray(K)
+        V2 = np.ascontiguousarray(V)
+        G, D = q2.shape
+        out = np.empty((G, D), np.float64)
+        self.lib.orc_attend(_ptr(q2), _ptr(K2), _ptr(V2), K2.shape[0], D, G, _dtype_code(q2),
+                            _ptr(out))
+        return out
+
+    # -- one (batch, KV head) unit -----------------------------------------
+    def unit_fill(self, W: np.ndarray, budget: int, Kin: np.ndarray, Vin: np.ndarray) -> UnitState:
+        n, D = Kin.shape
+        if n > budget:
+            raise ValueError("more fill tokens than the budget")
+        K = np.zeros((budget, D), Kin.dtype)
+        V = np.zeros((budget, D), Kin.dtype)
+        codes = np.zeros(budget, np.uint64)
+        occ = np.zeros(1, np.int32)
+        Kc, Vc, Wc = (np.ascontiguousarray(a) for a in (Kin, Vin, W))
+        self.lib.orc_unit_fill(_ptr(Wc), D, Wc.shape[1], _dtype_code(Kc), budget, _ptr(Kc),
+                               _ptr(Vc), n, _ptr(K), _ptr(V), _ptr(codes), _ptr(occ))
+        return UnitState(Wc, Wc.shape[1], budget, K, V, codes, int(occ[0]))
+
+    def unit_stream(self, st: UnitState, q: np.ndarray, k: np.ndarray, v: np.ndarray,
+                    want_out: np.ndarray | None = None, dist_log: bool = False) -> dict:
+        """Run tokens q [T][G][D], k, v [T][D] through the step (state updated
+        in place).  Returns evicted [T] (-1 = appended), written [T], out
+        [n_wanted][G][D] fp64 and, if asked, dist [T][budget]."""
+        T, G, D = q.shape
+        qc, kc, vc = (np.ascontiguousarray(a) for a in (q, k, v))
+        evicted = np.empty(T, np.int32)
+        written = np.empty(T, np.int32)
+        if want_out is None:
+            n_out = T
+            wo = None
+        else:
+            wo = np.ascontiguousarray(want_out, np.uint8)
+            n_out = int(wo.astype(bool).sum())
+        out = np.empty((n_out, G, D), np.float64)
+        dl = np.empty((T, st.budget), np.int32) if dist_log else None
+        occ = np.array([st.occupancy], np.int32)
+        self.lib.orc_unit_stream(_ptr(st.W), D, G, st.bits, _dtype_code(qc), st.budget, _ptr(st.K),
+                                 _ptr(st.V), _ptr(st.codes), _ptr(occ), T, _ptr(qc), _ptr(kc),
+                                 _ptr(vc), _ptr(evicted), _ptr(written), _ptr(wo), _ptr(out),
+                                 _ptr(dl))
+        st.occupancy = int(occ[0])
+        res = {"evicted": evicted, "written": written, "out": out}
+        if dist_log:
+            res["dist"] = dl
+        return res
+
+
+_cache: dict[int, Oracle] = {}
+
+
+def load(mutant: int = 0, build_dir: str | None = None) -> Oracle:
+    """The oracle library (built on first use).  Mutants are built into
+    ``build_dir`` (required for mutant > 0)."""
+    if mutant in _cache:
+        return _cache[mutant]
+    if mutant == 0:
+        path = build()
+    else:
+        if build_dir is None:
+            raise ValueError("mutant builds need a build_dir")
+        path = build(os.path.join(build_dir, f"liboracle_mutant{mutant}.so"), mutant)
+    o = Oracle(path)
+    _cache[mutant] = o
+    return o

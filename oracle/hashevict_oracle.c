@@ -1,0 +1,285 @@
+/*
+ * hashevict_oracle.c — CPU oracle of the HashEvict decode step.
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg may load or call this file.  It is plain, slow and written to
+ * be checked by eye against the method's description; it shares no code with
+ * the CUDA library.
+ *
+ * Source: "HashEvict: A Pre-Attention KV Cache Eviction Strategy using
+ * Locality-Sensitive Hashing" (arXiv 2412.16187), abstract and the method
+ * section's technical framework, steps 1-5:
+ *   1. Gaussian projection of the token's key (and of the query) to b dims,
+ *   2. binarisation of the projection,
+ *   3. Hamming distance between the query's code and each cached key's code,
+ *   4. eviction of the cached token most dissimilar to the current query,
+ *   5. the current token's key and value replace the evicted token's.
+ * Decode attention over the retained cache follows (TTKV page, introduction:
+ * every decode step attends the whole cache).
+ *
+ * Readings taken where the pages are silent (each is listed in the design notes):
+ *   - projection W[d][j] ~ N(0,1) (Irwin-Hall(12) counter-based draw, below),
+ *     shared by the query and the keys; no normalisation;
+ *   - the projection sum is fp32, fused multiply-add, d = 0..D-1 in order,
+ *     starting from +0; bit j = (sum > 0): exactly +-0 gives 0;
+ *   - bit j of the code is bit j of a 64-bit word (LSB first);
+ *   - GQA: a KV head's slots are scored by the sum of the Hamming distances to
+ *     the codes of the G query heads of its group;
+ *   - "most dissimilar" = largest summed distance; ties go to the lowest slot;
+ *   - scoring uses only the current step's distances (no accumulation);
+ *   - score the resident slots, then overwrite, then attend: the new token is
+ *     always resident and attended;
+ *   - while the cache holds fewer than `budget` tokens the new token is appended;
+ *   - attention: softmax(q.K / sqrt(D)) V in fp64 from the stored values,
+ *     no mask, no positional term.
+ *
+ * Element types: dtype 0 = bf16 (uint16 bit patterns), dtype 1 = fp32.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0 /* >0 plants a known mistake (used only by the pin tests) */
+#endif
+
+/* ------------------------------------------------------------------------- */
+/* Element access                                                             */
+/* ------------------------------------------------------------------------- */
+
+static float bf16_value(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+static float elem(const void* base, int dtype, size_t i) {
+  if (dtype == 1) return ((const float*)base)[i];
+  return bf16_value(((const uint16_t*)base)[i]);
+}
+
+static size_t elem_bytes(int dtype) { return dtype == 1 ? 4u : 2u; }
+
+/* ------------------------------------------------------------------------- */
+/* The projection matrix: a counter-based Gaussian draw from a seed.          */
+/* Generator: SplitMix64 finaliser (Steele, Lea, Flood, OOPSLA 2014) over the */
+/* counter, Irwin-Hall sum of 12 uniform 16-bit integers for N(0,1).          */
+/* W[d][j] (row-major, D rows of b columns), element e = d*b + j:             */
+/*   st  = mix(seed ^ 0x48455F50524F4A57)                                     */
+/*   u_r = mix(st + 3e + r), r = 0,1,2;  z = (sum of the 12 16-bit lanes      */
+/*         - 393210) / 65536;  W = bf16_rne(z) (dtype 0) or z (dtype 1).      */
+/* ------------------------------------------------------------------------- */
+
+static uint64_t mix(uint64_t x) {
+  uint64_t z = x + 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+static uint16_t round_to_bf16(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  uint32_t lsb = (u >> 16) & 1u;
+  u = u + 0x7FFFu + lsb; /* round half to even */
+  return (uint16_t)(u >> 16);
+}
+
+void orc_projection(uint64_t seed, int32_t D, int32_t bits, int32_t dtype, void* W) {
+  uint64_t st = mix(seed ^ 0x48455F50524F4A57ull);
+  for (int32_t d = 0; d < D; ++d) {
+    for (int32_t j = 0; j < bits; ++j) {
+      uint64_t e = (uint64_t)d * (uint64_t)bits + (uint64_t)j;
+      int64_t sum = 0;
+      for (int r = 0; r < 3; ++r) {
+        uint64_t u = mix(st + 3u * e + (uint64_t)r);
+        for (int lane = 0; lane < 4; ++lane) sum += (int64_t)((u >> (16 * lane)) & 0xFFFFu);
+      }
+      float z = (float)(sum - 393210) / 65536.0f;
+      if (dtype == 1)
+        ((float*)W)[e] = z;
+      else
+        ((uint16_t*)W)[e] = round_to_bf16(z);
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Steps 1-2: Gaussian projection and binarisation of one vector.             */
+/* ------------------------------------------------------------------------- */
+
+uint64_t orc_code(const void* x, int32_t dtype, int32_t D, const void* W, int32_t bits) {
+  uint64_t code = 0;
+  for (int32_t j = 0; j < bits; ++j) {
+    float acc = 0.0f;
+    for (int32_t d = 0; d < D; ++d) {
+      float xd = elem(x, dtype, (size_t)d);
+      float wdj = elem(W, dtype, (size_t)d * (size_t)bits + (size_t)j);
+#if ORACLE_MUTANT == 1 /* planted: projection uses the wrong W index (transpose) */
+      wdj = elem(W, dtype, ((size_t)j * (size_t)D + (size_t)d) % ((size_t)D * (size_t)bits));
+#endif
+      acc = fmaf(xd, wdj, acc);
+    }
+#if ORACLE_MUTANT == 2 /* planted: threshold >= instead of > */
+    if (acc >= 0.0f) code |= (uint64_t)1 << j;
+#else
+    if (acc > 0.0f) code |= (uint64_t)1 << j;
+#endif
+  }
+  return code;
+}
+
+void orc_code_many(const void* x, int32_t n, int32_t dtype, int32_t D, const void* W,
+                   int32_t bits, uint64_t* codes) {
+  const char* p = (const char*)x;
+  for (int32_t i = 0; i < n; ++i)
+    codes[i] = orc_code(p + (size_t)i * (size_t)D * elem_bytes(dtype), dtype, D, W, bits);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Step 3: Hamming distance, summed over the G query codes of a KV group.     */
+/* ------------------------------------------------------------------------- */
+
+static int32_t popcount64(uint64_t v) {
+  int32_t c = 0;
+  while (v) {
+    c += (int32_t)(v & 1u);
+    v >>= 1;
+  }
+  return c;
+}
+
+int32_t orc_group_distance(const uint64_t* code_q, int32_t G, uint64_t code_slot) {
+  int32_t dist = 0;
+  for (int32_t g = 0; g < G; ++g) {
+#if ORACLE_MUTANT == 3 /* planted: only the first query head of the group scores */
+    if (g > 0) break;
+#endif
+    dist += popcount64(code_q[g] ^ code_slot);
+  }
+  return dist;
+}
+
+/* Step 4: the slot with the largest distance; ties go to the lowest index. */
+int32_t orc_most_dissimilar(const int32_t* dist, int32_t n) {
+  int32_t best = 0;
+  for (int32_t s = 1; s < n; ++s) {
+#if ORACLE_MUTANT == 4 /* planted: ties go to the highest index */
+    if (dist[s] >= dist[best]) best = s;
+#elif ORACLE_MUTANT == 5 /* planted: evicts the most similar slot */
+    if (dist[s] < dist[best]) best = s;
+#else
+    if (dist[s] > dist[best]) best = s;
+#endif
+  }
+  return best;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Decode attention of G query heads over n cached rows, in fp64.             */
+/* ------------------------------------------------------------------------- */
+
+void orc_attend(const void* q, const void* K, const void* V, int32_t n, int32_t D, int32_t G,
+                int32_t dtype, double* out) {
+  double* logit = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+  double scale = 1.0 / sqrt((double)D);
+#if ORACLE_MUTANT == 6 /* planted: scale dropped */
+  scale = 1.0;
+#endif
+  for (int32_t g = 0; g < G; ++g) {
+    double m = -INFINITY;
+    for (int32_t s = 0; s < n; ++s) {
+      double dot = 0.0;
+      for (int32_t d = 0; d < D; ++d)
+        dot += (double)elem(q, dtype, (size_t)g * D + d) *
+               (double)elem(K, dtype, (size_t)s * D + d);
+      logit[s] = dot * scale;
+      if (logit[s] > m) m = logit[s];
+    }
+    double den = 0.0;
+    for (int32_t s = 0; s < n; ++s) den += exp(logit[s] - m);
+    for (int32_t d = 0; d < D; ++d) {
+      double num = 0.0;
+      for (int32_t s = 0; s < n; ++s) {
+#if ORACLE_MUTANT == 7 /* planted: value rows read with the key's index transposed */
+        num += exp(logit[s] - m) * (double)elem(V, dtype, ((size_t)d * n + s) % ((size_t)n * D));
+#else
+        num += exp(logit[s] - m) * (double)elem(V, dtype, (size_t)s * D + d);
+#endif
+      }
+      out[(size_t)g * D + d] = n > 0 ? num / den : 0.0;
+    }
+  }
+  free(logit);
+}
+
+/* ------------------------------------------------------------------------- */
+/* One (batch, KV head) unit: fill, then the per-token step.                  */
+/* State: K[budget][D], V[budget][D] (dtype), codes[budget], *occupancy.      */
+/* ------------------------------------------------------------------------- */
+
+void orc_unit_fill(const void* W, int32_t D, int32_t bits, int32_t dtype, int32_t budget,
+                   const void* Kin, const void* Vin, int32_t n, void* K, void* V,
+                   uint64_t* codes, int32_t* occupancy) {
+  size_t row = (size_t)D * elem_bytes(dtype);
+  (void)budget;
+  memcpy(K, Kin, row * (size_t)n);
+  memcpy(V, Vin, row * (size_t)n);
+  for (int32_t s = 0; s < n; ++s)
+    codes[s] = orc_code((const char*)Kin + (size_t)s * row, dtype, D, W, bits);
+  *occupancy = n;
+}
+
+/*
+ * Runs `nsteps` tokens through the step.  Inputs per token t: q[t][G][D],
+ * k[t][D], v[t][D].  Per token it records evicted[t] (slot overwritten, or -1
+ * when the token was appended to a cache not yet full), written[t] (the slot
+ * the token now occupies) and, when want_out is NULL or want_out[t] != 0,
+ * one [G][D] block of fp64 attention output, packed in token order into out.  dist_log, when not NULL, receives the distances of
+ * the scored slots, dist_log[t][budget] (0 for appended tokens).
+ */
+void orc_unit_stream(const void* W, int32_t D, int32_t G, int32_t bits, int32_t dtype,
+                     int32_t budget, void* K, void* V, uint64_t* codes, int32_t* occupancy,
+                     int32_t nsteps, const void* q, const void* k, const void* v,
+                     int32_t* evicted, int32_t* written, const uint8_t* want_out, double* out,
+                     int32_t* dist_log) {
+  size_t row = (size_t)D * elem_bytes(dtype);
+  int32_t* dist = (int32_t*)malloc(sizeof(int32_t) * (size_t)budget);
+  uint64_t* code_q = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)G);
+  size_t n_out = 0;
+  for (int32_t t = 0; t < nsteps; ++t) {
+    const char* qt = (const char*)q + (size_t)t * (size_t)G * row;
+    const char* kt = (const char*)k + (size_t)t * row;
+    const char* vt = (const char*)v + (size_t)t * row;
+    int32_t slot;
+    if (*occupancy == budget) {
+      /* steps 1-3: code the query heads of the group and score every slot */
+      for (int32_t g = 0; g < G; ++g) code_q[g] = orc_code(qt + (size_t)g * row, dtype, D, W, bits);
+      for (int32_t s = 0; s < budget; ++s) dist[s] = orc_group_distance(code_q, G, codes[s]);
+      /* step 4 */
+      slot = orc_most_dissimilar(dist, budget);
+      evicted[t] = slot;
+      if (dist_log) memcpy(dist_log + (size_t)t * budget, dist, sizeof(int32_t) * (size_t)budget);
+    } else {
+      slot = *occupancy;
+      *occupancy += 1;
+      evicted[t] = -1;
+      if (dist_log) memset(dist_log + (size_t)t * budget, 0, sizeof(int32_t) * (size_t)budget);
+    }
+    written[t] = slot;
+    /* step 5: the current token replaces the evicted one */
+    memcpy((char*)K + (size_t)slot * row, kt, row);
+    memcpy((char*)V + (size_t)slot * row, vt, row);
+    codes[slot] = orc_code(kt, dtype, D, W, bits);
+#if ORACLE_MUTANT == 8 /* planted: the new token's value is not written */
+    memset((char*)V + (size_t)slot * row, 0, row);
+#endif
+    /* attention over the retained cache */
+    if (!want_out || want_out[t])
+      orc_attend(qt, K, V, *occupancy, D, G, dtype, out + (n_out++) * (size_t)G * (size_t)D);
+  }
+  free(dist);
+  free(code_q);
+}

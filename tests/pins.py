@@ -1,0 +1,352 @@
+"""Pins of the CPU oracle to facts fixed outside the oracle itself.
+
+Each ``check_*`` takes an ``oracle.Oracle`` and raises AssertionError when the
+oracle disagrees with a hand-worked example, a closed form, a special case that
+reduces to a textbook routine, or a brute-force recomputation.  The same checks
+run against the real oracle (tests/test_oracle_pins.py) and against copies of
+it with a planted mistake (tests/test_oracle_mutants.py), which must each fail
+at least one check.
+
+Method: HashEvict (arXiv 2412.16187) — abstract and the technical framework's
+steps 1-5; attention over the retained cache — TTKV page, introduction.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ---------------------------------------------------------------------------
+# fixture readers
+# ---------------------------------------------------------------------------
+
+def _lines(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        for ln in f:
+            ln = ln.strip()
+            if ln and not ln.startswith("#"):
+                yield ln.split()
+
+
+def read_code_cases():
+    cases, cur = [], None
+    for tok in _lines("codes_hand.txt"):
+        if tok[0] == "case":
+            cur = {"name": tok[1], "W": []}
+            cases.append(cur)
+        elif tok[0] == "dims":
+            cur["D"], cur["bits"] = int(tok[1]), int(tok[2])
+        elif tok[0] == "W":
+            cur["W"].append([float(t) for t in tok[1:]])
+        elif tok[0] == "x":
+            cur["x"] = [float(t) for t in tok[1:]]
+        elif tok[0] == "code":
+            cur["code"] = int(tok[1])
+    return cases
+
+
+def read_eviction_case():
+    c = {"fill": [], "steps": []}
+    for tok in _lines("eviction_hand.txt"):
+        if tok[0] == "budget":
+            c["budget"] = int(tok[1])
+        elif tok[0] == "fill":
+            c["fill"].append([float(t) for t in tok[1:]])
+        elif tok[0] == "step":
+            i_k, i_e, i_s = tok.index("k"), tok.index("expect"), tok.index("slot")
+            c["steps"].append({"q": [float(t) for t in tok[2:i_k]],
+                               "k": [float(t) for t in tok[i_k + 1:i_e]],
+                               "expect": int(tok[i_e + 1]), "slot": int(tok[i_s + 1])})
+        elif tok[0] == "codes_final":
+            c["codes_final"] = [int(t) for t in tok[1:]]
+    return c
+
+
+def read_attention_cases():
+    cases, cur = [], None
+    for tok in _lines("attention_hand.txt"):
+        if tok[0] == "case":
+            cur = {"name": tok[1], "K": [], "V": []}
+            cases.append(cur)
+        elif tok[0] in ("K", "V"):
+            cur[tok[0]].append([float(t) for t in tok[1:]])
+        else:
+            cur[tok[0]] = [float(t) for t in tok[1:]]
+    return cases
+
+
+def f32(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+
+
+def bf16_bits(a):
+    """float array -> bf16 bit patterns (round to nearest even; exact inputs here)."""
+    u = np.asarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.astype(np.uint16)
+
+
+def bf16_to_f64(h):
+    return (np.asarray(h, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def popcount_brute(x: int) -> int:
+    return bin(int(x)).count("1")
+
+
+# ---------------------------------------------------------------------------
+# steps 1-2: codes
+# ---------------------------------------------------------------------------
+
+def check_codes_hand(o):
+    """Hand-worked codes (tests/golden/codes_hand.txt), fp32 and bf16."""
+    for c in read_code_cases():
+        W = f32(c["W"])
+        x = f32(c["x"])
+        got = int(o.code(x, W)[0])
+        assert got == c["code"], f"{c['name']}: code {got} != {c['code']}"
+        if c["name"] != "order":  # 1e8 is not a bf16 value
+            got16 = int(o.code(bf16_bits(x), bf16_bits(W))[0])
+            assert got16 == c["code"], f"{c['name']} (bf16): code {got16} != {c['code']}"
+
+
+def check_codes_identity_sign(o):
+    """W = identity columns: the code is the sign-bit pattern of x (textbook sign)."""
+    rng = np.random.default_rng(7)
+    for D in (8, 16, 64):
+        W = np.eye(D, dtype=np.float32)
+        x = rng.standard_normal((200, D)).astype(np.float32)
+        x[::7, 3] = 0.0  # exact zeros give 0
+        codes = o.code(x, W)
+        want = ((x > 0).astype(np.uint64) << np.arange(D, dtype=np.uint64)).sum(axis=1)
+        assert np.array_equal(codes, want.astype(np.uint64)), f"identity D={D}"
+
+
+def check_codes_invariances(o):
+    """C(2^k x) = C(x) (exact scaling) and C(-x) = ~C(x) when no sum is exactly 0."""
+    W = o.projection(99, 128, 64, "bf16")
+    rng = np.random.default_rng(3)
+    xf = rng.standard_normal((64, 128)).astype(np.float32)
+    x = bf16_bits(xf)
+    c = o.code(x, W)
+    for k in (-3, 1, 4):
+        assert np.array_equal(o.code(bf16_bits(bf16_to_f64(x) * 2.0 ** k), W), c), f"scale 2^{k}"
+    neg = o.code(x ^ np.uint16(0x8000), W)
+    assert np.array_equal(neg, ~c), "C(-x) != ~C(x)"
+
+
+def check_simhash_law(o, trials_per_theta=1_000_000):
+    """SimHash collision law: P[bit differs] = theta / pi for a random Gaussian
+    hyperplane (Goemans & Williamson 1995; Charikar 2002).  Within 3 sigma."""
+    D, bits = 64, 64
+    pairs_per_w = 16
+    n_w = int(math.ceil(trials_per_theta / (bits * pairs_per_w)))
+    rng = np.random.default_rng(11)
+    thetas = (math.pi / 6, math.pi / 3, math.pi / 2, 2 * math.pi / 3)
+    diff = {t: 0 for t in thetas}
+    total = n_w * pairs_per_w * bits
+    for wi in range(n_w):
+        W = o.projection(1000 + wi, D, bits, "fp32")
+        u = rng.standard_normal((pairs_per_w, D))
+        u /= np.linalg.norm(u, axis=1, keepdims=True)
+        z = rng.standard_normal((pairs_per_w, D))
+        z -= (z * u).sum(axis=1, keepdims=True) * u
+        z /= np.linalg.norm(z, axis=1, keepdims=True)
+        cu = o.code(f32(u), W)
+        for t in thetas:
+            v = math.cos(t) * u + math.sin(t) * z
+            cv = o.code(f32(v), W)
+            diff[t] += sum(popcount_brute(a ^ b) for a, b in zip(cu.tolist(), cv.tolist()))
+    for t in thetas:
+        p = t / math.pi
+        sigma = math.sqrt(p * (1 - p) / total)
+        est = diff[t] / total
+        assert abs(est - p) <= 3 * sigma, f"theta={t:.4f}: {est:.5f} vs {p:.5f} (3s={3 * sigma:.5f})"
+
+
+def check_projection_moments(o):
+    """The drawn W is ~N(0,1): mean ~0, variance ~1 (Irwin-Hall(12) has variance
+    (65536^2-1)/65536^2), support within +-6, distinct seeds give distinct W."""
+    W = bf16_to_f64(o.projection(5, 128, 64, "bf16"))
+    assert abs(W.mean()) < 0.05 and abs(W.var() - 1.0) < 0.06 and np.abs(W).max() <= 6.0
+    W2 = o.projection(6, 128, 64, "bf16")
+    assert not np.array_equal(W, bf16_to_f64(W2))
+    Wf = o.projection(5, 128, 64, "fp32").astype(np.float64)
+    # the bf16 matrix is the fp32 one rounded
+    assert np.array_equal(bf16_to_f64(bf16_bits(Wf)), W)
+
+
+# ---------------------------------------------------------------------------
+# steps 3-4: distances and the eviction choice
+# ---------------------------------------------------------------------------
+
+def check_distance_brute(o):
+    """Group distance = sum over the G query codes of the popcount of the XOR,
+    checked bit by bit."""
+    rng = np.random.default_rng(5)
+    for G in (1, 2, 4, 8):
+        for _ in range(50):
+            cq = rng.integers(0, 2 ** 63, size=G, dtype=np.uint64) * np.uint64(2) + rng.integers(
+                0, 2, size=G, dtype=np.uint64)
+            cs = int(rng.integers(0, 2 ** 63, dtype=np.uint64)) * 2 + 1
+            want = sum(sum(((int(a) >> i) & 1) != ((cs >> i) & 1) for i in range(64)) for a in cq)
+            assert o.group_distance(cq, cs) == want
+    assert o.group_distance(np.array([0], np.uint64), (1 << 64) - 1) == 64
+    assert o.group_distance(np.array([5, 5], np.uint64), 5) == 0
+
+
+def check_argmax_ties(o):
+    """Largest distance wins; ties go to the lowest slot (first maximum)."""
+    rng = np.random.default_rng(9)
+    for n in (1, 2, 3, 17, 300):
+        for _ in range(30):
+            d = rng.integers(0, 5, size=n).astype(np.int32)
+            assert o.most_dissimilar(d) == int(np.argmax(d))
+    assert o.most_dissimilar(np.array([3, 3, 3], np.int32)) == 0
+    assert o.most_dissimilar(np.array([0, 7, 2, 7], np.int32)) == 1
+
+
+def check_eviction_hand(o):
+    """Hand-worked eviction sequence (tests/golden/eviction_hand.txt)."""
+    c = read_eviction_case()
+    W = np.eye(4, dtype=np.float32)
+    fill = f32(c["fill"])
+    vals = f32(np.arange(len(c["fill"]) * 4).reshape(-1, 4))
+    st = o.unit_fill(W, c["budget"], fill, vals)
+    q = f32([[s["q"]] for s in c["steps"]])
+    k = f32([s["k"] for s in c["steps"]])
+    v = f32(np.arange(len(c["steps"]) * 4).reshape(-1, 4) + 100)
+    r = o.unit_stream(st, q, k, v)
+    assert r["evicted"].tolist() == [s["expect"] for s in c["steps"]], r["evicted"]
+    assert r["written"].tolist() == [s["slot"] for s in c["steps"]], r["written"]
+    assert st.codes.tolist() == c["codes_final"], st.codes
+    # the last token (written to slot 2) is resident with its K and V
+    assert np.array_equal(st.K[2], k[-1]) and np.array_equal(st.V[2], v[-1])
+
+
+def check_special_cases(o):
+    """All codes equal -> slot 0 every step; G = 1 with the query code equal to the
+    complement of exactly one slot's code -> that slot."""
+    D, B = 8, 6
+    W = np.eye(D, dtype=np.float32)
+    K = f32(np.ones((B, D)))
+    st = o.unit_fill(W, B, K, K)
+    T = 5
+    q = f32(np.random.default_rng(1).standard_normal((T, 2, D)))
+    r = o.unit_stream(st, q, f32(np.ones((T, D))), f32(np.ones((T, D))))
+    assert r["evicted"].tolist() == [0] * T
+    # complement case
+    rng = np.random.default_rng(2)
+    signs = rng.choice([-1.0, 1.0], size=(B, D))
+    signs[4] = -np.array([1, -1, 1, 1, -1, 1, -1, -1.0])
+    # make every other row differ from row 4 in at least one position
+    for s in range(B):
+        if s != 4 and np.array_equal(signs[s], signs[4]):
+            signs[s, 0] *= -1
+    st = o.unit_fill(W, B, f32(signs), f32(signs))
+    qv = f32([[[1, -1, 1, 1, -1, 1, -1, -1.0]]])
+    r = o.unit_stream(st, qv, f32(np.ones((1, D))), f32(np.ones((1, D))))
+    assert r["evicted"].tolist() == [4]
+
+
+def check_stream_invariants(o):
+    """Random small streams: occupancy never exceeds the budget; appends fill the
+    free slots in order; the evicted slot maximises the brute-force distance with
+    the lowest index on ties; exactly one slot changes per step; the new token is
+    resident with its K, V and code; the output is attention over the post-step
+    cache."""
+    rng = np.random.default_rng(17)
+    for (D, G, bits, B, n, T) in ((16, 2, 8, 7, 4, 40), (32, 4, 16, 12, 12, 30), (8, 1, 32, 5, 0, 12)):
+        W = o.projection(int(rng.integers(1 << 30)), D, bits, "fp32")
+        Kf = f32(rng.standard_normal((n, D)))
+        Vf = f32(rng.standard_normal((n, D)))
+        st = o.unit_fill(W, B, Kf, Vf)
+        for t in range(T):
+            q = f32(rng.standard_normal((1, G, D)))
+            k = f32(rng.standard_normal((1, D)))
+            v = f32(rng.standard_normal((1, D)))
+            before_K, before_V = st.K.copy(), st.V.copy()
+            before_codes, occ = st.codes.copy(), st.occupancy
+            r = o.unit_stream(st, q, k, v)
+            slot = int(r["written"][0])
+            assert st.occupancy == min(occ + 1, B) <= B
+            if occ < B:
+                assert r["evicted"][0] == -1 and slot == occ
+            else:
+                cq = o.code(q[0], W)
+                dist = [sum(popcount_brute(int(a) ^ int(cs)) for a in cq) for cs in before_codes]
+                assert slot == int(np.argmax(dist)) == r["evicted"][0]
+            changed = np.nonzero(np.any(st.K != before_K, axis=1) | np.any(st.V != before_V, axis=1)
+                                 | (st.codes != before_codes))[0]
+            assert set(changed.tolist()) <= {slot}
+            assert np.array_equal(st.K[slot], k[0]) and np.array_equal(st.V[slot], v[0])
+            assert int(st.codes[slot]) == int(o.code(k[0], W)[0])
+            want = o.attend(q[0], st.K[:st.occupancy], st.V[:st.occupancy])
+            assert np.allclose(r["out"][0], want, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# attention
+# ---------------------------------------------------------------------------
+
+def check_attention_hand(o):
+    """Hand-worked cases (tests/golden/attention_hand.txt): two-slot logistic
+    weights, uniform logits -> mean of V, scaled logits -> tanh(1)."""
+    for c in read_attention_cases():
+        got = o.attend(f32([c["q"]]), f32(c["K"]), f32(c["V"]))[0]
+        assert np.allclose(got, c["out"], rtol=0, atol=1e-13), (c["name"], got, c["out"])
+
+
+def check_attention_closed_forms(o):
+    """Closed forms and invariants on random data: two slots -> logistic weights;
+    one dominant key -> its value; permutation and logit-shift invariance."""
+    rng = np.random.default_rng(23)
+    D = 64
+    for _ in range(20):
+        q = f32(rng.standard_normal((1, D)))
+        K = f32(rng.standard_normal((2, D)))
+        V = f32(rng.standard_normal((2, D)))
+        l = (q.astype(np.float64) @ K.astype(np.float64).T)[0] / 8.0  # sqrt(64) = 8
+        w0 = 1.0 / (1.0 + math.exp(l[1] - l[0]))
+        want = w0 * V[0].astype(np.float64) + (1 - w0) * V[1].astype(np.float64)
+        assert np.allclose(o.attend(q, K, V)[0], want, rtol=0, atol=1e-12)
+    q = f32(rng.standard_normal((2, D)))
+    K = f32(rng.standard_normal((50, D)))
+    V = f32(rng.standard_normal((50, D)))
+    K[17] = 40.0 * q[0]  # logit gap >> 50 for head 0
+    out = o.attend(q, K, V)
+    assert np.allclose(out[0], V[17], rtol=0, atol=1e-12)
+    perm = rng.permutation(50)
+    assert np.allclose(o.attend(q, K[perm], V[perm]), out, rtol=0, atol=1e-12)
+    # adding the same vector u to every key shifts each head's logits by q.u
+    Ks = f32(np.round(rng.standard_normal((30, D)) * 64) / 64)  # +0.5 below stays exact
+    Vs = f32(rng.standard_normal((30, D)))
+    u = np.zeros(D, np.float32)
+    u[5] = 0.5
+    assert np.allclose(o.attend(q, Ks + u, Vs), o.attend(q, Ks, Vs), rtol=0, atol=1e-12)
+    # G heads are independent: attend on each head alone gives the same row
+    full = o.attend(q, Ks, Vs)
+    for g in range(2):
+        assert np.allclose(o.attend(q[g:g + 1], Ks, Vs)[0], full[g], rtol=0, atol=0)
+
+
+def check_attention_bf16_elements(o):
+    """bf16 tensors are read as their exact values: same result as the fp32
+    tensors holding the same values."""
+    rng = np.random.default_rng(29)
+    q, K, V = (bf16_bits(rng.standard_normal(s)) for s in ((4, 128), (33, 128), (33, 128)))
+    a = o.attend(q, K, V)
+    b = o.attend(f32(bf16_to_f64(q)), f32(bf16_to_f64(K)), f32(bf16_to_f64(V)))
+    assert np.array_equal(a, b)
+
+
+ALL_CHECKS = [
+    check_codes_hand, check_codes_identity_sign, check_codes_invariances, check_projection_moments,
+    check_distance_brute, check_argmax_ties, check_eviction_hand, check_special_cases,
+    check_stream_invariants, check_attention_hand, check_attention_closed_forms,
+    check_attention_bf16_elements,
+]

@@ -1,0 +1,30 @@
+"""Each planted mistake in the oracle (ORACLE_MUTANT builds of the same C file)
+must fail at least one pin — evidence that the pins would catch a dropped term,
+a wrong sign, index or tie-break.  CPU only."""
+import pytest
+
+import oracle
+import pins
+
+MUTANTS = {
+    1: "projection reads W transposed",
+    2: "binarisation threshold >= 0",
+    3: "only the first query head of a group is scored",
+    4: "ties go to the highest slot",
+    5: "evicts the most similar slot",
+    6: "attention scale 1/sqrt(D) dropped",
+    7: "value rows read with a transposed index",
+    8: "the new token's value is not written",
+}
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS), ids=lambda m: MUTANTS[m])
+def test_mutant_is_caught(mutant, tmp_path_factory):
+    o = oracle.load(mutant, build_dir=str(tmp_path_factory.mktemp(f"mut{mutant}")))
+    failed = []
+    for check in pins.ALL_CHECKS:
+        try:
+            check(o)
+        except AssertionError:
+            failed.append(check.__name__)
+    assert failed, f"mutant {mutant} ({MUTANTS[mutant]}) passed every pin"
