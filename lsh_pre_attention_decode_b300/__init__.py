@@ -1,0 +1,17 @@
+"""B300-native HashEvict decode step (pre-attention LSH eviction + attention over
+the fixed-budget cache).
+
+Python binding of ``libhashevict.so`` (C ABI in ``include/hashevict.h``):
+argument marshalling only — every step of the decode path runs in the CUDA
+kernels of the library.  There is no CPU fallback: importing the binding when
+the library is missing raises.
+
+Method: "HashEvict: A Pre-Attention KV Cache Eviction Strategy using
+Locality-Sensitive Hashing" (arXiv 2412.16187), abstract and technical
+framework steps 1-5.
+"""
+from ._binding import (  # noqa: F401
+    HE_DTYPE_BF16, HE_DTYPE_FP32, HashEvict, HashEvictError, HeCfg, he_codes, he_create,
+    he_destroy, he_fill, he_get_projection, he_last_evicted, he_launch_info, he_occupancy,
+    he_read_state, he_scores, he_step, he_step_bytes, he_step_host, he_strerror, lib, lib_path,
+)

@@ -1,0 +1,246 @@
+"""ctypes binding of libhashevict.so, one Python function per C entry point
+(same names), plus a small handle class.  Tensors are passed by data_ptr();
+streams default to torch's current CUDA stream."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB
+
+HE_DTYPE_BF16 = 0
+HE_DTYPE_FP32 = 1
+
+_i32 = ctypes.c_int32
+_vp = ctypes.c_void_p
+
+
+class HeCfg(ctypes.Structure):
+    _fields_ = [("batch", _i32), ("heads", _i32), ("kv_heads", _i32), ("head_dim", _i32),
+                ("bits", _i32), ("budget", _i32), ("dtype", _i32), ("reserved", _i32),
+                ("seed", ctypes.c_uint64)]
+
+
+class HashEvictError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn}: {code} ({he_strerror(code)})")
+        self.code = code
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return LIB
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library.  Raises if it has not been built: there is no fallback."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            raise ImportError(f"libhashevict.so is not built ({LIB}); run "
+                              "`python -m lsh_pre_attention_decode_b300._build`")
+        L = ctypes.CDLL(LIB)
+        P = ctypes.POINTER
+        L.he_create.argtypes = [P(HeCfg), P(_vp)]
+        L.he_fill.argtypes = [_vp, _vp, _vp, _i32, _vp]
+        L.he_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp]
+        L.he_step_host.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp]
+        L.he_destroy.argtypes = [_vp]
+        L.he_last_evicted.argtypes = [_vp, _vp]
+        L.he_read_state.argtypes = [_vp, _vp, _vp, _vp, _vp]
+        L.he_get_projection.argtypes = [_vp, _vp]
+        L.he_codes.argtypes = [_vp, _vp, _i32, _vp, _vp]
+        L.he_scores.argtypes = [_vp, _vp, _vp, _vp]
+        L.he_occupancy.argtypes = [_vp, P(_i32)]
+        L.he_step_bytes.argtypes = [_vp, P(ctypes.c_uint64)]
+        L.he_launch_info.argtypes = [_vp, P(_i32), P(_i32), P(_i32), P(_i32)]
+        L.he_strerror.argtypes = [ctypes.c_int]
+        L.he_strerror.restype = ctypes.c_char_p
+        for n in ("he_create", "he_fill", "he_step", "he_step_host", "he_destroy",
+                  "he_last_evicted", "he_read_state", "he_get_projection", "he_codes", "he_scores",
+                  "he_occupancy", "he_step_bytes", "he_launch_info"):
+            getattr(L, n).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != 0:
+        raise HashEvictError(fn, rc)
+
+
+def _ptr(x) -> int | None:
+    """Device or host address of a torch tensor / numpy array / int / None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if hasattr(x, "ctypes"):
+        return x.ctypes.data
+    raise TypeError(f"cannot take the address of {type(x)}")
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if hasattr(stream, "cuda_stream"):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def he_strerror(code: int) -> str:
+    return lib().he_strerror(code).decode()
+
+
+def he_create(cfg: HeCfg) -> int:
+    h = _vp()
+    _check("he_create", lib().he_create(ctypes.byref(cfg), ctypes.byref(h)))
+    return h.value
+
+
+def he_fill(h: int, K, V, n: int, stream=None) -> None:
+    _check("he_fill", lib().he_fill(h, _ptr(K), _ptr(V), n, _stream(stream)))
+
+
+def he_step(h: int, q, k, v, out, stream=None) -> None:
+    _check("he_step", lib().he_step(h, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _stream(stream)))
+
+
+def he_step_host(h: int, q, k, v, out, stream=None) -> None:
+    _check("he_step_host",
+           lib().he_step_host(h, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _stream(stream)))
+
+
+def he_destroy(h: int) -> None:
+    _check("he_destroy", lib().he_destroy(h))
+
+
+def he_last_evicted(h: int, host_slots) -> None:
+    _check("he_last_evicted", lib().he_last_evicted(h, _ptr(host_slots)))
+
+
+def he_read_state(h: int, K=None, V=None, codes=None, occupancy=None) -> None:
+    _check("he_read_state", lib().he_read_state(h, _ptr(K), _ptr(V), _ptr(codes),
+                                                _ptr(occupancy)))
+
+
+def he_get_projection(h: int, host_W) -> None:
+    _check("he_get_projection", lib().he_get_projection(h, _ptr(host_W)))
+
+
+def he_codes(h: int, x, n: int, codes, stream=None) -> None:
+    _check("he_codes", lib().he_codes(h, _ptr(x), n, _ptr(codes), _stream(stream)))
+
+
+def he_scores(h: int, q, dist, stream=None) -> None:
+    _check("he_scores", lib().he_scores(h, _ptr(q), _ptr(dist), _stream(stream)))
+
+
+def he_occupancy(h: int) -> int:
+    o = _i32()
+    _check("he_occupancy", lib().he_occupancy(h, ctypes.byref(o)))
+    return o.value
+
+
+def he_step_bytes(h: int) -> int:
+    b = ctypes.c_uint64()
+    _check("he_step_bytes", lib().he_step_bytes(h, ctypes.byref(b)))
+    return b.value
+
+
+def he_launch_info(h: int) -> dict:
+    a, b, c, d = _i32(), _i32(), _i32(), _i32()
+    _check("he_launch_info", lib().he_launch_info(h, ctypes.byref(a), ctypes.byref(b),
+                                                  ctypes.byref(c), ctypes.byref(d)))
+    return {"ctas": a.value, "ctas_per_sm": b.value, "tiles": c.value, "stages": d.value}
+
+
+class HashEvict:
+    """One layer's HashEvict cache on the current CUDA device (torch tensors)."""
+
+    def __init__(self, batch: int, heads: int, kv_heads: int, head_dim: int, bits: int,
+                 budget: int, dtype: str = "bf16", seed: int = 0):
+        self.cfg = HeCfg(batch=batch, heads=heads, kv_heads=kv_heads, head_dim=head_dim,
+                         bits=bits, budget=budget,
+                         dtype=HE_DTYPE_FP32 if dtype == "fp32" else HE_DTYPE_BF16, reserved=0,
+                         seed=seed)
+        self.dtype = dtype
+        self.h = he_create(self.cfg)
+
+    def close(self) -> None:
+        if self.h:
+            he_destroy(self.h)
+            self.h = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        self.close()
+
+    @property
+    def torch_dtype(self):
+        import torch
+        return torch.float32 if self.dtype == "fp32" else torch.bfloat16
+
+    def fill(self, K, V, stream=None) -> None:
+        """K, V: [batch][kv_heads][n][head_dim] device tensors."""
+        n = 0 if K is None else K.shape[2]
+        he_fill(self.h, K, V, n, stream)
+
+    def step(self, q, k, v, out=None, stream=None):
+        import torch
+        c = self.cfg
+        if out is None:
+            out = torch.empty((c.batch, c.heads, c.head_dim), dtype=torch.float32, device=q.device)
+        he_step(self.h, q, k, v, out, stream)
+        return out
+
+    def last_evicted(self):
+        import numpy as np
+        a = np.empty((self.cfg.batch, self.cfg.kv_heads), np.int32)
+        he_last_evicted(self.h, a)
+        return a
+
+    def state(self):
+        """Host snapshot: K, V [batch][kv][budget][D] (uint16 bf16 bits or float32),
+        codes [batch][kv][budget] (uint8/16/32/64), occupancy."""
+        import numpy as np
+        c = self.cfg
+        et = np.float32 if self.dtype == "fp32" else np.uint16
+        ct = {8: np.uint8, 16: np.uint16, 32: np.uint32, 64: np.uint64}[c.bits]
+        K = np.empty((c.batch, c.kv_heads, c.budget, c.head_dim), et)
+        V = np.empty_like(K)
+        codes = np.empty((c.batch, c.kv_heads, c.budget), ct)
+        occ = np.zeros(1, np.int32)
+        he_read_state(self.h, K, V, codes, occ)
+        return K, V, codes, int(occ[0])
+
+    def projection(self):
+        import numpy as np
+        c = self.cfg
+        W = np.empty((c.head_dim, c.bits), np.float32 if self.dtype == "fp32" else np.uint16)
+        he_get_projection(self.h, W)
+        return W
+
+    @property
+    def occupancy(self) -> int:
+        return he_occupancy(self.h)
+
+    @property
+    def step_bytes(self) -> int:
+        return he_step_bytes(self.h)
+
+    def launch_info(self) -> dict:
+        return he_launch_info(self.h)

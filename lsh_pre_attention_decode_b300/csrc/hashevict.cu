@@ -1,0 +1,454 @@
+// hashevict.cu — the C ABI of libhashevict.so (declared in include/hashevict.h):
+// handle life cycle, argument checks, launch shapes and the kernel dispatch.
+// Every step of the decode path runs in the kernels of he_step.cuh.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "hashevict.h"
+#include "he_step.cuh"
+
+namespace {
+
+using he::bf16_t;
+using he::StepParams;
+
+constexpr int kStages = 4;
+
+struct Kernels {
+  const void* step;
+  const void* score;
+  const void* code;
+  int step_smem;
+  int rec_floats;
+};
+
+template <typename T, int D, int G>
+Kernels kernels_for() {
+  using S = he::StepShape<T, D, G, kStages>;
+  return Kernels{reinterpret_cast<const void*>(&he::step_kernel<T, D, G, kStages>),
+                 reinterpret_cast<const void*>(&he::score_kernel<T, D, G>),
+                 reinterpret_cast<const void*>(&he::code_kernel<T, D>), S::SMEM, S::REC};
+}
+
+template <typename T, int D>
+bool pick_g(int G, Kernels* k) {
+  switch (G) {
+    case 1: *k = kernels_for<T, D, 1>(); return true;
+    case 2: *k = kernels_for<T, D, 2>(); return true;
+    case 4: *k = kernels_for<T, D, 4>(); return true;
+    case 8: *k = kernels_for<T, D, 8>(); return true;
+    default: return false;
+  }
+}
+
+bool pick_kernels(int dtype, int D, int G, Kernels* k) {
+  if (dtype == HE_DTYPE_BF16) {
+    if (D == 64) return pick_g<bf16_t, 64>(G, k);
+    if (D == 128) return pick_g<bf16_t, 128>(G, k);
+  } else if (dtype == HE_DTYPE_FP32) {
+    if (D == 64) return pick_g<float, 64>(G, k);
+    if (D == 128) return pick_g<float, 128>(G, k);
+  }
+  return false;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Keeps the caller's current device and switches to the handle's for the call.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) {
+      ok = false;
+      return;
+    }
+    if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+}  // namespace
+
+struct he_ctx {
+  he_cfg cfg;
+  int device = 0;
+  int G = 0;
+  int U = 0;
+  int eb = 0;           // element bytes
+  int code_bytes = 0;   // bits / 8
+  int code_stride = 0;  // bytes per unit row of codes, multiple of 16
+  Kernels kern{};
+  void* K = nullptr;
+  void* V = nullptr;
+  void* W = nullptr;
+  unsigned char* codes = nullptr;
+  int32_t* evicted = nullptr;
+  int32_t* counters = nullptr;
+  int32_t* err = nullptr;
+  float* partials = nullptr;
+  void* sq = nullptr;  // he_step_host staging
+  void* sk = nullptr;
+  void* sv = nullptr;
+  float* sout = nullptr;
+  int occupancy = 0;
+  bool filled = false;
+  int sticky = HE_OK;
+  int num_sms = 0;
+  int ctas_per_sm = 0;
+  int max_ctas = 0;
+};
+
+namespace {
+
+int fail_cuda(he_ctx* h, cudaError_t e) {
+  (void)cudaGetLastError();
+  if (h) h->sticky = HE_ECUDA;
+  (void)e;
+  return HE_ECUDA;
+}
+
+#define HE_TRY(h, call)                         \
+  do {                                          \
+    cudaError_t e_ = (call);                    \
+    if (e_ != cudaSuccess) return fail_cuda((h), e_); \
+  } while (0)
+
+size_t vec_bytes(const he_ctx* h, int heads) {
+  return (size_t)h->cfg.batch * heads * h->cfg.head_dim * h->eb;
+}
+
+void free_all(he_ctx* h) {
+  void* ptrs[] = {h->K, h->V, h->W, h->codes, h->evicted, h->counters, h->err, h->partials,
+                  h->sq, h->sk, h->sv, h->sout};
+  for (void* p : ptrs)
+    if (p) cudaFree(p);
+}
+
+StepParams base_params(const he_ctx* h) {
+  StepParams p{};
+  p.K = h->K;
+  p.V = h->V;
+  p.codes = h->codes;
+  p.W = h->W;
+  p.evicted = h->evicted;
+  p.partials = h->partials;
+  p.counters = h->counters;
+  p.err = h->err;
+  p.U = h->U;
+  p.kv_heads = h->cfg.kv_heads;
+  p.budget = h->cfg.budget;
+  p.occ = h->occupancy;
+  p.tpu = (h->occupancy + he::kTile - 1) / he::kTile;
+  p.total_tiles = h->U * p.tpu;
+  p.bits = h->cfg.bits;
+  p.code_stride = h->code_stride;
+  p.append_slot = h->occupancy < h->cfg.budget ? h->occupancy : -1;
+  p.qscale = (float)(1.4426950408889634 / std::sqrt((double)h->cfg.head_dim));
+  return p;
+}
+
+int launch_codes(he_ctx* h, const void* x, int64_t rows, int64_t per_unit, int64_t x_unit_rows,
+                 unsigned char* out, int64_t out_unit_bytes, cudaStream_t s) {
+  if (rows == 0) return HE_OK;
+  const int vb = he::kThreads / h->cfg.bits;
+  int64_t blocks = (rows + vb - 1) / vb;
+  const int64_t cap = (int64_t)h->num_sms * 16;
+  if (blocks > cap) blocks = cap;
+  const void* W = h->W;
+  int bits = h->cfg.bits;
+  void* args[] = {(void*)&x, (void*)&rows, (void*)&per_unit, (void*)&x_unit_rows, (void*)&W,
+                  (void*)&bits, (void*)&out, (void*)&out_unit_bytes};
+  HE_TRY(h, cudaLaunchKernel(h->kern.code, dim3((unsigned)blocks), dim3(he::kThreads), args, 0, s));
+  return HE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* he_strerror(int code) {
+  switch (code) {
+    case HE_OK: return "ok";
+    case HE_EINVAL: return "invalid argument (configuration, size, pointer or alignment)";
+    case HE_ENOTFILLED: return "the cache has not been filled (call he_fill first)";
+    case HE_ECUDA: return "a CUDA call failed; the handle refuses further work";
+    case HE_ENOMEM: return "device memory allocation failed";
+    case HE_EDEVICE: return "a kernel reported an internal error (a wait gave up)";
+    default: return "unknown error code";
+  }
+}
+
+int he_create(const he_cfg* cfg, he_handle* out) {
+  if (!cfg || !out) return HE_EINVAL;
+  *out = nullptr;
+  const he_cfg c = *cfg;
+  if (c.batch < 1 || c.heads < 1 || c.kv_heads < 1 || c.heads % c.kv_heads != 0) return HE_EINVAL;
+  if (c.bits != 8 && c.bits != 16 && c.bits != 32 && c.bits != 64) return HE_EINVAL;
+  if (c.budget < 1 || c.budget > (1 << 24) || c.reserved != 0) return HE_EINVAL;
+  if ((int64_t)c.batch * c.kv_heads > 65536) return HE_EINVAL;
+  const int G = c.heads / c.kv_heads;
+  Kernels kern;
+  if (!pick_kernels(c.dtype, c.head_dim, G, &kern)) return HE_EINVAL;
+  const int64_t U = (int64_t)c.batch * c.kv_heads;
+  if (U * ((c.budget + he::kTile - 1) / he::kTile) > INT32_MAX) return HE_EINVAL;
+
+  he_ctx* h = new (std::nothrow) he_ctx();
+  if (!h) return HE_ENOMEM;
+  h->cfg = c;
+  h->G = G;
+  h->U = (int)U;
+  h->eb = c.dtype == HE_DTYPE_FP32 ? 4 : 2;
+  h->code_bytes = c.bits / 8;
+  h->code_stride = (int)(((int64_t)c.budget * h->code_bytes + 15) / 16 * 16);
+  h->kern = kern;
+  if (cudaGetDevice(&h->device) != cudaSuccess) {
+    (void)cudaGetLastError();
+    delete h;
+    return HE_ECUDA;
+  }
+  int rc = HE_OK;
+  do {
+    if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) !=
+        cudaSuccess) { rc = HE_ECUDA; break; }
+    if (cudaFuncSetAttribute(kern.step, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kern.step_smem) != cudaSuccess) { rc = HE_ECUDA; break; }
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&h->ctas_per_sm, kern.step, he::kThreads,
+                                                      kern.step_smem) != cudaSuccess ||
+        h->ctas_per_sm < 1) { rc = HE_ECUDA; break; }
+    h->max_ctas = h->num_sms * h->ctas_per_sm;
+    const size_t cache = (size_t)U * c.budget * c.head_dim * h->eb;
+    const size_t nrec = (size_t)h->max_ctas + (size_t)U;
+    struct { void** p; size_t bytes; } allocs[] = {
+        {&h->K, cache},
+        {&h->V, cache},
+        {&h->W, (size_t)c.head_dim * c.bits * h->eb},
+        {(void**)&h->codes, (size_t)U * h->code_stride},
+        {(void**)&h->evicted, (size_t)U * sizeof(int32_t)},
+        {(void**)&h->counters, (size_t)U * sizeof(int32_t)},
+        {(void**)&h->err, sizeof(int32_t)},
+        {(void**)&h->partials, nrec * kern.rec_floats * sizeof(float)},
+    };
+    for (auto& a : allocs) {
+      if (cudaMalloc(a.p, a.bytes) != cudaSuccess) {
+        (void)cudaGetLastError();
+        rc = HE_ENOMEM;
+        break;
+      }
+    }
+    if (rc != HE_OK) break;
+    if (cudaMemset(h->codes, 0, (size_t)U * h->code_stride) != cudaSuccess ||
+        cudaMemset(h->counters, 0, (size_t)U * sizeof(int32_t)) != cudaSuccess ||
+        cudaMemset(h->err, 0, sizeof(int32_t)) != cudaSuccess ||
+        cudaMemset(h->evicted, 0xFF, (size_t)U * sizeof(int32_t)) != cudaSuccess) {
+      rc = HE_ECUDA;
+      break;
+    }
+    const int n = c.head_dim * c.bits;
+    he::projection_kernel<<<(n + 255) / 256, 256>>>(c.seed, c.head_dim, c.bits,
+                                                   c.dtype == HE_DTYPE_FP32 ? 1 : 0, h->W);
+    if (cudaGetLastError() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+      rc = HE_ECUDA;
+      break;
+    }
+  } while (0);
+  if (rc != HE_OK) {
+    (void)cudaGetLastError();
+    free_all(h);
+    delete h;
+    return rc;
+  }
+  *out = h;
+  return HE_OK;
+}
+
+int he_destroy(he_handle h) {
+  if (!h) return HE_OK;
+  DeviceGuard g(h->device);
+  cudaDeviceSynchronize();
+  (void)cudaGetLastError();
+  free_all(h);
+  delete h;
+  return HE_OK;
+}
+
+int he_fill(he_handle h, const void* K, const void* V, int32_t n, void* stream) {
+  if (!h || n < 0 || n > h->cfg.budget) return HE_EINVAL;
+  if (n > 0 && (!K || !V || !aligned16(K) || !aligned16(V))) return HE_EINVAL;
+  if (h->sticky) return h->sticky;
+  DeviceGuard g(h->device);
+  if (!g.ok) return fail_cuda(h, cudaErrorInvalidDevice);
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t row = (size_t)h->cfg.head_dim * h->eb;
+  if (n > 0) {
+    HE_TRY(h, cudaMemcpy2DAsync(h->K, (size_t)h->cfg.budget * row, K, (size_t)n * row,
+                                (size_t)n * row, (size_t)h->U, cudaMemcpyDeviceToDevice, s));
+    HE_TRY(h, cudaMemcpy2DAsync(h->V, (size_t)h->cfg.budget * row, V, (size_t)n * row,
+                                (size_t)n * row, (size_t)h->U, cudaMemcpyDeviceToDevice, s));
+    const int rc = launch_codes(h, h->K, (int64_t)h->U * n, n, h->cfg.budget, h->codes,
+                                h->code_stride, s);
+    if (rc != HE_OK) return rc;
+  }
+  HE_TRY(h, cudaMemsetAsync(h->counters, 0, (size_t)h->U * sizeof(int32_t), s));
+  h->occupancy = n;
+  h->filled = true;
+  return HE_OK;
+}
+
+int he_step(he_handle h, const void* q, const void* k, const void* v, float* out, void* stream) {
+  if (!h || !q || !k || !v || !out) return HE_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return HE_EINVAL;
+  if (h->sticky) return h->sticky;
+  if (!h->filled) return HE_ENOTFILLED;
+  DeviceGuard g(h->device);
+  if (!g.ok) return fail_cuda(h, cudaErrorInvalidDevice);
+  StepParams p = base_params(h);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  const int grid = p.total_tiles == 0 ? h->U
+                                      : (p.total_tiles < h->max_ctas ? p.total_tiles : h->max_ctas);
+  void* args[] = {(void*)&p};
+  HE_TRY(h, cudaLaunchKernel(h->kern.step, dim3(grid), dim3(he::kThreads), args,
+                             (size_t)h->kern.step_smem, (cudaStream_t)stream));
+  if (h->occupancy < h->cfg.budget) h->occupancy += 1;
+  return HE_OK;
+}
+
+int he_step_host(he_handle h, const void* q, const void* k, const void* v, float* out,
+                 void* stream) {
+  if (!h || !q || !k || !v || !out) return HE_EINVAL;
+  if (h->sticky) return h->sticky;
+  if (!h->filled) return HE_ENOTFILLED;
+  DeviceGuard g(h->device);
+  if (!g.ok) return fail_cuda(h, cudaErrorInvalidDevice);
+  const size_t qb = vec_bytes(h, h->cfg.heads), kb = vec_bytes(h, h->cfg.kv_heads);
+  const size_t ob = (size_t)h->cfg.batch * h->cfg.heads * h->cfg.head_dim * sizeof(float);
+  if (!h->sq) {
+    if (cudaMalloc(&h->sq, qb) != cudaSuccess || cudaMalloc(&h->sk, kb) != cudaSuccess ||
+        cudaMalloc(&h->sv, kb) != cudaSuccess || cudaMalloc((void**)&h->sout, ob) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return HE_ENOMEM;
+    }
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  HE_TRY(h, cudaMemcpyAsync(h->sq, q, qb, cudaMemcpyHostToDevice, s));
+  HE_TRY(h, cudaMemcpyAsync(h->sk, k, kb, cudaMemcpyHostToDevice, s));
+  HE_TRY(h, cudaMemcpyAsync(h->sv, v, kb, cudaMemcpyHostToDevice, s));
+  const int rc = he_step(h, h->sq, h->sk, h->sv, h->sout, stream);
+  if (rc != HE_OK) return rc;
+  HE_TRY(h, cudaMemcpyAsync(out, h->sout, ob, cudaMemcpyDeviceToHost, s));
+  HE_TRY(h, cudaStreamSynchronize(s));
+  return HE_OK;
+}
+
+static int check_device_error(he_ctx* h) {
+  int32_t e = 0;
+  HE_TRY(h, cudaDeviceSynchronize());
+  HE_TRY(h, cudaMemcpy(&e, h->err, sizeof e, cudaMemcpyDeviceToHost));
+  if (e != 0) {
+    h->sticky = HE_EDEVICE;
+    return HE_EDEVICE;
+  }
+  return HE_OK;
+}
+
+int he_last_evicted(he_handle h, int32_t* host_slots) {
+  if (!h || !host_slots) return HE_EINVAL;
+  DeviceGuard g(h->device);
+  const int rc = check_device_error(h);
+  if (rc != HE_OK) return rc;
+  HE_TRY(h, cudaMemcpy(host_slots, h->evicted, (size_t)h->U * sizeof(int32_t),
+                       cudaMemcpyDeviceToHost));
+  return h->sticky;
+}
+
+int he_read_state(he_handle h, void* K, void* V, void* codes, int32_t* occupancy) {
+  if (!h) return HE_EINVAL;
+  DeviceGuard g(h->device);
+  const int rc = check_device_error(h);
+  if (rc != HE_OK) return rc;
+  const size_t cache = (size_t)h->U * h->cfg.budget * h->cfg.head_dim * h->eb;
+  if (K) HE_TRY(h, cudaMemcpy(K, h->K, cache, cudaMemcpyDeviceToHost));
+  if (V) HE_TRY(h, cudaMemcpy(V, h->V, cache, cudaMemcpyDeviceToHost));
+  if (codes) {
+    const size_t w = (size_t)h->cfg.budget * h->code_bytes;
+    HE_TRY(h, cudaMemcpy2D(codes, w, h->codes, (size_t)h->code_stride, w, (size_t)h->U,
+                           cudaMemcpyDeviceToHost));
+  }
+  if (occupancy) *occupancy = h->occupancy;
+  return h->sticky;
+}
+
+int he_get_projection(he_handle h, void* host_W) {
+  if (!h || !host_W) return HE_EINVAL;
+  DeviceGuard g(h->device);
+  HE_TRY(h, cudaDeviceSynchronize());
+  HE_TRY(h, cudaMemcpy(host_W, h->W, (size_t)h->cfg.head_dim * h->cfg.bits * h->eb,
+                       cudaMemcpyDeviceToHost));
+  return HE_OK;
+}
+
+int he_codes(he_handle h, const void* x, int32_t n, void* codes, void* stream) {
+  if (!h || n < 0) return HE_EINVAL;
+  if (n > 0 && (!x || !codes || !aligned16(x) || !aligned16(codes))) return HE_EINVAL;
+  if (h->sticky) return h->sticky;
+  DeviceGuard g(h->device);
+  return launch_codes(h, x, n, n > 0 ? n : 1, n, (unsigned char*)codes,
+                      (int64_t)n * h->code_bytes, (cudaStream_t)stream);
+}
+
+int he_scores(he_handle h, const void* q, int32_t* dist, void* stream) {
+  if (!h || !q || !dist || !aligned16(q) || !aligned16(dist)) return HE_EINVAL;
+  if (h->sticky) return h->sticky;
+  if (!h->filled) return HE_ENOTFILLED;
+  DeviceGuard g(h->device);
+  StepParams p = base_params(h);
+  p.q = q;
+  void* args[] = {(void*)&p, (void*)&dist};
+  HE_TRY(h, cudaLaunchKernel(h->kern.score, dim3(h->U), dim3(he::kThreads), args, 0,
+                             (cudaStream_t)stream));
+  return HE_OK;
+}
+
+int he_occupancy(he_handle h, int32_t* occupancy) {
+  if (!h || !occupancy) return HE_EINVAL;
+  *occupancy = h->occupancy;
+  return HE_OK;
+}
+
+int he_step_bytes(he_handle h, uint64_t* bytes) {
+  if (!h || !bytes) return HE_EINVAL;
+  const uint64_t U = (uint64_t)h->U, B = (uint64_t)h->cfg.budget, D = (uint64_t)h->cfg.head_dim;
+  const uint64_t e = (uint64_t)h->eb, w = (uint64_t)h->code_bytes;
+  const uint64_t Bt = (uint64_t)h->cfg.batch, H = (uint64_t)h->cfg.heads;
+  *bytes = U * B * (2 * D * e + w)        // retained K, V and codes read
+           + U * (2 * D * e + w)          // the overwritten slot
+           + Bt * H * D * e + U * 2 * D * e  // q, k, v in
+           + Bt * H * D * 4                // out
+           + D * (uint64_t)h->cfg.bits * e;  // W
+  return HE_OK;
+}
+
+int he_launch_info(he_handle h, int32_t* ctas, int32_t* ctas_per_sm, int32_t* tiles,
+                   int32_t* stages) {
+  if (!h) return HE_EINVAL;
+  const int tpu = (h->occupancy + he::kTile - 1) / he::kTile;
+  const int T = h->U * tpu;
+  if (ctas) *ctas = T == 0 ? h->U : (T < h->max_ctas ? T : h->max_ctas);
+  if (ctas_per_sm) *ctas_per_sm = h->ctas_per_sm;
+  if (tiles) *tiles = T;
+  if (stages) *stages = kStages;
+  return HE_OK;
+}
+
+}  // extern "C"

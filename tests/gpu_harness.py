@@ -1,0 +1,151 @@
+"""Shared helpers of the GPU parity tests: run a workload's token stream through
+the CUDA library (via the C ABI binding) and through the CPU oracle, and
+compare.  The oracle's inputs always come from the host build of the generator;
+the GPU side takes either the same host tensors or the device build of the
+generator (checked bit-exact against the host build in test_gpu_generator).
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+from dataclasses import dataclass
+
+import numpy as np
+
+import oracle
+import synth
+
+# Attention-output tolerance against the fp64 oracle on the identical retained cache.
+MAX_ABS_TOL = 1e-2
+MEAN_ABS_TOL = 1e-3
+
+
+def torch_from_host(a: np.ndarray, device="cuda"):
+    import torch
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16).to(device)
+    return torch.from_numpy(a.copy()).to(device)
+
+
+def host_from_torch(t) -> np.ndarray:
+    import torch
+    t = t.detach().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+@dataclass
+class GpuRun:
+    evicted: np.ndarray        # [steps][batch][kv_heads]
+    outs: dict                 # step index -> out [batch][heads][D] float32
+    state: tuple | None        # (K, V, codes, occupancy) after the run
+
+
+def make_handle(w: synth.Workload, layer: int = 0):
+    from lsh_pre_attention_decode_b300 import HashEvict
+    return HashEvict(w.batch, w.heads, w.kv_heads, w.head_dim, w.bits, w.budget, w.dtype,
+                     seed=w.projection_seed(layer))
+
+
+def run_gpu(w: synth.Workload, fill_n: int, steps: int, out_steps=(), layer: int = 0,
+            device_gen: bool = False, read_state: bool = False, chunk: int = 256) -> GpuRun:
+    """Fill with prompt tokens [0, fill_n), then stream tokens fill_n .. fill_n+steps-1."""
+    import torch
+    out_steps = set(out_steps)
+    he = make_handle(w, layer)
+    try:
+        if fill_n > 0:
+            if device_gen:
+                K = synth.gpu_kv(w, "key", 0, fill_n, layer)
+                V = synth.gpu_kv(w, "value", 0, fill_n, layer)
+            else:
+                K = torch_from_host(synth.host_kv(w, "key", 0, fill_n, layer))
+                V = torch_from_host(synth.host_kv(w, "value", 0, fill_n, layer))
+            he.fill(K, V)
+            del K, V
+        else:
+            he.fill(None, None)
+        evicted = np.empty((steps, w.batch, w.kv_heads), np.int32)
+        outs = {}
+        out = torch.empty((w.batch, w.heads, w.head_dim), dtype=torch.float32, device="cuda")
+        for c0 in range(0, steps, chunk):
+            n = min(chunk, steps - c0)
+            t0 = fill_n + c0
+            if device_gen:
+                q = synth.gpu_queries(w, t0, n, layer)
+                k = synth.gpu_kv(w, "key", t0, n, layer, token_major=True)
+                v = synth.gpu_kv(w, "value", t0, n, layer, token_major=True)
+            else:
+                q = torch_from_host(synth.host_queries(w, t0, n, layer))
+                k = torch_from_host(synth.host_kv(w, "key", t0, n, layer, token_major=True))
+                v = torch_from_host(synth.host_kv(w, "value", t0, n, layer, token_major=True))
+            for i in range(n):
+                he.step(q[i], k[i], v[i], out)
+                evicted[c0 + i] = he.last_evicted()
+                if c0 + i in out_steps:
+                    outs[c0 + i] = out.cpu().numpy().copy()
+        state = he.state() if read_state else None
+        return GpuRun(evicted, outs, state)
+    finally:
+        he.close()
+
+
+@dataclass
+class OracleRun:
+    evicted: np.ndarray      # [steps]
+    outs: np.ndarray         # [len(out_steps)][G][D] float64
+    codes: np.ndarray
+    K: np.ndarray
+    V: np.ndarray
+    occupancy: int
+
+
+def run_oracle_unit(w: synth.Workload, b: int, j: int, fill_n: int, steps: int, out_steps=(),
+                    layer: int = 0) -> OracleRun:
+    o = oracle.load()
+    W = o.projection(w.projection_seed(layer), w.head_dim, w.bits, w.dtype)
+    Kin = synth.host_unit_kv(w, "key", b, j, 0, fill_n, layer)
+    Vin = synth.host_unit_kv(w, "value", b, j, 0, fill_n, layer)
+    st = o.unit_fill(W, w.budget, Kin, Vin)
+    q = synth.host_unit_queries(w, b, j, fill_n, steps, layer)
+    k = synth.host_unit_kv(w, "key", b, j, fill_n, steps, layer)
+    v = synth.host_unit_kv(w, "value", b, j, fill_n, steps, layer)
+    want = np.zeros(steps, np.uint8)
+    for s in out_steps:
+        want[s] = 1
+    r = o.unit_stream(st, q, k, v, want_out=want)
+    return OracleRun(r["evicted"], r["out"], st.codes, st.K, st.V, st.occupancy)
+
+
+def run_oracle_units(w, units, fill_n, steps, out_steps=(), layer=0, threads=8):
+    """Oracle over several (b, j) units in parallel threads (ctypes releases the GIL)."""
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        futs = {u: ex.submit(run_oracle_unit, w, u[0], u[1], fill_n, steps, out_steps, layer)
+                for u in units}
+        return {u: f.result() for u, f in futs.items()}
+
+
+def compare(w: synth.Workload, g: GpuRun, orc: dict, out_steps=(), check_state: bool = False):
+    """Bit-exact evictions, outputs within tolerance, optional cache state."""
+    out_steps = sorted(out_steps)
+    worst_max, worst_mean = 0.0, 0.0
+    for (b, j), r in orc.items():
+        ge = g.evicted[:, b, j]
+        if not np.array_equal(ge, r.evicted):
+            bad = np.nonzero(ge != r.evicted)[0]
+            raise AssertionError(f"unit ({b},{j}): evictions differ first at step {bad[0]}: "
+                                 f"gpu {ge[bad[0]]} oracle {r.evicted[bad[0]]} "
+                                 f"({len(bad)} of {len(ge)} steps differ)")
+        for i, s in enumerate(out_steps):
+            got = g.outs[s][b, j * w.group:(j + 1) * w.group].astype(np.float64)
+            err = np.abs(got - r.outs[i])
+            worst_max = max(worst_max, float(err.max()))
+            worst_mean = max(worst_mean, float(err.mean()))
+        if check_state:
+            K, V, codes, occ = g.state
+            assert occ == r.occupancy
+            assert np.array_equal(codes[b, j].astype(np.uint64), r.codes), f"codes ({b},{j})"
+            assert np.array_equal(K[b, j], r.K) and np.array_equal(V[b, j], r.V), f"K/V ({b},{j})"
+    assert worst_max <= MAX_ABS_TOL, f"max-abs error {worst_max}"
+    assert worst_mean <= MEAN_ABS_TOL, f"mean-abs error {worst_mean}"
+    return worst_max, worst_mean
