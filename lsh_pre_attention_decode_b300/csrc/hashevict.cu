@@ -8,31 +8,86 @@
 #include <cstdint>
 #include <cstring>
 #include <new>
+#include <type_traits>
+
+#include <cudaTypedefs.h>
 
 #include "hashevict.h"
-#include "he_step.cuh"
+#include "he_pipeline.cuh"
+#include "he_step_simt.cuh"
 
 namespace {
 
 using he::bf16_t;
 using he::StepParams;
 
-constexpr int kStages = 4;
+// Launch configuration of the two step engines.
+constexpr int kSimtStages = 4;    // CUDA-core engine (fp32 caches): 32-slot tiles
+constexpr int kStreamStages = 3;  // tensor-core pipeline (bf16 caches): 64-slot tiles
+constexpr bool kPSplit = true;    // attention weights as bf16 hi + lo parts
 
 struct Kernels {
-  const void* step;
+  const void* step;    // fp32: the fused step; bf16: the stream kernel
+  const void* prep;    // bf16 pipeline only
+  const void* merge;   // bf16 pipeline only
   const void* score;
   const void* code;
   int step_smem;
+  int step_threads;
+  int prep_smem;
+  int merge_smem_per_contrib;
+  int merge_smem_base;
+  int tile;
   int rec_floats;
+  bool pipeline;
 };
 
 template <typename T, int D, int G>
 Kernels kernels_for() {
-  using S = he::StepShape<T, D, G, kStages>;
-  return Kernels{reinterpret_cast<const void*>(&he::step_kernel<T, D, G, kStages>),
-                 reinterpret_cast<const void*>(&he::score_kernel<T, D, G>),
-                 reinterpret_cast<const void*>(&he::code_kernel<T, D>), S::SMEM, S::REC};
+  Kernels k{};
+  k.score = reinterpret_cast<const void*>(&he::score_kernel<T, D, G>);
+  k.code = reinterpret_cast<const void*>(&he::code_kernel<T, D>);
+  if constexpr (std::is_same<T, bf16_t>::value) {
+    using S = he::StreamShape<D, G, kStreamStages>;
+    k.step = reinterpret_cast<const void*>(&he::stream_kernel<D, G, kStreamStages, kPSplit>);
+    k.prep = reinterpret_cast<const void*>(&he::prep_kernel<D, G>);
+    k.merge = reinterpret_cast<const void*>(&he::merge_kernel<D, G>);
+    k.step_smem = S::SMEM_ALLOC;
+    k.step_threads = S::NT;
+    k.prep_smem = he::PrepShape<D, G>::SMEM;
+    k.merge_smem_base = he::merge_smem<D, G>(0);
+    k.merge_smem_per_contrib = 2 * G * 4;
+    k.tile = S::TS;
+    k.rec_floats = he::PRec<G, D>::FLOATS;
+    k.pipeline = true;
+  } else {
+    using S = he::SimtShape<T, D, G, kSimtStages>;
+    k.step = reinterpret_cast<const void*>(&he::step_kernel_simt<T, D, G, kSimtStages>);
+    k.step_smem = S::SMEM;
+    k.step_threads = he::kThreads;
+    k.tile = he::kTile;
+    k.rec_floats = he::Record<G, D>::FLOATS;
+    k.pipeline = false;
+  }
+  return k;
+}
+
+// Launch with programmatic stream serialisation: the kernel may start before
+// the previous kernel in the stream finishes; it orders itself with
+// griddepcontrol.wait.
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 template <typename T, int D>
@@ -57,6 +112,29 @@ bool pick_kernels(int dtype, int D, int G, Kernels* k) {
   return false;
 }
 
+// 2-D tensor map over a cache viewed as [rows][D] bf16 rows; boxes of
+// 64 elements (128 bytes) x `box_rows` rows, 128B swizzle.
+bool encode_cache_map(CUtensorMap* map, void* base, uint64_t rows, int D, int box_rows) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Keeps the caller's current device and switches to the handle's for the call.
@@ -78,6 +156,12 @@ struct DeviceGuard {
 
 }  // namespace
 
+#ifdef HE_TIMELINE
+extern "C" int he_debug_set_timeline(int64_t* dev) {
+  return cudaMemcpyToSymbol(he::g_he_timeline, &dev, sizeof dev) == cudaSuccess ? HE_OK : HE_ECUDA;
+}
+#endif
+
 struct he_ctx {
   he_cfg cfg;
   int device = 0;
@@ -87,6 +171,8 @@ struct he_ctx {
   int code_bytes = 0;   // bits / 8
   int code_stride = 0;  // bytes per unit row of codes, multiple of 16
   Kernels kern{};
+  CUtensorMap tmK{};  // tensor-core engine: 2-D maps over K and V
+  CUtensorMap tmV{};
   void* K = nullptr;
   void* V = nullptr;
   void* W = nullptr;
@@ -95,6 +181,7 @@ struct he_ctx {
   int32_t* counters = nullptr;
   int32_t* err = nullptr;
   float* partials = nullptr;
+  he::UnitOut* uo = nullptr;  // bf16 pipeline: per-unit results of prep
   void* sq = nullptr;  // he_step_host staging
   void* sk = nullptr;
   void* sv = nullptr;
@@ -128,7 +215,7 @@ size_t vec_bytes(const he_ctx* h, int heads) {
 
 void free_all(he_ctx* h) {
   void* ptrs[] = {h->K, h->V, h->W, h->codes, h->evicted, h->counters, h->err, h->partials,
-                  h->sq, h->sk, h->sv, h->sout};
+                  h->uo, h->sq, h->sk, h->sv, h->sout};
   for (void* p : ptrs)
     if (p) cudaFree(p);
 }
@@ -147,7 +234,8 @@ StepParams base_params(const he_ctx* h) {
   p.kv_heads = h->cfg.kv_heads;
   p.budget = h->cfg.budget;
   p.occ = h->occupancy;
-  p.tpu = (h->occupancy + he::kTile - 1) / he::kTile;
+  p.tile = h->kern.tile;
+  p.tpu = (h->occupancy + p.tile - 1) / p.tile;
   p.total_tiles = h->U * p.tpu;
   p.bits = h->cfg.bits;
   p.code_stride = h->code_stride;
@@ -159,7 +247,7 @@ StepParams base_params(const he_ctx* h) {
 int launch_codes(he_ctx* h, const void* x, int64_t rows, int64_t per_unit, int64_t x_unit_rows,
                  unsigned char* out, int64_t out_unit_bytes, cudaStream_t s) {
   if (rows == 0) return HE_OK;
-  const int vb = he::kThreads / h->cfg.bits;
+  const int vb = he::kAuxThreads / h->cfg.bits;
   int64_t blocks = (rows + vb - 1) / vb;
   const int64_t cap = (int64_t)h->num_sms * 16;
   if (blocks > cap) blocks = cap;
@@ -167,7 +255,8 @@ int launch_codes(he_ctx* h, const void* x, int64_t rows, int64_t per_unit, int64
   int bits = h->cfg.bits;
   void* args[] = {(void*)&x, (void*)&rows, (void*)&per_unit, (void*)&x_unit_rows, (void*)&W,
                   (void*)&bits, (void*)&out, (void*)&out_unit_bytes};
-  HE_TRY(h, cudaLaunchKernel(h->kern.code, dim3((unsigned)blocks), dim3(he::kThreads), args, 0, s));
+  HE_TRY(h, cudaLaunchKernel(h->kern.code, dim3((unsigned)blocks), dim3(he::kAuxThreads), args, 0,
+                             s));
   return HE_OK;
 }
 
@@ -199,7 +288,8 @@ int he_create(const he_cfg* cfg, he_handle* out) {
   Kernels kern;
   if (!pick_kernels(c.dtype, c.head_dim, G, &kern)) return HE_EINVAL;
   const int64_t U = (int64_t)c.batch * c.kv_heads;
-  if (U * ((c.budget + he::kTile - 1) / he::kTile) > INT32_MAX) return HE_EINVAL;
+  if (U * ((c.budget + kern.tile - 1) / kern.tile) > INT32_MAX) return HE_EINVAL;
+  if (U * c.budget >= ((int64_t)1 << 31)) return HE_EINVAL;  // TMA row coordinate
 
   he_ctx* h = new (std::nothrow) he_ctx();
   if (!h) return HE_ENOMEM;
@@ -221,11 +311,19 @@ int he_create(const he_cfg* cfg, he_handle* out) {
         cudaSuccess) { rc = HE_ECUDA; break; }
     if (cudaFuncSetAttribute(kern.step, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kern.step_smem) != cudaSuccess) { rc = HE_ECUDA; break; }
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&h->ctas_per_sm, kern.step, he::kThreads,
-                                                      kern.step_smem) != cudaSuccess ||
+    if (kern.pipeline &&
+        (cudaFuncSetAttribute(kern.prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kern.prep_smem) != cudaSuccess ||
+         cudaFuncSetAttribute(kern.merge, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              96 * 1024) != cudaSuccess)) { rc = HE_ECUDA; break; }
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&h->ctas_per_sm, kern.step,
+                                                      kern.step_threads, kern.step_smem) !=
+            cudaSuccess ||
         h->ctas_per_sm < 1) { rc = HE_ECUDA; break; }
     h->max_ctas = h->num_sms * h->ctas_per_sm;
-    const size_t cache = (size_t)U * c.budget * c.head_dim * h->eb;
+    // one spare tile of rows after the last unit keeps every tile load in bounds;
+    // the cache starts zeroed so rows no token has written are finite
+    const size_t cache = ((size_t)U * c.budget + kern.tile) * c.head_dim * h->eb;
     const size_t nrec = (size_t)h->max_ctas + (size_t)U;
     struct { void** p; size_t bytes; } allocs[] = {
         {&h->K, cache},
@@ -236,6 +334,7 @@ int he_create(const he_cfg* cfg, he_handle* out) {
         {(void**)&h->counters, (size_t)U * sizeof(int32_t)},
         {(void**)&h->err, sizeof(int32_t)},
         {(void**)&h->partials, nrec * kern.rec_floats * sizeof(float)},
+        {(void**)&h->uo, (size_t)U * sizeof(he::UnitOut)},
     };
     for (auto& a : allocs) {
       if (cudaMalloc(a.p, a.bytes) != cudaSuccess) {
@@ -245,10 +344,18 @@ int he_create(const he_cfg* cfg, he_handle* out) {
       }
     }
     if (rc != HE_OK) break;
-    if (cudaMemset(h->codes, 0, (size_t)U * h->code_stride) != cudaSuccess ||
+    if (cudaMemset(h->K, 0, cache) != cudaSuccess || cudaMemset(h->V, 0, cache) != cudaSuccess ||
+        cudaMemset(h->codes, 0, (size_t)U * h->code_stride) != cudaSuccess ||
         cudaMemset(h->counters, 0, (size_t)U * sizeof(int32_t)) != cudaSuccess ||
+        cudaMemset(h->uo, 0, (size_t)U * sizeof(he::UnitOut)) != cudaSuccess ||
         cudaMemset(h->err, 0, sizeof(int32_t)) != cudaSuccess ||
         cudaMemset(h->evicted, 0xFF, (size_t)U * sizeof(int32_t)) != cudaSuccess) {
+      rc = HE_ECUDA;
+      break;
+    }
+    const uint64_t rows = (uint64_t)U * c.budget + kern.tile;
+    if (kern.pipeline && (!encode_cache_map(&h->tmK, h->K, rows, c.head_dim, kern.tile) ||
+                     !encode_cache_map(&h->tmV, h->V, rows, c.head_dim, kern.tile))) {
       rc = HE_ECUDA;
       break;
     }
@@ -298,6 +405,7 @@ int he_fill(he_handle h, const void* K, const void* V, int32_t n, void* stream) 
     if (rc != HE_OK) return rc;
   }
   HE_TRY(h, cudaMemsetAsync(h->counters, 0, (size_t)h->U * sizeof(int32_t), s));
+  if (h->uo) HE_TRY(h, cudaMemsetAsync(h->uo, 0, (size_t)h->U * sizeof(he::UnitOut), s));
   h->occupancy = n;
   h->filled = true;
   return HE_OK;
@@ -315,11 +423,35 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
   p.k = k;
   p.v = v;
   p.out = out;
-  const int grid = p.total_tiles == 0 ? h->U
-                                      : (p.total_tiles < h->max_ctas ? p.total_tiles : h->max_ctas);
-  void* args[] = {(void*)&p};
-  HE_TRY(h, cudaLaunchKernel(h->kern.step, dim3(grid), dim3(he::kThreads), args,
-                             (size_t)h->kern.step_smem, (cudaStream_t)stream));
+  cudaStream_t s = (cudaStream_t)stream;
+  const int stream_ctas = p.total_tiles == 0
+                              ? 0
+                              : (p.total_tiles < h->max_ctas ? p.total_tiles : h->max_ctas);
+  if (!h->kern.pipeline) {
+    const int grid = stream_ctas == 0 ? h->U : stream_ctas;
+    void* args[] = {(void*)&p};
+    HE_TRY(h, cudaLaunchKernel(h->kern.step, dim3(grid), dim3(h->kern.step_threads), args,
+                               (size_t)h->kern.step_smem, s));
+  } else {
+    const bool full = p.append_slot < 0;
+    int splits = full ? (p.occ + he::kPrepChunk - 1) / he::kPrepChunk : 1;
+    if (splits < 1) splits = 1;
+    he::UnitOut* uo = h->uo;
+    void* pa[] = {(void*)&p, (void*)&uo, (void*)&splits};
+    HE_TRY(h, launch_pdl(h->kern.prep, dim3(h->U * splits), dim3(he::kPrepThreads),
+                         (size_t)h->kern.prep_smem, s, pa));
+    if (stream_ctas > 0) {
+      const he::UnitOut* cuo = h->uo;
+      void* sa[] = {(void*)&p, (void*)&cuo, (void*)&h->tmK, (void*)&h->tmV};
+      HE_TRY(h, launch_pdl(h->kern.step, dim3(stream_ctas), dim3(h->kern.step_threads),
+                           (size_t)h->kern.step_smem, s, sa));
+    }
+    int sc = stream_ctas;
+    void* ma[] = {(void*)&p, (void*)&uo, (void*)&sc};
+    const size_t msmem = (size_t)h->kern.merge_smem_base +
+                         (size_t)(stream_ctas > 0 ? stream_ctas : 1) * h->kern.merge_smem_per_contrib;
+    HE_TRY(h, launch_pdl(h->kern.merge, dim3(h->U), dim3(he::kMergeThreads), msmem, s, ma));
+  }
   if (h->occupancy < h->cfg.budget) h->occupancy += 1;
   return HE_OK;
 }
@@ -415,7 +547,7 @@ int he_scores(he_handle h, const void* q, int32_t* dist, void* stream) {
   StepParams p = base_params(h);
   p.q = q;
   void* args[] = {(void*)&p, (void*)&dist};
-  HE_TRY(h, cudaLaunchKernel(h->kern.score, dim3(h->U), dim3(he::kThreads), args, 0,
+  HE_TRY(h, cudaLaunchKernel(h->kern.score, dim3(h->U), dim3(he::kAuxThreads), args, 0,
                              (cudaStream_t)stream));
   return HE_OK;
 }
@@ -442,12 +574,12 @@ int he_step_bytes(he_handle h, uint64_t* bytes) {
 int he_launch_info(he_handle h, int32_t* ctas, int32_t* ctas_per_sm, int32_t* tiles,
                    int32_t* stages) {
   if (!h) return HE_EINVAL;
-  const int tpu = (h->occupancy + he::kTile - 1) / he::kTile;
+  const int tpu = (h->occupancy + h->kern.tile - 1) / h->kern.tile;
   const int T = h->U * tpu;
   if (ctas) *ctas = T == 0 ? h->U : (T < h->max_ctas ? T : h->max_ctas);
   if (ctas_per_sm) *ctas_per_sm = h->ctas_per_sm;
   if (tiles) *tiles = T;
-  if (stages) *stages = kStages;
+  if (stages) *stages = h->kern.pipeline ? kStreamStages : kSimtStages;
   return HE_OK;
 }
 

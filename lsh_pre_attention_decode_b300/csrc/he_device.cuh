@@ -152,4 +152,46 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// ---------------------------------------------------------------------------
+// Phase timer (diagnostic builds with -DHE_TIMELINE only; compiled out
+// otherwise): thread 0 of a step CTA accumulates nanoseconds per phase in the
+// CTA's shared block and, at exit, writes [start, end, phase 0..21] to
+// g_he_timeline[cta * 24 ..].
+// ---------------------------------------------------------------------------
+#ifdef HE_TIMELINE
+static __device__ int64_t* g_he_timeline = nullptr;
+struct PhaseTimer {
+  int64_t acc[22];
+  int64_t last;
+  int64_t start;
+};
+#define HE_TL_FIELDS he::PhaseTimer tl;
+#define HE_TL_INIT(m)                                 \
+  if (tid == 0) {                                     \
+    for (int k_ = 0; k_ < 22; ++k_) (m).tl.acc[k_] = 0; \
+    (m).tl.start = (m).tl.last = (int64_t)he::global_ns(); \
+  }
+#define HE_TL_MARK(m, k)                              \
+  if (tid == 0) {                                     \
+    const int64_t n_ = (int64_t)he::global_ns();      \
+    (m).tl.acc[k] += n_ - (m).tl.last;                \
+    (m).tl.last = n_;                                 \
+  }
+#define HE_TL_COUNT(m, k, inc) \
+  if (tid == 0) (m).tl.acc[k] += (inc);
+#define HE_TL_DONE(m)                                                  \
+  if (tid == 0 && he::g_he_timeline) {                                 \
+    int64_t* o_ = he::g_he_timeline + (size_t)blockIdx.x * 24;         \
+    o_[0] = (m).tl.start;                                              \
+    o_[1] = (int64_t)he::global_ns();                                  \
+    for (int k_ = 0; k_ < 22; ++k_) o_[2 + k_] = (m).tl.acc[k_];       \
+  }
+#else
+#define HE_TL_FIELDS
+#define HE_TL_INIT(m)
+#define HE_TL_MARK(m, k)
+#define HE_TL_COUNT(m, k, inc)
+#define HE_TL_DONE(m)
+#endif
+
 }  // namespace he
