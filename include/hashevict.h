@@ -138,6 +138,12 @@ int he_step_bytes(he_handle h, uint64_t* bytes);
 int he_launch_info(he_handle h, int32_t* ctas, int32_t* ctas_per_sm, int32_t* tiles,
                    int32_t* stages);
 
+/* Number of times, since he_fill, that the attention partial holding the
+ * evicted slot was recomputed exactly instead of having the slot's weight
+ * subtracted (the slot carried more than half of that partial's softmax mass).
+ * Always 0 for fp32 handles.  Synchronises. */
+int he_recompute_count(he_handle h, int64_t* total);
+
 /* Human-readable name of a return code. */
 const char* he_strerror(int code);
 

@@ -56,11 +56,12 @@ def lib() -> ctypes.CDLL:
         L.he_occupancy.argtypes = [_vp, P(_i32)]
         L.he_step_bytes.argtypes = [_vp, P(ctypes.c_uint64)]
         L.he_launch_info.argtypes = [_vp, P(_i32), P(_i32), P(_i32), P(_i32)]
+        L.he_recompute_count.argtypes = [_vp, P(ctypes.c_int64)]
         L.he_strerror.argtypes = [ctypes.c_int]
         L.he_strerror.restype = ctypes.c_char_p
         for n in ("he_create", "he_fill", "he_step", "he_step_host", "he_destroy",
                   "he_last_evicted", "he_read_state", "he_get_projection", "he_codes", "he_scores",
-                  "he_occupancy", "he_step_bytes", "he_launch_info"):
+                  "he_occupancy", "he_step_bytes", "he_launch_info", "he_recompute_count"):
             getattr(L, n).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -151,6 +152,12 @@ def he_step_bytes(h: int) -> int:
     b = ctypes.c_uint64()
     _check("he_step_bytes", lib().he_step_bytes(h, ctypes.byref(b)))
     return b.value
+
+
+def he_recompute_count(h: int) -> int:
+    t = ctypes.c_int64()
+    _check("he_recompute_count", lib().he_recompute_count(h, ctypes.byref(t)))
+    return t.value
 
 
 def he_launch_info(h: int) -> dict:
@@ -244,3 +251,7 @@ class HashEvict:
 
     def launch_info(self) -> dict:
         return he_launch_info(self.h)
+
+    @property
+    def recompute_count(self) -> int:
+        return he_recompute_count(self.h)

@@ -23,23 +23,22 @@ using he::StepParams;
 
 // Launch configuration of the two step engines.
 constexpr int kSimtStages = 4;    // CUDA-core engine (fp32 caches): 32-slot tiles
-constexpr int kStreamStages = 3;  // tensor-core pipeline (bf16 caches): 64-slot tiles
+constexpr int kTcStages = 2;      // tensor-core pipeline (bf16 caches): 64-slot tiles
 constexpr bool kPSplit = true;    // attention weights as bf16 hi + lo parts
 
 struct Kernels {
   const void* step;    // fp32: the fused step; bf16: the stream kernel
-  const void* prep;    // bf16 pipeline only
-  const void* merge;   // bf16 pipeline only
+  const void* prep;    // bf16 pipeline
+  const void* merge;   // bf16 pipeline
   const void* score;
   const void* code;
   int step_smem;
   int step_threads;
   int prep_smem;
-  int merge_smem_per_contrib;
-  int merge_smem_base;
+  int merge_smem;
   int tile;
   int rec_floats;
-  bool pipeline;
+  bool tc;  // tensor-core pipeline (tensor maps, programmatic dependent launch)
 };
 
 template <typename T, int D, int G>
@@ -48,18 +47,17 @@ Kernels kernels_for() {
   k.score = reinterpret_cast<const void*>(&he::score_kernel<T, D, G>);
   k.code = reinterpret_cast<const void*>(&he::code_kernel<T, D>);
   if constexpr (std::is_same<T, bf16_t>::value) {
-    using S = he::StreamShape<D, G, kStreamStages>;
-    k.step = reinterpret_cast<const void*>(&he::stream_kernel<D, G, kStreamStages, kPSplit>);
+    using S = he::StreamShape<D, G, kTcStages>;
+    k.step = reinterpret_cast<const void*>(&he::stream_kernel<D, G, kTcStages, kPSplit>);
     k.prep = reinterpret_cast<const void*>(&he::prep_kernel<D, G>);
     k.merge = reinterpret_cast<const void*>(&he::merge_kernel<D, G>);
     k.step_smem = S::SMEM_ALLOC;
     k.step_threads = S::NT;
     k.prep_smem = he::PrepShape<D, G>::SMEM;
-    k.merge_smem_base = he::merge_smem<D, G>(0);
-    k.merge_smem_per_contrib = 2 * G * 4;
+    k.merge_smem = he::merge_smem_bytes<D, G>();
     k.tile = S::TS;
     k.rec_floats = he::PRec<G, D>::FLOATS;
-    k.pipeline = true;
+    k.tc = true;
   } else {
     using S = he::SimtShape<T, D, G, kSimtStages>;
     k.step = reinterpret_cast<const void*>(&he::step_kernel_simt<T, D, G, kSimtStages>);
@@ -67,7 +65,7 @@ Kernels kernels_for() {
     k.step_threads = he::kThreads;
     k.tile = he::kTile;
     k.rec_floats = he::Record<G, D>::FLOATS;
-    k.pipeline = false;
+    k.tc = false;
   }
   return k;
 }
@@ -311,11 +309,23 @@ int he_create(const he_cfg* cfg, he_handle* out) {
         cudaSuccess) { rc = HE_ECUDA; break; }
     if (cudaFuncSetAttribute(kern.step, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kern.step_smem) != cudaSuccess) { rc = HE_ECUDA; break; }
-    if (kern.pipeline &&
+    // the three kernels of the bf16 pipeline run side by side on an SM: give
+    // them one L1/shared split so that none waits for the SM to reconfigure
+    if (kern.tc &&
         (cudaFuncSetAttribute(kern.prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kern.prep_smem) != cudaSuccess ||
          cudaFuncSetAttribute(kern.merge, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              96 * 1024) != cudaSuccess)) { rc = HE_ECUDA; break; }
+                              kern.merge_smem) != cudaSuccess ||
+         cudaFuncSetAttribute(kern.step, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+         cudaFuncSetAttribute(kern.prep, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+         cudaFuncSetAttribute(kern.merge, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)) {
+      rc = HE_ECUDA;
+      break;
+    }
+
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&h->ctas_per_sm, kern.step,
                                                       kern.step_threads, kern.step_smem) !=
             cudaSuccess ||
@@ -354,7 +364,7 @@ int he_create(const he_cfg* cfg, he_handle* out) {
       break;
     }
     const uint64_t rows = (uint64_t)U * c.budget + kern.tile;
-    if (kern.pipeline && (!encode_cache_map(&h->tmK, h->K, rows, c.head_dim, kern.tile) ||
+    if (kern.tc && (!encode_cache_map(&h->tmK, h->K, rows, c.head_dim, kern.tile) ||
                      !encode_cache_map(&h->tmV, h->V, rows, c.head_dim, kern.tile))) {
       rc = HE_ECUDA;
       break;
@@ -427,7 +437,7 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
   const int stream_ctas = p.total_tiles == 0
                               ? 0
                               : (p.total_tiles < h->max_ctas ? p.total_tiles : h->max_ctas);
-  if (!h->kern.pipeline) {
+  if (!h->kern.tc) {
     const int grid = stream_ctas == 0 ? h->U : stream_ctas;
     void* args[] = {(void*)&p};
     HE_TRY(h, cudaLaunchKernel(h->kern.step, dim3(grid), dim3(h->kern.step_threads), args,
@@ -437,20 +447,20 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
     int splits = full ? (p.occ + he::kPrepChunk - 1) / he::kPrepChunk : 1;
     if (splits < 1) splits = 1;
     he::UnitOut* uo = h->uo;
-    void* pa[] = {(void*)&p, (void*)&uo, (void*)&splits};
-    HE_TRY(h, launch_pdl(h->kern.prep, dim3(h->U * splits), dim3(he::kPrepThreads),
-                         (size_t)h->kern.prep_smem, s, pa));
     if (stream_ctas > 0) {
-      const he::UnitOut* cuo = h->uo;
-      void* sa[] = {(void*)&p, (void*)&cuo, (void*)&h->tmK, (void*)&h->tmV};
+      void* sa[] = {(void*)&p, (void*)&h->tmK, (void*)&h->tmV};
       HE_TRY(h, launch_pdl(h->kern.step, dim3(stream_ctas), dim3(h->kern.step_threads),
                            (size_t)h->kern.step_smem, s, sa));
     }
+    int first_of_step = stream_ctas > 0 ? 0 : 1;
+    void* pa[] = {(void*)&p, (void*)&uo, (void*)&splits, (void*)&first_of_step};
+    const int prep_ctas = h->U * splits < h->num_sms ? h->U * splits : h->num_sms;
+    HE_TRY(h, launch_pdl(h->kern.prep, dim3(prep_ctas), dim3(he::kPrepThreads),
+                         (size_t)h->kern.prep_smem, s, pa));
     int sc = stream_ctas;
     void* ma[] = {(void*)&p, (void*)&uo, (void*)&sc};
-    const size_t msmem = (size_t)h->kern.merge_smem_base +
-                         (size_t)(stream_ctas > 0 ? stream_ctas : 1) * h->kern.merge_smem_per_contrib;
-    HE_TRY(h, launch_pdl(h->kern.merge, dim3(h->U), dim3(he::kMergeThreads), msmem, s, ma));
+    HE_TRY(h, launch_pdl(h->kern.merge, dim3(h->U), dim3(he::kMergeThreads),
+                         (size_t)h->kern.merge_smem, s, ma));
   }
   if (h->occupancy < h->cfg.budget) h->occupancy += 1;
   return HE_OK;
@@ -552,6 +562,23 @@ int he_scores(he_handle h, const void* q, int32_t* dist, void* stream) {
   return HE_OK;
 }
 
+int he_recompute_count(he_handle h, int64_t* total) {
+  if (!h || !total) return HE_EINVAL;
+  DeviceGuard g(h->device);
+  *total = 0;
+  if (!h->kern.tc) return HE_OK;
+  HE_TRY(h, cudaDeviceSynchronize());
+  int32_t* host = new (std::nothrow) int32_t[h->U];
+  if (!host) return HE_ENOMEM;
+  const cudaError_t e = cudaMemcpy(host, h->counters, (size_t)h->U * sizeof(int32_t),
+                                   cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess)
+    for (int i = 0; i < h->U; ++i) *total += host[i];
+  delete[] host;
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  return HE_OK;
+}
+
 int he_occupancy(he_handle h, int32_t* occupancy) {
   if (!h || !occupancy) return HE_EINVAL;
   *occupancy = h->occupancy;
@@ -579,7 +606,7 @@ int he_launch_info(he_handle h, int32_t* ctas, int32_t* ctas_per_sm, int32_t* ti
   if (ctas) *ctas = T == 0 ? h->U : (T < h->max_ctas ? T : h->max_ctas);
   if (ctas_per_sm) *ctas_per_sm = h->ctas_per_sm;
   if (tiles) *tiles = T;
-  if (stages) *stages = h->kern.pipeline ? kStreamStages : kSimtStages;
+  if (stages) *stages = h->kern.tc ? kTcStages : kSimtStages;
   return HE_OK;
 }
 

@@ -186,12 +186,18 @@ struct PhaseTimer {
     o_[1] = (int64_t)he::global_ns();                                  \
     for (int k_ = 0; k_ < 22; ++k_) o_[2 + k_] = (m).tl.acc[k_];       \
   }
+// Stamps: thread 0 of a CTA writes the time at a numbered point of a kernel
+// (region r: prep 0, stream 1, merge 2) to g_he_timeline[(r*65536 + cta)*8 + k].
+#define HE_STAMP(r, k)                                                              \
+  if (threadIdx.x == 0 && he::g_he_timeline)                                       \
+    he::g_he_timeline[((size_t)(r) * 65536 + blockIdx.x) * 8 + (k)] = (int64_t)he::global_ns();
 #else
 #define HE_TL_FIELDS
 #define HE_TL_INIT(m)
 #define HE_TL_MARK(m, k)
 #define HE_TL_COUNT(m, k, inc)
 #define HE_TL_DONE(m)
+#define HE_STAMP(r, k)
 #endif
 
 }  // namespace he

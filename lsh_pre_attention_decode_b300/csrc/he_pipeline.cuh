@@ -1,6 +1,7 @@
 // he_pipeline.cuh — the bf16 HashEvict decode step as three kernels chained by
-// programmatic dependent launch (PDL), so that no latency-bound work runs
-// inside the kernel that streams the cache at HBM bandwidth.
+// programmatic dependent launch (PDL).  The eviction decision is off the
+// critical path: it is computed concurrently with the attention, and the
+// evicted slot is taken out of the attention afterwards.
 //
 //   prep   (one CTA per unit and code chunk)  method steps 1-4: project the G
 //          query heads and the new key onto W and binarise (the fixed-order
@@ -8,80 +9,46 @@
 //          logits, scan a chunk of the unit's packed codes (XOR + popcount,
 //          group-summed) and fold the chunk's best (distance, slot) into the
 //          unit's eviction key with an order-independent atomicMax.
-//   stream (stream-K over 64-slot tiles, one producer + four consumer warps)
-//          the decode attention over the resident slots except the evicted
-//          one: 2-D tensor TMA into a 3-stage ring, logits and value
+//   stream (stream-K over 64-slot tiles, one producer + four consumer warps;
+//          runs while prep runs) the decode attention over every resident
+//          slot: 2-D tensor TMA into an NS-stage ring, logits and value
 //          accumulation on the tensor cores (mma.sync m16n8k16 bf16), online
 //          softmax in fp32; one partial (max, sum, accumulator) per CTA and unit.
-//   merge  (one CTA per unit) log-sum-exp merge of the unit's partials plus the
-//          new token, the output, and method step 5: the new token's key,
+//   merge  (one CTA per unit) removes the evicted slot from the one partial that
+//          contains it, log-sum-exp merges the partials, adds the new token,
+//          writes the output, and does method step 5: the new token's key,
 //          value and code overwrite the evicted slot.
 //
-// The arithmetic is the specification's "score, evict, overwrite, attend":
-// the evicted slot never enters the softmax and the new token always does.
-// PDL ordering: prep waits for the previous step to finish, then lets stream
-// launch; stream may prefetch K/V and read q before its own wait (everything
-// it reads was final before prep's wait returned) and reads the eviction keys
-// only after it; merge waits for stream (hence for prep) before reading.
+// Removal: with p the evicted slot's weight in its partial (same max), the
+// partial becomes (l - p, A - p V).  When p <= l / 2 the subtraction loses at
+// most one bit of the partial's sum; otherwise merge recomputes that partial
+// from the cache without the slot (CUDA cores) — so the result is the
+// specification's "score, evict, overwrite, attend" to fp32 accuracy either way.
+//
+// Launch order and PDL: stream, prep, merge.  stream waits for the previous
+// step, then lets prep launch (prep's CTAs take the room stream's CTAs leave on
+// each SM, so they never delay the stream); prep reads a final cache without
+// waiting and waits for stream at its very end (it cannot complete before
+// stream has); merge waits for prep, hence for both.
 #pragma once
 
 #include <cuda.h>
 #include <cuda_bf16.h>
 
 #include "he_common.cuh"
+#include "he_tc.cuh"
 
 namespace he {
 
-// ---------------------------------------------------------------------------
-// PTX wrappers
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() {
-  asm volatile("griddepcontrol.launch_dependents;" :::);
-}
-
-// 2-D tensor TMA load (global -> shared), completion on an mbarrier.  x is the
-// innermost (element) coordinate: a multiple of 64 here, so 16-byte aligned.
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-// D = A . B + D, A 16x16 bf16 (row), B 16x8 bf16 (col), D 16x8 fp32.
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                               uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
-      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Per-unit results of prep, read by stream and merge.
+// Per-unit results of prep, read by merge.
 struct UnitOut {
   unsigned long long key;  // eviction key (distance << 32 | ~slot); 0 between steps
   unsigned long long codek;
   float lnew[8];           // the new token's base-2 logits, per query head
+  float lstar[8];          // the evicted slot's base-2 logits, per query head
+  int32_t arrived;         // prep CTAs of the unit done (reset by the last one)
+  int32_t pad[3];
+  uint16_t vstar[128];     // the evicted slot's value row (bf16)
 };
 
 // Partial record of one (stream CTA, unit): [m G][l G] padded to 4, acc [G][D].
@@ -94,7 +61,7 @@ struct PRec {
 // ---------------------------------------------------------------------------
 // prep
 // ---------------------------------------------------------------------------
-constexpr int kPrepThreads = 256;
+constexpr int kPrepThreads = 128;  // one warp per SM sub-partition: fits beside two stream CTAs
 constexpr int kPrepChunk = 4096;  // code slots scanned per CTA
 
 template <int D, int G>
@@ -104,13 +71,16 @@ struct PrepShape {
   static constexpr int OFF_C = OFF_X + ((G + 1) * D * 2 + 15) / 16 * 16;  // code chunk
   static constexpr int OFF_BITS = OFF_C + kPrepChunk * 8;
   static constexpr int OFF_RED = OFF_BITS + ((G + 1) * 64 / 32) * 4;
-  static constexpr int OFF_BAR = (OFF_RED + 8 * 8 + 15) / 16 * 16;
+  static constexpr int OFF_BAR = (OFF_RED + 8 * 8 + 16 + 15) / 16 * 16;
   static constexpr int SMEM = OFF_BAR + 16;
 };
 
+// One CTA per SM at most: a CTA takes the (unit, code chunk) items
+// blockIdx.x, blockIdx.x + gridDim.x, ... in turn, so that prep never crowds
+// the stream kernel's CTAs off an SM.
 template <int D, int G>
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, UnitOut* uo,
-                                                            int splits) {
+                                                            int splits, int first_of_step) {
   using S = PrepShape<D, G>;
   extern __shared__ __align__(16) unsigned char smem_prep[];
   unsigned char* smem = smem_prep;
@@ -119,104 +89,147 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
   const unsigned char* cs = smem + S::OFF_C;
   uint32_t* sbits = reinterpret_cast<uint32_t*>(smem + S::OFF_BITS);
   uint64_t* red = reinterpret_cast<uint64_t*>(smem + S::OFF_RED);
+  int* last = reinterpret_cast<int*>(red + kPrepThreads / 32);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + S::OFF_BAR);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int u = blockIdx.x / splits, split = blockIdx.x - u * splits;
   const int bits = p.bits, wb = bits >> 3;
   const bool full = p.append_slot < 0;
-  const int s0 = split * kPrepChunk;
-  const int s1 = full ? min(s0 + kPrepChunk, p.occ) : s0;
+  const int nitems = p.U * splits;
 
-  pdl_wait();     // the previous step is complete: codes, cache and W are final
-  pdl_trigger();  // stream may launch and prefetch the cache
+  HE_STAMP(0, 0);
+  // launched behind stream, which waited for the previous step before letting
+  // prep launch: codes, cache and W are final.  With an empty cache there is no
+  // stream kernel and prep waits for the previous step itself.
+  if (first_of_step) pdl_wait();
+  pdl_trigger();  // merge may launch; it waits for this grid before reading
+  HE_STAMP(0, 1);
 
   if (tid == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
-    const int b = u / p.kv_heads, j = u - b * p.kv_heads;
-    const uint32_t wbytes = (uint32_t)(D * bits * 2), qbytes = (uint32_t)(G * D * 2),
-                   kbytes = (uint32_t)(D * 2);
-    const uint32_t cbytes = s1 > s0 ? (uint32_t)(((s1 - s0) * wb + 15) & ~15) : 0u;
-    mbar_arrive_expect_tx(bar, wbytes + qbytes + kbytes + cbytes);
-    bulk_g2s(smem + S::OFF_W, p.W, wbytes, bar);
-    bulk_g2s(smem + S::OFF_X,
-             reinterpret_cast<const uint16_t*>(p.q) + (size_t)(b * p.kv_heads + j) * G * D, qbytes,
-             bar);
-    bulk_g2s(smem + S::OFF_X + qbytes, reinterpret_cast<const uint16_t*>(p.k) + (size_t)u * D,
-             kbytes, bar);
-    if (cbytes)
-      bulk_g2s(smem + S::OFF_C, p.codes + (size_t)u * p.code_stride + (size_t)s0 * wb, cbytes,
-               bar);
   }
   __syncthreads();
-  if (!__syncthreads_and(mbar_wait_bounded(bar, 0u))) {
-    // gave up: record it and leave once the copies have landed
+
+  uint32_t phase = 0;
+  for (int it = blockIdx.x; it < nitems; it += gridDim.x, phase ^= 1u) {
+    const int u = it / splits, split = it - u * splits;
+    const int s0 = split * kPrepChunk;
+    const int s1 = full ? min(s0 + kPrepChunk, p.occ) : s0;
     if (tid == 0) {
-      atomicExch(p.err, 1);
-      (void)mbar_wait_bounded(bar, 0u, 500000000ull);
+      const int b = u / p.kv_heads, j = u - b * p.kv_heads;
+      const uint32_t wbytes = it == (int)blockIdx.x ? (uint32_t)(D * bits * 2) : 0u;
+      const uint32_t qbytes = (uint32_t)(G * D * 2), kbytes = (uint32_t)(D * 2);
+      const uint32_t cbytes = s1 > s0 ? (uint32_t)(((s1 - s0) * wb + 15) & ~15) : 0u;
+      mbar_arrive_expect_tx(bar, wbytes + qbytes + kbytes + cbytes);
+      if (wbytes) bulk_g2s(smem + S::OFF_W, p.W, wbytes, bar);
+      bulk_g2s(smem + S::OFF_X,
+               reinterpret_cast<const uint16_t*>(p.q) + (size_t)(b * p.kv_heads + j) * G * D,
+               qbytes, bar);
+      bulk_g2s(smem + S::OFF_X + qbytes, reinterpret_cast<const uint16_t*>(p.k) + (size_t)u * D,
+               kbytes, bar);
+      if (cbytes)
+        bulk_g2s(smem + S::OFF_C, p.codes + (size_t)u * p.code_stride + (size_t)s0 * wb, cbytes,
+                 bar);
     }
-    return;
-  }
+    if (!__syncthreads_and(mbar_wait_bounded(bar, phase))) {
+      // gave up: record it and leave once the copies have landed
+      if (tid == 0) {
+        atomicExch(p.err, 1);
+        (void)mbar_wait_bounded(bar, phase, 500000000ull);
+      }
+      return;
+    }
+    HE_STAMP(0, 2);
 
-  // method steps 1-2: bit j of vector v (v < G: query head, v == G: the key) is
-  // the sign of the fp32 fused multiply-add chain over d = 0..D-1 from +0
-  const int ntask = (G + 1) * bits;
-  for (int t0 = warp * 32; t0 < ntask; t0 += kPrepThreads) {
-    const int t = t0 + lane;
-    const int v = t < ntask ? t / bits : G, jj = t - (t / bits) * bits;
-    uint32_t bit = 0;
-    if (t < ntask && (full || v == G)) {
-      const uint16_t* x = xs + v * D;
-      float acc = 0.0f;
+    // method steps 1-2: bit j of vector v (v < G: query head, v == G: the key)
+    // is the sign of the fp32 fused multiply-add chain over d = 0..D-1 from +0
+    const int ntask = (G + 1) * bits;
+    for (int t0 = warp * 32; t0 < ntask; t0 += kPrepThreads) {
+      const int t = t0 + lane;
+      const int v = t < ntask ? t / bits : G, jj = t - (t / bits) * bits;
+      uint32_t bit = 0;
+      if (t < ntask && (full || v == G)) {
+        const uint16_t* x = xs + v * D;
+        float acc = 0.0f;
 #pragma unroll 16
-      for (int d = 0; d < D; ++d)
-        acc = __fmaf_rn(__uint_as_float((uint32_t)x[d] << 16),
-                        __uint_as_float((uint32_t)Ws[d * bits + jj] << 16), acc);
-      bit = acc > 0.0f ? 1u : 0u;
+        for (int d = 0; d < D; ++d)
+          acc = __fmaf_rn(__uint_as_float((uint32_t)x[d] << 16),
+                          __uint_as_float((uint32_t)Ws[d * bits + jj] << 16), acc);
+        bit = acc > 0.0f ? 1u : 0u;
+      }
+      const uint32_t word = __ballot_sync(kFull, bit);
+      if (lane == 0) sbits[t0 >> 5] = word;
     }
-    const uint32_t word = __ballot_sync(kFull, bit);
-    if (lane == 0) sbits[t0 >> 5] = word;
-  }
-  // the new token's logits (only the first chunk's CTA publishes them)
-  if (split == 0) {
-    for (int g = warp; g < G; g += kPrepThreads / 32) {
-      float a = 0.0f;
-      for (int d = lane; d < D; d += 32)
-        a = fmaf(__uint_as_float((uint32_t)xs[g * D + d] << 16),
-                 __uint_as_float((uint32_t)xs[G * D + d] << 16), a);
-      a = warp_sum(a);
-      if (lane == 0) uo[u].lnew[g] = a * p.qscale;
+    // the new token's logits (only the unit's first chunk publishes them)
+    if (split == 0) {
+      for (int g = warp; g < G; g += kPrepThreads / 32) {
+        float a = 0.0f;
+        for (int d = lane; d < D; d += 32)
+          a = fmaf(__uint_as_float((uint32_t)xs[g * D + d] << 16),
+                   __uint_as_float((uint32_t)xs[G * D + d] << 16), a);
+        a = warp_sum(a);
+        if (lane == 0) uo[u].lnew[g] = a * p.qscale;
+      }
     }
-  }
-  __syncthreads();
-  if (split == 0 && tid == 0) uo[u].codek = code_from_bits(sbits, bits, G);
-  if (!full) return;
+    __syncthreads();
+    if (split == 0 && tid == 0) uo[u].codek = code_from_bits(sbits, bits, G);
 
-  // method steps 3-4 on this chunk: the largest group-summed distance, lowest slot
-  uint64_t cq[G];
+    if (full) {
+      // method steps 3-4 on this chunk: the largest group-summed distance, lowest slot
+      uint64_t cq[G];
 #pragma unroll
-  for (int g = 0; g < G; ++g) cq[g] = code_from_bits(sbits, bits, g);
-  uint64_t best = 0;
-  for (int s = s0 + tid; s < s1; s += kPrepThreads) {
-    const unsigned char* c = cs + (size_t)(s - s0) * wb;
-    uint64_t code;
-    switch (wb) {
-      case 1: code = *c; break;
-      case 2: code = *reinterpret_cast<const uint16_t*>(c); break;
-      case 4: code = *reinterpret_cast<const uint32_t*>(c); break;
-      default: code = *reinterpret_cast<const uint64_t*>(c); break;
+      for (int g = 0; g < G; ++g) cq[g] = code_from_bits(sbits, bits, g);
+      uint64_t best = 0;
+      for (int s = s0 + tid; s < s1; s += kPrepThreads) {
+        const unsigned char* c = cs + (size_t)(s - s0) * wb;
+        uint64_t code;
+        switch (wb) {
+          case 1: code = *c; break;
+          case 2: code = *reinterpret_cast<const uint16_t*>(c); break;
+          case 4: code = *reinterpret_cast<const uint32_t*>(c); break;
+          default: code = *reinterpret_cast<const uint64_t*>(c); break;
+        }
+        const uint64_t key = evict_key(group_distance<G>(cq, code), (uint32_t)s);
+        best = key > best ? key : best;
+      }
+      best = warp_max_u64(best);
+      if (lane == 0) red[warp] = best;
+      __syncthreads();
+      if (tid == 0) {
+        uint64_t b2 = 0;
+        for (int w2 = 0; w2 < kPrepThreads / 32; ++w2) b2 = red[w2] > b2 ? red[w2] : b2;
+        if (b2) atomicMax(&uo[u].key, (unsigned long long)b2);
+        __threadfence();
+        *last = atomicAdd(&uo[u].arrived, 1) == splits - 1;
+        __threadfence();
+      }
+      __syncthreads();
+      if (*last) {
+        // the unit's eviction is decided: hand merge the evicted slot's logits
+        // and value row, so that merge needs no dependent load
+        const int winner = (int)evict_key_slot(__ldcg(&uo[u].key));
+        const uint16_t* Krow =
+            reinterpret_cast<const uint16_t*>(p.K) + ((size_t)u * p.budget + winner) * D;
+        const uint16_t* Vrow =
+            reinterpret_cast<const uint16_t*>(p.V) + ((size_t)u * p.budget + winner) * D;
+        for (int g = warp; g < G; g += kPrepThreads / 32) {
+          float a = 0.0f;
+          for (int d = lane; d < D; d += 32)
+            a = fmaf(__uint_as_float((uint32_t)xs[g * D + d] << 16),
+                     __uint_as_float((uint32_t)__ldcg(Krow + d) << 16), a);
+          a = warp_sum(a);
+          if (lane == 0) uo[u].lstar[g] = a * p.qscale;
+        }
+        for (int d = tid; d < D; d += kPrepThreads) uo[u].vstar[d] = __ldcg(Vrow + d);
+        if (tid == 0) uo[u].arrived = 0;
+      }
     }
-    const uint64_t key = evict_key(group_distance<G>(cq, code), (uint32_t)s);
-    best = key > best ? key : best;
+    __syncthreads();  // the staging buffers are reused by the next item
   }
-  best = warp_max_u64(best);
-  if (lane == 0) red[warp] = best;
-  __syncthreads();
-  if (tid == 0) {
-    uint64_t b2 = 0;
-    for (int w2 = 0; w2 < kPrepThreads / 32; ++w2) b2 = red[w2] > b2 ? red[w2] : b2;
-    if (b2) atomicMax(&uo[u].key, (unsigned long long)b2);
-  }
+  HE_STAMP(0, 3);
+  // this grid completes only after stream has, so that merge's wait on this
+  // grid covers stream's partials too
+  if (tid == 0) pdl_wait();
 }
 
 // ---------------------------------------------------------------------------
@@ -250,7 +263,7 @@ struct StreamShape {
 
 template <int D, int G, int NS, bool PSPLIT>
 __global__ void __launch_bounds__(StreamShape<D, G, NS>::NT, 2)
-    stream_kernel(const StepParams p, const UnitOut* uo, const __grid_constant__ CUtensorMap tmK,
+    stream_kernel(const StepParams p, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV) {
   using S = StreamShape<D, G, NS>;
   using R = PRec<G, D>;
@@ -267,13 +280,14 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS>::NT, 2)
   uint64_t* empty_bar = full_bar + NS;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool full = p.append_slot < 0;
   const int64_t TT = p.total_tiles, NCTA = gridDim.x;
   const int tb = (int)((int64_t)blockIdx.x * TT / NCTA);
   const int te = (int)(((int64_t)blockIdx.x + 1) * TT / NCTA);
   const int ntiles = te - tb;
 
-  pdl_trigger();  // merge may launch; it waits for this grid before reading
+  HE_STAMP(1, 0);
+  pdl_wait();     // the previous step is complete: the cache is final
+  pdl_trigger();  // prep may launch now: its CTAs take the room stream leaves
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full_bar[s], 1);
@@ -323,7 +337,6 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS>::NT, 2)
 
   int i = 0;            // CTA-local tile counter
   int drain_from = -1;  // first tile this warp did not wait for (after a give-up)
-  bool waited = false;  // prep's results are visible once the grid dependency resolved
   for (int u = u_first; u <= u_last; ++u) {
     const int seg_t0 = max(tb, u * p.tpu), seg_t1 = min(te, (u + 1) * p.tpu);
     const int hi = min((seg_t1 - u * p.tpu) * S::TS, p.occ);
@@ -340,12 +353,6 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS>::NT, 2)
         for (int r = 0; r < 2; ++r)
           qb[ks][r] = g8 < G ? __ldg(qw + (g8 * D + 16 * ks + 8 * r + 2 * t4) / 2) : 0u;
     }
-    if (!waited) {
-      pdl_wait();
-      waited = true;
-    }
-    // the slot this step evicts is left out of the softmax (method step 4)
-    const int evict = full ? (int)evict_key_slot(__ldcg(&uo[u].key)) : -1;
 
     float mrun0 = -1e30f, mrun1 = -1e30f, lrun0 = 0.0f, lrun1 = 0.0f;
     float acc[S::MT][4];
@@ -381,8 +388,8 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS>::NT, 2)
       // c[0]: slot g8, head h0; c[1]: slot g8, h1; c[2]: slot g8+8, h0; c[3]: slot g8+8, h1
       float x00 = c[0] * qscale, x01 = c[1] * qscale, x10 = c[2] * qscale, x11 = c[3] * qscale;
       const int sA = slot_base + g8, sB = sA + 8;
-      if (sA >= hi || sA == evict) x00 = x01 = -INFINITY;
-      if (sB >= hi || sB == evict) x10 = x11 = -INFINITY;
+      if (sA >= hi) x00 = x01 = -INFINITY;
+      if (sB >= hi) x10 = x11 = -INFINITY;
       if (!real0) x00 = x10 = -INFINITY;
       if (!real1) x01 = x11 = -INFINITY;
 
@@ -508,143 +515,303 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS>::NT, 2)
     }
     group_sync<NC, 1>();  // the merge area is reused by the next segment
   }
+  HE_STAMP(1, 1);
 }
 
 // ---------------------------------------------------------------------------
 // merge
 // ---------------------------------------------------------------------------
 constexpr int kMergeThreads = 512;
+constexpr int kRecomputeWarps = 8;
 
-// Dynamic shared memory of merge: headers/weights of up to `max_contrib`
-// partials ([c][2G] floats) + the per-group sums [NQ][G*D/4] float4.
 template <int D, int G>
-__host__ __device__ constexpr int merge_smem(int max_contrib) {
-  return (max_contrib * 2 * G * 4 + 15) / 16 * 16 + kMergeThreads * 16 + 80;
+struct MergeShape {
+  static constexpr int GD4 = G * D / 4;           // float4 outputs per unit
+  static constexpr int NQ = kMergeThreads / GD4;  // contributor groups
+};
+
+// Exact partial over slots [lo, hi) of unit u without slot `skip` (CUDA cores,
+// fp32): per head the base-2 max, sum and accumulator -> xm, xl, xa [G][D].
+// Warps 0..kRecomputeWarps-1 each run an online softmax over a strided share
+// of the slots (lane owns D/32 elements), then merge in a fixed order.
+template <int D, int G>
+__device__ void recompute_partial(const StepParams& p, int u, int lo, int hi, int skip,
+                                  const float* qf, float* wstate, float* xm, float* xl,
+                                  float* xa, int tid) {
+  constexpr int E = D / 32;
+  const int lane = tid & 31, warp = tid >> 5;
+  if (warp < kRecomputeWarps) {
+    const uint16_t* Kc = reinterpret_cast<const uint16_t*>(p.K) + (size_t)u * p.budget * D;
+    const uint16_t* Vc = reinterpret_cast<const uint16_t*>(p.V) + (size_t)u * p.budget * D;
+    float mr[G], lr[G], ar[G][E];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      mr[g] = -1e30f;
+      lr[g] = 0.0f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) ar[g][e] = 0.0f;
+    }
+    for (int s = lo + warp; s < hi; s += kRecomputeWarps) {
+      if (s == skip) continue;
+      float kx[E], vx[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        kx[e] = __uint_as_float((uint32_t)Kc[(size_t)s * D + lane * E + e] << 16);
+        vx[e] = __uint_as_float((uint32_t)Vc[(size_t)s * D + lane * E + e] << 16);
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float dot = 0.0f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) dot = fmaf(qf[g * D + lane * E + e], kx[e], dot);
+        const float x = warp_sum(dot) * p.qscale;
+        const float mn = fmaxf(mr[g], x);
+        const float so = exp2f(mr[g] - mn), sn = exp2f(x - mn);
+        lr[g] = lr[g] * so + sn;
+#pragma unroll
+        for (int e = 0; e < E; ++e) ar[g][e] = ar[g][e] * so + sn * vx[e];
+        mr[g] = mn;
+      }
+    }
+    // warp state -> wstate [warp][G][2 + D]
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float* ws = wstate + ((size_t)warp * G + g) * (2 + D);
+      if (lane == 0) {
+        ws[0] = mr[g];
+        ws[1] = lr[g];
+      }
+#pragma unroll
+      for (int e = 0; e < E; ++e) ws[2 + lane * E + e] = ar[g][e];
+    }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < G * D; idx += kMergeThreads) {
+    const int g = idx / D, d = idx - g * D;
+    float mx = -1e30f;
+    for (int w = 0; w < kRecomputeWarps; ++w) mx = fmaxf(mx, wstate[((size_t)w * G + g) * (2 + D)]);
+    float a = 0.0f, l = 0.0f;
+    for (int w = 0; w < kRecomputeWarps; ++w) {
+      const float* ws = wstate + ((size_t)w * G + g) * (2 + D);
+      const float sc = exp2f(ws[0] - mx);
+      a += ws[2 + d] * sc;
+      l += ws[1] * sc;
+    }
+    xa[idx] = a;
+    if (d == 0) {
+      xm[g] = mx;
+      xl[g] = l;
+    }
+  }
+  __syncthreads();
+}
+
+// One CTA per unit.  Every load is issued up front (one memory round trip):
+// thread (q, o) holds the partials of contributors c = q, q + NQ, ... (four
+// outputs o each), folds them into a running (max, sum, accumulator), taking
+// the evicted slot out of its partial; the NQ group states are merged in a
+// fixed order, the new token is added, the output written and the slot
+// overwritten.  If the evicted slot carries more than half of its partial's
+// mass, that partial is recomputed exactly and the fold redone.
+constexpr int kMergeRegs = 4;  // partials held in registers per thread (more are looped)
+
+template <int D, int G>
+__device__ __forceinline__ void fold_one(float mc, float lc, float4 x, bool is_crel,
+                                         float lst, const float4& vs, float& mx, float& sum,
+                                         float4& a) {
+  if (is_crel) {  // take the evicted slot out (its weight is at most half)
+    const float pw = exp2f(lst - mc);
+    lc -= pw;
+    x.x -= pw * vs.x;
+    x.y -= pw * vs.y;
+    x.z -= pw * vs.z;
+    x.w -= pw * vs.w;
+  }
+  const float mn = fmaxf(mx, mc);
+  const float so = exp2f(mx - mn), sn = exp2f(mc - mn);
+  sum = sum * so + lc * sn;
+  a.x = a.x * so + x.x * sn;
+  a.y = a.y * so + x.y * sn;
+  a.z = a.z * so + x.z * sn;
+  a.w = a.w * so + x.w * sn;
+  mx = mn;
 }
 
 template <int D, int G>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const StepParams p, UnitOut* uo,
                                                               int stream_ctas) {
   using R = PRec<G, D>;
-  constexpr int GD4 = G * D / 4;              // float4 outputs per unit
-  constexpr int NQ = kMergeThreads / GD4;     // contributor groups
+  using M = MergeShape<D, G>;
+  constexpr int GD4 = M::GD4, NQ = M::NQ;
   static_assert(GD4 <= kMergeThreads && kMergeThreads % GD4 == 0, "merge shape");
+  static_assert(D <= 128 && D <= kMergeThreads, "evicted value row buffer");
   extern __shared__ __align__(16) unsigned char smem_merge[];
-  unsigned char* smem = smem_merge;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float4* sacc = reinterpret_cast<float4*>(smem_merge);            // [512]
+  float* smax = reinterpret_cast<float*>(sacc + kMergeThreads);     // [512]
+  float* ssum = smax + kMergeThreads;                               // [512]
+  float* qf = ssum + kMergeThreads;                                 // [G][D] query heads (fp32)
+  float* xa = qf + G * D;                                           // [G][D] recomputed partial
+  float* xm = xa + G * D;                                           // [8]
+  float* xl = xm + 8;                                               // [8]
+  int* sflag = reinterpret_cast<int*>(xl + 8);                      // [4]
+  float* wstate = reinterpret_cast<float*>(sflag + 4);              // recompute scratch
+  const int tid = threadIdx.x;
   const int u = blockIdx.x;
   const bool full = p.append_slot < 0;
 
+  HE_STAMP(2, 0);
   pdl_wait();     // stream (and so prep) is complete and visible
   pdl_trigger();  // the next step's prep may launch; it waits for this grid
+  HE_STAMP(2, 1);
 
   int first = 0, n = 0;
+  const int64_t TT = p.total_tiles, NCT = stream_ctas;
   if (p.total_tiles > 0) {
-    const int64_t TT = p.total_tiles, NC = stream_ctas;
-    first = (int)((((int64_t)u * p.tpu + 1) * NC - 1) / TT);
-    const int last = (int)((((int64_t)u * p.tpu + p.tpu) * NC - 1) / TT);
+    first = (int)((((int64_t)u * p.tpu + 1) * NCT - 1) / TT);
+    const int last = (int)((((int64_t)u * p.tpu + p.tpu) * NCT - 1) / TT);
     n = last - first + 1;
   }
-  float* wts = reinterpret_cast<float*>(smem);                  // [n][G]: m, then weight
-  float* lsum = wts + (size_t)n * G;                            // [n][G]: l
-  float4* part = reinterpret_cast<float4*>(smem + (((size_t)n * 2 * G * 4 + 15) & ~(size_t)15));
-  float* hm = reinterpret_cast<float*>(part + kMergeThreads);   // [G]
-  float* hl = hm + 8;                                           // [G]
-  int* win = reinterpret_cast<int*>(hl + 8);
   const float* recs = p.partials + (size_t)(first + u) * R::FLOATS;
-
-  for (int c = tid; c < n; c += kMergeThreads) {
-    const float* r = recs + (size_t)c * R::FLOATS;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      wts[c * G + g] = __ldcg(r + g);
-      lsum[c * G + g] = __ldcg(r + G + g);
-    }
-  }
-  __syncthreads();
-  // per-head stabiliser and denominator (fixed order: lanes then the warp tree)
-  for (int g = warp; g < G; g += kMergeThreads / 32) {
-    const float ln = __ldcg(&uo[u].lnew[g]);
-    float mx = ln;
-    for (int c = lane; c < n; c += 32) mx = fmaxf(mx, wts[c * G + g]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-    float sum = 0.0f;
-    for (int c = lane; c < n; c += 32) sum += lsum[c * G + g] * exp2f(wts[c * G + g] - mx);
-    sum = warp_sum(sum);
-    if (lane == 0) {
-      hm[g] = mx;
-      hl[g] = sum + exp2f(ln - mx);
-    }
-  }
-  if (tid == 0) {
-    const unsigned long long key = __ldcg(&uo[u].key);
-    *win = full ? (key ? (int)evict_key_slot(key) : -1) : p.append_slot;
-  }
-  __syncthreads();
-  for (int i2 = tid; i2 < n * G; i2 += kMergeThreads) {
-    const int g = i2 - (i2 / G) * G;
-    wts[i2] = exp2f(wts[i2] - hm[g]);
-  }
-  __syncthreads();
-
-  // accumulators: group q sums the contributors c = q, q + NQ, ... (fixed order)
+  const int b = u / p.kv_heads, j = u - b * p.kv_heads;
   const int q = tid / GD4, o = tid - q * GD4;
-  const int g_o = (4 * o) / D;
-  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-  for (int c = q; c < n; c += NQ) {
-    const float4 x = __ldcg(reinterpret_cast<const float4*>(recs + (size_t)c * R::FLOATS + R::HDR) + o);
-    const float w = wts[c * G + g_o];
-    a.x += x.x * w;
-    a.y += x.y * w;
-    a.z += x.z * w;
-    a.w += x.w * w;
-  }
-  part[q * GD4 + o] = a;
-  __syncthreads();
+  const int g = (4 * o) / D;
+  const int d0 = 4 * o - g * D;
 
-  const int winner = *win;
+  // ---- loads, all independent ----
+  const unsigned long long key = full ? __ldcg(&uo[u].key) : 0ull;
+  const float lst = full ? __ldcg(&uo[u].lstar[g]) : 0.0f;
+  const uint2 vs2 = full ? __ldcg(reinterpret_cast<const uint2*>(uo[u].vstar + d0)) : make_uint2(0u, 0u);
+  const float ln = __ldcg(&uo[u].lnew[g]);
+  const unsigned long long codek = __ldcg(&uo[u].codek);
+  const uint16_t* kt = reinterpret_cast<const uint16_t*>(p.k) + (size_t)u * D;
+  const uint16_t* vtp = reinterpret_cast<const uint16_t*>(p.v) + (size_t)u * D;
+  const uint16_t kt1 = tid < D ? __ldcg(kt + tid) : (uint16_t)0;
+  const uint16_t vt1 = tid < D ? __ldcg(vtp + tid) : (uint16_t)0;
+  const uint2 vt2 = __ldcg(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(p.v) +
+                                                          (size_t)u * D + d0));
+  float rm[kMergeRegs], rl[kMergeRegs];
+  float4 rx[kMergeRegs];
+#pragma unroll
+  for (int i = 0; i < kMergeRegs; ++i) {
+    const int c = q + i * NQ;
+    if (c < n) {
+      const float* r = recs + (size_t)c * R::FLOATS;
+      rm[i] = __ldcg(r + g);
+      rl[i] = __ldcg(r + G + g);
+      rx[i] = __ldcg(reinterpret_cast<const float4*>(r + R::HDR) + o);
+    }
+  }
+
+  const int winner = full ? (key ? (int)evict_key_slot(key) : -1) : p.append_slot;
   if (winner < 0 || winner >= p.budget) {  // cannot happen: never write outside the cache
     if (tid == 0) atomicExch(p.err, 2);
     return;
   }
-  const int b = u / p.kv_heads, j = u - b * p.kv_heads;
-  const uint16_t* vt = reinterpret_cast<const uint16_t*>(p.v) + (size_t)u * D;
-  if (tid < GD4) {
-    float4 s = part[tid];
-    for (int q2 = 1; q2 < NQ; ++q2) {
-      const float4 y = part[q2 * GD4 + tid];
-      s.x += y.x;
-      s.y += y.y;
-      s.z += y.z;
-      s.w += y.w;
+  // the evicted slot's contributor: owner of tile winner / tile
+  const int crel = (full && n > 0)
+                       ? (int)((((int64_t)u * p.tpu + winner / p.tile + 1) * NCT - 1) / TT) - first
+                       : -1;
+  const float4 vs = make_float4(__uint_as_float(vs2.x << 16), __uint_as_float(vs2.x & 0xFFFF0000u),
+                                __uint_as_float(vs2.y << 16), __uint_as_float(vs2.y & 0xFFFF0000u));
+  if (tid == 0) sflag[0] = 0;
+  __syncthreads();
+
+  float mx = -1e30f, sum = 0.0f;
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < kMergeRegs; ++i) {
+    const int c = q + i * NQ;
+    if (c < n) {
+      if (c == crel && d0 == 0 && !(exp2f(lst - rm[i]) <= 0.5f * rl[i])) atomicExch(&sflag[0], 1);
+      fold_one<D, G>(rm[i], rl[i], rx[i], c == crel, lst, vs, mx, sum, a);
     }
-    const int g = (4 * tid) / D, d = 4 * tid - g * D;
-    const float wn = exp2f(__ldcg(&uo[u].lnew[g]) - hm[g]);
-    const float inv = 1.0f / hl[g];
+  }
+  for (int c = q + kMergeRegs * NQ; c < n; c += NQ) {
+    const float* r = recs + (size_t)c * R::FLOATS;
+    const float mc = __ldcg(r + g), lc = __ldcg(r + G + g);
+    const float4 x = __ldcg(reinterpret_cast<const float4*>(r + R::HDR) + o);
+    if (c == crel && d0 == 0 && !(exp2f(lst - mc) <= 0.5f * lc)) atomicExch(&sflag[0], 1);
+    fold_one<D, G>(mc, lc, x, c == crel, lst, vs, mx, sum, a);
+  }
+  __syncthreads();
+  const bool recomputed = sflag[0] != 0;
+  if (recomputed) {
+    // the evicted slot dominates its partial: recompute that partial without it
+    const uint16_t* qg = reinterpret_cast<const uint16_t*>(p.q) + (size_t)(b * p.kv_heads + j) * G * D;
+    for (int i2 = tid; i2 < G * D; i2 += kMergeThreads) qf[i2] = __uint_as_float((uint32_t)qg[i2] << 16);
+    __syncthreads();
+    const int c = first + crel;
+    const int tb = (int)((int64_t)c * TT / NCT), te = (int)(((int64_t)c + 1) * TT / NCT);
+    const int lo = (max(tb, u * p.tpu) - u * p.tpu) * p.tile;
+    const int hi = min((min(te, (u + 1) * p.tpu) - u * p.tpu) * p.tile, p.occ);
+    recompute_partial<D, G>(p, u, lo, hi, winner, qf, wstate, xm, xl, xa, tid);
+    mx = -1e30f;
+    sum = 0.0f;
+    a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c2 = q; c2 < n; c2 += NQ) {
+      if (c2 == crel) {
+        fold_one<D, G>(xm[g], xl[g], reinterpret_cast<const float4*>(xa)[o], false, lst, vs, mx,
+                       sum, a);
+      } else {
+        const float* r = recs + (size_t)c2 * R::FLOATS;
+        fold_one<D, G>(__ldcg(r + g), __ldcg(r + G + g),
+                       __ldcg(reinterpret_cast<const float4*>(r + R::HDR) + o), false, lst, vs,
+                       mx, sum, a);
+      }
+    }
+  }
+  sacc[tid] = a;
+  smax[tid] = mx;
+  ssum[tid] = sum;
+  __syncthreads();
+
+  if (tid < GD4) {
+    // fold the groups in order, then the new token
+    float m2 = ln;
+    for (int q2 = 0; q2 < NQ; ++q2) m2 = fmaxf(m2, smax[q2 * GD4 + tid]);
+    float l2 = 0.0f;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q2 = 0; q2 < NQ; ++q2) {
+      const float w = exp2f(smax[q2 * GD4 + tid] - m2);
+      const float4 y = sacc[q2 * GD4 + tid];
+      l2 += ssum[q2 * GD4 + tid] * w;
+      s.x += y.x * w;
+      s.y += y.y * w;
+      s.z += y.z * w;
+      s.w += y.w * w;
+    }
+    const float wn = exp2f(ln - m2);
+    const float inv = 1.0f / (l2 + wn);
     float4 r;
-    r.x = (s.x + wn * __uint_as_float((uint32_t)vt[d] << 16)) * inv;
-    r.y = (s.y + wn * __uint_as_float((uint32_t)vt[d + 1] << 16)) * inv;
-    r.z = (s.z + wn * __uint_as_float((uint32_t)vt[d + 2] << 16)) * inv;
-    r.w = (s.w + wn * __uint_as_float((uint32_t)vt[d + 3] << 16)) * inv;
+    r.x = (s.x + wn * __uint_as_float(vt2.x << 16)) * inv;
+    r.y = (s.y + wn * __uint_as_float(vt2.x & 0xFFFF0000u)) * inv;
+    r.z = (s.z + wn * __uint_as_float(vt2.y << 16)) * inv;
+    r.w = (s.w + wn * __uint_as_float(vt2.y & 0xFFFF0000u)) * inv;
     reinterpret_cast<float4*>(p.out + ((size_t)b * p.kv_heads * G + (size_t)j * G) * D)[tid] = r;
   }
 
   // method step 5: the current token's key, value and code replace the slot
   uint16_t* Kw = reinterpret_cast<uint16_t*>(p.K) + ((size_t)u * p.budget + winner) * D;
   uint16_t* Vw = reinterpret_cast<uint16_t*>(p.V) + ((size_t)u * p.budget + winner) * D;
-  const uint16_t* kt = reinterpret_cast<const uint16_t*>(p.k) + (size_t)u * D;
-  for (int d = tid; d < D; d += kMergeThreads) {
-    Kw[d] = kt[d];
-    Vw[d] = vt[d];
+  if (tid < D) {
+    Kw[tid] = kt1;
+    Vw[tid] = vt1;
   }
   if (tid == 0) {
     store_code(p.codes + (size_t)u * p.code_stride + (size_t)winner * (p.bits >> 3), p.bits,
-               __ldcg(&uo[u].codek));
+               codek);
     p.evicted[u] = full ? winner : -1;
     uo[u].key = 0;  // ready for the next step's atomicMax
+    if (recomputed) atomicAdd(p.counters + u, 1);  // how often the exact path ran
   }
+  HE_STAMP(2, 2);
+}
+
+// Dynamic shared memory of merge.
+template <int D, int G>
+constexpr int merge_smem_bytes() {
+  return kMergeThreads * (16 + 4 + 4) + (G * D + G * D + 8 + 8) * 4 + 16 +
+         kRecomputeWarps * G * (2 + D) * 4;
 }
 
 }  // namespace he

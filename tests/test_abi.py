@@ -81,6 +81,7 @@ def test_null_arguments_are_rejected(L):
     assert L.he_occupancy(None, None) == -1
     assert L.he_step_bytes(None, None) == -1
     assert L.he_launch_info(None, None, None, None, None) == -1
+    assert L.he_recompute_count(None, None) == -1
 
 
 def test_python_errors_raise(L):

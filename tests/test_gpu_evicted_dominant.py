@@ -1,0 +1,77 @@
+"""The evicted slot carries most of the softmax mass of its attention partial.
+
+The bf16 step takes the evicted slot out of the attention partial that holds it;
+when the slot carries more than half of that partial's mass it recomputes the
+partial exactly instead of subtracting.  Here a key is built to be both the most
+Hamming-dissimilar to the query (all code bits flipped: evicted) and the key
+with by far the largest logit, so the exact path must run, and the result must
+still equal the oracle's (which never attends to the evicted slot).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_harness import MAX_ABS_TOL, MEAN_ABS_TOL, make_handle, torch_from_host
+
+pytestmark = pytest.mark.gpu
+
+
+def bf16_bits(a):
+    u = np.asarray(a, np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def to_f64(h):
+    return (np.asarray(h, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("bits", [8, 16])
+def test_dominant_evicted_slot_is_recomputed(bits):
+    import torch
+    w = synth.WORKLOADS["llama8b_b8"].with_(batch=1, heads=4, kv_heads=1, budget=256, bits=bits,
+                                            prompt=512)
+    D, B, G = w.head_dim, w.budget, w.group
+    o = oracle.load()
+    rng = np.random.default_rng(bits)
+    W = o.projection(w.projection_seed(), D, bits, "bf16")
+    Wf = to_f64(W)
+    q0 = to_f64(bf16_bits(rng.standard_normal(D)))
+    # k* = alpha q0 + r, r orthogonal to q0, with every projection sign flipped
+    s = np.sign(Wf.T @ q0)
+    P = np.eye(D) - np.outer(q0, q0) / (q0 @ q0)
+    A = (P @ Wf).T                       # [bits][D]
+    alpha = 30.0 * np.sqrt(D) / (q0 @ q0) / np.log2(np.e)
+    b = -alpha * (Wf.T @ q0) - s * 40.0
+    r = A.T @ np.linalg.solve(A @ A.T, b)
+    kstar = bf16_bits(alpha * q0 + r)
+    cq = o.code(bf16_bits(q0)[None, :], W)[0]
+    ck = o.code(kstar[None, :], W)[0]
+    assert bin(int(cq) ^ int(ck)).count("1") == bits, "construction did not flip every bit"
+    K = bf16_bits(rng.standard_normal((B, D)) * 0.5)
+    V = bf16_bits(rng.standard_normal((B, D)))
+    slot = 77
+    K[slot] = kstar
+    q = np.broadcast_to(bf16_bits(q0), (G, D)).copy()
+    knew = bf16_bits(rng.standard_normal(D))
+    vnew = bf16_bits(rng.standard_normal(D))
+
+    st = o.unit_fill(W, B, K, V)
+    # the evicted key must dominate its 64-slot tile in the cache before the step
+    logits = (to_f64(K[64:128]) @ q0) / np.sqrt(D)
+    assert np.argmax(logits) == slot - 64 and logits.max() - np.sort(logits)[-2] > 10
+    r_or = o.unit_stream(st, q[None], knew[None], vnew[None])
+    assert r_or["evicted"].tolist() == [slot]
+
+    he = make_handle(w)
+    try:
+        he.fill(torch_from_host(K[None, None]), torch_from_host(V[None, None]))
+        out = he.step(torch_from_host(q[None]), torch_from_host(knew[None, None]),
+                      torch_from_host(vnew[None, None]))
+        assert he.last_evicted().tolist() == [[slot]]
+        got = out.cpu().numpy()[0].astype(np.float64)
+        assert he.recompute_count == 1
+    finally:
+        he.close()
+    err = np.abs(got - r_or["out"][0])
+    assert err.max() <= MAX_ABS_TOL and err.mean() <= MEAN_ABS_TOL, (err.max(), err.mean())
