@@ -82,7 +82,10 @@ int he_create(const he_cfg* cfg, he_handle* out);
  * Errors: HE_EINVAL (NULL handle, n out of range, NULL or misaligned K/V), HE_ECUDA. */
 int he_fill(he_handle h, const void* K, const void* V, int32_t n, void* stream);
 
-/* One decode step (method steps 1-5, then attention), one kernel launch.
+/* One decode step (method steps 1-5, then attention).  bf16 handles launch
+ * three kernels on `stream` (attention partials over the cache, codes and
+ * eviction, then merge and overwrite), chained by programmatic dependent
+ * launch; fp32 handles launch one fused kernel.
  * q: device [batch][heads][head_dim]; k, v: device [batch][kv_heads][head_dim];
  * out: device fp32 [batch][heads][head_dim].  Updates the cache in place.
  * Errors: HE_EINVAL (NULL handle or pointer, misalignment), HE_ENOTFILLED, HE_ECUDA. */
@@ -133,8 +136,9 @@ int he_occupancy(he_handle h, int32_t* occupancy);
  * write of the overwritten slot, q/k/v in, out, W) — the roofline numerator. */
 int he_step_bytes(he_handle h, uint64_t* bytes);
 
-/* Launch shape of the step kernel for the current occupancy: CTAs, CTAs per SM,
- * cache tiles (32 slots each) and pipeline stages. */
+/* Launch shape of the cache-streaming kernel for the current occupancy: CTAs,
+ * CTAs per SM, cache tiles (64 slots each for bf16 handles, 32 for fp32) and
+ * pipeline stages. */
 int he_launch_info(he_handle h, int32_t* ctas, int32_t* ctas_per_sm, int32_t* tiles,
                    int32_t* stages);
 

@@ -523,7 +523,7 @@ __device__ __forceinline__ uint64_t splitmix_finalise(uint64_t x) {
   return z ^ (z >> 31);
 }
 
-__global__ void projection_kernel(uint64_t seed, int D, int bits, int is_fp32, void* W) {
+static __global__ void projection_kernel(uint64_t seed, int D, int bits, int is_fp32, void* W) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= D * bits) return;
   const uint64_t st = splitmix_finalise(seed ^ 0x48455F50524F4A57ull);
