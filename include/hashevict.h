@@ -148,6 +148,34 @@ int he_launch_info(he_handle h, int32_t* ctas, int32_t* ctas_per_sm, int32_t* ti
  * Always 0 for fp32 handles.  Synchronises. */
 int he_recompute_count(he_handle h, int64_t* total);
 
+/* Allocation-free decode attention.  This entry point has no counterpart in
+ * the method's description: it is an integration aid for callers that cannot
+ * let a library allocate device memory — code that runs while a CUDA graph is
+ * being captured, runtimes whose device memory is owned by their own pool or
+ * arena, deployments that fix every byte of device memory up front.
+ *   out[b][h][:] = sum_{s < n} softmax_s(q[b][h] . K[b][kv][s] / sqrt(head_dim))
+ *                  V[b][kv][s],   kv = h / (heads / kv_heads)
+ * K, V: device bf16 [batch][kv_heads][budget][head_dim] (rows s >= n of each
+ * (batch, kv) are read and ignored: they must hold finite values); q: device
+ * bf16 [batch][heads][head_dim]; out: device fp32 [batch][heads][head_dim].
+ * The same split-K tensor-core kernel as he_step runs with its partial results
+ * in one static device array of HE_NOALLOC_SCRATCH_BYTES per GPU (every GPU that
+ * loads the library holds it until the process exits).  Limit: with C = min(the
+ * number of 64-slot tiles, SMs x resident CTAs per SM) and R = 4 * (4 *
+ * ceil(2G / 4) + G * head_dim) bytes per partial record (G = heads / kv_heads),
+ * (C + batch * kv_heads) * R + 256 <= HE_NOALLOC_SCRATCH_BYTES, else HE_EINVAL.
+ * The first call on each device does a one-off set-up (the array's device
+ * address, kernel attributes) on the current device: make it before any stream
+ * capture.  Every call uses the same array, so calls that overlap on the GPU
+ * race: order them (one stream, or events).  No part of the array needs to
+ * start at zero.  Not thread-safe on a device's first call.
+ * Errors: HE_EINVAL (sizes, NULL or misaligned pointers, scratch too small),
+ * HE_ECUDA. */
+#define HE_NOALLOC_SCRATCH_BYTES (8u << 20)
+int he_attend_noalloc(int32_t batch, int32_t heads, int32_t kv_heads, int32_t head_dim,
+                      int32_t budget, int32_t n, const void* K, const void* V, const void* q,
+                      float* out, void* stream);
+
 /* Human-readable name of a return code. */
 const char* he_strerror(int code);
 

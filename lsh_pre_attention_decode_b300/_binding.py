@@ -57,11 +57,13 @@ def lib() -> ctypes.CDLL:
         L.he_step_bytes.argtypes = [_vp, P(ctypes.c_uint64)]
         L.he_launch_info.argtypes = [_vp, P(_i32), P(_i32), P(_i32), P(_i32)]
         L.he_recompute_count.argtypes = [_vp, P(ctypes.c_int64)]
+        L.he_attend_noalloc.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp]
         L.he_strerror.argtypes = [ctypes.c_int]
         L.he_strerror.restype = ctypes.c_char_p
         for n in ("he_create", "he_fill", "he_step", "he_step_host", "he_destroy",
                   "he_last_evicted", "he_read_state", "he_get_projection", "he_codes", "he_scores",
-                  "he_occupancy", "he_step_bytes", "he_launch_info", "he_recompute_count"):
+                  "he_occupancy", "he_step_bytes", "he_launch_info", "he_recompute_count",
+                  "he_attend_noalloc"):
             getattr(L, n).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -158,6 +160,13 @@ def he_recompute_count(h: int) -> int:
     t = ctypes.c_int64()
     _check("he_recompute_count", lib().he_recompute_count(h, ctypes.byref(t)))
     return t.value
+
+
+def he_attend_noalloc(batch: int, heads: int, kv_heads: int, head_dim: int, budget: int, n: int,
+                      K, V, q, out, stream=None) -> None:
+    _check("he_attend_noalloc",
+           lib().he_attend_noalloc(batch, heads, kv_heads, head_dim, budget, n, _ptr(K), _ptr(V),
+                                   _ptr(q), _ptr(out), _stream(stream)))
 
 
 def he_launch_info(h: int) -> dict:

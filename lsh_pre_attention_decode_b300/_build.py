@@ -9,7 +9,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libhashevict.so")
-SOURCES = [os.path.join(CSRC, "hashevict.cu")]
+SOURCES = [os.path.join(CSRC, "hashevict.cu"), os.path.join(CSRC, "he_noalloc.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh")] + [
     os.path.join(INCLUDE, "hashevict.h")]
 
