@@ -1,10 +1,11 @@
 #!/usr/bin/env python3
 """Benchmark of the HashEvict decode step (hash + evict + attend) on B300.
 
-One step = one call of the fused step (one kernel launch) for one attention
-layer over the whole batch: code the query heads and the new key, score every
-cached slot by group-summed Hamming distance, evict the most dissimilar slot,
-write the new token into it, and attend over the retained cache.
+One step = one `he_step` call for one attention layer over the whole batch:
+code the query heads and the new key, score every cached slot by group-summed
+Hamming distance, evict the most dissimilar slot, write the new token into it,
+and attend over the retained cache.  A bf16 step is three kernel launches
+(cache-streaming attention, codes and eviction, merge and overwrite).
 
 Default workload: the Llama-3-8B-shaped layer (batch 8, 32 query / 8 KV heads,
 head_dim 128, bf16, 32-bit codes, budget 4096 of an 8192-token prompt).  The
@@ -36,7 +37,7 @@ import synth  # noqa: E402
 
 DEFAULT_WORKLOAD = "llama8b_b8"
 FALLBACK_HBM_GBS = 6400.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "step_kernel_llama8b_b8.md")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "stream_kernel_llama8b_b8.md")
 
 
 def parse_args():
@@ -52,6 +53,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=400)
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU work of the oracle baseline sample")
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="target wall time of the timed oracle steps of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -80,8 +83,8 @@ def kernel_source_sha() -> str:
 
 
 def profiled_traffic():
-    """DRAM bytes per launch of the step kernel from the committed ncu summary, if
-    it was taken on the current kernel source; else None."""
+    """DRAM bytes per launch of the cache-streaming kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
     if not os.path.exists(PROFILE_SUMMARY):
         return None
     txt = open(PROFILE_SUMMARY).read()
@@ -166,26 +169,30 @@ def config_of(w: synth.Workload, args, extra=None):
 # CPU oracle (reported baseline; test infrastructure, never on the product path)
 # ---------------------------------------------------------------------------
 
-def run_cpu_baseline(w: synth.Workload, target_s: float):
-    """Times the CPU oracle, as it stands, on a bounded sample of the workload:
-    every (batch, KV head) unit of one layer, the first S streamed tokens, all
-    cores (one thread per unit, the oracle releases the GIL).  Returns
-    (steps_per_s, cores, sample description, seconds)."""
+def run_cpu_baseline(w: synth.Workload, target_s: float, steps: int | None = None):
+    """Times the CPU oracle, as it stands, on a bounded sample of the workload.
+
+    The unit of work is a unit-step: one streamed token through one (batch, KV
+    head) unit of layer 0 with a full cache (hash, evict, overwrite, fp64
+    attention).  A full step of the workload is batch * kv_heads unit-steps, so
+    the throughput is reported as unit-steps / (batch * kv_heads) / second.
+    With `steps` = K each timed step is a sample of s units (s sized so that
+    the K steps take about target_s of wall time, 1 <= s <= batch * kv_heads);
+    without it the sample is every unit for about target_s.  One thread per
+    unit on all host cores (the oracle releases the GIL).
+    Returns (full steps per second, cores, sample description, seconds)."""
     import concurrent.futures as cf
     import oracle
     o = oracle.load()
     cores = os.cpu_count() or 1
-    units = [(b, j) for b in range(w.batch) for j in range(w.kv_heads)]
+    all_units = [(b, j) for b in range(w.batch) for j in range(w.kv_heads)]
+    U = len(all_units)
     W = o.projection(w.projection_seed(0), w.head_dim, w.bits, w.dtype)
 
     def prep(u):
         b, j = u
-        st = o.unit_fill(W, w.budget, synth.host_unit_kv(w, "key", b, j, 0, w.budget),
-                         synth.host_unit_kv(w, "value", b, j, 0, w.budget))
-        return st
-
-    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
-        states = list(ex.map(prep, units))
+        return o.unit_fill(W, w.budget, synth.host_unit_kv(w, "key", b, j, 0, w.budget),
+                           synth.host_unit_kv(w, "value", b, j, 0, w.budget))
 
     def run(u, st, t0, n):
         b, j = u
@@ -196,20 +203,38 @@ def run_cpu_baseline(w: synth.Workload, target_s: float):
         o.unit_stream(st, q, k, v)
         return time.perf_counter() - t
 
-    # calibrate with one step, then size the sample to about target_s of wall time
+    # calibrate: one token through min(U, cores) units in parallel
+    cal = all_units[:min(U, cores)]
     with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        cal_states = list(ex.map(prep, cal))
         t = time.perf_counter()
-        list(ex.map(lambda a: run(*a, 0, 1), zip(units, states)))
-        one = time.perf_counter() - t
-    n = max(1, min(w.streamed - 1, int(target_s / max(one, 1e-6))))
+        list(ex.map(lambda a: run(*a, 0, 1), zip(cal, cal_states)))
+        per_wave = time.perf_counter() - t
+    par_unit_s = per_wave / len(cal)  # wall time per unit-step with all cores busy
+    budget_unit_steps = max(1, int(target_s / max(par_unit_s, 1e-9)))
+    if steps:
+        per_step = max(1, min(U, budget_unit_steps // steps))
+        total = steps * per_step
+    else:
+        per_step = None
+        total = max(U, budget_unit_steps)
+    n_units = min(U, total)
+    units = all_units[:n_units]
+    toks = [total // n_units + (1 if i < total % n_units else 0) for i in range(n_units)]
+    toks = [min(x, w.streamed - 2) for x in toks]
+    done = sum(toks)
     with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        states = list(ex.map(prep, units))
         t = time.perf_counter()
-        list(ex.map(lambda a: run(*a, 1, n), zip(units, states)))
+        list(ex.map(lambda a: run(a[0], a[1], 1, a[2]), zip(units, states, toks)))
         el = time.perf_counter() - t
-    sample = (f"{w.name}, layer 0, all {len(units)} (batch, KV head) units, streamed tokens "
-              f"1..{n} after a full cache ({n} steps), hash+evict+attend (fp64 attention), "
-              f"{cores} threads over units; input generation excluded")
-    return n / el, cores, sample, el
+    how = (f"{steps} steps x {per_step} unit(s) per step" if steps else
+           f"{done} unit-steps over {n_units} units")
+    sample = (f"{w.name}, layer 0: {how} = {done} unit-steps (one streamed token through one "
+              f"(batch, KV head) unit with a full cache: hash, evict, overwrite, fp64 attention), "
+              f"{n_units} of {U} units, {min(cores, n_units)} threads; throughput scaled to full "
+              f"steps as unit-steps / {U}; input generation excluded")
+    return done / U / el, min(cores, n_units), sample, el
 
 
 # ---------------------------------------------------------------------------
@@ -219,7 +244,8 @@ def run_cpu_baseline(w: synth.Workload, target_s: float):
 def run_ours(args, rank: int, world: int, dist_on: bool):
     import torch
     import lsh_pre_attention_decode_b300 as hepkg
-    from lsh_pre_attention_decode_b300 import HashEvict, he_step, he_step_host
+    from lsh_pre_attention_decode_b300 import HashEvict, he_step, he_step_host, layer_shard, \
+        max_over_ranks
 
     w = workload_from(args)
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -227,7 +253,7 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     L = args.layers
     R = args.ring
     # independent shards: rank r takes layers r*L .. r*L+L-1 (weak scaling, no collective)
-    layers = [rank * L + i for i in range(L)]
+    layers = layer_shard(rank, world, L)
     handles, inputs = [], []
     for layer in layers:
         he = HashEvict(w.batch, w.heads, w.kv_heads, w.head_dim, w.bits, w.budget, w.dtype,
@@ -272,22 +298,26 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
         torch.cuda.synchronize()
     if dist_on:
         torch.distributed.barrier()
-    elapsed_ms = e0.elapsed_time(e1)
-    if dist_on:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(e0.elapsed_time(e1), dev)
 
-    # per-launch durations of the step kernel (events bracket each launch)
+    # per-kernel durations: a separate pass in the library's kernel timing mode
+    # (CUDA events on the launching stream before the cache-streaming kernel and
+    # after each kernel of the step; the events serialise the three kernels)
     nk = min(K, 2000)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(nk)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(nk)]
-    for i in range(nk):
-        starts[i].record(stream)
+    for he in handles:
+        he.profile_start(nk // L + 1)
+    for _ in range(nk):
         step()
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    kern_ms = float(np.mean([s.elapsed_time(e) for s, e in zip(starts, ends)]))
+    prof = {"stream_ms": 0.0, "prep_ms": 0.0, "merge_ms": 0.0, "step_ms": 0.0, "steps": 0}
+    for he in handles:
+        r = he.profile_stop()
+        for key in prof:
+            prof[key] += r[key]
+    n_prof = prof["steps"]
+    stream_ms = prof["stream_ms"] / n_prof
+    prep_ms = prof["prep_ms"] / n_prof
+    merge_ms = prof["merge_ms"] / n_prof
+    serial_step_ms = prof["step_ms"] / n_prof
 
     step_bytes = handles[0].step_bytes
     info = handles[0].launch_info()
@@ -312,10 +342,7 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
         t = i % R
         he_step_host(he0.h, qh[t], kh[t], vh[t], oh, stream)
     e2e_s = time.perf_counter() - t0
-    if dist_on:
-        tt = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(tt.item())
+    e2e_s = max_over_ranks(e2e_s, dev)
     h2d = qh[0].numel() * qh.element_size() + 2 * kh[0].numel() * kh.element_size()
     d2h = oh.numel() * oh.element_size()
 
@@ -325,7 +352,13 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     steps_total = K * world
     value = steps_total / (elapsed_ms / 1e3)
     peak, peak_kind = measured_peaks()
-    achieved = step_bytes / (kern_ms / 1e3) / 1e9
+    eb = 2 if w.dtype == "bf16" else 4
+    occ = w.budget
+    U = w.batch * w.kv_heads
+    stream_bytes = U * occ * 2 * w.head_dim * eb  # K and V rows of every resident slot
+    achieved = stream_bytes / (stream_ms / 1e3) / 1e9
+    step_gbs = step_bytes / (elapsed_ms / K / 1e3) / 1e9
+    launches_per_step = 3 if w.dtype == "bf16" else 1
     res = {
         "metric": "HashEvict decode steps/s (hash+evict+attend); achieved HBM GB/s vs B300 peak",
         "value": value,
@@ -347,14 +380,26 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
             "parallelism": f"{world} independent replica(s), layers sharded by rank, no collective",
             "launch": info}),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json "
-                     "hbm_gbs)" if peak_kind == "measured" else "fallback 6.4 TB/s",
-                     "traffic": profiled_traffic(), "algorithmic_bytes_per_launch": step_bytes,
-                     "kernel_ms": kern_ms, "kernel": "he::step_kernel (one launch per step)"},
+                     "frac": achieved / peak,
+                     "peak_source": (f"{peak_kind}: MEASURED_PEAKS.json hbm_gbs (of measured)"
+                                     if peak_kind == "measured" else "fallback 6.4 TB/s"),
+                     "traffic": profiled_traffic(),
+                     "kernel": "he::stream_kernel (cache-streaming attention partials)",
+                     "algorithmic_bytes_per_launch": stream_bytes,
+                     "kernel_ms": stream_ms,
+                     "timing": f"CUDA events on the launching stream around each launch, "
+                               f"mean over {n_prof} launches in a pass after the timed region",
+                     "other_kernels_ms": {"prep (codes + eviction)": prep_ms,
+                                          "merge (LSE merge + overwrite)": merge_ms,
+                                          "serialised step": serial_step_ms},
+                     "step": {"algorithmic_bytes": step_bytes, "achieved": step_gbs,
+                              "frac": step_gbs / peak,
+                              "note": "he_step_bytes / ms_per_step of the timed region "
+                                      "(pipelined: prep overlaps the stream kernel)"}},
         "e2e": {"value": n_e2e / e2e_s * world, "unit": "steps/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "api": "he_step_host (host buffers; copies and synchronisation inside)"},
-        "gpu_launches": K,
+        "gpu_launches": launches_per_step * K,
         "clocks": clk.summary(),
     }
     return res, w
@@ -370,7 +415,7 @@ def main():
         if rank != 0:
             return 0
         w = workload_from(args)
-        val, cores, sample, el = run_cpu_baseline(w, args.cpu_seconds)
+        val, cores, sample, el = run_cpu_baseline(w, args.ref_seconds, steps=args.steps)
         res = {
             "metric": "HashEvict decode steps/s (hash+evict+attend); achieved HBM GB/s vs B300 peak",
             "impl": "reference", "value": val, "unit": "steps/s", "n_gpus": 0,

@@ -142,6 +142,21 @@ int he_step_bytes(he_handle h, uint64_t* bytes);
 int he_launch_info(he_handle h, int32_t* ctas, int32_t* ctas_per_sm, int32_t* tiles,
                    int32_t* stages);
 
+/* Kernel timing mode.  After he_profile_start(h, max_steps) the next max_steps
+ * he_step calls record CUDA events on their stream before the cache-streaming
+ * kernel and after each of the step's kernels.  The events serialise the
+ * kernels (a timed bf16 step does not overlap its codes/eviction kernel with the
+ * cache stream, nor the next step with this one), so time steps this way in a
+ * pass of their own.  he_profile_stop sums the elapsed times over the recorded
+ * steps into ms[4]: [0] the cache-streaming attention kernel (the one fused
+ * kernel for fp32 handles), [1] the codes/eviction kernel (0 for fp32), [2] the
+ * merge/overwrite kernel (0 for fp32), [3] the whole step; *steps = steps
+ * recorded.  It synchronises on the events and leaves timing mode.
+ * Errors: HE_EINVAL (NULL handle or pointers, max_steps outside 1..65536),
+ * HE_ENOMEM (events could not be created), HE_ECUDA. */
+int he_profile_start(he_handle h, int32_t max_steps);
+int he_profile_stop(he_handle h, float* ms, int32_t* steps);
+
 /* Number of times, since he_fill, that the attention partial holding the
  * evicted slot was recomputed exactly instead of having the slot's weight
  * subtracted (the slot carried more than half of that partial's softmax mass).

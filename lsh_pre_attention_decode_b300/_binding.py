@@ -58,12 +58,14 @@ def lib() -> ctypes.CDLL:
         L.he_launch_info.argtypes = [_vp, P(_i32), P(_i32), P(_i32), P(_i32)]
         L.he_recompute_count.argtypes = [_vp, P(ctypes.c_int64)]
         L.he_attend_noalloc.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp]
+        L.he_profile_start.argtypes = [_vp, _i32]
+        L.he_profile_stop.argtypes = [_vp, P(ctypes.c_float), P(_i32)]
         L.he_strerror.argtypes = [ctypes.c_int]
         L.he_strerror.restype = ctypes.c_char_p
         for n in ("he_create", "he_fill", "he_step", "he_step_host", "he_destroy",
                   "he_last_evicted", "he_read_state", "he_get_projection", "he_codes", "he_scores",
                   "he_occupancy", "he_step_bytes", "he_launch_info", "he_recompute_count",
-                  "he_attend_noalloc"):
+                  "he_attend_noalloc", "he_profile_start", "he_profile_stop"):
             getattr(L, n).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -160,6 +162,19 @@ def he_recompute_count(h: int) -> int:
     t = ctypes.c_int64()
     _check("he_recompute_count", lib().he_recompute_count(h, ctypes.byref(t)))
     return t.value
+
+
+def he_profile_start(h: int, max_steps: int) -> None:
+    _check("he_profile_start", lib().he_profile_start(h, max_steps))
+
+
+def he_profile_stop(h: int) -> dict:
+    """Summed event times (ms) of the steps recorded since he_profile_start."""
+    ms = (ctypes.c_float * 4)()
+    n = _i32()
+    _check("he_profile_stop", lib().he_profile_stop(h, ms, ctypes.byref(n)))
+    return {"stream_ms": ms[0], "prep_ms": ms[1], "merge_ms": ms[2], "step_ms": ms[3],
+            "steps": n.value}
 
 
 def he_attend_noalloc(batch: int, heads: int, kv_heads: int, head_dim: int, budget: int, n: int,
@@ -264,3 +279,9 @@ class HashEvict:
     @property
     def recompute_count(self) -> int:
         return he_recompute_count(self.h)
+
+    def profile_start(self, max_steps: int) -> None:
+        he_profile_start(self.h, max_steps)
+
+    def profile_stop(self) -> dict:
+        return he_profile_stop(self.h)

@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstring>
 #include <new>
+#include <vector>
 #include <type_traits>
 
 #include <cudaTypedefs.h>
@@ -190,6 +191,11 @@ struct he_ctx {
   int num_sms = 0;
   int ctas_per_sm = 0;
   int max_ctas = 0;
+  // kernel timing mode: four events per profiled step (before the cache
+  // stream, after it, after codes/eviction, after merge)
+  std::vector<cudaEvent_t> prof_ev;
+  int prof_cap = 0;
+  int prof_n = 0;
 };
 
 namespace {
@@ -211,7 +217,16 @@ size_t vec_bytes(const he_ctx* h, int heads) {
   return (size_t)h->cfg.batch * heads * h->cfg.head_dim * h->eb;
 }
 
+void free_profile(he_ctx* h) {
+  for (cudaEvent_t e : h->prof_ev)
+    if (e) cudaEventDestroy(e);
+  h->prof_ev.clear();
+  h->prof_cap = 0;
+  h->prof_n = 0;
+}
+
 void free_all(he_ctx* h) {
+  free_profile(h);
   void* ptrs[] = {h->K, h->V, h->W, h->codes, h->evicted, h->counters, h->err, h->partials,
                   h->uo, h->sq, h->sk, h->sv, h->sout};
   for (void* p : ptrs)
@@ -434,6 +449,9 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
   p.v = v;
   p.out = out;
   cudaStream_t s = (cudaStream_t)stream;
+  // kernel timing mode: events between the launches serialise the kernels
+  cudaEvent_t* ev = h->prof_n < h->prof_cap ? &h->prof_ev[4 * (size_t)h->prof_n] : nullptr;
+  if (ev) HE_TRY(h, cudaEventRecord(ev[0], s));
   const int stream_ctas = p.total_tiles == 0
                               ? 0
                               : (p.total_tiles < h->max_ctas ? p.total_tiles : h->max_ctas);
@@ -442,6 +460,10 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
     void* args[] = {(void*)&p};
     HE_TRY(h, cudaLaunchKernel(h->kern.step, dim3(grid), dim3(h->kern.step_threads), args,
                                (size_t)h->kern.step_smem, s));
+    if (ev) {
+      HE_TRY(h, cudaEventRecord(ev[1], s));
+      HE_TRY(h, cudaEventRecord(ev[2], s));
+    }
   } else {
     const bool full = p.append_slot < 0;
     int splits = full ? (p.occ + he::kPrepChunk - 1) / he::kPrepChunk : 1;
@@ -452,15 +474,21 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
       HE_TRY(h, launch_pdl(h->kern.step, dim3(stream_ctas), dim3(h->kern.step_threads),
                            (size_t)h->kern.step_smem, s, sa));
     }
+    if (ev) HE_TRY(h, cudaEventRecord(ev[1], s));
     int first_of_step = stream_ctas > 0 ? 0 : 1;
     void* pa[] = {(void*)&p, (void*)&uo, (void*)&splits, (void*)&first_of_step};
     const int prep_ctas = h->U * splits < h->num_sms ? h->U * splits : h->num_sms;
     HE_TRY(h, launch_pdl(h->kern.prep, dim3(prep_ctas), dim3(he::kPrepThreads),
                          (size_t)h->kern.prep_smem, s, pa));
+    if (ev) HE_TRY(h, cudaEventRecord(ev[2], s));
     int sc = stream_ctas;
     void* ma[] = {(void*)&p, (void*)&uo, (void*)&sc};
     HE_TRY(h, launch_pdl(h->kern.merge, dim3(h->U), dim3(he::kMergeThreads),
                          (size_t)h->kern.merge_smem, s, ma));
+  }
+  if (ev) {
+    HE_TRY(h, cudaEventRecord(ev[3], s));
+    h->prof_n += 1;
   }
   if (h->occupancy < h->cfg.budget) h->occupancy += 1;
   return HE_OK;
@@ -595,6 +623,50 @@ int he_step_bytes(he_handle h, uint64_t* bytes) {
            + Bt * H * D * e + U * 2 * D * e  // q, k, v in
            + Bt * H * D * 4                // out
            + D * (uint64_t)h->cfg.bits * e;  // W
+  return HE_OK;
+}
+
+int he_profile_start(he_handle h, int32_t max_steps) {
+  if (!h || max_steps < 1 || max_steps > (1 << 16)) return HE_EINVAL;
+  if (h->sticky) return h->sticky;
+  DeviceGuard g(h->device);
+  if (!g.ok) return fail_cuda(h, cudaErrorInvalidDevice);
+  free_profile(h);
+  h->prof_ev.assign(4 * (size_t)max_steps, nullptr);
+  for (cudaEvent_t& e : h->prof_ev) {
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      e = nullptr;
+      free_profile(h);
+      (void)cudaGetLastError();
+      return HE_ENOMEM;
+    }
+  }
+  h->prof_cap = max_steps;
+  h->prof_n = 0;
+  return HE_OK;
+}
+
+int he_profile_stop(he_handle h, float* ms, int32_t* steps) {
+  if (!h || !ms || !steps) return HE_EINVAL;
+  if (h->sticky) return h->sticky;
+  DeviceGuard g(h->device);
+  if (!g.ok) return fail_cuda(h, cudaErrorInvalidDevice);
+  double sum[4] = {0, 0, 0, 0};
+  const int n = h->prof_n;
+  for (int i = 0; i < n; ++i) {
+    cudaEvent_t* ev = &h->prof_ev[4 * (size_t)i];
+    float t = 0.f;
+    for (int k = 0; k < 3; ++k) {
+      HE_TRY(h, cudaEventSynchronize(ev[k + 1]));
+      HE_TRY(h, cudaEventElapsedTime(&t, ev[k], ev[k + 1]));
+      sum[k] += t;
+    }
+    HE_TRY(h, cudaEventElapsedTime(&t, ev[0], ev[3]));
+    sum[3] += t;
+  }
+  for (int k = 0; k < 4; ++k) ms[k] = (float)sum[k];
+  *steps = n;
+  free_profile(h);
   return HE_OK;
 }
 

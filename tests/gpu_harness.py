@@ -39,6 +39,7 @@ class GpuRun:
     evicted: np.ndarray        # [steps][batch][kv_heads]
     outs: dict                 # step index -> out [batch][heads][D] float32
     state: tuple | None        # (K, V, codes, occupancy) after the run
+    prof: dict | None = None   # summed kernel times of the library's timing mode
 
 
 def make_handle(w: synth.Workload, layer: int = 0):
@@ -48,7 +49,8 @@ def make_handle(w: synth.Workload, layer: int = 0):
 
 
 def run_gpu(w: synth.Workload, fill_n: int, steps: int, out_steps=(), layer: int = 0,
-            device_gen: bool = False, read_state: bool = False, chunk: int = 256) -> GpuRun:
+            device_gen: bool = False, read_state: bool = False, chunk: int = 256,
+            profile: bool = False) -> GpuRun:
     """Fill with prompt tokens [0, fill_n), then stream tokens fill_n .. fill_n+steps-1."""
     import torch
     out_steps = set(out_steps)
@@ -65,6 +67,8 @@ def run_gpu(w: synth.Workload, fill_n: int, steps: int, out_steps=(), layer: int
             del K, V
         else:
             he.fill(None, None)
+        if profile:
+            he.profile_start(steps)
         evicted = np.empty((steps, w.batch, w.kv_heads), np.int32)
         outs = {}
         out = torch.empty((w.batch, w.heads, w.head_dim), dtype=torch.float32, device="cuda")
@@ -84,8 +88,9 @@ def run_gpu(w: synth.Workload, fill_n: int, steps: int, out_steps=(), layer: int
                 evicted[c0 + i] = he.last_evicted()
                 if c0 + i in out_steps:
                     outs[c0 + i] = out.cpu().numpy().copy()
+        prof = he.profile_stop() if profile else None
         state = he.state() if read_state else None
-        return GpuRun(evicted, outs, state)
+        return GpuRun(evicted, outs, state, prof)
     finally:
         he.close()
 
