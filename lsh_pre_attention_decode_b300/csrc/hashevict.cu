@@ -36,11 +36,19 @@ struct Kernels {
   int step_smem;
   int step_threads;
   int prep_smem;
-  int merge_smem;
+  int merge_smem;                  // dynamic shared memory of the largest merge CTA
+  int (*merge_cfg)(int, int*);     // merge threads (and smem) for n partials per unit
   int tile;
   int rec_floats;
   bool tc;  // tensor-core pipeline (tensor maps, programmatic dependent launch)
 };
+
+template <int D, int G>
+int merge_cfg(int n, int* smem) {
+  const int t = he::MergeShape<D, G>::threads(n);
+  *smem = he::merge_smem_bytes<D, G>(t);
+  return t;
+}
 
 template <typename T, int D, int G>
 Kernels kernels_for() {
@@ -55,7 +63,8 @@ Kernels kernels_for() {
     k.step_smem = S::SMEM_ALLOC;
     k.step_threads = S::NT;
     k.prep_smem = he::PrepShape<D, G>::SMEM;
-    k.merge_smem = he::merge_smem_bytes<D, G>();
+    k.merge_smem = he::merge_smem_bytes<D, G>(he::kMergeMaxThreads);
+    k.merge_cfg = &merge_cfg<D, G>;
     k.tile = S::TS;
     k.rec_floats = he::PRec<G, D>::FLOATS;
     k.tc = true;
@@ -448,6 +457,10 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
   p.k = k;
   p.v = v;
   p.out = out;
+#ifdef HE_TIMELINE
+  static int tl_counter = 0;
+  p.tl_step = (tl_counter++) & 7;
+#endif
   cudaStream_t s = (cudaStream_t)stream;
   // kernel timing mode: events between the launches serialise the kernels
   cudaEvent_t* ev = h->prof_n < h->prof_cap ? &h->prof_ev[4 * (size_t)h->prof_n] : nullptr;
@@ -483,8 +496,12 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
     if (ev) HE_TRY(h, cudaEventRecord(ev[2], s));
     int sc = stream_ctas;
     void* ma[] = {(void*)&p, (void*)&uo, (void*)&sc};
-    HE_TRY(h, launch_pdl(h->kern.merge, dim3(h->U), dim3(he::kMergeThreads),
-                         (size_t)h->kern.merge_smem, s, ma));
+    // partials per unit: at most ceil(tiles per unit * CTAs / tiles) + 1
+    const int64_t TT = p.total_tiles;
+    const int nmax = TT > 0 ? (int)(((int64_t)p.tpu * stream_ctas + TT - 1) / TT) + 1 : 0;
+    int msmem = 0;
+    const int mthreads = h->kern.merge_cfg(nmax, &msmem);
+    HE_TRY(h, launch_pdl(h->kern.merge, dim3(h->U), dim3(mthreads), (size_t)msmem, s, ma));
   }
   if (ev) {
     HE_TRY(h, cudaEventRecord(ev[3], s));

@@ -53,6 +53,9 @@ struct StepParams {
   int32_t code_stride;   // bytes per unit row of codes (multiple of 16)
   int32_t append_slot;   // -1: cache full, evict; else the slot the token is appended to
   float qscale;          // log2(e) / sqrt(D): logits kept in base 2
+#ifdef HE_TIMELINE
+  int32_t tl_step;       // diagnostic builds: step slot of the stamps
+#endif
 };
 
 // Misc shared-memory block of a step CTA.

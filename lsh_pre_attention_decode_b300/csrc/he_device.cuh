@@ -187,10 +187,12 @@ struct PhaseTimer {
     for (int k_ = 0; k_ < 22; ++k_) o_[2 + k_] = (m).tl.acc[k_];       \
   }
 // Stamps: thread 0 of a CTA writes the time at a numbered point of a kernel
-// (region r: prep 0, stream 1, merge 2) to g_he_timeline[(r*65536 + cta)*8 + k].
+// (region r: prep 0, stream 1, merge 2; step slot s = p.tl_step, 0..7) to
+// g_he_timeline[((s*3 + r)*4096 + cta)*8 + k].
 #define HE_STAMP(r, k)                                                              \
-  if (threadIdx.x == 0 && he::g_he_timeline)                                       \
-    he::g_he_timeline[((size_t)(r) * 65536 + blockIdx.x) * 8 + (k)] = (int64_t)he::global_ns();
+  if (threadIdx.x == 0 && he::g_he_timeline && blockIdx.x < 4096)                  \
+    he::g_he_timeline[(((size_t)p.tl_step * 3 + (r)) * 4096 + blockIdx.x) * 8 + (k)] = \
+        (int64_t)he::global_ns();
 #else
 #define HE_TL_FIELDS
 #define HE_TL_INIT(m)

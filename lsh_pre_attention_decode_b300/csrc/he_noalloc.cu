@@ -45,16 +45,19 @@ const void* stream_fn() {
   return reinterpret_cast<const void*>(&he::stream_kernel<D, G, kStages, kPSplit>);
 }
 
+constexpr int kAttendMergeThreads = 512;
+constexpr int kStreamThreads = he::StreamShape<128, 4, kStages>::NT;  // the same for every shape
+
 // Log-sum-exp merge of a unit's partials (no eviction, no new token).
 template <int D, int G>
-__global__ void __launch_bounds__(he::kMergeThreads) attend_merge_kernel(const he::StepParams p,
+__global__ void __launch_bounds__(kAttendMergeThreads) attend_merge_kernel(const he::StepParams p,
                                                                        int stream_ctas) {
   using R = he::PRec<G, D>;
   constexpr int GD4 = G * D / 4;
-  constexpr int NQ = he::kMergeThreads / GD4;
-  __shared__ float4 sacc[he::kMergeThreads];
-  __shared__ float smax[he::kMergeThreads];
-  __shared__ float ssum[he::kMergeThreads];
+  constexpr int NQ = kAttendMergeThreads / GD4;
+  __shared__ float4 sacc[kAttendMergeThreads];
+  __shared__ float smax[kAttendMergeThreads];
+  __shared__ float ssum[kAttendMergeThreads];
   const int tid = threadIdx.x;
   const int u = blockIdx.x;
   const int64_t TT = p.total_tiles, NCT = stream_ctas;
@@ -186,7 +189,7 @@ int setup_device(int dev) {
       const int smem = stream_smem(Ds[di], Gs[gi]);
       if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
               cudaSuccess ||
-          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&s.ctas_per_sm[gi][di], fn, 160, smem) !=
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&s.ctas_per_sm[gi][di], fn, kStreamThreads, smem) !=
               cudaSuccess ||
           s.ctas_per_sm[gi][di] < 1) {
         (void)cudaGetLastError();
@@ -278,14 +281,14 @@ extern "C" int he_attend_noalloc(int32_t batch, int32_t heads, int32_t kv_heads,
 
   cudaStream_t st = (cudaStream_t)stream;
   void* sa[] = {(void*)&p, (void*)&tmK, (void*)&tmV};
-  if (cudaLaunchKernel(pick_stream(head_dim, G), dim3(ctas), dim3(160), sa,
+  if (cudaLaunchKernel(pick_stream(head_dim, G), dim3(ctas), dim3(kStreamThreads), sa,
                        (size_t)stream_smem(head_dim, G), st) != cudaSuccess) {
     (void)cudaGetLastError();
     return HE_ECUDA;
   }
   int sc = ctas;
   void* ma[] = {(void*)&p, (void*)&sc};
-  if (cudaLaunchKernel(pick_merge(head_dim, G), dim3((unsigned)U), dim3(he::kMergeThreads), ma, 0,
+  if (cudaLaunchKernel(pick_merge(head_dim, G), dim3((unsigned)U), dim3(kAttendMergeThreads), ma, 0,
                        st) != cudaSuccess) {
     (void)cudaGetLastError();
     return HE_ECUDA;

@@ -235,6 +235,21 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
 // ---------------------------------------------------------------------------
 // stream
 // ---------------------------------------------------------------------------
+// Work of one step: the U units' tiles of 64 slots, split statically
+// (stream-K): CTA c takes a contiguous range of the U * tpu tiles and keeps one
+// partial per unit it touches (record c + u).
+//
+// A producer warp issues the loads; for every ring stage it writes a
+// descriptor (unit, tile, flags, record) that the four consumer warps read
+// after the stage's full barrier, and the unit's G query rows come into the
+// stage with the first tile of each segment (TMA, so no consumer thread waits
+// on a global load).  A sentinel descriptor ends the stream.  Consumer-wide
+// synchronisation uses mbarriers with bounded waits, so a wait that gives up
+// unwinds every warp without a hang.
+constexpr int kDescFirst = 1;  // first tile of a segment: load q, reset the state
+constexpr int kDescLast = 2;   // last tile of a segment: write the partial
+constexpr int kDescEnd = 4;    // no more tiles
+
 template <int D, int G, int NS>
 struct StreamShape {
   static constexpr int NCW = 4;              // consumer warps
@@ -245,21 +260,36 @@ struct StreamShape {
   static constexpr int BOXB = TS * 128;      // bytes per TMA box
   static constexpr int TILEB = NHALF * BOXB; // bytes per K (or V) tile
   static constexpr int STAGEB = 2 * TILEB;   // K + V
+  static constexpr int QB = G * D * 2;       // the unit's query rows (bf16)
   static constexpr int KS = D / 16;          // k-steps of the logit MMA
   static constexpr int MT = D / 16;          // d blocks of the value MMA
   static constexpr int PB = 8 * 16 * 2;      // bytes of one P^T block [8 heads][16 slots] bf16
   static constexpr int WACC = NCW * G * D;   // floats of the warp-merge area
   static constexpr int OFF_STAGE = 0;        // 1024-byte aligned (128B swizzle)
-  static constexpr int OFF_WACC = NS * STAGEB;
+  static constexpr int OFF_Q = NS * STAGEB;  // [NS][QB]
+  static constexpr int OFF_WACC = OFF_Q + NS * QB;
   static constexpr int OFF_P = OFF_WACC + WACC * 4;
   static constexpr int OFF_WM = OFF_P + NCW * 2 * PB;
-  static constexpr int OFF_FLAG = OFF_WM + 2 * NCW * G * 4;
-  static constexpr int OFF_BAR = OFF_FLAG + 16;
-  static constexpr int SMEM = OFF_BAR + 2 * NS * 8;
+  static constexpr int OFF_DESC = OFF_WM + 2 * NCW * G * 4;  // int4 [NS]
+  static constexpr int OFF_FLAG = OFF_DESC + 16 * NS;       // abort, issued, producer done, pad
+  static constexpr int OFF_BAR = OFF_FLAG + 16;             // full[NS], empty[NS], sync[2]
+  static constexpr int SMEM = OFF_BAR + (2 * NS + 2) * 8;
   static constexpr int SMEM_ALLOC = SMEM + 1024;  // slack to align the base to 1024
   static_assert(D % 64 == 0 && G >= 1 && G <= 8 && (G & (G - 1)) == 0, "shape");
-  static_assert(STAGEB % 1024 == 0 && BOXB % 1024 == 0, "swizzle atoms");
+  static_assert(STAGEB % 1024 == 0 && BOXB % 1024 == 0 && QB % 16 == 0, "alignment");
 };
+
+// Bounded barrier of the four consumer warps on an mbarrier of count NCW
+// (lane 0 of each warp arrives); false if the wait gave up.
+template <int NCW>
+__device__ __forceinline__ bool consumer_sync(uint64_t* bar, uint32_t& phase, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+  const bool ok = mbar_wait_bounded(bar, phase & 1u);
+  ++phase;
+  __syncwarp();
+  return ok;
+}
 
 template <int D, int G, int NS, bool PSPLIT>
 __global__ void __launch_bounds__(StreamShape<D, G, NS>::NT, 2)
@@ -267,60 +297,104 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS>::NT, 2)
                   const __grid_constant__ CUtensorMap tmV) {
   using S = StreamShape<D, G, NS>;
   using R = PRec<G, D>;
-  constexpr int NC = S::NC;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   unsigned char* stage = smem + S::OFF_STAGE;
+  const unsigned char* qstage = smem + S::OFF_Q;
   float* wacc = reinterpret_cast<float*>(smem + S::OFF_WACC);
   float* wm = reinterpret_cast<float*>(smem + S::OFF_WM);
   float* wl = wm + S::NCW * G;
+  int4* desc = reinterpret_cast<int4*>(smem + S::OFF_DESC);
   volatile int32_t* v_abort = reinterpret_cast<int32_t*>(smem + S::OFF_FLAG);
-  volatile int32_t* v_issued = v_abort + 1;
+  volatile int32_t* v_issued = v_abort + 1;   // stages issued (descriptors written)
+  volatile int32_t* v_prod_done = v_abort + 2;
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + S::OFF_BAR);
   uint64_t* empty_bar = full_bar + NS;
+  uint64_t* sync_bar = empty_bar + NS;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t TT = p.total_tiles, NCTA = gridDim.x;
-  const int tb = (int)((int64_t)blockIdx.x * TT / NCTA);
-  const int te = (int)(((int64_t)blockIdx.x + 1) * TT / NCTA);
-  const int ntiles = te - tb;
+  const int tps = p.tpu;
+  const int64_t TSS = (int64_t)p.U * tps, NCTA = gridDim.x;
+  const int sb = (int)((int64_t)blockIdx.x * TSS / NCTA);
+  const int se = (int)(((int64_t)blockIdx.x + 1) * TSS / NCTA);
+  const int npre = se - sb < NS ? se - sb : NS;  // tiles fetched before the wait
+
+  // one stage: its descriptor, then (unless it is the sentinel) K, V and, at a
+  // segment's first tile, the unit's query rows, all on the stage's barrier
+  auto put = [&](int k, int u, int lt, int flags, int rec) {
+    const int st = k % NS;
+    desc[st] = make_int4(u, lt, flags, rec);
+    if (flags & kDescEnd) {
+      mbar_arrive(&full_bar[st]);
+    } else {
+      unsigned char* dst = stage + st * S::STAGEB;
+      const int y = u * p.budget + lt * S::TS;
+      mbar_arrive_expect_tx(&full_bar[st],
+                            (uint32_t)(S::STAGEB + ((flags & kDescFirst) ? S::QB : 0)));
+      if (flags & kDescFirst)
+        bulk_g2s(const_cast<unsigned char*>(qstage) + st * S::QB,
+                 reinterpret_cast<const uint16_t*>(p.q) + (size_t)u * G * D, (uint32_t)S::QB,
+                 &full_bar[st]);
+#pragma unroll
+      for (int h = 0; h < S::NHALF; ++h)
+        tma_load_2d(dst + h * S::BOXB, &tmK, 64 * h, y, &full_bar[st]);
+#pragma unroll
+      for (int h = 0; h < S::NHALF; ++h)
+        tma_load_2d(dst + S::TILEB + h * S::BOXB, &tmV, 64 * h, y, &full_bar[st]);
+    }
+    *v_issued = k + 1;
+  };
+  auto put_static = [&](int k) {
+    const int t = sb + k;
+    const int u = t / tps, lt = t - u * tps;
+    const int flags = ((k == 0 || lt == 0) ? kDescFirst : 0) |
+                      ((t == se - 1 || lt == tps - 1) ? kDescLast : 0);
+    put(k, u, lt, flags, (int)blockIdx.x + u);
+  };
 
   HE_STAMP(1, 0);
-  pdl_wait();     // the previous step is complete: the cache is final
-  pdl_trigger();  // prep may launch now: its CTAs take the room stream leaves
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], S::NCW);
     }
+    mbar_init(&sync_bar[0], S::NCW);
+    mbar_init(&sync_bar[1], S::NCW);
     v_abort[0] = 0;
     v_issued[0] = 0;
+    v_prod_done[0] = 0;
     fence_mbar_init();
   }
   __syncthreads();
+  // The first tiles are fetched while the previous step's merge may
+  // still be writing: every cache row but the one slot per unit that it
+  // overwrites is final already, and the consumers re-read that row after the
+  // wait.  (The query rows are this step's input, final before the launch.)
+  if (warp == S::NCW && lane == 0)
+    for (int k = 0; k < npre; ++k) put_static(k);
+  pdl_wait();     // the previous step is complete: the cache is final
+  pdl_trigger();  // prep may launch now: its CTAs take the room stream leaves
 
   // ---------------- producer warp ----------------
   if (warp == S::NCW) {
     if (lane == 0) {
-      for (int i = 0; i < ntiles; ++i) {
-        const int st = i % NS;
-        if (i >= NS && !mbar_wait_bounded(&empty_bar[st], (uint32_t)(((i / NS) - 1) & 1))) {
+      int k = npre;
+      bool ok = true;
+      auto acquire = [&](int kk) {  // the stage of kk is free again
+        if (kk >= NS && !mbar_wait_bounded(&empty_bar[kk % NS], (uint32_t)(((kk / NS) - 1) & 1))) {
           atomicExch(p.err, 1);
-          break;
+          *v_abort = 1;
+          return false;
         }
-        const int t = tb + i;
-        const int u = t / p.tpu;
-        const int y = u * p.budget + (t - u * p.tpu) * S::TS;
-        unsigned char* dst = stage + st * S::STAGEB;
-        mbar_arrive_expect_tx(&full_bar[st], (uint32_t)S::STAGEB);
-#pragma unroll
-        for (int h = 0; h < S::NHALF; ++h)
-          tma_load_2d(dst + h * S::BOXB, &tmK, 64 * h, y, &full_bar[st]);
-#pragma unroll
-        for (int h = 0; h < S::NHALF; ++h)
-          tma_load_2d(dst + S::TILEB + h * S::BOXB, &tmV, 64 * h, y, &full_bar[st]);
-        *v_issued = i + 1;
+        return *v_abort == 0;
+      };
+      for (; k < se - sb && ok; ++k) {
+        ok = acquire(k);
+        if (ok) put_static(k);
       }
+      if (ok && acquire(k)) put(k, -1, 0, kDescEnd, 0);
+      __threadfence_block();
+      *v_prod_done = 1;
     }
     return;
   }
@@ -333,187 +407,221 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS>::NT, 2)
   __nv_bfloat16* Phi = reinterpret_cast<__nv_bfloat16*>(smem + S::OFF_P + cw * 2 * S::PB);
   __nv_bfloat16* Plo = Phi + 8 * 16;
   const float qscale = p.qscale;
-  const int u_first = tb / p.tpu, u_last = (te - 1) / p.tpu;
+  const int row0 = 16 * cw;
 
-  int i = 0;            // CTA-local tile counter
-  int drain_from = -1;  // first tile this warp did not wait for (after a give-up)
-  for (int u = u_first; u <= u_last; ++u) {
-    const int seg_t0 = max(tb, u * p.tpu), seg_t1 = min(te, (u + 1) * p.tpu);
-    const int hi = min((seg_t1 - u * p.tpu) * S::TS, p.occ);
+  uint32_t qb[S::KS][2];
+  float mrun0 = -1e30f, mrun1 = -1e30f, lrun0 = 0.0f, lrun1 = 0.0f;
+  float acc[S::MT][4];
+  int wslot = -1;
+  uint32_t sync_phase[2] = {0u, 0u};
+  int k = 0;
+  bool aborted = false;
+  for (;; ++k) {
+    const int st = k % NS;
+    if (!mbar_wait_bounded(&full_bar[st], (uint32_t)((k / NS) & 1))) {
+      atomicExch(p.err, 1);
+      *v_abort = 1;
+      aborted = true;
+      break;
+    }
+    const int4 dsc = desc[st];
+    if (dsc.z & kDescEnd) break;
+    const int u = dsc.x, lt = dsc.y;
+    const unsigned char* Ks = stage + st * S::STAGEB;
+    const unsigned char* Vs = Ks + S::TILEB;
+    const int slot_base = lt * S::TS + row0;
+    const int hi = p.occ;
 
-    // query fragments (B operand of the logit MMA): head g8, d = 16ks + 8r + 2t4 (+1)
-    uint32_t qb[S::KS][2];
-    {
-      const int b = u / p.kv_heads, jj = u - b * p.kv_heads;
-      const uint32_t* qw = reinterpret_cast<const uint32_t*>(
-          reinterpret_cast<const uint16_t*>(p.q) + ((size_t)(b * p.kv_heads + jj) * G) * D);
+    if (dsc.z & kDescFirst) {
+      // query fragments (B operand of the logit MMA): head g8, d = 16ks + 8r + 2t4 (+1)
+      const uint32_t* qw = reinterpret_cast<const uint32_t*>(qstage + st * S::QB);
 #pragma unroll
       for (int ks = 0; ks < S::KS; ++ks)
 #pragma unroll
         for (int r = 0; r < 2; ++r)
-          qb[ks][r] = g8 < G ? __ldg(qw + (g8 * D + 16 * ks + 8 * r + 2 * t4) / 2) : 0u;
+          qb[ks][r] = g8 < G ? qw[(g8 * D + 16 * ks + 8 * r + 2 * t4) / 2] : 0u;
+      mrun0 = mrun1 = -1e30f;
+      lrun0 = lrun1 = 0.0f;
+#pragma unroll
+      for (int mt = 0; mt < S::MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
+      // the slot the previous step of this cache wrote in unit u (the evicted
+      // slot, or the last appended one): stale in a tile fetched before the wait
+      wslot = -1;
+      if (p.evicted != nullptr && k < npre) {
+        wslot = __ldcg(p.evicted + u);
+        if (wslot < 0) wslot = p.occ - 1;
+      }
     }
-
-    float mrun0 = -1e30f, mrun1 = -1e30f, lrun0 = 0.0f, lrun1 = 0.0f;
-    float acc[S::MT][4];
-#pragma unroll
-    for (int mt = 0; mt < S::MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
-
-    for (int lt = seg_t0 - u * p.tpu; lt < seg_t1 - u * p.tpu; ++lt, ++i) {
-      const int st = i % NS;
-      if (drain_from < 0) {
-        if (*v_abort) {
-          drain_from = i;
-        } else if (!mbar_wait_bounded(&full_bar[st], (uint32_t)((i / NS) & 1))) {
-          atomicExch(p.err, 1);
-          *v_abort = 1;
-          drain_from = i;
-        }
-      }
-      const unsigned char* Ks = stage + st * S::STAGEB;
-      const unsigned char* Vs = Ks + S::TILEB;
-      const int row0 = 16 * cw;
-      const int slot_base = lt * S::TS + row0;
-
-      // logits for this warp's 16 slots x 8 (padded) heads
-      float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-      for (int ks = 0; ks < S::KS; ++ks) {
-        const int row = row0 + (lane & 15);
-        const int chunk = ((ks & 3) << 1) + (lane >> 4);
-        uint32_t a[4];
-        ldsm_x4(a, smem_u32(Ks + (ks >> 2) * S::BOXB + row * 128 + ((chunk ^ (row & 7)) << 4)));
-        mma_bf16_16816(c, a, qb[ks][0], qb[ks][1]);
-      }
-      // c[0]: slot g8, head h0; c[1]: slot g8, h1; c[2]: slot g8+8, h0; c[3]: slot g8+8, h1
-      float x00 = c[0] * qscale, x01 = c[1] * qscale, x10 = c[2] * qscale, x11 = c[3] * qscale;
-      const int sA = slot_base + g8, sB = sA + 8;
-      if (sA >= hi) x00 = x01 = -INFINITY;
-      if (sB >= hi) x10 = x11 = -INFINITY;
-      if (!real0) x00 = x10 = -INFINITY;
-      if (!real1) x01 = x11 = -INFINITY;
-
-      // online softmax per head over the warp's slots (lanes sharing t4)
-      float t0m = fmaxf(x00, x10), t1m = fmaxf(x01, x11);
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        t0m = fmaxf(t0m, __shfl_xor_sync(kFull, t0m, o));
-        t1m = fmaxf(t1m, __shfl_xor_sync(kFull, t1m, o));
-      }
-      const float mn0 = fmaxf(mrun0, t0m), mn1 = fmaxf(mrun1, t1m);
-      const float sc0 = exp2f(mrun0 - mn0), sc1 = exp2f(mrun1 - mn1);
-      mrun0 = mn0;
-      mrun1 = mn1;
-      const float p00 = exp2f(x00 - mn0), p10 = exp2f(x10 - mn0);
-      const float p01 = exp2f(x01 - mn1), p11 = exp2f(x11 - mn1);
-      lrun0 = lrun0 * sc0 + (p00 + p10);
-      lrun1 = lrun1 * sc1 + (p01 + p11);
-#pragma unroll
-      for (int mt = 0; mt < S::MT; ++mt) {
-        acc[mt][0] *= sc0;
-        acc[mt][2] *= sc0;
-        acc[mt][1] *= sc1;
-        acc[mt][3] *= sc1;
-      }
-
-      // P^T [8 heads][16 slots] in bf16 (hi, and the rounding remainder lo)
-      {
-        const __nv_bfloat16 a00 = __float2bfloat16_rn(p00), a01 = __float2bfloat16_rn(p01);
-        const __nv_bfloat16 a10 = __float2bfloat16_rn(p10), a11 = __float2bfloat16_rn(p11);
-        Phi[h0 * 16 + g8] = a00;
-        Phi[h1 * 16 + g8] = a01;
-        Phi[h0 * 16 + g8 + 8] = a10;
-        Phi[h1 * 16 + g8 + 8] = a11;
-        if (PSPLIT) {
-          Plo[h0 * 16 + g8] = __float2bfloat16_rn(p00 - __bfloat162float(a00));
-          Plo[h1 * 16 + g8] = __float2bfloat16_rn(p01 - __bfloat162float(a01));
-          Plo[h0 * 16 + g8 + 8] = __float2bfloat16_rn(p10 - __bfloat162float(a10));
-          Plo[h1 * 16 + g8 + 8] = __float2bfloat16_rn(p11 - __bfloat162float(a11));
-        }
+    if (k < npre && (unsigned)(wslot - slot_base) < 16u) {
+      // re-read the row written by the previous step (now visible) into the tile
+      const int row = wslot - lt * S::TS;
+      constexpr int CH = D / 8;  // 16-byte chunks per row
+      if (lane < 2 * CH) {
+        const int c = lane < CH ? lane : lane - CH;
+        const uint16_t* src = reinterpret_cast<const uint16_t*>(lane < CH ? p.K : p.V) +
+                              ((size_t)u * p.budget + wslot) * D + 8 * c;
+        const uint4 x = __ldcg(reinterpret_cast<const uint4*>(src));
+        unsigned char* dst = const_cast<unsigned char*>(lane < CH ? Ks : Vs) +
+                             (c >> 3) * S::BOXB + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+        *reinterpret_cast<uint4*>(dst) = x;
+        fence_proxy_async_smem();  // the stage is refilled by TMA later
       }
       __syncwarp();
-      const uint32_t* Phw = reinterpret_cast<const uint32_t*>(Phi);
-      const uint32_t* Plw = reinterpret_cast<const uint32_t*>(Plo);
-      const uint32_t bh0 = Phw[g8 * 8 + t4], bh1 = Phw[g8 * 8 + 4 + t4];
-      const uint32_t bl0 = PSPLIT ? Plw[g8 * 8 + t4] : 0u;
-      const uint32_t bl1 = PSPLIT ? Plw[g8 * 8 + 4 + t4] : 0u;
-
-      // values: O^T[d][head] += V^T[d][slots] P^T[slots][head]
-#pragma unroll
-      for (int mt = 0; mt < S::MT; ++mt) {
-        const int row = row0 + (lane & 7) + ((lane >> 4) << 3);
-        const int chunk = ((mt & 3) << 1) + ((lane >> 3) & 1);
-        uint32_t a[4];
-        ldsm_x4_trans(a, smem_u32(Vs + (mt >> 2) * S::BOXB + row * 128 +
-                                  ((chunk ^ (row & 7)) << 4)));
-        mma_bf16_16816(acc[mt], a, bh0, bh1);
-        if (PSPLIT) mma_bf16_16816(acc[mt], a, bl0, bl1);
-      }
-      __syncwarp();
-      if (lane == 0 && drain_from < 0) mbar_arrive(&empty_bar[st]);  // stage free for refill
     }
 
-    // warp states -> shared memory -> this CTA's partial for unit u
+    // logits for this warp's 16 slots x 8 (padded) heads
+    float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int ks = 0; ks < S::KS; ++ks) {
+      const int row = row0 + (lane & 15);
+      const int chunk = ((ks & 3) << 1) + (lane >> 4);
+      uint32_t a[4];
+      ldsm_x4(a, smem_u32(Ks + (ks >> 2) * S::BOXB + row * 128 + ((chunk ^ (row & 7)) << 4)));
+      mma_bf16_16816(c, a, qb[ks][0], qb[ks][1]);
+    }
+    // c[0]: slot g8, head h0; c[1]: slot g8, h1; c[2]: slot g8+8, h0; c[3]: slot g8+8, h1
+    float x00 = c[0] * qscale, x01 = c[1] * qscale, x10 = c[2] * qscale, x11 = c[3] * qscale;
+    const int sA = slot_base + g8, sB = sA + 8;
+    if (sA >= hi) x00 = x01 = -INFINITY;
+    if (sB >= hi) x10 = x11 = -INFINITY;
+    if (!real0) x00 = x10 = -INFINITY;
+    if (!real1) x01 = x11 = -INFINITY;
+
+    // online softmax per head over the warp's slots (lanes sharing t4)
+    float t0m = fmaxf(x00, x10), t1m = fmaxf(x01, x11);
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
-      lrun0 += __shfl_xor_sync(kFull, lrun0, o);
-      lrun1 += __shfl_xor_sync(kFull, lrun1, o);
+      t0m = fmaxf(t0m, __shfl_xor_sync(kFull, t0m, o));
+      t1m = fmaxf(t1m, __shfl_xor_sync(kFull, t1m, o));
     }
-    if (g8 == 0) {
-      if (real0) {
-        wm[cw * G + h0] = mrun0;
-        wl[cw * G + h0] = lrun0;
-      }
-      if (real1) {
-        wm[cw * G + h1] = mrun1;
-        wl[cw * G + h1] = lrun1;
-      }
-    }
+    const float mn0 = fmaxf(mrun0, t0m), mn1 = fmaxf(mrun1, t1m);
+    const float sc0 = exp2f(mrun0 - mn0), sc1 = exp2f(mrun1 - mn1);
+    mrun0 = mn0;
+    mrun1 = mn1;
+    const float p00 = exp2f(x00 - mn0), p10 = exp2f(x10 - mn0);
+    const float p01 = exp2f(x01 - mn1), p11 = exp2f(x11 - mn1);
+    lrun0 = lrun0 * sc0 + (p00 + p10);
+    lrun1 = lrun1 * sc1 + (p01 + p11);
 #pragma unroll
     for (int mt = 0; mt < S::MT; ++mt) {
-      const int d = 16 * mt + g8;
-      if (real0) {
-        wacc[(cw * G + h0) * D + d] = acc[mt][0];
-        wacc[(cw * G + h0) * D + d + 8] = acc[mt][2];
+      acc[mt][0] *= sc0;
+      acc[mt][2] *= sc0;
+      acc[mt][1] *= sc1;
+      acc[mt][3] *= sc1;
+    }
+
+    // P^T [8 heads][16 slots] in bf16 (hi, and the rounding remainder lo)
+    {
+      const __nv_bfloat16 a00 = __float2bfloat16_rn(p00), a01 = __float2bfloat16_rn(p01);
+      const __nv_bfloat16 a10 = __float2bfloat16_rn(p10), a11 = __float2bfloat16_rn(p11);
+      Phi[h0 * 16 + g8] = a00;
+      Phi[h1 * 16 + g8] = a01;
+      Phi[h0 * 16 + g8 + 8] = a10;
+      Phi[h1 * 16 + g8 + 8] = a11;
+      if (PSPLIT) {
+        Plo[h0 * 16 + g8] = __float2bfloat16_rn(p00 - __bfloat162float(a00));
+        Plo[h1 * 16 + g8] = __float2bfloat16_rn(p01 - __bfloat162float(a01));
+        Plo[h0 * 16 + g8 + 8] = __float2bfloat16_rn(p10 - __bfloat162float(a10));
+        Plo[h1 * 16 + g8 + 8] = __float2bfloat16_rn(p11 - __bfloat162float(a11));
       }
-      if (real1) {
-        wacc[(cw * G + h1) * D + d] = acc[mt][1];
-        wacc[(cw * G + h1) * D + d + 8] = acc[mt][3];
+    }
+    __syncwarp();
+    const uint32_t* Phw = reinterpret_cast<const uint32_t*>(Phi);
+    const uint32_t* Plw = reinterpret_cast<const uint32_t*>(Plo);
+    const uint32_t bh0 = Phw[g8 * 8 + t4], bh1 = Phw[g8 * 8 + 4 + t4];
+    const uint32_t bl0 = PSPLIT ? Plw[g8 * 8 + t4] : 0u;
+    const uint32_t bl1 = PSPLIT ? Plw[g8 * 8 + 4 + t4] : 0u;
+
+    // values: O^T[d][head] += V^T[d][slots] P^T[slots][head]
+#pragma unroll
+    for (int mt = 0; mt < S::MT; ++mt) {
+      const int row = row0 + (lane & 7) + ((lane >> 4) << 3);
+      const int chunk = ((mt & 3) << 1) + ((lane >> 3) & 1);
+      uint32_t a[4];
+      ldsm_x4_trans(a, smem_u32(Vs + (mt >> 2) * S::BOXB + row * 128 +
+                                ((chunk ^ (row & 7)) << 4)));
+      mma_bf16_16816(acc[mt], a, bh0, bh1);
+      if (PSPLIT) mma_bf16_16816(acc[mt], a, bl0, bl1);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty_bar[st]);  // stage free for refill
+
+    if (dsc.z & kDescLast) {
+      // warp states -> shared memory -> the partial record of this segment
+      float l0 = lrun0, l1 = lrun1;
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        l0 += __shfl_xor_sync(kFull, l0, o);
+        l1 += __shfl_xor_sync(kFull, l1, o);
+      }
+      if (g8 == 0) {
+        if (real0) {
+          wm[cw * G + h0] = mrun0;
+          wl[cw * G + h0] = l0;
+        }
+        if (real1) {
+          wm[cw * G + h1] = mrun1;
+          wl[cw * G + h1] = l1;
+        }
+      }
+#pragma unroll
+      for (int mt = 0; mt < S::MT; ++mt) {
+        const int d = 16 * mt + g8;
+        if (real0) {
+          wacc[(cw * G + h0) * D + d] = acc[mt][0];
+          wacc[(cw * G + h0) * D + d + 8] = acc[mt][2];
+        }
+        if (real1) {
+          wacc[(cw * G + h1) * D + d] = acc[mt][1];
+          wacc[(cw * G + h1) * D + d + 8] = acc[mt][3];
+        }
+      }
+      if (!consumer_sync<S::NCW>(&sync_bar[0], sync_phase[0], lane)) {
+        atomicExch(p.err, 1);
+        *v_abort = 1;
+        aborted = true;
+        break;
+      }
+      float* rec = p.partials + (size_t)dsc.w * R::FLOATS;
+      for (int idx = tid; idx < G * D; idx += S::NC) {
+        const int g = idx / D, d = idx - g * D;
+        float mx = -1e30f;
+#pragma unroll
+        for (int w2 = 0; w2 < S::NCW; ++w2) mx = fmaxf(mx, wm[w2 * G + g]);
+        float a = 0.0f;
+#pragma unroll
+        for (int w2 = 0; w2 < S::NCW; ++w2)
+          a += wacc[(w2 * G + g) * D + d] * exp2f(wm[w2 * G + g] - mx);
+        rec[R::HDR + idx] = a;
+      }
+      if (tid < G) {
+        const int g = tid;
+        float mx = -1e30f, sum = 0.0f;
+#pragma unroll
+        for (int w2 = 0; w2 < S::NCW; ++w2) mx = fmaxf(mx, wm[w2 * G + g]);
+#pragma unroll
+        for (int w2 = 0; w2 < S::NCW; ++w2) sum += wl[w2 * G + g] * exp2f(wm[w2 * G + g] - mx);
+        rec[g] = mx;
+        rec[G + g] = sum;
+      }
+      // the merge area is reused by the next segment
+      if (!consumer_sync<S::NCW>(&sync_bar[1], sync_phase[1], lane)) {
+        atomicExch(p.err, 1);
+        *v_abort = 1;
+        aborted = true;
+        break;
       }
     }
-    group_sync<NC, 1>();
-    if (*v_abort) {
-      // a wait gave up: let the copies already issued land, then leave
-      if (tid == 0) {
-        const int issued = *v_issued;
-        for (int r = drain_from < 0 ? i : drain_from; r < issued; ++r)
-          (void)mbar_wait_bounded(&full_bar[r % NS], (uint32_t)((r / NS) & 1), 500000000ull);
-      }
-      return;
+  }
+  if (aborted && tid == 0) {
+    // a wait gave up: once the producer has stopped, let every copy it issued
+    // land before the CTA's shared memory is released
+    const uint64_t t0 = global_ns();
+    while (*v_prod_done == 0 && global_ns() - t0 < 500000000ull) {
     }
-    float* rec = p.partials + (size_t)(blockIdx.x + u) * R::FLOATS;
-    for (int idx = tid; idx < G * D; idx += NC) {
-      const int g = idx / D, d = idx - g * D;
-      float mx = -1e30f;
-#pragma unroll
-      for (int w2 = 0; w2 < S::NCW; ++w2) mx = fmaxf(mx, wm[w2 * G + g]);
-      float a = 0.0f;
-#pragma unroll
-      for (int w2 = 0; w2 < S::NCW; ++w2)
-        a += wacc[(w2 * G + g) * D + d] * exp2f(wm[w2 * G + g] - mx);
-      rec[R::HDR + idx] = a;
-    }
-    if (tid < G) {
-      const int g = tid;
-      float mx = -1e30f, sum = 0.0f;
-#pragma unroll
-      for (int w2 = 0; w2 < S::NCW; ++w2) mx = fmaxf(mx, wm[w2 * G + g]);
-#pragma unroll
-      for (int w2 = 0; w2 < S::NCW; ++w2) sum += wl[w2 * G + g] * exp2f(wm[w2 * G + g] - mx);
-      rec[g] = mx;
-      rec[G + g] = sum;
-    }
-    group_sync<NC, 1>();  // the merge area is reused by the next segment
+    const int issued = *v_issued;
+    for (int r = issued - NS > 0 ? issued - NS : 0; r < issued; ++r)
+      (void)mbar_wait_bounded(&full_bar[r % NS], (uint32_t)((r / NS) & 1), 500000000ull);
   }
   HE_STAMP(1, 1);
 }
@@ -521,26 +629,42 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS>::NT, 2)
 // ---------------------------------------------------------------------------
 // merge
 // ---------------------------------------------------------------------------
-constexpr int kMergeThreads = 512;
-constexpr int kRecomputeWarps = 8;
+// A merge CTA has GD4 * NQ threads: NQ contributor groups of GD4 = G * D / 4
+// threads (one float4 of the unit's output each).  The host picks NQ from the
+// number of partials per unit: small CTAs (128 threads) where units have few
+// partials, so that one fits on an SM beside two stream CTAs and the next
+// step's stream CTAs launch everywhere while merge runs; up to 512 threads
+// where a unit has dozens of partials (long contexts).
+constexpr int kMergeMaxThreads = 512;
+constexpr int kMergeMinThreads = 512;
+constexpr int kMergeRegs = 8;  // partials held in registers per thread (more are looped)
 
 template <int D, int G>
 struct MergeShape {
-  static constexpr int GD4 = G * D / 4;           // float4 outputs per unit
-  static constexpr int NQ = kMergeThreads / GD4;  // contributor groups
+  static constexpr int GD4 = G * D / 4;  // float4 outputs per unit
+  static constexpr int NQ_MIN = GD4 >= kMergeMinThreads ? 1 : kMergeMinThreads / GD4;
+  static constexpr int NQ_MAX = GD4 >= kMergeMaxThreads ? 1 : kMergeMaxThreads / GD4;
+  static_assert(GD4 <= kMergeMaxThreads && D <= kMergeMinThreads, "merge shape");
+  // threads for units with at most n partials each
+  static int threads(int n) {
+    int nq = (n + kMergeRegs - 1) / kMergeRegs;
+    nq = nq < NQ_MIN ? NQ_MIN : (nq > NQ_MAX ? NQ_MAX : nq);
+    return GD4 * nq;
+  }
 };
 
 // Exact partial over slots [lo, hi) of unit u without slot `skip` (CUDA cores,
 // fp32): per head the base-2 max, sum and accumulator -> xm, xl, xa [G][D].
-// Warps 0..kRecomputeWarps-1 each run an online softmax over a strided share
-// of the slots (lane owns D/32 elements), then merge in a fixed order.
+// Every warp of the CTA runs an online softmax over a strided share of the
+// slots (lane owns D/32 elements), then the warp states merge in a fixed order.
 template <int D, int G>
 __device__ void recompute_partial(const StepParams& p, int u, int lo, int hi, int skip,
                                   const float* qf, float* wstate, float* xm, float* xl,
                                   float* xa, int tid) {
   constexpr int E = D / 32;
+  const int RW = (int)(blockDim.x >> 5);
   const int lane = tid & 31, warp = tid >> 5;
-  if (warp < kRecomputeWarps) {
+  {
     const uint16_t* Kc = reinterpret_cast<const uint16_t*>(p.K) + (size_t)u * p.budget * D;
     const uint16_t* Vc = reinterpret_cast<const uint16_t*>(p.V) + (size_t)u * p.budget * D;
     float mr[G], lr[G], ar[G][E];
@@ -551,7 +675,7 @@ __device__ void recompute_partial(const StepParams& p, int u, int lo, int hi, in
 #pragma unroll
       for (int e = 0; e < E; ++e) ar[g][e] = 0.0f;
     }
-    for (int s = lo + warp; s < hi; s += kRecomputeWarps) {
+    for (int s = lo + warp; s < hi; s += RW) {
       if (s == skip) continue;
       float kx[E], vx[E];
 #pragma unroll
@@ -586,12 +710,12 @@ __device__ void recompute_partial(const StepParams& p, int u, int lo, int hi, in
     }
   }
   __syncthreads();
-  for (int idx = tid; idx < G * D; idx += kMergeThreads) {
+  for (int idx = tid; idx < G * D; idx += (int)blockDim.x) {
     const int g = idx / D, d = idx - g * D;
     float mx = -1e30f;
-    for (int w = 0; w < kRecomputeWarps; ++w) mx = fmaxf(mx, wstate[((size_t)w * G + g) * (2 + D)]);
+    for (int w = 0; w < RW; ++w) mx = fmaxf(mx, wstate[((size_t)w * G + g) * (2 + D)]);
     float a = 0.0f, l = 0.0f;
-    for (int w = 0; w < kRecomputeWarps; ++w) {
+    for (int w = 0; w < RW; ++w) {
       const float* ws = wstate + ((size_t)w * G + g) * (2 + D);
       const float sc = exp2f(ws[0] - mx);
       a += ws[2 + d] * sc;
@@ -613,7 +737,6 @@ __device__ void recompute_partial(const StepParams& p, int u, int lo, int hi, in
 // fixed order, the new token is added, the output written and the slot
 // overwritten.  If the evicted slot carries more than half of its partial's
 // mass, that partial is recomputed exactly and the fold redone.
-constexpr int kMergeRegs = 4;  // partials held in registers per thread (more are looped)
 
 template <int D, int G>
 __device__ __forceinline__ void fold_one(float mc, float lc, float4 x, bool is_crel,
@@ -638,18 +761,16 @@ __device__ __forceinline__ void fold_one(float mc, float lc, float4 x, bool is_c
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const StepParams p, UnitOut* uo,
-                                                              int stream_ctas) {
+__global__ void __launch_bounds__(kMergeMaxThreads)
+    merge_kernel(const StepParams p, UnitOut* uo, int stream_ctas) {
   using R = PRec<G, D>;
-  using M = MergeShape<D, G>;
-  constexpr int GD4 = M::GD4, NQ = M::NQ;
-  static_assert(GD4 <= kMergeThreads && kMergeThreads % GD4 == 0, "merge shape");
-  static_assert(D <= 128 && D <= kMergeThreads, "evicted value row buffer");
+  constexpr int GD4 = MergeShape<D, G>::GD4;
+  const int MT = (int)blockDim.x, NQ = MT / GD4;
   extern __shared__ __align__(16) unsigned char smem_merge[];
-  float4* sacc = reinterpret_cast<float4*>(smem_merge);            // [512]
-  float* smax = reinterpret_cast<float*>(sacc + kMergeThreads);     // [512]
-  float* ssum = smax + kMergeThreads;                               // [512]
-  float* qf = ssum + kMergeThreads;                                 // [G][D] query heads (fp32)
+  float4* sacc = reinterpret_cast<float4*>(smem_merge);  // [MT]
+  float* smax = reinterpret_cast<float*>(sacc + MT);      // [MT]
+  float* ssum = smax + MT;                                // [MT]
+  float* qf = ssum + MT;                                  // [G][D] query heads (fp32)
   float* xa = qf + G * D;                                           // [G][D] recomputed partial
   float* xm = xa + G * D;                                           // [8]
   float* xl = xm + 8;                                               // [8]
@@ -664,14 +785,17 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const StepParams p
   pdl_trigger();  // the next step's prep may launch; it waits for this grid
   HE_STAMP(2, 1);
 
+  // contributors: the CTAs whose ranges cover the unit's tiles (records first+u ..)
+  const int tps = p.tpu;
+  const int64_t TSS = (int64_t)p.U * tps, NCT = stream_ctas;
   int first = 0, n = 0;
-  const int64_t TT = p.total_tiles, NCT = stream_ctas;
-  if (p.total_tiles > 0) {
-    first = (int)((((int64_t)u * p.tpu + 1) * NCT - 1) / TT);
-    const int last = (int)((((int64_t)u * p.tpu + p.tpu) * NCT - 1) / TT);
+  if (TSS > 0 && NCT > 0) {
+    first = (int)((((int64_t)u * tps + 1) * NCT - 1) / TSS);
+    const int last = (int)((((int64_t)u * tps + tps) * NCT - 1) / TSS);
     n = last - first + 1;
   }
   const float* recs = p.partials + (size_t)(first + u) * R::FLOATS;
+  auto rec_of = [&](int c) { return recs + (size_t)c * R::FLOATS; };
   const int b = u / p.kv_heads, j = u - b * p.kv_heads;
   const int q = tid / GD4, o = tid - q * GD4;
   const int g = (4 * o) / D;
@@ -695,7 +819,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const StepParams p
   for (int i = 0; i < kMergeRegs; ++i) {
     const int c = q + i * NQ;
     if (c < n) {
-      const float* r = recs + (size_t)c * R::FLOATS;
+      const float* r = rec_of(c);
       rm[i] = __ldcg(r + g);
       rl[i] = __ldcg(r + G + g);
       rx[i] = __ldcg(reinterpret_cast<const float4*>(r + R::HDR) + o);
@@ -708,8 +832,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const StepParams p
     return;
   }
   // the evicted slot's contributor: owner of tile winner / tile
+  // the evicted slot's contributor: the owner of tile winner / tile
   const int crel = (full && n > 0)
-                       ? (int)((((int64_t)u * p.tpu + winner / p.tile + 1) * NCT - 1) / TT) - first
+                       ? (int)((((int64_t)u * tps + winner / p.tile + 1) * NCT - 1) / TSS) - first
                        : -1;
   const float4 vs = make_float4(__uint_as_float(vs2.x << 16), __uint_as_float(vs2.x & 0xFFFF0000u),
                                 __uint_as_float(vs2.y << 16), __uint_as_float(vs2.y & 0xFFFF0000u));
@@ -727,7 +852,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const StepParams p
     }
   }
   for (int c = q + kMergeRegs * NQ; c < n; c += NQ) {
-    const float* r = recs + (size_t)c * R::FLOATS;
+    const float* r = rec_of(c);
     const float mc = __ldcg(r + g), lc = __ldcg(r + G + g);
     const float4 x = __ldcg(reinterpret_cast<const float4*>(r + R::HDR) + o);
     if (c == crel && d0 == 0 && !(exp2f(lst - mc) <= 0.5f * lc)) atomicExch(&sflag[0], 1);
@@ -738,12 +863,13 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const StepParams p
   if (recomputed) {
     // the evicted slot dominates its partial: recompute that partial without it
     const uint16_t* qg = reinterpret_cast<const uint16_t*>(p.q) + (size_t)(b * p.kv_heads + j) * G * D;
-    for (int i2 = tid; i2 < G * D; i2 += kMergeThreads) qf[i2] = __uint_as_float((uint32_t)qg[i2] << 16);
+    for (int i2 = tid; i2 < G * D; i2 += MT) qf[i2] = __uint_as_float((uint32_t)qg[i2] << 16);
     __syncthreads();
+    // the slots of that contributor
     const int c = first + crel;
-    const int tb = (int)((int64_t)c * TT / NCT), te = (int)(((int64_t)c + 1) * TT / NCT);
-    const int lo = (max(tb, u * p.tpu) - u * p.tpu) * p.tile;
-    const int hi = min((min(te, (u + 1) * p.tpu) - u * p.tpu) * p.tile, p.occ);
+    const int tb = (int)((int64_t)c * TSS / NCT), te = (int)(((int64_t)c + 1) * TSS / NCT);
+    const int lo = (max(tb, u * tps) - u * tps) * p.tile;
+    const int hi = min((min(te, (u + 1) * tps) - u * tps) * p.tile, p.occ);
     recompute_partial<D, G>(p, u, lo, hi, winner, qf, wstate, xm, xl, xa, tid);
     mx = -1e30f;
     sum = 0.0f;
@@ -753,7 +879,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const StepParams p
         fold_one<D, G>(xm[g], xl[g], reinterpret_cast<const float4*>(xa)[o], false, lst, vs, mx,
                        sum, a);
       } else {
-        const float* r = recs + (size_t)c2 * R::FLOATS;
+        const float* r = rec_of(c2);
         fold_one<D, G>(__ldcg(r + g), __ldcg(r + G + g),
                        __ldcg(reinterpret_cast<const float4*>(r + R::HDR) + o), false, lst, vs,
                        mx, sum, a);
@@ -809,9 +935,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const StepParams p
 
 // Dynamic shared memory of merge.
 template <int D, int G>
-constexpr int merge_smem_bytes() {
-  return kMergeThreads * (16 + 4 + 4) + (G * D + G * D + 8 + 8) * 4 + 16 +
-         kRecomputeWarps * G * (2 + D) * 4;
+constexpr int merge_smem_bytes(int threads) {
+  return threads * (16 + 4 + 4) + (G * D + G * D + 8 + 8) * 4 + 16 +
+         (threads / 32) * G * (2 + D) * 4;
 }
 
 }  // namespace he

@@ -26,11 +26,14 @@ def to_f64(h):
     return (np.asarray(h, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-@pytest.mark.parametrize("bits", [8, 16])
-def test_dominant_evicted_slot_is_recomputed(bits):
+# (bits, budget, slot): one unit of 4 tiles, and one of 375 tiles spread over
+# every stream CTA, with the slot (tile 340) inside one CTA's range (32-bit
+# codes there: no random key of 24000 ties the constructed distance).
+@pytest.mark.parametrize("bits,budget,slot", [(8, 256, 77), (16, 256, 77), (32, 24000, 21773)])
+def test_dominant_evicted_slot_is_recomputed(bits, budget, slot):
     import torch
-    w = synth.WORKLOADS["llama8b_b8"].with_(batch=1, heads=4, kv_heads=1, budget=256, bits=bits,
-                                            prompt=512)
+    w = synth.WORKLOADS["llama8b_b8"].with_(batch=1, heads=4, kv_heads=1, budget=budget,
+                                            bits=bits, prompt=2 * budget)
     D, B, G = w.head_dim, w.budget, w.group
     o = oracle.load()
     rng = np.random.default_rng(bits)
@@ -50,16 +53,17 @@ def test_dominant_evicted_slot_is_recomputed(bits):
     assert bin(int(cq) ^ int(ck)).count("1") == bits, "construction did not flip every bit"
     K = bf16_bits(rng.standard_normal((B, D)) * 0.5)
     V = bf16_bits(rng.standard_normal((B, D)))
-    slot = 77
     K[slot] = kstar
     q = np.broadcast_to(bf16_bits(q0), (G, D)).copy()
     knew = bf16_bits(rng.standard_normal(D))
     vnew = bf16_bits(rng.standard_normal(D))
 
     st = o.unit_fill(W, B, K, V)
-    # the evicted key must dominate its 64-slot tile in the cache before the step
-    logits = (to_f64(K[64:128]) @ q0) / np.sqrt(D)
-    assert np.argmax(logits) == slot - 64 and logits.max() - np.sort(logits)[-2] > 10
+    # the evicted key must dominate the 128 slots around it in the cache before
+    # the step (a stream CTA's range holds at least one 64-slot tile)
+    lo = slot // 128 * 128
+    logits = (to_f64(K[lo:lo + 128]) @ q0) / np.sqrt(D)
+    assert np.argmax(logits) == slot - lo and logits.max() - np.sort(logits)[-2] > 10
     r_or = o.unit_stream(st, q[None], knew[None], vnew[None])
     assert r_or["evicted"].tolist() == [slot]
 

@@ -163,6 +163,13 @@ def test_many_units_per_cta_and_many_ctas_per_unit():
                        decode=4), 20000, 12, out_every=5)
 
 
+def test_units_of_many_tiles():
+    """64 units of 32 tiles (budget 2048): every stream CTA covers several
+    segments of up to seven tiles; every unit, outputs sampled."""
+    w = small("llama8b_b8", batch=8, budget=2048, prompt=4096, decode=4)
+    _stream_case(w, w.budget, 24, out_every=5)
+
+
 def test_all_keys_equal_tie_goes_to_slot_zero():
     """Identical cached keys: every distance ties, so slot 0 is evicted; the new
     token (identical key) keeps the tie for the next step."""
