@@ -13,6 +13,11 @@ cache of a layer (129 MiB) is about the size of L2 (126 MB), so the timed steps
 rotate over several independent layers (4 by default, 516 MiB): every step
 reads a cache that the previous steps evicted from L2.
 
+The timed region replays a CUDA graph of captured he_step calls (the three
+launches per step issued once, then replayed), so the number is the device's
+step rate; the same steps issued one call at a time from Python are reported
+beside it ("eager"), and "e2e" goes through the host-buffer entry point.
+
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle (the
 reported baseline) on a bounded sample of the same workload instead.
 """
@@ -50,6 +55,8 @@ def parse_args():
     ap.add_argument("--bits", type=int, default=None, help="override the code length")
     ap.add_argument("--layers", type=int, default=4, help="independent layer caches rotated")
     ap.add_argument("--ring", type=int, default=512, help="distinct step inputs per layer")
+    ap.add_argument("--graph-ring", type=int, default=64,
+                    help="tokens per layer in the captured step graph (even)")
     ap.add_argument("--e2e-steps", type=int, default=400)
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU work of the oracle baseline sample")
@@ -270,35 +277,84 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
         inputs.append((q, k, v, out))
     torch.cuda.synchronize()
 
+    # raw entry-point calls with the input addresses taken once (the Python
+    # wrapper's per-call conversions cost more host time than a step takes)
+    from lsh_pre_attention_decode_b300._binding import HashEvictError
+    he_step_raw = hepkg.lib().he_step
+    hs = [he.h for he in handles]
+    qp = [[x[0][t].data_ptr() for t in range(R)] for x in inputs]
+    kp = [[x[1][t].data_ptr() for t in range(R)] for x in inputs]
+    vp = [[x[2][t].data_ptr() for t in range(R)] for x in inputs]
+    op = [x[3].data_ptr() for x in inputs]
     cursor = [0]
 
-    def step():
+    def step(sp=None):
         i = cursor[0]
         li = i % L
         t = (i // L) % R
-        q, k, v, out = inputs[li]
-        he_step(handles[li].h, q[t], k[t], v[t], out, stream)
+        rc = he_step_raw(hs[li], qp[li][t], kp[li][t], vp[li][t], op[li],
+                         stream.cuda_stream if sp is None else sp)
+        if rc:
+            raise HashEvictError("he_step", rc)
         cursor[0] += 1
 
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
+
+    # eager: one he_step call per step from this thread
+    n_eager = min(args.steps, 4000)
+    ee0 = torch.cuda.Event(enable_timing=True)
+    ee1 = torch.cuda.Event(enable_timing=True)
+    ee0.record(stream)
+    th0 = time.perf_counter()
+    for _ in range(n_eager):
+        step()
+    host_s = time.perf_counter() - th0
+    ee1.record(stream)
+    torch.cuda.synchronize()
+    eager_ms = ee0.elapsed_time(ee1)
+
+    # the timed region replays a CUDA graph of GS steps (graph_ring tokens per
+    # layer, in the same round-robin order; an even count per cache keeps the
+    # library's per-step double buffering in phase): the host issues one launch
+    # per GS steps instead of three per step
+    Rg = min(args.graph_ring, R)
+    Rg -= Rg % 2
+    GS = L * Rg
+    cursor[0] = 0
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        cap = torch.cuda.current_stream().cuda_stream
+        for _ in range(GS):
+            i = cursor[0]
+            li, t = i % L, (i // L) % Rg
+            rc = he_step_raw(hs[li], qp[li][t], kp[li][t], vp[li][t], op[li], cap)
+            if rc:
+                raise HashEvictError("he_step (capture)", rc)
+            cursor[0] += 1
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
     if dist_on:
         torch.distributed.barrier()
     torch.cuda.synchronize()
 
-    K = args.steps
+    replays = max(1, (args.steps + GS - 1) // GS)
+    K = replays * GS
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device()) as clk:
         e0.record(stream)
-        for _ in range(K):
-            step()
+        for _ in range(replays):
+            graph.replay()
         e1.record(stream)
         torch.cuda.synchronize()
     if dist_on:
         torch.distributed.barrier()
     elapsed_ms = max_over_ranks(e0.elapsed_time(e1), dev)
+    del graph
+    cursor[0] = 0
 
     # per-kernel durations: a separate pass in the library's kernel timing mode
     # (CUDA events on the launching stream before the cache-streaming kernel and
@@ -367,6 +423,9 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
         "steps": K,
         "warmup": max(args.warmup, 3),
         "ms_per_step": elapsed_ms / K,
+        "eager": {"value": n_eager * world / (eager_ms / 1e3), "unit": "steps/s",
+                  "ms_per_step": eager_ms / n_eager, "host_ms_per_step": host_s * 1e3 / n_eager,
+                  "note": "one he_step call per step from Python (ctypes), no graph"},
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -375,6 +434,8 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
         "tokens_per_s": value * w.batch,
         "config": config_of(w, args, {
             "layers_rotated": L, "ring_tokens_per_layer": R,
+            "timed_region": f"{replays} replays of a CUDA graph of {GS} he_step calls "
+                            f"({Rg} tokens per layer, round robin over the {L} layers)",
             "l2": f"inputs larger than L2: steps rotate over {L} layer caches of "
                   f"{step_bytes / 2**20:.0f} MiB each",
             "parallelism": f"{world} independent replica(s), layers sharded by rank, no collective",
