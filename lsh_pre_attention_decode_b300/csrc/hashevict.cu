@@ -190,6 +190,8 @@ struct he_ctx {
   int32_t* err = nullptr;
   float* partials = nullptr;
   he::UnitOut* uo = nullptr;  // bf16 pipeline: per-unit results of prep
+  int kpar = 0;               // parity of the next step's eviction key
+  int prev_w1 = 0;            // the previous step's written slot (StepParams::prev_w1)
   void* sq = nullptr;  // he_step_host staging
   void* sk = nullptr;
   void* sv = nullptr;
@@ -440,6 +442,7 @@ int he_fill(he_handle h, const void* K, const void* V, int32_t n, void* stream) 
   }
   HE_TRY(h, cudaMemsetAsync(h->counters, 0, (size_t)h->U * sizeof(int32_t), s));
   if (h->uo) HE_TRY(h, cudaMemsetAsync(h->uo, 0, (size_t)h->U * sizeof(he::UnitOut), s));
+  h->prev_w1 = 0;  // no step has written a slot of the filled cache
   h->occupancy = n;
   h->filled = true;
   return HE_OK;
@@ -482,6 +485,9 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
     int splits = full ? (p.occ + he::kPrepChunk - 1) / he::kPrepChunk : 1;
     if (splits < 1) splits = 1;
     he::UnitOut* uo = h->uo;
+    p.uo = uo;
+    p.kpar = h->kpar;
+    p.prev_w1 = h->prev_w1;
     if (stream_ctas > 0) {
       void* sa[] = {(void*)&p, (void*)&h->tmK, (void*)&h->tmV};
       HE_TRY(h, launch_pdl(h->kern.step, dim3(stream_ctas), dim3(h->kern.step_threads),
@@ -506,6 +512,10 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
   if (ev) {
     HE_TRY(h, cudaEventRecord(ev[3], s));
     h->prof_n += 1;
+  }
+  if (h->kern.tc) {
+    h->prev_w1 = p.append_slot >= 0 ? p.append_slot + 1 : -1;
+    h->kpar ^= 1;
   }
   if (h->occupancy < h->cfg.budget) h->occupancy += 1;
   return HE_OK;

@@ -29,6 +29,8 @@
 
 namespace he {
 
+struct UnitOut;  // bf16 pipeline: per-unit results of the codes/eviction kernel
+
 struct StepParams {
   void* K;               // cache keys   [U][budget][D]
   void* V;               // cache values [U][budget][D]
@@ -53,6 +55,12 @@ struct StepParams {
   int32_t code_stride;   // bytes per unit row of codes (multiple of 16)
   int32_t append_slot;   // -1: cache full, evict; else the slot the token is appended to
   float qscale;          // log2(e) / sqrt(D): logits kept in base 2
+  // bf16 pipeline: per-unit results, the parity of this step's eviction key,
+  // and the slot the previous step of this cache wrote: 0 none (or not
+  // tracked), s + 1 appended at slot s, -1 evicted (slot in the other key)
+  UnitOut* uo;
+  int32_t kpar;
+  int32_t prev_w1;
 #ifdef HE_TIMELINE
   int32_t tl_step;       // diagnostic builds: step slot of the stamps
 #endif

@@ -42,7 +42,10 @@ namespace he {
 
 // Per-unit results of prep, read by merge.
 struct UnitOut {
-  unsigned long long key;  // eviction key (distance << 32 | ~slot); 0 between steps
+  // eviction key (distance << 32 | ~slot) of the steps of parity 0 and 1: a
+  // step folds into key[kpar] while the next step's stream kernel may still
+  // read key[kpar ^ 1] (the previous step's decision); merge zeroes key[kpar ^ 1]
+  unsigned long long key[2];
   unsigned long long codek;
   float lnew[8];           // the new token's base-2 logits, per query head
   float lstar[8];          // the evicted slot's base-2 logits, per query head
@@ -198,7 +201,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
       if (tid == 0) {
         uint64_t b2 = 0;
         for (int w2 = 0; w2 < kPrepThreads / 32; ++w2) b2 = red[w2] > b2 ? red[w2] : b2;
-        if (b2) atomicMax(&uo[u].key, (unsigned long long)b2);
+        if (b2) atomicMax(&uo[u].key[p.kpar], (unsigned long long)b2);
         __threadfence();
         *last = atomicAdd(&uo[u].arrived, 1) == splits - 1;
         __threadfence();
@@ -207,7 +210,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
       if (*last) {
         // the unit's eviction is decided: hand merge the evicted slot's logits
         // and value row, so that merge needs no dependent load
-        const int winner = (int)evict_key_slot(__ldcg(&uo[u].key));
+        const int winner = (int)evict_key_slot(__ldcg(&uo[u].key[p.kpar]));
         const uint16_t* Krow =
             reinterpret_cast<const uint16_t*>(p.K) + ((size_t)u * p.budget + winner) * D;
         const uint16_t* Vrow =
@@ -273,7 +276,9 @@ struct StreamShape {
   static constexpr int OFF_DESC = OFF_WM + 2 * NCW * G * 4;  // int4 [NS]
   static constexpr int OFF_FLAG = OFF_DESC + 16 * NS;       // abort, issued, producer done, pad
   static constexpr int OFF_BAR = OFF_FLAG + 16;             // full[NS], empty[NS], sync[2]
-  static constexpr int SMEM = OFF_BAR + (2 * NS + 2) * 8;
+  static constexpr int OFF_PREW = OFF_BAR + (2 * NS + 2) * 8;  // int [NS]
+  static constexpr int SMEM = OFF_PREW + 16;
+  static_assert(NS <= 4, "written-slot table");
   static constexpr int SMEM_ALLOC = SMEM + 1024;  // slack to align the base to 1024
   static_assert(D % 64 == 0 && G >= 1 && G <= 8 && (G & (G - 1)) == 0, "shape");
   static_assert(STAGEB % 1024 == 0 && BOXB % 1024 == 0 && QB % 16 == 0, "alignment");
@@ -353,7 +358,14 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS>::NT, 2)
   };
 
   HE_STAMP(1, 0);
-  if (tid == 0) {
+  // The first tiles are fetched while the previous step's merge may still be
+  // writing: every cache row but the one slot per unit that it overwrites is
+  // final already, and the consumers re-read that row after the wait.  (The
+  // query rows are this step's input, final before the launch.)  Which slot
+  // that is, is final too (the previous step's eviction key, or the host's
+  // append slot), so it is read here, while the first tiles are in flight.
+  int32_t* prew = reinterpret_cast<int32_t*>(smem + S::OFF_PREW);
+  if (warp == S::NCW && lane == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], S::NCW);
@@ -364,14 +376,20 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS>::NT, 2)
     v_issued[0] = 0;
     v_prod_done[0] = 0;
     fence_mbar_init();
+    for (int k = 0; k < npre; ++k) put_static(k);
+  }
+  if (tid < npre) {
+    const int u = (sb + tid) / tps;  // the unit of tile tid
+    int w = -1;
+    if (p.prev_w1 > 0) {
+      w = p.prev_w1 - 1;  // the previous step appended here
+    } else if (p.prev_w1 < 0 && p.uo != nullptr) {
+      const unsigned long long key = __ldcg(&p.uo[u].key[p.kpar ^ 1]);
+      w = key ? (int)evict_key_slot(key) : -1;
+    }
+    prew[tid] = w;
   }
   __syncthreads();
-  // The first tiles are fetched while the previous step's merge may
-  // still be writing: every cache row but the one slot per unit that it
-  // overwrites is final already, and the consumers re-read that row after the
-  // wait.  (The query rows are this step's input, final before the launch.)
-  if (warp == S::NCW && lane == 0)
-    for (int k = 0; k < npre; ++k) put_static(k);
   pdl_wait();     // the previous step is complete: the cache is final
   pdl_trigger();  // prep may launch now: its CTAs take the room stream leaves
 
@@ -446,11 +464,7 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS>::NT, 2)
       for (int mt = 0; mt < S::MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
       // the slot the previous step of this cache wrote in unit u (the evicted
       // slot, or the last appended one): stale in a tile fetched before the wait
-      wslot = -1;
-      if (p.evicted != nullptr && k < npre) {
-        wslot = __ldcg(p.evicted + u);
-        if (wslot < 0) wslot = p.occ - 1;
-      }
+      wslot = k < npre ? prew[k] : -1;
     }
     if (k < npre && (unsigned)(wslot - slot_base) < 16u) {
       // re-read the row written by the previous step (now visible) into the tile
@@ -802,7 +816,7 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
   const int d0 = 4 * o - g * D;
 
   // ---- loads, all independent ----
-  const unsigned long long key = full ? __ldcg(&uo[u].key) : 0ull;
+  const unsigned long long key = full ? __ldcg(&uo[u].key[p.kpar]) : 0ull;
   const float lst = full ? __ldcg(&uo[u].lstar[g]) : 0.0f;
   const uint2 vs2 = full ? __ldcg(reinterpret_cast<const uint2*>(uo[u].vstar + d0)) : make_uint2(0u, 0u);
   const float ln = __ldcg(&uo[u].lnew[g]);
@@ -927,7 +941,7 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
     store_code(p.codes + (size_t)u * p.code_stride + (size_t)winner * (p.bits >> 3), p.bits,
                codek);
     p.evicted[u] = full ? winner : -1;
-    uo[u].key = 0;  // ready for the next step's atomicMax
+    uo[u].key[p.kpar ^ 1] = 0;  // ready for the next step's atomicMax
     if (recomputed) atomicAdd(p.counters + u, 1);  // how often the exact path ran
   }
   HE_STAMP(2, 2);
