@@ -53,7 +53,9 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--bits", type=int, default=None, help="override the code length")
-    ap.add_argument("--layers", type=int, default=4, help="independent layer caches rotated")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="independent layer caches rotated (default: the workload's own "
+                         "layer count if above 1, else 4)")
     ap.add_argument("--ring", type=int, default=512, help="distinct step inputs per layer")
     ap.add_argument("--graph-ring", type=int, default=64,
                     help="tokens per layer in the captured step graph (even)")
@@ -257,7 +259,7 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     w = workload_from(args)
     dev = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.current_stream()
-    L = args.layers
+    L = args.layers if args.layers else (w.layers if w.layers > 1 else 4)
     R = args.ring
     # independent shards: rank r takes layers r*L .. r*L+L-1 (weak scaling, no collective)
     layers = layer_shard(rank, world, L)
@@ -432,6 +434,7 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
         "dtype": w.dtype,
         "data": "synthetic",
         "tokens_per_s": value * w.batch,
+        "model_steps_per_s": (value / L if w.layers > 1 and L == w.layers else None),
         "config": config_of(w, args, {
             "layers_rotated": L, "ring_tokens_per_layer": R,
             "timed_region": f"{replays} replays of a CUDA graph of {GS} he_step calls "
