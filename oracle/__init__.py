@@ -61,7 +61,9 @@ def _ptr(a: np.ndarray | None):
 
 @dataclass
 class UnitState:
-    """Cache of one (batch, KV head) unit: K, V [budget][D], codes [budget]."""
+    """Cache of one (batch, KV head) unit: K, V [budget][D], codes [budget]; with
+    score memory, the per-slot scores A [budget] (fp32); tau: binarisation
+    threshold of every code of this unit."""
     W: np.ndarray
     bits: int
     budget: int
@@ -69,6 +71,8 @@ class UnitState:
     V: np.ndarray
     codes: np.ndarray
     occupancy: int
+    tau: float = 0.0
+    score: np.ndarray | None = None
 
 
 class Oracle:
@@ -80,6 +84,17 @@ class Oracle:
         lib.orc_code.restype = _u64
         lib.orc_code_many.argtypes = [_vp, _i32, _i32, _i32, _vp, _i32, _vp]
         lib.orc_code_many.restype = None
+        lib.orc_code_many_tau.argtypes = [_vp, _i32, _i32, _i32, _vp, _i32, ctypes.c_float, _vp]
+        lib.orc_code_many_tau.restype = None
+        lib.orc_most_dissimilar_score.argtypes = [_vp, _i32]
+        lib.orc_most_dissimilar_score.restype = _i32
+        lib.orc_unit_fill_tau.argtypes = [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _i32,
+                                          ctypes.c_float, _vp, _vp, _vp, _vp]
+        lib.orc_unit_fill_tau.restype = None
+        lib.orc_unit_stream_ext.argtypes = [_vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp,
+                                            _vp, _vp, _i32, _vp, _vp, _vp, ctypes.c_float,
+                                            ctypes.c_float, _vp, _vp, _vp, _vp, _vp]
+        lib.orc_unit_stream_ext.restype = None
         lib.orc_group_distance.argtypes = [_vp, _i32, _u64]
         lib.orc_group_distance.restype = _i32
         lib.orc_most_dissimilar.argtypes = [_vp, _i32]
@@ -101,15 +116,20 @@ class Oracle:
         self.lib.orc_projection(seed, head_dim, bits, _dtype_code(W), _ptr(W))
         return W
 
-    def code(self, x: np.ndarray, W: np.ndarray) -> np.ndarray:
-        """Codes of the rows of x [n][D] (or one vector [D]) -> uint64 [n]."""
+    def code(self, x: np.ndarray, W: np.ndarray, tau: float = 0.0) -> np.ndarray:
+        """Codes of the rows of x [n][D] (or one vector [D]) -> uint64 [n];
+        bit j = (projection > tau)."""
         x2 = np.ascontiguousarray(x.reshape(-1, x.shape[-1]))
         Wc = np.ascontiguousarray(W)
         if _dtype_code(x2) != _dtype_code(Wc):
             raise TypeError("x and W must have the same element type")
         out = np.empty(x2.shape[0], np.uint64)
-        self.lib.orc_code_many(_ptr(x2), x2.shape[0], _dtype_code(x2), x2.shape[1], _ptr(Wc),
-                               Wc.shape[1], _ptr(out))
+        if tau == 0.0:
+            self.lib.orc_code_many(_ptr(x2), x2.shape[0], _dtype_code(x2), x2.shape[1], _ptr(Wc),
+                                   Wc.shape[1], _ptr(out))
+        else:
+            self.lib.orc_code_many_tau(_ptr(x2), x2.shape[0], _dtype_code(x2), x2.shape[1],
+                                       _ptr(Wc), Wc.shape[1], float(tau), _ptr(out))
         return out
 
     # -- steps 3-4 -----------------------------------------------------------
@@ -120,6 +140,10 @@ class Oracle:
     def most_dissimilar(self, dist: np.ndarray) -> int:
         d = np.ascontiguousarray(dist, np.int32)
         return int(self.lib.orc_most_dissimilar(_ptr(d), d.size))
+
+    def most_dissimilar_score(self, score: np.ndarray) -> int:
+        a = np.ascontiguousarray(score, np.float32)
+        return int(self.lib.orc_most_dissimilar_score(_ptr(a), a.size))
 
     # -- attention -----------------------------------------------------------
     def attend(self, q: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
@@ -134,7 +158,10 @@ class Oracle:
         return out
 
     # -- one (batch, KV head) unit -----------------------------------------
-    def unit_fill(self, W: np.ndarray, budget: int, Kin: np.ndarray, Vin: np.ndarray) -> UnitState:
+    def unit_fill(self, W: np.ndarray, budget: int, Kin: np.ndarray, Vin: np.ndarray,
+                  tau: float = 0.0, memory: bool = False) -> UnitState:
+        """A unit filled with the rows of Kin, Vin.  ``memory``: keep per-slot
+        scores (zero after the fill) for streams with score memory."""
         n, D = Kin.shape
         if n > budget:
             raise ValueError("more fill tokens than the budget")
@@ -143,15 +170,24 @@ class Oracle:
         codes = np.zeros(budget, np.uint64)
         occ = np.zeros(1, np.int32)
         Kc, Vc, Wc = (np.ascontiguousarray(a) for a in (Kin, Vin, W))
-        self.lib.orc_unit_fill(_ptr(Wc), D, Wc.shape[1], _dtype_code(Kc), budget, _ptr(Kc),
-                               _ptr(Vc), n, _ptr(K), _ptr(V), _ptr(codes), _ptr(occ))
-        return UnitState(Wc, Wc.shape[1], budget, K, V, codes, int(occ[0]))
+        if tau == 0.0:
+            self.lib.orc_unit_fill(_ptr(Wc), D, Wc.shape[1], _dtype_code(Kc), budget, _ptr(Kc),
+                                   _ptr(Vc), n, _ptr(K), _ptr(V), _ptr(codes), _ptr(occ))
+        else:
+            self.lib.orc_unit_fill_tau(_ptr(Wc), D, Wc.shape[1], _dtype_code(Kc), budget,
+                                       _ptr(Kc), _ptr(Vc), n, float(tau), _ptr(K), _ptr(V),
+                                       _ptr(codes), _ptr(occ))
+        score = np.zeros(budget, np.float32) if memory else None
+        return UnitState(Wc, Wc.shape[1], budget, K, V, codes, int(occ[0]), float(tau), score)
 
     def unit_stream(self, st: UnitState, q: np.ndarray, k: np.ndarray, v: np.ndarray,
-                    want_out: np.ndarray | None = None, dist_log: bool = False) -> dict:
+                    want_out: np.ndarray | None = None, dist_log: bool = False,
+                    decay: float = 0.0) -> dict:
         """Run tokens q [T][G][D], k, v [T][D] through the step (state updated
         in place).  Returns evicted [T] (-1 = appended), written [T], out
-        [n_wanted][G][D] fp64 and, if asked, dist [T][budget]."""
+        [n_wanted][G][D] fp64 and, if asked, dist [T][budget].  A unit filled
+        with ``memory`` evicts by scores with memory ``decay`` (the unit's tau
+        applies to every code)."""
         T, G, D = q.shape
         qc, kc, vc = (np.ascontiguousarray(a) for a in (q, k, v))
         evicted = np.empty(T, np.int32)
@@ -165,10 +201,21 @@ class Oracle:
         out = np.empty((n_out, G, D), np.float64)
         dl = np.empty((T, st.budget), np.int32) if dist_log else None
         occ = np.array([st.occupancy], np.int32)
-        self.lib.orc_unit_stream(_ptr(st.W), D, G, st.bits, _dtype_code(qc), st.budget, _ptr(st.K),
-                                 _ptr(st.V), _ptr(st.codes), _ptr(occ), T, _ptr(qc), _ptr(kc),
-                                 _ptr(vc), _ptr(evicted), _ptr(written), _ptr(wo), _ptr(out),
-                                 _ptr(dl))
+        if st.score is None and st.tau == 0.0:
+            if decay != 0.0:
+                raise ValueError("score memory needs a unit filled with memory=True")
+            self.lib.orc_unit_stream(_ptr(st.W), D, G, st.bits, _dtype_code(qc), st.budget,
+                                     _ptr(st.K), _ptr(st.V), _ptr(st.codes), _ptr(occ), T,
+                                     _ptr(qc), _ptr(kc), _ptr(vc), _ptr(evicted), _ptr(written),
+                                     _ptr(wo), _ptr(out), _ptr(dl))
+        else:
+            if st.score is None and decay != 0.0:
+                raise ValueError("score memory needs a unit filled with memory=True")
+            self.lib.orc_unit_stream_ext(_ptr(st.W), D, G, st.bits, _dtype_code(qc), st.budget,
+                                         _ptr(st.K), _ptr(st.V), _ptr(st.codes), _ptr(st.score),
+                                         _ptr(occ), T, _ptr(qc), _ptr(kc), _ptr(vc),
+                                         float(st.tau), float(decay), _ptr(evicted),
+                                         _ptr(written), _ptr(wo), _ptr(out), _ptr(dl))
         st.occupancy = int(occ[0])
         res = {"evicted": evicted, "written": written, "out": out}
         if dist_log:

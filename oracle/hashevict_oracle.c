@@ -27,6 +27,12 @@
  *     the codes of the G query heads of its group;
  *   - "most dissimilar" = largest summed distance; ties go to the lowest slot;
  *   - scoring uses only the current step's distances (no accumulation);
+ *     the extended stream below also takes the binarisation threshold tau
+ *     (bit j = sum > tau; the method's design choices name the threshold) and a
+ *     score memory gamma in [0, 1]: every resident slot s keeps a score
+ *     A(s) = fmaf(gamma, A(s), d(s)) in fp32 at each scoring step, the largest
+ *     A is evicted (ties: lowest slot) and a written slot starts at A = 0;
+ *     gamma = 0 gives A = d, the method as described;
  *   - score the resident slots, then overwrite, then attend: the new token is
  *     always resident and attended;
  *   - while the cache holds fewer than `budget` tokens the new token is appended;
@@ -110,7 +116,8 @@ void orc_projection(uint64_t seed, int32_t D, int32_t bits, int32_t dtype, void*
 /* Steps 1-2: Gaussian projection and binarisation of one vector.             */
 /* ------------------------------------------------------------------------- */
 
-uint64_t orc_code(const void* x, int32_t dtype, int32_t D, const void* W, int32_t bits) {
+uint64_t orc_code_tau(const void* x, int32_t dtype, int32_t D, const void* W, int32_t bits,
+                      float tau) {
   uint64_t code = 0;
   for (int32_t j = 0; j < bits; ++j) {
     float acc = 0.0f;
@@ -123,19 +130,31 @@ uint64_t orc_code(const void* x, int32_t dtype, int32_t D, const void* W, int32_
       acc = fmaf(xd, wdj, acc);
     }
 #if ORACLE_MUTANT == 2 /* planted: threshold >= instead of > */
-    if (acc >= 0.0f) code |= (uint64_t)1 << j;
+    if (acc >= tau) code |= (uint64_t)1 << j;
+#elif ORACLE_MUTANT == 11 /* planted: threshold with the wrong sign */
+    if (acc > -tau) code |= (uint64_t)1 << j;
 #else
-    if (acc > 0.0f) code |= (uint64_t)1 << j;
+    if (acc > tau) code |= (uint64_t)1 << j;
 #endif
   }
   return code;
 }
 
-void orc_code_many(const void* x, int32_t n, int32_t dtype, int32_t D, const void* W,
-                   int32_t bits, uint64_t* codes) {
+/* The method's sign test: threshold 0. */
+uint64_t orc_code(const void* x, int32_t dtype, int32_t D, const void* W, int32_t bits) {
+  return orc_code_tau(x, dtype, D, W, bits, 0.0f);
+}
+
+void orc_code_many_tau(const void* x, int32_t n, int32_t dtype, int32_t D, const void* W,
+                       int32_t bits, float tau, uint64_t* codes) {
   const char* p = (const char*)x;
   for (int32_t i = 0; i < n; ++i)
-    codes[i] = orc_code(p + (size_t)i * (size_t)D * elem_bytes(dtype), dtype, D, W, bits);
+    codes[i] = orc_code_tau(p + (size_t)i * (size_t)D * elem_bytes(dtype), dtype, D, W, bits, tau);
+}
+
+void orc_code_many(const void* x, int32_t n, int32_t dtype, int32_t D, const void* W,
+                   int32_t bits, uint64_t* codes) {
+  orc_code_many_tau(x, n, dtype, D, W, bits, 0.0f, codes);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -172,6 +191,20 @@ int32_t orc_most_dissimilar(const int32_t* dist, int32_t n) {
     if (dist[s] < dist[best]) best = s;
 #else
     if (dist[s] > dist[best]) best = s;
+#endif
+  }
+  return best;
+}
+
+/* Step 4 with score memory: the slot with the largest score; ties go to the
+ * lowest index. */
+int32_t orc_most_dissimilar_score(const float* score, int32_t n) {
+  int32_t best = 0;
+  for (int32_t s = 1; s < n; ++s) {
+#if ORACLE_MUTANT == 12 /* planted: ties go to the highest index */
+    if (score[s] >= score[best]) best = s;
+#else
+    if (score[s] > score[best]) best = s;
 #endif
   }
   return best;
@@ -220,16 +253,22 @@ void orc_attend(const void* q, const void* K, const void* V, int32_t n, int32_t 
 /* State: K[budget][D], V[budget][D] (dtype), codes[budget], *occupancy.      */
 /* ------------------------------------------------------------------------- */
 
-void orc_unit_fill(const void* W, int32_t D, int32_t bits, int32_t dtype, int32_t budget,
-                   const void* Kin, const void* Vin, int32_t n, void* K, void* V,
-                   uint64_t* codes, int32_t* occupancy) {
+void orc_unit_fill_tau(const void* W, int32_t D, int32_t bits, int32_t dtype, int32_t budget,
+                       const void* Kin, const void* Vin, int32_t n, float tau, void* K, void* V,
+                       uint64_t* codes, int32_t* occupancy) {
   size_t row = (size_t)D * elem_bytes(dtype);
   (void)budget;
   memcpy(K, Kin, row * (size_t)n);
   memcpy(V, Vin, row * (size_t)n);
   for (int32_t s = 0; s < n; ++s)
-    codes[s] = orc_code((const char*)Kin + (size_t)s * row, dtype, D, W, bits);
+    codes[s] = orc_code_tau((const char*)Kin + (size_t)s * row, dtype, D, W, bits, tau);
   *occupancy = n;
+}
+
+void orc_unit_fill(const void* W, int32_t D, int32_t bits, int32_t dtype, int32_t budget,
+                   const void* Kin, const void* Vin, int32_t n, void* K, void* V,
+                   uint64_t* codes, int32_t* occupancy) {
+  orc_unit_fill_tau(W, D, bits, dtype, budget, Kin, Vin, n, 0.0f, K, V, codes, occupancy);
 }
 
 /*
@@ -240,11 +279,18 @@ void orc_unit_fill(const void* W, int32_t D, int32_t bits, int32_t dtype, int32_
  * one [G][D] block of fp64 attention output, packed in token order into out.  dist_log, when not NULL, receives the distances of
  * the scored slots, dist_log[t][budget] (0 for appended tokens).
  */
-void orc_unit_stream(const void* W, int32_t D, int32_t G, int32_t bits, int32_t dtype,
-                     int32_t budget, void* K, void* V, uint64_t* codes, int32_t* occupancy,
-                     int32_t nsteps, const void* q, const void* k, const void* v,
-                     int32_t* evicted, int32_t* written, const uint8_t* want_out, double* out,
-                     int32_t* dist_log) {
+/*
+ * The same stream with a binarisation threshold tau and, when `score` is not
+ * NULL, score memory gamma = `decay`: score[budget] holds A(s) (zero after a
+ * fill) and is updated in place.  With score == NULL the eviction uses the
+ * step's distances directly.
+ */
+void orc_unit_stream_ext(const void* W, int32_t D, int32_t G, int32_t bits, int32_t dtype,
+                         int32_t budget, void* K, void* V, uint64_t* codes, float* score,
+                         int32_t* occupancy, int32_t nsteps, const void* q, const void* k,
+                         const void* v, float tau, float decay, int32_t* evicted,
+                         int32_t* written, const uint8_t* want_out, double* out,
+                         int32_t* dist_log) {
   size_t row = (size_t)D * elem_bytes(dtype);
   int32_t* dist = (int32_t*)malloc(sizeof(int32_t) * (size_t)budget);
   uint64_t* code_q = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)G);
@@ -256,10 +302,22 @@ void orc_unit_stream(const void* W, int32_t D, int32_t G, int32_t bits, int32_t 
     int32_t slot;
     if (*occupancy == budget) {
       /* steps 1-3: code the query heads of the group and score every slot */
-      for (int32_t g = 0; g < G; ++g) code_q[g] = orc_code(qt + (size_t)g * row, dtype, D, W, bits);
+      for (int32_t g = 0; g < G; ++g)
+        code_q[g] = orc_code_tau(qt + (size_t)g * row, dtype, D, W, bits, tau);
       for (int32_t s = 0; s < budget; ++s) dist[s] = orc_group_distance(code_q, G, codes[s]);
       /* step 4 */
-      slot = orc_most_dissimilar(dist, budget);
+      if (score) {
+        for (int32_t s = 0; s < budget; ++s) {
+#if ORACLE_MUTANT == 9 /* planted: the memory weighs the new distance, not the old score */
+          score[s] = fmaf(decay, (float)dist[s], score[s]);
+#else
+          score[s] = fmaf(decay, score[s], (float)dist[s]);
+#endif
+        }
+        slot = orc_most_dissimilar_score(score, budget);
+      } else {
+        slot = orc_most_dissimilar(dist, budget);
+      }
       evicted[t] = slot;
       if (dist_log) memcpy(dist_log + (size_t)t * budget, dist, sizeof(int32_t) * (size_t)budget);
     } else {
@@ -272,7 +330,10 @@ void orc_unit_stream(const void* W, int32_t D, int32_t G, int32_t bits, int32_t 
     /* step 5: the current token replaces the evicted one */
     memcpy((char*)K + (size_t)slot * row, kt, row);
     memcpy((char*)V + (size_t)slot * row, vt, row);
-    codes[slot] = orc_code(kt, dtype, D, W, bits);
+    codes[slot] = orc_code_tau(kt, dtype, D, W, bits, tau);
+#if ORACLE_MUTANT != 10 /* (planted when 10: the new token inherits the evicted score) */
+    if (score) score[slot] = 0.0f; /* the new token has not been scored yet */
+#endif
 #if ORACLE_MUTANT == 8 /* planted: the new token's value is not written */
     memset((char*)V + (size_t)slot * row, 0, row);
 #endif
@@ -282,4 +343,14 @@ void orc_unit_stream(const void* W, int32_t D, int32_t G, int32_t bits, int32_t 
   }
   free(dist);
   free(code_q);
+}
+
+/* The method as described: threshold 0, the step's own distances. */
+void orc_unit_stream(const void* W, int32_t D, int32_t G, int32_t bits, int32_t dtype,
+                     int32_t budget, void* K, void* V, uint64_t* codes, int32_t* occupancy,
+                     int32_t nsteps, const void* q, const void* k, const void* v,
+                     int32_t* evicted, int32_t* written, const uint8_t* want_out, double* out,
+                     int32_t* dist_log) {
+  orc_unit_stream_ext(W, D, G, bits, dtype, budget, K, V, codes, NULL, occupancy, nsteps, q, k,
+                      v, 0.0f, 0.0f, evicted, written, want_out, out, dist_log);
 }

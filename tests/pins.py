@@ -66,6 +66,36 @@ def read_eviction_case():
     return c
 
 
+def read_tau_cases():
+    x, cases = None, []
+    for tok in _lines("codes_tau_hand.txt"):
+        if tok[0] == "x":
+            x = [float(t) for t in tok[1:]]
+        elif tok[0] == "tau":
+            cases.append((float(tok[1]), int(tok[3])))
+    return x, cases
+
+
+def read_decay_case():
+    c = {"fill": [], "steps": []}
+    for tok in _lines("decay_hand.txt"):
+        if tok[0] == "decay":
+            c["decay"] = float(tok[1])
+        elif tok[0] == "budget":
+            c["budget"] = int(tok[1])
+        elif tok[0] == "fill":
+            c["fill"].append([float(t) for t in tok[1:]])
+        elif tok[0] == "step":
+            i_k, i_e, i_s = tok.index("k"), tok.index("expect"), tok.index("scores")
+            c["steps"].append({"q": [float(t) for t in tok[2:i_k]],
+                               "k": [float(t) for t in tok[i_k + 1:i_e]],
+                               "expect": int(tok[i_e + 1]),
+                               "scores": [float(t) for t in tok[i_s + 1:]]})
+        elif tok[0] == "codes_final":
+            c["codes_final"] = [int(t) for t in tok[1:]]
+    return c
+
+
 def read_attention_cases():
     cases, cur = [], None
     for tok in _lines("attention_hand.txt"):
@@ -344,9 +374,74 @@ def check_attention_bf16_elements(o):
     assert np.array_equal(a, b)
 
 
+def check_codes_tau_hand(o):
+    """Threshold tau (tests/golden/codes_tau_hand.txt): bit j = (x_j > tau) with
+    W = identity."""
+    x, cases = read_tau_cases()
+    W = np.eye(8, dtype=np.float32)
+    for tau, code in cases:
+        assert int(o.code(f32(x), W, tau)[0]) == code, (tau, int(o.code(f32(x), W, tau)[0]))
+
+
+def check_codes_tau_monotone(o):
+    """Raising tau can only clear bits; tau below every projection sets all
+    bits, tau above every projection sets none (random W, bf16 and fp32)."""
+    rng = np.random.default_rng(21)
+    D, bits = 64, 32
+    W = f32(rng.standard_normal((D, bits)))
+    x = f32(rng.standard_normal((20, D)))
+    proj = x.astype(np.float64) @ W.astype(np.float64)
+    lo, hi = float(proj.min()) - 1.0, float(proj.max()) + 1.0
+    assert all(int(c) == (1 << bits) - 1 for c in o.code(x, W, lo))
+    assert all(int(c) == 0 for c in o.code(x, W, hi))
+    prev = o.code(x, W, -3.0)
+    for tau in (-1.5, -0.25, 0.0, 0.3, 2.0):
+        cur = o.code(x, W, tau)
+        assert all((int(c) & ~int(p)) == 0 for c, p in zip(cur, prev)), tau
+        prev = cur
+
+
+def check_decay_hand(o):
+    """Score memory (tests/golden/decay_hand.txt): evictions and the scores after
+    every step, exactly (dyadic values)."""
+    c = read_decay_case()
+    W = np.eye(4, dtype=np.float32)
+    fill = f32(c["fill"])
+    st = o.unit_fill(W, c["budget"], fill, fill, memory=True)
+    for s in c["steps"]:
+        r = o.unit_stream(st, f32([[s["q"]]]), f32([s["k"]]), f32([s["k"]]), decay=c["decay"])
+        assert r["evicted"].tolist() == [s["expect"]], (s, r["evicted"])
+        assert st.score.tolist() == s["scores"], (s, st.score)
+    assert st.codes.tolist() == c["codes_final"], st.codes
+
+
+def check_decay_zero_is_per_step(o):
+    """gamma = 0 with score memory is the method as described: the same
+    evictions, cache and outputs as the per-step path, on random streams with
+    ties (small codes) and appends."""
+    rng = np.random.default_rng(33)
+    for trial in range(6):
+        D, bits, G, B = 16, 8, 2, 9
+        W = o.projection(100 + trial, D, bits, "fp32")
+        n0 = int(rng.integers(3, B + 1))
+        K0 = f32(rng.standard_normal((n0, D)))
+        V0 = f32(rng.standard_normal((n0, D)))
+        T = 12
+        q = f32(rng.standard_normal((T, G, D)))
+        k = f32(rng.standard_normal((T, D)))
+        v = f32(rng.standard_normal((T, D)))
+        a = o.unit_fill(W, B, K0, V0)
+        b = o.unit_fill(W, B, K0, V0, memory=True)
+        ra = o.unit_stream(a, q, k, v)
+        rb = o.unit_stream(b, q, k, v, decay=0.0)
+        assert ra["evicted"].tolist() == rb["evicted"].tolist()
+        assert np.array_equal(ra["out"], rb["out"]) and np.array_equal(a.codes, b.codes)
+
+
 ALL_CHECKS = [
     check_codes_hand, check_codes_identity_sign, check_codes_invariances, check_projection_moments,
     check_distance_brute, check_argmax_ties, check_eviction_hand, check_special_cases,
     check_stream_invariants, check_attention_hand, check_attention_closed_forms,
-    check_attention_bf16_elements,
+    check_attention_bf16_elements, check_codes_tau_hand, check_codes_tau_monotone,
+    check_decay_hand, check_decay_zero_is_per_step,
 ]

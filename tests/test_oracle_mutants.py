@@ -15,6 +15,10 @@ MUTANTS = {
     6: "attention scale 1/sqrt(D) dropped",
     7: "value rows read with a transposed index",
     8: "the new token's value is not written",
+    9: "score memory weighs the new distance instead of the old score",
+    10: "the written slot keeps the evicted token's score",
+    11: "binarisation threshold with the wrong sign",
+    12: "score ties go to the highest slot",
 }
 
 
