@@ -57,6 +57,10 @@ def parse_args():
                     help="independent layer caches rotated (default: the workload's own "
                          "layer count if above 1, else 4)")
     ap.add_argument("--ring", type=int, default=512, help="distinct step inputs per layer")
+    ap.add_argument("--threshold", type=float, default=0.0,
+                    help="binarisation threshold tau (0: the sign test of the method)")
+    ap.add_argument("--decay", type=float, default=0.0,
+                    help="score memory gamma (0: the step's own distances, the method)")
     ap.add_argument("--graph-ring", type=int, default=64,
                     help="tokens per layer in the captured step graph (even)")
     ap.add_argument("--e2e-steps", type=int, default=400)
@@ -164,7 +168,10 @@ def workload_from(args) -> synth.Workload:
 
 
 def config_of(w: synth.Workload, args, extra=None):
-    c = {"workload": f"{w.name}: {w.description}", "batch": w.batch, "heads": w.heads,
+    c = {"workload": f"{w.name}: {w.description}" + (
+            f"; threshold {args.threshold}, score memory {args.decay}"
+            if (args.threshold or args.decay) else ""),
+         "batch": w.batch, "heads": w.heads,
          "kv_heads": w.kv_heads, "head_dim": w.head_dim, "bits": w.bits, "budget": w.budget,
          "prompt": w.prompt, "dtype": w.dtype,
          "cache_fill": "first `budget` prompt tokens; timed steps are streamed tokens "
@@ -178,7 +185,8 @@ def config_of(w: synth.Workload, args, extra=None):
 # CPU oracle (reported baseline; test infrastructure, never on the product path)
 # ---------------------------------------------------------------------------
 
-def run_cpu_baseline(w: synth.Workload, target_s: float, steps: int | None = None):
+def run_cpu_baseline(w: synth.Workload, target_s: float, steps: int | None = None,
+                     threshold: float = 0.0, decay: float = 0.0):
     """Times the CPU oracle, as it stands, on a bounded sample of the workload.
 
     The unit of work is a unit-step: one streamed token through one (batch, KV
@@ -201,7 +209,8 @@ def run_cpu_baseline(w: synth.Workload, target_s: float, steps: int | None = Non
     def prep(u):
         b, j = u
         return o.unit_fill(W, w.budget, synth.host_unit_kv(w, "key", b, j, 0, w.budget),
-                           synth.host_unit_kv(w, "value", b, j, 0, w.budget))
+                           synth.host_unit_kv(w, "value", b, j, 0, w.budget), tau=threshold,
+                           memory=decay > 0.0)
 
     def run(u, st, t0, n):
         b, j = u
@@ -209,7 +218,7 @@ def run_cpu_baseline(w: synth.Workload, target_s: float, steps: int | None = Non
         k = synth.host_unit_kv(w, "key", b, j, w.budget + t0, n)
         v = synth.host_unit_kv(w, "value", b, j, w.budget + t0, n)
         t = time.perf_counter()
-        o.unit_stream(st, q, k, v)
+        o.unit_stream(st, q, k, v, decay=decay)
         return time.perf_counter() - t
 
     # calibrate: one token through min(U, cores) units in parallel
@@ -266,7 +275,8 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     handles, inputs = [], []
     for layer in layers:
         he = HashEvict(w.batch, w.heads, w.kv_heads, w.head_dim, w.bits, w.budget, w.dtype,
-                       seed=w.projection_seed(layer))
+                       seed=w.projection_seed(layer), threshold=args.threshold,
+                       decay=args.decay)
         K = synth.gpu_kv(w, "key", 0, w.budget, layer)
         V = synth.gpu_kv(w, "value", 0, w.budget, layer)
         he.fill(K, V)
@@ -479,7 +489,8 @@ def main():
         if rank != 0:
             return 0
         w = workload_from(args)
-        val, cores, sample, el = run_cpu_baseline(w, args.ref_seconds, steps=args.steps)
+        val, cores, sample, el = run_cpu_baseline(w, args.ref_seconds, steps=args.steps,
+                                                  threshold=args.threshold, decay=args.decay)
         res = {
             "metric": "HashEvict decode steps/s (hash+evict+attend); achieved HBM GB/s vs B300 peak",
             "impl": "reference", "value": val, "unit": "steps/s", "n_gpus": 0,
@@ -506,7 +517,8 @@ def main():
     res, w = run_ours(args, rank, world, dist_on)
     if rank == 0:
         if not args.no_cpu_baseline:
-            val, cores, sample, el = run_cpu_baseline(w, args.cpu_seconds)
+            val, cores, sample, el = run_cpu_baseline(w, args.cpu_seconds,
+                                                      threshold=args.threshold, decay=args.decay)
             res["cpu_baseline"] = {"value": val, "unit": "steps/s", "cores": cores,
                                    "kind": "oracle", "sample": sample}
         print(json.dumps(res))

@@ -54,7 +54,9 @@ extern "C" {
 
 /* Handle configuration.  Supported: head_dim in {64, 128};
  * G = heads / kv_heads in {1, 2, 4, 8}; bits in {8, 16, 32, 64};
- * 1 <= budget <= 2^24; batch * kv_heads <= 2^16; dtype HE_DTYPE_*. */
+ * 1 <= budget <= 2^24; batch * kv_heads <= 2^16; dtype HE_DTYPE_*;
+ * threshold finite; 0 <= decay <= 1.  A zero-initialised tail (threshold 0,
+ * decay 0) is the method as the paper describes it. */
 typedef struct {
   int32_t batch;
   int32_t heads;     /* query heads */
@@ -63,8 +65,16 @@ typedef struct {
   int32_t bits;      /* code length b (projection width) */
   int32_t budget;    /* cache slots per (batch, KV head) */
   int32_t dtype;     /* HE_DTYPE_BF16 or HE_DTYPE_FP32 */
-  int32_t reserved;  /* must be 0 */
+  float threshold;   /* binarisation threshold tau: bit j = (projection_j > tau), the
+                        "binarisation threshold" design choice of the method section;
+                        0 = the sign test */
   uint64_t seed;     /* draws W; one handle (and one seed) per layer */
+  float decay;       /* score memory gamma: every resident slot keeps a score
+                        A = fmaf(gamma, A, d) (fp32) updated at each evicting step
+                        (d its group-summed Hamming distance); the largest A is
+                        evicted (ties: lowest slot); a written or filled slot starts
+                        at A = 0.  0 = the step's own distances (the paper's method) */
+  int32_t reserved;  /* must be 0 */
 } he_cfg;
 
 typedef struct he_ctx* he_handle;
@@ -118,7 +128,7 @@ int he_read_state(he_handle h, void* K, void* V, void* codes, int32_t* occupancy
 int he_get_projection(he_handle h, void* host_W);
 
 /* Codes of n vectors (method steps 1-2): x device [n][head_dim] (element type),
- * codes device [n] words of bits/8 bytes.  bit j = (sum_d x[d] W[d][j] > 0),
+ * codes device [n] words of bits/8 bytes.  bit j = (sum_d x[d] W[d][j] > threshold),
  * the sum in fp32, fused multiply-add, d = 0..head_dim-1 in order from +0.
  * Errors: HE_EINVAL, HE_ECUDA. */
 int he_codes(he_handle h, const void* x, int32_t n, void* codes, void* stream);
@@ -129,11 +139,17 @@ int he_codes(he_handle h, const void* x, int32_t n, void* codes, void* stream);
  * Errors: HE_EINVAL, HE_ENOTFILLED, HE_ECUDA. */
 int he_scores(he_handle h, const void* q, int32_t* dist, void* stream);
 
+/* Per-slot eviction scores A of a handle with score memory (decay > 0), host
+ * fp32 [batch][kv_heads][budget] (slots >= occupancy hold 0).  Synchronises.
+ * Errors: HE_EINVAL (NULL arguments, or a handle without score memory). */
+int he_read_scores(he_handle h, float* host_scores);
+
 /* Number of resident tokens (host-side state; no synchronisation). */
 int he_occupancy(he_handle h, int32_t* occupancy);
 
 /* Algorithmic HBM bytes of one full-cache step (read of retained K, V and codes,
- * write of the overwritten slot, q/k/v in, out, W) — the roofline numerator. */
+ * write of the overwritten slot, q/k/v in, out, W; with score memory also the
+ * read and write of every slot's score) — the roofline numerator. */
 int he_step_bytes(he_handle h, uint64_t* bytes);
 
 /* Launch shape of the cache-streaming kernel for the current occupancy: CTAs,

@@ -17,8 +17,8 @@ _vp = ctypes.c_void_p
 
 class HeCfg(ctypes.Structure):
     _fields_ = [("batch", _i32), ("heads", _i32), ("kv_heads", _i32), ("head_dim", _i32),
-                ("bits", _i32), ("budget", _i32), ("dtype", _i32), ("reserved", _i32),
-                ("seed", ctypes.c_uint64)]
+                ("bits", _i32), ("budget", _i32), ("dtype", _i32), ("threshold", ctypes.c_float),
+                ("seed", ctypes.c_uint64), ("decay", ctypes.c_float), ("reserved", _i32)]
 
 
 class HashEvictError(RuntimeError):
@@ -58,6 +58,7 @@ def lib() -> ctypes.CDLL:
         L.he_launch_info.argtypes = [_vp, P(_i32), P(_i32), P(_i32), P(_i32)]
         L.he_recompute_count.argtypes = [_vp, P(ctypes.c_int64)]
         L.he_attend_noalloc.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp]
+        L.he_read_scores.argtypes = [_vp, _vp]
         L.he_profile_start.argtypes = [_vp, _i32]
         L.he_profile_stop.argtypes = [_vp, P(ctypes.c_float), P(_i32)]
         L.he_strerror.argtypes = [ctypes.c_int]
@@ -65,7 +66,7 @@ def lib() -> ctypes.CDLL:
         for n in ("he_create", "he_fill", "he_step", "he_step_host", "he_destroy",
                   "he_last_evicted", "he_read_state", "he_get_projection", "he_codes", "he_scores",
                   "he_occupancy", "he_step_bytes", "he_launch_info", "he_recompute_count",
-                  "he_attend_noalloc", "he_profile_start", "he_profile_stop"):
+                  "he_attend_noalloc", "he_profile_start", "he_profile_stop", "he_read_scores"):
             getattr(L, n).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -152,6 +153,10 @@ def he_occupancy(h: int) -> int:
     return o.value
 
 
+def he_read_scores(h: int, host_scores) -> None:
+    _check("he_read_scores", lib().he_read_scores(h, _ptr(host_scores)))
+
+
 def he_step_bytes(h: int) -> int:
     b = ctypes.c_uint64()
     _check("he_step_bytes", lib().he_step_bytes(h, ctypes.byref(b)))
@@ -195,11 +200,12 @@ class HashEvict:
     """One layer's HashEvict cache on the current CUDA device (torch tensors)."""
 
     def __init__(self, batch: int, heads: int, kv_heads: int, head_dim: int, bits: int,
-                 budget: int, dtype: str = "bf16", seed: int = 0):
+                 budget: int, dtype: str = "bf16", seed: int = 0, threshold: float = 0.0,
+                 decay: float = 0.0):
         self.cfg = HeCfg(batch=batch, heads=heads, kv_heads=kv_heads, head_dim=head_dim,
                          bits=bits, budget=budget,
-                         dtype=HE_DTYPE_FP32 if dtype == "fp32" else HE_DTYPE_BF16, reserved=0,
-                         seed=seed)
+                         dtype=HE_DTYPE_FP32 if dtype == "fp32" else HE_DTYPE_BF16,
+                         threshold=threshold, seed=seed, decay=decay, reserved=0)
         self.dtype = dtype
         self.h = he_create(self.cfg)
 
@@ -257,6 +263,14 @@ class HashEvict:
         occ = np.zeros(1, np.int32)
         he_read_state(self.h, K, V, codes, occ)
         return K, V, codes, int(occ[0])
+
+    def scores(self):
+        """Per-slot eviction scores [batch][kv_heads][budget] (score memory only)."""
+        import numpy as np
+        c = self.cfg
+        a = np.empty((c.batch, c.kv_heads, c.budget), np.float32)
+        he_read_scores(self.h, a)
+        return a
 
     def projection(self):
         import numpy as np

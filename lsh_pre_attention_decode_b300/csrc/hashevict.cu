@@ -30,6 +30,7 @@ constexpr bool kPSplit = true;    // attention weights as bf16 hi + lo parts
 struct Kernels {
   const void* step;    // fp32: the fused step; bf16: the stream kernel
   const void* prep;    // bf16 pipeline
+  const void* prep_mem;  // bf16 pipeline with score memory
   const void* merge;   // bf16 pipeline
   const void* score;
   const void* code;
@@ -58,7 +59,8 @@ Kernels kernels_for() {
   if constexpr (std::is_same<T, bf16_t>::value) {
     using S = he::StreamShape<D, G, kTcStages>;
     k.step = reinterpret_cast<const void*>(&he::stream_kernel<D, G, kTcStages, kPSplit>);
-    k.prep = reinterpret_cast<const void*>(&he::prep_kernel<D, G>);
+    k.prep = reinterpret_cast<const void*>(&he::prep_kernel<D, G, false>);
+    k.prep_mem = reinterpret_cast<const void*>(&he::prep_kernel<D, G, true>);
     k.merge = reinterpret_cast<const void*>(&he::merge_kernel<D, G>);
     k.step_smem = S::SMEM_ALLOC;
     k.step_threads = S::NT;
@@ -186,6 +188,7 @@ struct he_ctx {
   void* W = nullptr;
   unsigned char* codes = nullptr;
   int32_t* evicted = nullptr;
+  float* score = nullptr;  // per-slot scores with score memory (decay > 0), else null
   int32_t* counters = nullptr;
   int32_t* err = nullptr;
   float* partials = nullptr;
@@ -239,6 +242,7 @@ void free_profile(he_ctx* h) {
 void free_all(he_ctx* h) {
   free_profile(h);
   void* ptrs[] = {h->K, h->V, h->W, h->codes, h->evicted, h->counters, h->err, h->partials,
+                  h->score,
                   h->uo, h->sq, h->sk, h->sv, h->sout};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -265,6 +269,9 @@ StepParams base_params(const he_ctx* h) {
   p.code_stride = h->code_stride;
   p.append_slot = h->occupancy < h->cfg.budget ? h->occupancy : -1;
   p.qscale = (float)(1.4426950408889634 / std::sqrt((double)h->cfg.head_dim));
+  p.tau = h->cfg.threshold;
+  p.decay = h->cfg.decay;
+  p.score = h->score;
   return p;
 }
 
@@ -277,8 +284,9 @@ int launch_codes(he_ctx* h, const void* x, int64_t rows, int64_t per_unit, int64
   if (blocks > cap) blocks = cap;
   const void* W = h->W;
   int bits = h->cfg.bits;
+  float tau = h->cfg.threshold;
   void* args[] = {(void*)&x, (void*)&rows, (void*)&per_unit, (void*)&x_unit_rows, (void*)&W,
-                  (void*)&bits, (void*)&out, (void*)&out_unit_bytes};
+                  (void*)&bits, (void*)&tau, (void*)&out, (void*)&out_unit_bytes};
   HE_TRY(h, cudaLaunchKernel(h->kern.code, dim3((unsigned)blocks), dim3(he::kAuxThreads), args, 0,
                              s));
   return HE_OK;
@@ -307,6 +315,7 @@ int he_create(const he_cfg* cfg, he_handle* out) {
   if (c.batch < 1 || c.heads < 1 || c.kv_heads < 1 || c.heads % c.kv_heads != 0) return HE_EINVAL;
   if (c.bits != 8 && c.bits != 16 && c.bits != 32 && c.bits != 64) return HE_EINVAL;
   if (c.budget < 1 || c.budget > (1 << 24) || c.reserved != 0) return HE_EINVAL;
+  if (!std::isfinite(c.threshold) || !(c.decay >= 0.0f && c.decay <= 1.0f)) return HE_EINVAL;
   if ((int64_t)c.batch * c.kv_heads > 65536) return HE_EINVAL;
   const int G = c.heads / c.kv_heads;
   Kernels kern;
@@ -346,6 +355,10 @@ int he_create(const he_cfg* cfg, he_handle* out) {
                               (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
          cudaFuncSetAttribute(kern.prep, cudaFuncAttributePreferredSharedMemoryCarveout,
                               (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+         cudaFuncSetAttribute(kern.prep_mem, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kern.prep_smem) != cudaSuccess ||
+         cudaFuncSetAttribute(kern.prep_mem, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
          cudaFuncSetAttribute(kern.merge, cudaFuncAttributePreferredSharedMemoryCarveout,
                               (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)) {
       rc = HE_ECUDA;
@@ -371,8 +384,10 @@ int he_create(const he_cfg* cfg, he_handle* out) {
         {(void**)&h->err, sizeof(int32_t)},
         {(void**)&h->partials, nrec * kern.rec_floats * sizeof(float)},
         {(void**)&h->uo, (size_t)U * sizeof(he::UnitOut)},
+        {(void**)&h->score, c.decay > 0.0f ? (size_t)U * c.budget * sizeof(float) : 0},
     };
     for (auto& a : allocs) {
+      if (a.bytes == 0) continue;
       if (cudaMalloc(a.p, a.bytes) != cudaSuccess) {
         (void)cudaGetLastError();
         rc = HE_ENOMEM;
@@ -442,6 +457,8 @@ int he_fill(he_handle h, const void* K, const void* V, int32_t n, void* stream) 
   }
   HE_TRY(h, cudaMemsetAsync(h->counters, 0, (size_t)h->U * sizeof(int32_t), s));
   if (h->uo) HE_TRY(h, cudaMemsetAsync(h->uo, 0, (size_t)h->U * sizeof(he::UnitOut), s));
+  if (h->score)  // filled slots start with no accumulated score
+    HE_TRY(h, cudaMemsetAsync(h->score, 0, (size_t)h->U * h->cfg.budget * sizeof(float), s));
   h->prev_w1 = 0;  // no step has written a slot of the filled cache
   h->occupancy = n;
   h->filled = true;
@@ -497,7 +514,8 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
     int first_of_step = stream_ctas > 0 ? 0 : 1;
     void* pa[] = {(void*)&p, (void*)&uo, (void*)&splits, (void*)&first_of_step};
     const int prep_ctas = h->U * splits < h->num_sms ? h->U * splits : h->num_sms;
-    HE_TRY(h, launch_pdl(h->kern.prep, dim3(prep_ctas), dim3(he::kPrepThreads),
+    HE_TRY(h, launch_pdl(h->score ? h->kern.prep_mem : h->kern.prep, dim3(prep_ctas),
+                         dim3(he::kPrepThreads),
                          (size_t)h->kern.prep_smem, s, pa));
     if (ev) HE_TRY(h, cudaEventRecord(ev[2], s));
     int sc = stream_ctas;
@@ -634,6 +652,18 @@ int he_recompute_count(he_handle h, int64_t* total) {
   return HE_OK;
 }
 
+int he_read_scores(he_handle h, float* host_scores) {
+  if (!h || !host_scores || !h->score) return HE_EINVAL;
+  if (h->sticky) return h->sticky;
+  DeviceGuard g(h->device);
+  if (!g.ok) return fail_cuda(h, cudaErrorInvalidDevice);
+  const int rc = check_device_error(h);
+  if (rc != HE_OK) return rc;
+  HE_TRY(h, cudaMemcpy(host_scores, h->score, (size_t)h->U * h->cfg.budget * sizeof(float),
+                       cudaMemcpyDeviceToHost));
+  return HE_OK;
+}
+
 int he_occupancy(he_handle h, int32_t* occupancy) {
   if (!h || !occupancy) return HE_EINVAL;
   *occupancy = h->occupancy;
@@ -650,6 +680,7 @@ int he_step_bytes(he_handle h, uint64_t* bytes) {
            + Bt * H * D * e + U * 2 * D * e  // q, k, v in
            + Bt * H * D * 4                // out
            + D * (uint64_t)h->cfg.bits * e;  // W
+  if (h->score) *bytes += U * B * 2 * sizeof(float);  // scores read and written
   return HE_OK;
 }
 

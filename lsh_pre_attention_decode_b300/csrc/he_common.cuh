@@ -55,6 +55,9 @@ struct StepParams {
   int32_t code_stride;   // bytes per unit row of codes (multiple of 16)
   int32_t append_slot;   // -1: cache full, evict; else the slot the token is appended to
   float qscale;          // log2(e) / sqrt(D): logits kept in base 2
+  float tau;             // binarisation threshold: bit = (projection > tau)
+  float decay;           // score memory gamma (with score != nullptr)
+  float* score;          // per-slot scores [U][budget] (null: evict by the step's distances)
   // bf16 pipeline: per-unit results, the parity of this step's eviction key,
   // and the slot the previous step of this cache wrote: 0 none (or not
   // tracked), s + 1 appended at slot s, -1 evicted (slot in the other key)
@@ -132,7 +135,7 @@ __device__ __forceinline__ uint32_t group_distance(const uint64_t (&cq)[G], uint
 template <int G, int WB>
 __device__ __forceinline__ uint64_t scan_codes_w(const unsigned char* row, int lo, int hi,
                                                  const uint64_t (&cq)[G], int tid, int nthreads,
-                                                 int32_t* dist_out) {
+                                                 int32_t* dist_out, float* score, float decay) {
   constexpr int PER = 16 / WB;
   const int c0 = (lo * WB) >> 4;
   const int c1 = (hi * WB + 15) >> 4;
@@ -152,7 +155,13 @@ __device__ __forceinline__ uint64_t scan_codes_w(const unsigned char* row, int l
       if (s >= lo && s < hi) {
         const uint32_t dist = group_distance<G>(cq, code);
         if (dist_out) dist_out[s] = (int32_t)dist;
-        const uint64_t key = evict_key(dist, (uint32_t)s);
+        uint32_t rank = dist;
+        if (score) {  // score memory: A = gamma A + d; a non-negative fp32 orders as its bits
+          const float a = __fmaf_rn(decay, score[s], (float)dist);
+          score[s] = a;
+          rank = __float_as_uint(a);
+        }
+        const uint64_t key = evict_key(rank, (uint32_t)s);
         best = key > best ? key : best;
       }
     }
@@ -163,12 +172,13 @@ __device__ __forceinline__ uint64_t scan_codes_w(const unsigned char* row, int l
 template <int G>
 __device__ __forceinline__ uint64_t scan_codes(const unsigned char* row, int bits, int lo, int hi,
                                                const uint64_t (&cq)[G], int tid, int nthreads,
-                                               int32_t* dist_out) {
+                                               int32_t* dist_out, float* score = nullptr,
+                                               float decay = 0.0f) {
   switch (bits) {
-    case 8: return scan_codes_w<G, 1>(row, lo, hi, cq, tid, nthreads, dist_out);
-    case 16: return scan_codes_w<G, 2>(row, lo, hi, cq, tid, nthreads, dist_out);
-    case 32: return scan_codes_w<G, 4>(row, lo, hi, cq, tid, nthreads, dist_out);
-    default: return scan_codes_w<G, 8>(row, lo, hi, cq, tid, nthreads, dist_out);
+    case 8: return scan_codes_w<G, 1>(row, lo, hi, cq, tid, nthreads, dist_out, score, decay);
+    case 16: return scan_codes_w<G, 2>(row, lo, hi, cq, tid, nthreads, dist_out, score, decay);
+    case 32: return scan_codes_w<G, 4>(row, lo, hi, cq, tid, nthreads, dist_out, score, decay);
+    default: return scan_codes_w<G, 8>(row, lo, hi, cq, tid, nthreads, dist_out, score, decay);
   }
 }
 
@@ -178,8 +188,8 @@ __device__ __forceinline__ uint64_t scan_codes(const unsigned char* row, int bit
 // ballots.  Run by the first NT threads; ends with a group barrier.
 template <typename T, int D, int G, int NT, int BAR>
 __device__ __forceinline__ void code_queries_and_key(const float* s_q, const float* s_k,
-                                                     const T* W, int bits, bool with_queries,
-                                                     Misc& m, int tid) {
+                                                     const T* W, int bits, float tau,
+                                                     bool with_queries, Misc& m, int tid) {
   const int lane = tid & 31, warp = tid >> 5;
   const int ntask = (G + 1) * bits;
   for (int t0 = warp * 32; t0 < ntask; t0 += NT) {
@@ -188,9 +198,9 @@ __device__ __forceinline__ void code_queries_and_key(const float* s_q, const flo
     if (t < ntask) {
       const int h = t / bits, j = t - h * bits;
       if (h == G)
-        bit = projection_bit<T, D>(s_k, W, bits, j);
+        bit = projection_bit<T, D>(s_k, W, bits, j, tau);
       else if (with_queries)
-        bit = projection_bit<T, D>(s_q + h * D, W, bits, j);
+        bit = projection_bit<T, D>(s_q + h * D, W, bits, j, tau);
     }
     const uint32_t word = __ballot_sync(kFull, bit);
     if (lane == 0) m.bits[t0 >> 5] = word;
@@ -224,7 +234,7 @@ __device__ __forceinline__ void unit_prologue(const StepParams& p, int u, float*
     if (lane == 0) m.lnew[g] = a * p.qscale;
   }
   code_queries_and_key<T, D, G, NT, BAR>(s_q, s_k, reinterpret_cast<const T*>(p.W), p.bits,
-                                         p.append_slot < 0, m, tid);
+                                         p.tau, p.append_slot < 0, m, tid);
 }
 
 // Local eviction candidate over slots [lo, hi) of unit u -> m.cand_slot/dist;
@@ -237,7 +247,8 @@ __device__ __forceinline__ void local_candidate(const StepParams& p, int u, int 
 #pragma unroll
   for (int g = 0; g < G; ++g) cq[g] = m.cq[g];
   uint64_t best = scan_codes<G>(p.codes + (size_t)u * p.code_stride, p.bits, lo, hi, cq, tid, NT,
-                                nullptr);
+                                nullptr, p.score ? p.score + (size_t)u * p.budget : nullptr,
+                                p.decay);
   best = warp_max_u64(best);
   if (lane == 0) m.red64[warp] = best;
   group_sync<NT, BAR>();
@@ -420,6 +431,7 @@ __device__ void combine_unit(const StepParams& p, int u, int first, int n, Misc&
   if (tid == 0) {
     store_code(p.codes + (size_t)u * p.code_stride + (size_t)winner * (p.bits >> 3), p.bits,
                m.codek);
+    if (p.score) p.score[(size_t)u * p.budget + winner] = 0.0f;  // not scored yet
     p.evicted[u] = full ? winner : -1;
     p.counters[u] = 0;
   }
@@ -466,7 +478,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kAuxThreads) code_kernel(const T* __restrict__ x, int64_t rows,
                                                            int64_t per_unit, int64_t x_unit_rows,
                                                            const T* __restrict__ W, int bits,
-                                                           unsigned char* out,
+                                                           float tau, unsigned char* out,
                                                            int64_t out_unit_bytes) {
   __shared__ float xs[kAuxThreads / 8][D];  // up to 32 vectors (bits = 8)
   __shared__ uint32_t sbits[kAuxThreads / 32];
@@ -485,7 +497,7 @@ __global__ void __launch_bounds__(kAuxThreads) code_kernel(const T* __restrict__
     }
     __syncthreads();
     const int vi = tid / bits, j = tid - vi * bits;
-    const uint32_t bit = (r0 + vi < rows) ? projection_bit<T, D>(xs[vi], W, bits, j) : 0u;
+    const uint32_t bit = (r0 + vi < rows) ? projection_bit<T, D>(xs[vi], W, bits, j, tau) : 0u;
     const uint32_t word = __ballot_sync(kFull, bit);
     if (lane == 0) sbits[warp] = word;
     __syncthreads();
@@ -514,7 +526,7 @@ __global__ void __launch_bounds__(kAuxThreads) score_kernel(const StepParams p, 
   for (int i = tid; i < D; i += kAuxThreads) s_k[i] = 0.0f;
   __syncthreads();
   code_queries_and_key<T, D, G, kAuxThreads, 0>(s_q, s_k, reinterpret_cast<const T*>(p.W),
-                                                p.bits, true, m, tid);
+                                                p.bits, p.tau, true, m, tid);
   uint64_t cq[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) cq[g] = m.cq[g];

@@ -105,16 +105,18 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 // ---------------------------------------------------------------------------
 // Method steps 1-2 for one bit: the projection of x onto column j of W, summed
 // in fp32 with fused multiply-adds in the fixed order d = 0..D-1 from +0, and
-// the sign test (an exact zero gives 0).  x is staged in shared memory as fp32
+// test against the threshold tau (with tau = 0, the sign test: an exact zero
+// gives 0).  x is staged in shared memory as fp32
 // (exact copies of the stored elements).
 // ---------------------------------------------------------------------------
 template <typename T, int D>
 __device__ __forceinline__ uint32_t projection_bit(const float* __restrict__ x,
-                                                   const T* __restrict__ W, int bits, int j) {
+                                                   const T* __restrict__ W, int bits, int j,
+                                                   float tau) {
   float acc = 0.0f;
 #pragma unroll 16
   for (int d = 0; d < D; ++d) acc = __fmaf_rn(x[d], ldg_f32(W + (size_t)d * bits + j), acc);
-  return acc > 0.0f ? 1u : 0u;
+  return acc > tau ? 1u : 0u;
 }
 
 // Extract the `bits`-bit code number `idx` from a packed bit string (32-bit words).

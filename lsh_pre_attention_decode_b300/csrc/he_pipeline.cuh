@@ -78,10 +78,11 @@ struct PrepShape {
   static constexpr int SMEM = OFF_BAR + 16;
 };
 
-// One CTA per SM at most: a CTA takes the (unit, code chunk) items
+// MEM: score memory (p.score, p.decay), a separate instantiation because its
+// register use is higher.  One CTA per SM at most: a CTA takes the (unit, code chunk) items
 // blockIdx.x, blockIdx.x + gridDim.x, ... in turn, so that prep never crowds
 // the stream kernel's CTAs off an SM.
-template <int D, int G>
+template <int D, int G, bool MEM>
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, UnitOut* uo,
                                                             int splits, int first_of_step) {
   using S = PrepShape<D, G>;
@@ -158,7 +159,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
         for (int d = 0; d < D; ++d)
           acc = __fmaf_rn(__uint_as_float((uint32_t)x[d] << 16),
                           __uint_as_float((uint32_t)Ws[d * bits + jj] << 16), acc);
-        bit = acc > 0.0f ? 1u : 0u;
+        bit = acc > p.tau ? 1u : 0u;
       }
       const uint32_t word = __ballot_sync(kFull, bit);
       if (lane == 0) sbits[t0 >> 5] = word;
@@ -183,17 +184,46 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
 #pragma unroll
       for (int g = 0; g < G; ++g) cq[g] = code_from_bits(sbits, bits, g);
       uint64_t best = 0;
-      for (int s = s0 + tid; s < s1; s += kPrepThreads) {
+      auto code_at = [&](int s) -> uint64_t {
         const unsigned char* c = cs + (size_t)(s - s0) * wb;
-        uint64_t code;
         switch (wb) {
-          case 1: code = *c; break;
-          case 2: code = *reinterpret_cast<const uint16_t*>(c); break;
-          case 4: code = *reinterpret_cast<const uint32_t*>(c); break;
-          default: code = *reinterpret_cast<const uint64_t*>(c); break;
+          case 1: return *c;
+          case 2: return *reinterpret_cast<const uint16_t*>(c);
+          case 4: return *reinterpret_cast<const uint32_t*>(c);
+          default: return *reinterpret_cast<const uint64_t*>(c);
         }
-        const uint64_t key = evict_key(group_distance<G>(cq, code), (uint32_t)s);
-        best = key > best ? key : best;
+      };
+      if constexpr (!MEM) {  // (the method: 32 registers, so prep fits beside two stream CTAs)
+        for (int s = s0 + tid; s < s1; s += kPrepThreads) {
+          const uint64_t key = evict_key(group_distance<G>(cq, code_at(s)), (uint32_t)s);
+          best = key > best ? key : best;
+        }
+      } else {
+        // score memory: A = gamma A + d (a non-negative fp32 orders as its bits).
+        // The scores of a batch of this thread's slots are all loaded before any
+        // is used (one memory round trip per batch).
+        constexpr int NB = 16;
+        constexpr int IT = kPrepChunk / kPrepThreads;
+        static_assert(IT % NB == 0, "score batches");
+        float* sc = p.score + (size_t)u * p.budget;
+        for (int i0 = 0; i0 < IT; i0 += NB) {
+          float a[NB];
+#pragma unroll
+          for (int i = 0; i < NB; ++i) {
+            const int s = s0 + tid + (i0 + i) * kPrepThreads;
+            a[i] = s < s1 ? __ldcg(sc + s) : 0.0f;
+          }
+#pragma unroll
+          for (int i = 0; i < NB; ++i) {
+            const int s = s0 + tid + (i0 + i) * kPrepThreads;
+            if (s < s1) {
+              const float v = __fmaf_rn(p.decay, a[i], (float)group_distance<G>(cq, code_at(s)));
+              sc[s] = v;
+              const uint64_t key = evict_key(__float_as_uint(v), (uint32_t)s);
+              best = key > best ? key : best;
+            }
+          }
+        }
       }
       best = warp_max_u64(best);
       if (lane == 0) red[warp] = best;
@@ -941,6 +971,7 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
     store_code(p.codes + (size_t)u * p.code_stride + (size_t)winner * (p.bits >> 3), p.bits,
                codek);
     p.evicted[u] = full ? winner : -1;
+    if (p.score != nullptr) p.score[(size_t)u * p.budget + winner] = 0.0f;  // not scored yet
     uo[u].key[p.kpar ^ 1] = 0;  // ready for the next step's atomicMax
     if (recomputed) atomicAdd(p.counters + u, 1);  // how often the exact path ran
   }

@@ -51,7 +51,7 @@ def test_strerror(L):
 
 def cfg(**kw):
     d = dict(batch=1, heads=32, kv_heads=8, head_dim=128, bits=32, budget=256, dtype=0,
-             reserved=0, seed=1)
+             threshold=0.0, seed=1, decay=0.0, reserved=0)
     d.update(kw)
     return pkg.HeCfg(**d)
 
@@ -60,7 +60,9 @@ def cfg(**kw):
                                  dict(bits=128), dict(budget=0), dict(budget=(1 << 24) + 1),
                                  dict(head_dim=96), dict(head_dim=256), dict(dtype=2),
                                  dict(heads=64, kv_heads=4), dict(reserved=1),
-                                 dict(batch=70000)])
+                                 dict(batch=70000), dict(decay=-0.5), dict(decay=1.5),
+                                 dict(decay=float("nan")), dict(threshold=float("inf")),
+                                 dict(threshold=float("nan"))])
 def test_create_rejects_bad_configs(L, bad):
     h = ctypes.c_void_p()
     assert L.he_create(ctypes.byref(cfg(**bad)), ctypes.byref(h)) == -1
@@ -82,6 +84,7 @@ def test_null_arguments_are_rejected(L):
     assert L.he_step_bytes(None, None) == -1
     assert L.he_launch_info(None, None, None, None, None) == -1
     assert L.he_recompute_count(None, None) == -1
+    assert L.he_read_scores(None, None) == -1
 
 
 def test_python_errors_raise(L):
