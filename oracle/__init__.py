@@ -73,6 +73,8 @@ class UnitState:
     occupancy: int
     tau: float = 0.0
     score: np.ndarray | None = None
+    Vq: np.ndarray | None = None     # quantised value cache: int8 [budget][D] ...
+    Vs: np.ndarray | None = None     # ... and one fp32 scale per row (then V is unused)
 
 
 class Oracle:
@@ -95,6 +97,17 @@ class Oracle:
                                             _vp, _vp, _i32, _vp, _vp, _vp, ctypes.c_float,
                                             ctypes.c_float, _vp, _vp, _vp, _vp, _vp]
         lib.orc_unit_stream_ext.restype = None
+        lib.orc_quantize_row.argtypes = [_vp, _i32, _i32, _vp, _vp]
+        lib.orc_quantize_row.restype = None
+        lib.orc_attend_vq.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp]
+        lib.orc_attend_vq.restype = None
+        lib.orc_unit_fill_vq.argtypes = [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _i32,
+                                         ctypes.c_float, _vp, _vp, _vp, _vp, _vp]
+        lib.orc_unit_fill_vq.restype = None
+        lib.orc_unit_stream_vq.argtypes = [_vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp,
+                                           _vp, _vp, _i32, _vp, _vp, _vp, ctypes.c_float,
+                                           ctypes.c_float, _vp, _vp, _vp, _vp]
+        lib.orc_unit_stream_vq.restype = None
         lib.orc_group_distance.argtypes = [_vp, _i32, _u64]
         lib.orc_group_distance.restype = _i32
         lib.orc_most_dissimilar.argtypes = [_vp, _i32]
@@ -145,6 +158,29 @@ class Oracle:
         a = np.ascontiguousarray(score, np.float32)
         return int(self.lib.orc_most_dissimilar_score(_ptr(a), a.size))
 
+    # -- quantised values ----------------------------------------------------
+    def quantize_rows(self, v: np.ndarray):
+        """int8 rows and fp32 scales of v [n][D] (bf16 bits or fp32)."""
+        v2 = np.ascontiguousarray(v.reshape(-1, v.shape[-1]))
+        n, D = v2.shape
+        q = np.empty((n, D), np.int8)
+        sc = np.empty(n, np.float32)
+        row = D * v2.itemsize
+        for i in range(n):
+            self.lib.orc_quantize_row(ctypes.c_void_p(v2.ctypes.data + i * row), _dtype_code(v2), D,
+                                      ctypes.c_void_p(q.ctypes.data + i * D),
+                                      ctypes.c_void_p(sc.ctypes.data + 4 * i))
+        return q, sc
+
+    def attend_vq(self, q: np.ndarray, K: np.ndarray, Vq: np.ndarray, Vs: np.ndarray) -> np.ndarray:
+        q2 = np.ascontiguousarray(q.reshape(-1, q.shape[-1]))
+        K2, Vq2, Vs2 = (np.ascontiguousarray(a) for a in (K, Vq, Vs))
+        G, D = q2.shape
+        out = np.empty((G, D), np.float64)
+        self.lib.orc_attend_vq(_ptr(q2), _ptr(K2), _ptr(Vq2), _ptr(Vs2), K2.shape[0], D, G,
+                               _dtype_code(q2), _ptr(out))
+        return out
+
     # -- attention -----------------------------------------------------------
     def attend(self, q: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
         """fp64 softmax(q K^T / sqrt(D)) V for q [G][D], K, V [n][D]."""
@@ -159,12 +195,26 @@ class Oracle:
 
     # -- one (batch, KV head) unit -----------------------------------------
     def unit_fill(self, W: np.ndarray, budget: int, Kin: np.ndarray, Vin: np.ndarray,
-                  tau: float = 0.0, memory: bool = False) -> UnitState:
+                  tau: float = 0.0, memory: bool = False, vq: bool = False) -> UnitState:
         """A unit filled with the rows of Kin, Vin.  ``memory``: keep per-slot
-        scores (zero after the fill) for streams with score memory."""
+        scores (zero after the fill) for streams with score memory.  ``vq``:
+        a quantised value cache (int8 rows, one fp32 scale per row)."""
         n, D = Kin.shape
         if n > budget:
             raise ValueError("more fill tokens than the budget")
+        if vq:
+            K = np.zeros((budget, D), Kin.dtype)
+            Vq = np.zeros((budget, D), np.int8)
+            Vs = np.zeros(budget, np.float32)
+            codes = np.zeros(budget, np.uint64)
+            occ = np.zeros(1, np.int32)
+            Kc, Vc, Wc = (np.ascontiguousarray(a) for a in (Kin, Vin, W))
+            self.lib.orc_unit_fill_vq(_ptr(Wc), D, Wc.shape[1], _dtype_code(Kc), budget, _ptr(Kc),
+                                      _ptr(Vc), n, float(tau), _ptr(K), _ptr(Vq), _ptr(Vs),
+                                      _ptr(codes), _ptr(occ))
+            score = np.zeros(budget, np.float32) if memory else None
+            return UnitState(Wc, Wc.shape[1], budget, K, None, codes, int(occ[0]), float(tau),
+                             score, Vq, Vs)
         K = np.zeros((budget, D), Kin.dtype)
         V = np.zeros((budget, D), Kin.dtype)
         codes = np.zeros(budget, np.uint64)
@@ -201,7 +251,17 @@ class Oracle:
         out = np.empty((n_out, G, D), np.float64)
         dl = np.empty((T, st.budget), np.int32) if dist_log else None
         occ = np.array([st.occupancy], np.int32)
-        if st.score is None and st.tau == 0.0:
+        if st.Vq is not None:
+            if st.score is None and decay != 0.0:
+                raise ValueError("score memory needs a unit filled with memory=True")
+            self.lib.orc_unit_stream_vq(_ptr(st.W), D, G, st.bits, _dtype_code(qc), st.budget,
+                                        _ptr(st.K), _ptr(st.Vq), _ptr(st.Vs), _ptr(st.codes),
+                                        _ptr(st.score), _ptr(occ), T, _ptr(qc), _ptr(kc),
+                                        _ptr(vc), float(st.tau), float(decay), _ptr(evicted),
+                                        _ptr(written), _ptr(wo), _ptr(out))
+            if dist_log:
+                raise ValueError("no distance log for the quantised value cache")
+        elif st.score is None and st.tau == 0.0:
             if decay != 0.0:
                 raise ValueError("score memory needs a unit filled with memory=True")
             self.lib.orc_unit_stream(_ptr(st.W), D, G, st.bits, _dtype_code(qc), st.budget,

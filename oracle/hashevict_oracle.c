@@ -345,6 +345,130 @@ void orc_unit_stream_ext(const void* W, int32_t D, int32_t G, int32_t bits, int3
   free(code_q);
 }
 
+/* ------------------------------------------------------------------------- */
+/* Quantised value cache (int8 rows with one fp32 scale per row).             */
+/* Reading (the survey's "quantised V with bf16 K"; the value-compression     */
+/* remarks of the DASH-KV and TTKV pages): s = max_d |v_d| / 127 in fp32,     */
+/* q_d = v_d / s (fp32 division) rounded half to even, clamped to [-127, 127];*/
+/* a zero row has s = 0 and q = 0.  The stored value is q_d * s.  Keys stay   */
+/* in the element type: codes and logits are those of the method.            */
+/* ------------------------------------------------------------------------- */
+
+void orc_quantize_row(const void* v, int32_t dtype, int32_t D, int8_t* q, float* scale) {
+  float m = 0.0f;
+  for (int32_t d = 0; d < D; ++d) {
+    float a = fabsf(elem(v, dtype, (size_t)d));
+    if (a > m) m = a;
+  }
+#if ORACLE_MUTANT == 13 /* planted: scale by 128 */
+  float s = m / 128.0f;
+#else
+  float s = m / 127.0f;
+#endif
+  *scale = s;
+  for (int32_t d = 0; d < D; ++d) {
+    float r = 0.0f;
+    if (s > 0.0f) {
+      float x = elem(v, dtype, (size_t)d) / s;
+#if ORACLE_MUTANT == 14 /* planted: rounds half away from zero */
+      r = roundf(x);
+#else
+      r = nearbyintf(x); /* round half to even (default rounding mode) */
+#endif
+      if (r > 127.0f) r = 127.0f;
+      if (r < -127.0f) r = -127.0f;
+    }
+    q[d] = (int8_t)r;
+  }
+}
+
+/* Attention of G query heads over n rows with keys K (element type) and
+ * values q[s][d] * scale[s], in fp64. */
+void orc_attend_vq(const void* qv, const void* K, const int8_t* Vq, const float* Vs, int32_t n,
+                   int32_t D, int32_t G, int32_t dtype, double* out) {
+  double* logit = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+  const double scale = 1.0 / sqrt((double)D);
+  for (int32_t g = 0; g < G; ++g) {
+    double m = -INFINITY;
+    for (int32_t s = 0; s < n; ++s) {
+      double dot = 0.0;
+      for (int32_t d = 0; d < D; ++d)
+        dot += (double)elem(qv, dtype, (size_t)g * D + d) *
+               (double)elem(K, dtype, (size_t)s * D + d);
+      logit[s] = dot * scale;
+      if (logit[s] > m) m = logit[s];
+    }
+    double den = 0.0;
+    for (int32_t s = 0; s < n; ++s) den += exp(logit[s] - m);
+    for (int32_t d = 0; d < D; ++d) {
+      double num = 0.0;
+      for (int32_t s = 0; s < n; ++s)
+        num += exp(logit[s] - m) * (double)Vq[(size_t)s * D + d] * (double)Vs[s];
+      out[(size_t)g * D + d] = n > 0 ? num / den : 0.0;
+    }
+  }
+  free(logit);
+}
+
+/* Fill of a unit with a quantised value cache: K copied, V quantised row by row. */
+void orc_unit_fill_vq(const void* W, int32_t D, int32_t bits, int32_t dtype, int32_t budget,
+                      const void* Kin, const void* Vin, int32_t n, float tau, void* K,
+                      int8_t* Vq, float* Vs, uint64_t* codes, int32_t* occupancy) {
+  size_t row = (size_t)D * elem_bytes(dtype);
+  (void)budget;
+  memcpy(K, Kin, row * (size_t)n);
+  for (int32_t s = 0; s < n; ++s) {
+    orc_quantize_row((const char*)Vin + (size_t)s * row, dtype, D, Vq + (size_t)s * D, Vs + s);
+    codes[s] = orc_code_tau((const char*)Kin + (size_t)s * row, dtype, D, W, bits, tau);
+  }
+  *occupancy = n;
+}
+
+/* The step with a quantised value cache: as orc_unit_stream_ext, but the new
+ * token's value is quantised when written and attention reads q * scale. */
+void orc_unit_stream_vq(const void* W, int32_t D, int32_t G, int32_t bits, int32_t dtype,
+                        int32_t budget, void* K, int8_t* Vq, float* Vs, uint64_t* codes,
+                        float* score, int32_t* occupancy, int32_t nsteps, const void* q,
+                        const void* k, const void* v, float tau, float decay, int32_t* evicted,
+                        int32_t* written, const uint8_t* want_out, double* out) {
+  size_t row = (size_t)D * elem_bytes(dtype);
+  int32_t* dist = (int32_t*)malloc(sizeof(int32_t) * (size_t)budget);
+  uint64_t* code_q = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)G);
+  size_t n_out = 0;
+  for (int32_t t = 0; t < nsteps; ++t) {
+    const char* qt = (const char*)q + (size_t)t * (size_t)G * row;
+    const char* kt = (const char*)k + (size_t)t * row;
+    const char* vt = (const char*)v + (size_t)t * row;
+    int32_t slot;
+    if (*occupancy == budget) {
+      for (int32_t g = 0; g < G; ++g)
+        code_q[g] = orc_code_tau(qt + (size_t)g * row, dtype, D, W, bits, tau);
+      for (int32_t s = 0; s < budget; ++s) dist[s] = orc_group_distance(code_q, G, codes[s]);
+      if (score) {
+        for (int32_t s = 0; s < budget; ++s) score[s] = fmaf(decay, score[s], (float)dist[s]);
+        slot = orc_most_dissimilar_score(score, budget);
+      } else {
+        slot = orc_most_dissimilar(dist, budget);
+      }
+      evicted[t] = slot;
+    } else {
+      slot = *occupancy;
+      *occupancy += 1;
+      evicted[t] = -1;
+    }
+    written[t] = slot;
+    memcpy((char*)K + (size_t)slot * row, kt, row);
+    orc_quantize_row(vt, dtype, D, Vq + (size_t)slot * D, Vs + slot);
+    codes[slot] = orc_code_tau(kt, dtype, D, W, bits, tau);
+    if (score) score[slot] = 0.0f;
+    if (!want_out || want_out[t])
+      orc_attend_vq(qt, K, Vq, Vs, *occupancy, D, G, dtype,
+                    out + (n_out++) * (size_t)G * (size_t)D);
+  }
+  free(dist);
+  free(code_q);
+}
+
 /* The method as described: threshold 0, the step's own distances. */
 void orc_unit_stream(const void* W, int32_t D, int32_t G, int32_t bits, int32_t dtype,
                      int32_t budget, void* K, void* V, uint64_t* codes, int32_t* occupancy,

@@ -96,6 +96,16 @@ def read_decay_case():
     return c
 
 
+def read_vquant_rows():
+    rows = []
+    for tok in _lines("vquant_hand.txt"):
+        if tok[0] == "row":
+            i_s, i_q = tok.index("scale"), tok.index("q")
+            rows.append(([float(t) for t in tok[1:i_s]], float(tok[i_s + 1]),
+                         [int(t) for t in tok[i_q + 1:]]))
+    return rows
+
+
 def read_attention_cases():
     cases, cur = [], None
     for tok in _lines("attention_hand.txt"):
@@ -438,10 +448,63 @@ def check_decay_zero_is_per_step(o):
         assert np.array_equal(ra["out"], rb["out"]) and np.array_equal(a.codes, b.codes)
 
 
+def check_vquant_hand(o):
+    """int8 value rows (tests/golden/vquant_hand.txt): scales and half-to-even
+    rounding."""
+    for v, scale, q in read_vquant_rows():
+        qq, ss = o.quantize_rows(f32([v]))
+        assert float(ss[0]) == scale and qq[0].tolist() == q, (v, ss, qq)
+
+
+def check_vquant_attention(o):
+    """Attention over a quantised value cache equals fp64 attention over the
+    dequantised rows q * s (uniform logits: their mean; random: the pinned fp64
+    attention on fp32 rows q * s, to fp32 rounding)."""
+    rng = np.random.default_rng(44)
+    D, n, G = 16, 11, 2
+    v = f32(rng.standard_normal((n, D)) * 3)
+    q8, sc = o.quantize_rows(v)
+    deq = q8.astype(np.float64) * sc.astype(np.float64)[:, None]
+    K = f32(rng.standard_normal((n, D)))
+    out = o.attend_vq(f32(np.zeros((G, D))), K, q8, sc)
+    assert np.allclose(out, deq.mean(0)[None].repeat(G, 0), rtol=0, atol=1e-12)
+    qv = f32(rng.standard_normal((G, D)))
+    ref = o.attend(qv, K, f32(deq))
+    assert np.allclose(o.attend_vq(qv, K, q8, sc), ref, rtol=0, atol=1e-5)
+    # every stored value is within half a step of the input, and the row maximum is exact
+    assert np.all(np.abs(deq - v) <= 0.5 * sc[:, None] * (1 + 1e-6))
+
+
+def check_vquant_stream(o):
+    """A quantised value cache evicts exactly as the method (codes come from
+    the keys) and attends over the retained keys with q * s values."""
+    rng = np.random.default_rng(45)
+    for dtype in ("fp32", "bf16"):
+        D, bits, G, B, T = 16, 8, 2, 7, 14
+        W = o.projection(7, D, bits, dtype)
+        cast = f32 if dtype == "fp32" else bf16_bits
+        K0, V0 = cast(rng.standard_normal((5, D))), cast(rng.standard_normal((5, D)))
+        q, k, v = (cast(rng.standard_normal(sh)) for sh in ((T, G, D), (T, D), (T, D)))
+        a = o.unit_fill(W, B, K0, V0)
+        b = o.unit_fill(W, B, K0, V0, vq=True)
+        ra = o.unit_stream(a, q, k, v)
+        rb = o.unit_stream(b, q, k, v)
+        assert ra["evicted"].tolist() == rb["evicted"].tolist()
+        assert np.array_equal(a.codes, b.codes) and np.array_equal(a.K, b.K)
+        qa, sa = o.quantize_rows(a.V)
+        assert np.array_equal(qa[:a.occupancy], b.Vq[:b.occupancy])
+        assert np.array_equal(sa[:a.occupancy], b.Vs[:b.occupancy])
+        deq = f32(qa.astype(np.float64) * sa.astype(np.float64)[:, None])
+        exact = (lambda x: x) if dtype == "fp32" else (lambda x: f32(bf16_to_f64(x)))
+        last = o.attend(exact(q[-1]), exact(a.K[:a.occupancy]), deq[:a.occupancy])
+        assert np.allclose(rb["out"][-1], last, rtol=0, atol=1e-5)
+
+
 ALL_CHECKS = [
     check_codes_hand, check_codes_identity_sign, check_codes_invariances, check_projection_moments,
     check_distance_brute, check_argmax_ties, check_eviction_hand, check_special_cases,
     check_stream_invariants, check_attention_hand, check_attention_closed_forms,
     check_attention_bf16_elements, check_codes_tau_hand, check_codes_tau_monotone,
-    check_decay_hand, check_decay_zero_is_per_step,
+    check_decay_hand, check_decay_zero_is_per_step, check_vquant_hand, check_vquant_attention,
+    check_vquant_stream,
 ]

@@ -19,6 +19,8 @@ MUTANTS = {
     10: "the written slot keeps the evicted token's score",
     11: "binarisation threshold with the wrong sign",
     12: "score ties go to the highest slot",
+    13: "value rows scaled by max / 128",
+    14: "value rows rounded half away from zero",
 }
 
 
