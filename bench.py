@@ -61,6 +61,8 @@ def parse_args():
                     help="binarisation threshold tau (0: the sign test of the method)")
     ap.add_argument("--decay", type=float, default=0.0,
                     help="score memory gamma (0: the step's own distances, the method)")
+    ap.add_argument("--v-int8", action="store_true",
+                    help="int8 value cache with one scale per slot (keys stay bf16)")
     ap.add_argument("--graph-ring", type=int, default=64,
                     help="tokens per layer in the captured step graph (even)")
     ap.add_argument("--e2e-steps", type=int, default=400)
@@ -170,7 +172,8 @@ def workload_from(args) -> synth.Workload:
 def config_of(w: synth.Workload, args, extra=None):
     c = {"workload": f"{w.name}: {w.description}" + (
             f"; threshold {args.threshold}, score memory {args.decay}"
-            if (args.threshold or args.decay) else ""),
+            if (args.threshold or args.decay) else "") + (
+            "; int8 value cache" if args.v_int8 else ""),
          "batch": w.batch, "heads": w.heads,
          "kv_heads": w.kv_heads, "head_dim": w.head_dim, "bits": w.bits, "budget": w.budget,
          "prompt": w.prompt, "dtype": w.dtype,
@@ -186,7 +189,7 @@ def config_of(w: synth.Workload, args, extra=None):
 # ---------------------------------------------------------------------------
 
 def run_cpu_baseline(w: synth.Workload, target_s: float, steps: int | None = None,
-                     threshold: float = 0.0, decay: float = 0.0):
+                     threshold: float = 0.0, decay: float = 0.0, v_int8: bool = False):
     """Times the CPU oracle, as it stands, on a bounded sample of the workload.
 
     The unit of work is a unit-step: one streamed token through one (batch, KV
@@ -210,7 +213,7 @@ def run_cpu_baseline(w: synth.Workload, target_s: float, steps: int | None = Non
         b, j = u
         return o.unit_fill(W, w.budget, synth.host_unit_kv(w, "key", b, j, 0, w.budget),
                            synth.host_unit_kv(w, "value", b, j, 0, w.budget), tau=threshold,
-                           memory=decay > 0.0)
+                           memory=decay > 0.0, vq=v_int8)
 
     def run(u, st, t0, n):
         b, j = u
@@ -276,7 +279,7 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     for layer in layers:
         he = HashEvict(w.batch, w.heads, w.kv_heads, w.head_dim, w.bits, w.budget, w.dtype,
                        seed=w.projection_seed(layer), threshold=args.threshold,
-                       decay=args.decay)
+                       decay=args.decay, v_int8=args.v_int8)
         K = synth.gpu_kv(w, "key", 0, w.budget, layer)
         V = synth.gpu_kv(w, "value", 0, w.budget, layer)
         he.fill(K, V)
@@ -423,7 +426,10 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     eb = 2 if w.dtype == "bf16" else 4
     occ = w.budget
     U = w.batch * w.kv_heads
-    stream_bytes = U * occ * 2 * w.head_dim * eb  # K and V rows of every resident slot
+    # K and V rows of every resident slot (int8 value rows and their scales with
+    # an int8 value cache)
+    stream_bytes = U * occ * (w.head_dim * eb + (w.head_dim + 4 if args.v_int8
+                                                   else w.head_dim * eb))
     achieved = stream_bytes / (stream_ms / 1e3) / 1e9
     step_gbs = step_bytes / (elapsed_ms / K / 1e3) / 1e9
     launches_per_step = 3 if w.dtype == "bf16" else 1
@@ -490,7 +496,8 @@ def main():
             return 0
         w = workload_from(args)
         val, cores, sample, el = run_cpu_baseline(w, args.ref_seconds, steps=args.steps,
-                                                  threshold=args.threshold, decay=args.decay)
+                                                  threshold=args.threshold, decay=args.decay,
+                                                  v_int8=args.v_int8)
         res = {
             "metric": "HashEvict decode steps/s (hash+evict+attend); achieved HBM GB/s vs B300 peak",
             "impl": "reference", "value": val, "unit": "steps/s", "n_gpus": 0,
@@ -518,7 +525,8 @@ def main():
     if rank == 0:
         if not args.no_cpu_baseline:
             val, cores, sample, el = run_cpu_baseline(w, args.cpu_seconds,
-                                                      threshold=args.threshold, decay=args.decay)
+                                                      threshold=args.threshold, decay=args.decay,
+                                                      v_int8=args.v_int8)
             res["cpu_baseline"] = {"value": val, "unit": "steps/s", "cores": cores,
                                    "kind": "oracle", "sample": sample}
         print(json.dumps(res))

@@ -52,11 +52,14 @@ extern "C" {
 #define HE_DTYPE_BF16 0
 #define HE_DTYPE_FP32 1
 
+#define HE_VFMT_ELEM 0  /* values stored in the element type */
+#define HE_VFMT_INT8 1  /* values stored as int8 rows with one fp32 scale per slot (bf16 only) */
+
 /* Handle configuration.  Supported: head_dim in {64, 128};
  * G = heads / kv_heads in {1, 2, 4, 8}; bits in {8, 16, 32, 64};
  * 1 <= budget <= 2^24; batch * kv_heads <= 2^16; dtype HE_DTYPE_*;
- * threshold finite; 0 <= decay <= 1.  A zero-initialised tail (threshold 0,
- * decay 0) is the method as the paper describes it. */
+ * threshold finite; 0 <= decay <= 1; v_format HE_VFMT_*.  A zero-initialised
+ * tail (threshold 0, decay 0, v_format 0) is the method as the paper describes it. */
 typedef struct {
   int32_t batch;
   int32_t heads;     /* query heads */
@@ -74,7 +77,9 @@ typedef struct {
                         (d its group-summed Hamming distance); the largest A is
                         evicted (ties: lowest slot); a written or filled slot starts
                         at A = 0.  0 = the step's own distances (the paper's method) */
-  int32_t reserved;  /* must be 0 */
+  int32_t v_format;  /* HE_VFMT_ELEM, or HE_VFMT_INT8: each value row v is stored as
+                        q = v / s rounded half to even with s = max|v| / 127 (fp32), and
+                        attended as q * s; keys, codes and evictions are unchanged */
 } he_cfg;
 
 typedef struct he_ctx* he_handle;
@@ -116,7 +121,8 @@ int he_destroy(he_handle h);
 int he_last_evicted(he_handle h, int32_t* host_slots);
 
 /* Snapshot of the cache into host buffers (any may be NULL):
- * K, V [batch][kv_heads][budget][head_dim] (element type), codes
+ * K, V [batch][kv_heads][budget][head_dim] (element type; V int8 with an int8
+ * value cache), codes
  * [batch][kv_heads][budget] (bits/8-byte words), occupancy (one int).  Synchronises. */
 int he_read_state(he_handle h, void* K, void* V, void* codes, int32_t* occupancy);
 
@@ -138,6 +144,12 @@ int he_codes(he_handle h, const void* x, int32_t n, void* codes, void* stream);
  * dist device int32 [batch][kv_heads][budget] (slots >= occupancy get 0).
  * Errors: HE_EINVAL, HE_ENOTFILLED, HE_ECUDA. */
 int he_scores(he_handle h, const void* q, int32_t* dist, void* stream);
+
+/* Per-slot value scales of a handle with an int8 value cache (v_format
+ * HE_VFMT_INT8), host fp32 [batch][kv_heads][budget]; he_read_state then
+ * returns the value rows as int8 [batch][kv_heads][budget][head_dim].
+ * Synchronises.  Errors: HE_EINVAL (NULL arguments, or another value format). */
+int he_read_vscales(he_handle h, float* host_scales);
 
 /* Per-slot eviction scores A of a handle with score memory (decay > 0), host
  * fp32 [batch][kv_heads][budget] (slots >= occupancy hold 0).  Synchronises.

@@ -10,6 +10,8 @@ from ._build import LIB
 
 HE_DTYPE_BF16 = 0
 HE_DTYPE_FP32 = 1
+HE_VFMT_ELEM = 0
+HE_VFMT_INT8 = 1
 
 _i32 = ctypes.c_int32
 _vp = ctypes.c_void_p
@@ -18,7 +20,7 @@ _vp = ctypes.c_void_p
 class HeCfg(ctypes.Structure):
     _fields_ = [("batch", _i32), ("heads", _i32), ("kv_heads", _i32), ("head_dim", _i32),
                 ("bits", _i32), ("budget", _i32), ("dtype", _i32), ("threshold", ctypes.c_float),
-                ("seed", ctypes.c_uint64), ("decay", ctypes.c_float), ("reserved", _i32)]
+                ("seed", ctypes.c_uint64), ("decay", ctypes.c_float), ("v_format", _i32)]
 
 
 class HashEvictError(RuntimeError):
@@ -59,6 +61,7 @@ def lib() -> ctypes.CDLL:
         L.he_recompute_count.argtypes = [_vp, P(ctypes.c_int64)]
         L.he_attend_noalloc.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp]
         L.he_read_scores.argtypes = [_vp, _vp]
+        L.he_read_vscales.argtypes = [_vp, _vp]
         L.he_profile_start.argtypes = [_vp, _i32]
         L.he_profile_stop.argtypes = [_vp, P(ctypes.c_float), P(_i32)]
         L.he_strerror.argtypes = [ctypes.c_int]
@@ -66,7 +69,8 @@ def lib() -> ctypes.CDLL:
         for n in ("he_create", "he_fill", "he_step", "he_step_host", "he_destroy",
                   "he_last_evicted", "he_read_state", "he_get_projection", "he_codes", "he_scores",
                   "he_occupancy", "he_step_bytes", "he_launch_info", "he_recompute_count",
-                  "he_attend_noalloc", "he_profile_start", "he_profile_stop", "he_read_scores"):
+                  "he_attend_noalloc", "he_profile_start", "he_profile_stop", "he_read_scores",
+                  "he_read_vscales"):
             getattr(L, n).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -153,6 +157,10 @@ def he_occupancy(h: int) -> int:
     return o.value
 
 
+def he_read_vscales(h: int, host_scales) -> None:
+    _check("he_read_vscales", lib().he_read_vscales(h, _ptr(host_scales)))
+
+
 def he_read_scores(h: int, host_scores) -> None:
     _check("he_read_scores", lib().he_read_scores(h, _ptr(host_scores)))
 
@@ -201,11 +209,13 @@ class HashEvict:
 
     def __init__(self, batch: int, heads: int, kv_heads: int, head_dim: int, bits: int,
                  budget: int, dtype: str = "bf16", seed: int = 0, threshold: float = 0.0,
-                 decay: float = 0.0):
+                 decay: float = 0.0, v_int8: bool = False):
         self.cfg = HeCfg(batch=batch, heads=heads, kv_heads=kv_heads, head_dim=head_dim,
                          bits=bits, budget=budget,
                          dtype=HE_DTYPE_FP32 if dtype == "fp32" else HE_DTYPE_BF16,
-                         threshold=threshold, seed=seed, decay=decay, reserved=0)
+                         threshold=threshold, seed=seed, decay=decay,
+                         v_format=HE_VFMT_INT8 if v_int8 else HE_VFMT_ELEM)
+        self.v_int8 = v_int8
         self.dtype = dtype
         self.h = he_create(self.cfg)
 
@@ -258,11 +268,19 @@ class HashEvict:
         et = np.float32 if self.dtype == "fp32" else np.uint16
         ct = {8: np.uint8, 16: np.uint16, 32: np.uint32, 64: np.uint64}[c.bits]
         K = np.empty((c.batch, c.kv_heads, c.budget, c.head_dim), et)
-        V = np.empty_like(K)
+        V = np.empty(K.shape, np.int8 if self.v_int8 else et)
         codes = np.empty((c.batch, c.kv_heads, c.budget), ct)
         occ = np.zeros(1, np.int32)
         he_read_state(self.h, K, V, codes, occ)
         return K, V, codes, int(occ[0])
+
+    def vscales(self):
+        """Per-slot value scales [batch][kv_heads][budget] (int8 value cache only)."""
+        import numpy as np
+        c = self.cfg
+        a = np.empty((c.batch, c.kv_heads, c.budget), np.float32)
+        he_read_vscales(self.h, a)
+        return a
 
     def scores(self):
         """Per-slot eviction scores [batch][kv_heads][budget] (score memory only)."""

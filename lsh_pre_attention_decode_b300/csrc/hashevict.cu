@@ -42,6 +42,7 @@ struct Kernels {
   int tile;
   int rec_floats;
   bool tc;  // tensor-core pipeline (tensor maps, programmatic dependent launch)
+  const void* vq_fill;  // int8 value cache: quantisation of filled value rows
 };
 
 template <int D, int G>
@@ -51,17 +52,18 @@ int merge_cfg(int n, int* smem) {
   return t;
 }
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool VQ = false>
 Kernels kernels_for() {
   Kernels k{};
   k.score = reinterpret_cast<const void*>(&he::score_kernel<T, D, G>);
   k.code = reinterpret_cast<const void*>(&he::code_kernel<T, D>);
   if constexpr (std::is_same<T, bf16_t>::value) {
-    using S = he::StreamShape<D, G, kTcStages>;
-    k.step = reinterpret_cast<const void*>(&he::stream_kernel<D, G, kTcStages, kPSplit>);
-    k.prep = reinterpret_cast<const void*>(&he::prep_kernel<D, G, false>);
-    k.prep_mem = reinterpret_cast<const void*>(&he::prep_kernel<D, G, true>);
-    k.merge = reinterpret_cast<const void*>(&he::merge_kernel<D, G>);
+    using S = he::StreamShape<D, G, kTcStages, VQ>;
+    k.step = reinterpret_cast<const void*>(&he::stream_kernel<D, G, kTcStages, kPSplit, VQ>);
+    k.prep = reinterpret_cast<const void*>(&he::prep_kernel<D, G, false, VQ>);
+    k.prep_mem = reinterpret_cast<const void*>(&he::prep_kernel<D, G, true, VQ>);
+    k.merge = reinterpret_cast<const void*>(&he::merge_kernel<D, G, VQ>);
+    k.vq_fill = reinterpret_cast<const void*>(&he::vq_fill_kernel<D>);
     k.step_smem = S::SMEM_ALLOC;
     k.step_threads = S::NT;
     k.prep_smem = he::PrepShape<D, G>::SMEM;
@@ -100,22 +102,25 @@ cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaS
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-template <typename T, int D>
+template <typename T, int D, bool VQ = false>
 bool pick_g(int G, Kernels* k) {
   switch (G) {
-    case 1: *k = kernels_for<T, D, 1>(); return true;
-    case 2: *k = kernels_for<T, D, 2>(); return true;
-    case 4: *k = kernels_for<T, D, 4>(); return true;
-    case 8: *k = kernels_for<T, D, 8>(); return true;
+    case 1: *k = kernels_for<T, D, 1, VQ>(); return true;
+    case 2: *k = kernels_for<T, D, 2, VQ>(); return true;
+    case 4: *k = kernels_for<T, D, 4, VQ>(); return true;
+    case 8: *k = kernels_for<T, D, 8, VQ>(); return true;
     default: return false;
   }
 }
 
-bool pick_kernels(int dtype, int D, int G, Kernels* k) {
-  if (dtype == HE_DTYPE_BF16) {
+bool pick_kernels(int dtype, int D, int G, bool vq, Kernels* k) {
+  if (dtype == HE_DTYPE_BF16 && vq) {
+    if (D == 64) return pick_g<bf16_t, 64, true>(G, k);
+    if (D == 128) return pick_g<bf16_t, 128, true>(G, k);
+  } else if (dtype == HE_DTYPE_BF16) {
     if (D == 64) return pick_g<bf16_t, 64>(G, k);
     if (D == 128) return pick_g<bf16_t, 128>(G, k);
-  } else if (dtype == HE_DTYPE_FP32) {
+  } else if (dtype == HE_DTYPE_FP32 && !vq) {
     if (D == 64) return pick_g<float, 64>(G, k);
     if (D == 128) return pick_g<float, 128>(G, k);
   }
@@ -141,6 +146,29 @@ bool encode_cache_map(CUtensorMap* map, void* base, uint64_t rows, int D, int bo
   const cuuint32_t estr[2] = {1, 1};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D tensor map over an int8 value cache viewed as [rows][D] bytes; boxes of
+// one whole row (D bytes) x `box_rows` rows, no swizzle.
+bool encode_vq_map(CUtensorMap* map, void* base, uint64_t rows, int D, int box_rows) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)D};
+  const cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -189,6 +217,9 @@ struct he_ctx {
   unsigned char* codes = nullptr;
   int32_t* evicted = nullptr;
   float* score = nullptr;  // per-slot scores with score memory (decay > 0), else null
+  bool vq = false;         // int8 value cache: V holds int8 rows, vs their scales
+  float* vs = nullptr;     // [U][vs_stride]
+  int vs_stride = 0;       // budget rounded up to whole 64-slot tiles
   int32_t* counters = nullptr;
   int32_t* err = nullptr;
   float* partials = nullptr;
@@ -242,7 +273,7 @@ void free_profile(he_ctx* h) {
 void free_all(he_ctx* h) {
   free_profile(h);
   void* ptrs[] = {h->K, h->V, h->W, h->codes, h->evicted, h->counters, h->err, h->partials,
-                  h->score,
+                  h->score, h->vs,
                   h->uo, h->sq, h->sk, h->sv, h->sout};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -269,6 +300,8 @@ StepParams base_params(const he_ctx* h) {
   p.code_stride = h->code_stride;
   p.append_slot = h->occupancy < h->cfg.budget ? h->occupancy : -1;
   p.qscale = (float)(1.4426950408889634 / std::sqrt((double)h->cfg.head_dim));
+  p.vs = h->vs;
+  p.vs_stride = h->vs_stride;
   p.tau = h->cfg.threshold;
   p.decay = h->cfg.decay;
   p.score = h->score;
@@ -314,12 +347,15 @@ int he_create(const he_cfg* cfg, he_handle* out) {
   const he_cfg c = *cfg;
   if (c.batch < 1 || c.heads < 1 || c.kv_heads < 1 || c.heads % c.kv_heads != 0) return HE_EINVAL;
   if (c.bits != 8 && c.bits != 16 && c.bits != 32 && c.bits != 64) return HE_EINVAL;
-  if (c.budget < 1 || c.budget > (1 << 24) || c.reserved != 0) return HE_EINVAL;
+  if (c.budget < 1 || c.budget > (1 << 24)) return HE_EINVAL;
+  if (c.v_format != HE_VFMT_ELEM && !(c.v_format == HE_VFMT_INT8 && c.dtype == HE_DTYPE_BF16))
+    return HE_EINVAL;
   if (!std::isfinite(c.threshold) || !(c.decay >= 0.0f && c.decay <= 1.0f)) return HE_EINVAL;
   if ((int64_t)c.batch * c.kv_heads > 65536) return HE_EINVAL;
   const int G = c.heads / c.kv_heads;
   Kernels kern;
-  if (!pick_kernels(c.dtype, c.head_dim, G, &kern)) return HE_EINVAL;
+  const bool vq = c.v_format == HE_VFMT_INT8;
+  if (!pick_kernels(c.dtype, c.head_dim, G, vq, &kern)) return HE_EINVAL;
   const int64_t U = (int64_t)c.batch * c.kv_heads;
   if (U * ((c.budget + kern.tile - 1) / kern.tile) > INT32_MAX) return HE_EINVAL;
   if (U * c.budget >= ((int64_t)1 << 31)) return HE_EINVAL;  // TMA row coordinate
@@ -333,6 +369,8 @@ int he_create(const he_cfg* cfg, he_handle* out) {
   h->code_bytes = c.bits / 8;
   h->code_stride = (int)(((int64_t)c.budget * h->code_bytes + 15) / 16 * 16);
   h->kern = kern;
+  h->vq = vq;
+  h->vs_stride = (c.budget + 63) / 64 * 64;
   if (cudaGetDevice(&h->device) != cudaSuccess) {
     (void)cudaGetLastError();
     delete h;
@@ -373,10 +411,12 @@ int he_create(const he_cfg* cfg, he_handle* out) {
     // one spare tile of rows after the last unit keeps every tile load in bounds;
     // the cache starts zeroed so rows no token has written are finite
     const size_t cache = ((size_t)U * c.budget + kern.tile) * c.head_dim * h->eb;
+    const size_t vcache = vq ? ((size_t)U * c.budget + kern.tile) * c.head_dim : cache;
     const size_t nrec = (size_t)h->max_ctas + (size_t)U;
     struct { void** p; size_t bytes; } allocs[] = {
         {&h->K, cache},
-        {&h->V, cache},
+        {&h->V, vcache},
+        {(void**)&h->vs, vq ? (size_t)U * h->vs_stride * sizeof(float) : 0},
         {&h->W, (size_t)c.head_dim * c.bits * h->eb},
         {(void**)&h->codes, (size_t)U * h->code_stride},
         {(void**)&h->evicted, (size_t)U * sizeof(int32_t)},
@@ -395,7 +435,8 @@ int he_create(const he_cfg* cfg, he_handle* out) {
       }
     }
     if (rc != HE_OK) break;
-    if (cudaMemset(h->K, 0, cache) != cudaSuccess || cudaMemset(h->V, 0, cache) != cudaSuccess ||
+    if (cudaMemset(h->K, 0, cache) != cudaSuccess || cudaMemset(h->V, 0, vcache) != cudaSuccess ||
+        (vq && cudaMemset(h->vs, 0, (size_t)U * h->vs_stride * sizeof(float)) != cudaSuccess) ||
         cudaMemset(h->codes, 0, (size_t)U * h->code_stride) != cudaSuccess ||
         cudaMemset(h->counters, 0, (size_t)U * sizeof(int32_t)) != cudaSuccess ||
         cudaMemset(h->uo, 0, (size_t)U * sizeof(he::UnitOut)) != cudaSuccess ||
@@ -406,7 +447,8 @@ int he_create(const he_cfg* cfg, he_handle* out) {
     }
     const uint64_t rows = (uint64_t)U * c.budget + kern.tile;
     if (kern.tc && (!encode_cache_map(&h->tmK, h->K, rows, c.head_dim, kern.tile) ||
-                     !encode_cache_map(&h->tmV, h->V, rows, c.head_dim, kern.tile))) {
+                     !(vq ? encode_vq_map(&h->tmV, h->V, rows, c.head_dim, kern.tile)
+                          : encode_cache_map(&h->tmV, h->V, rows, c.head_dim, kern.tile)))) {
       rc = HE_ECUDA;
       break;
     }
@@ -449,8 +491,20 @@ int he_fill(he_handle h, const void* K, const void* V, int32_t n, void* stream) 
   if (n > 0) {
     HE_TRY(h, cudaMemcpy2DAsync(h->K, (size_t)h->cfg.budget * row, K, (size_t)n * row,
                                 (size_t)n * row, (size_t)h->U, cudaMemcpyDeviceToDevice, s));
-    HE_TRY(h, cudaMemcpy2DAsync(h->V, (size_t)h->cfg.budget * row, V, (size_t)n * row,
-                                (size_t)n * row, (size_t)h->U, cudaMemcpyDeviceToDevice, s));
+    if (h->vq) {  // value rows quantised into the int8 cache
+      const int64_t rows = (int64_t)h->U * n;
+      int64_t blocks = (rows + 7) / 8;
+      if (blocks > (int64_t)h->num_sms * 16) blocks = (int64_t)h->num_sms * 16;
+      int nn = n, budget = h->cfg.budget, vstride = h->vs_stride;
+      int8_t* Vq = reinterpret_cast<int8_t*>(h->V);
+      float* vs = h->vs;
+      void* args[] = {(void*)&V, (void*)&rows, (void*)&nn, (void*)&budget, (void*)&Vq,
+                      (void*)&vs, (void*)&vstride};
+      HE_TRY(h, cudaLaunchKernel(h->kern.vq_fill, dim3((unsigned)blocks), dim3(256), args, 0, s));
+    } else {
+      HE_TRY(h, cudaMemcpy2DAsync(h->V, (size_t)h->cfg.budget * row, V, (size_t)n * row,
+                                  (size_t)n * row, (size_t)h->U, cudaMemcpyDeviceToDevice, s));
+    }
     const int rc = launch_codes(h, h->K, (int64_t)h->U * n, n, h->cfg.budget, h->codes,
                                 h->code_stride, s);
     if (rc != HE_OK) return rc;
@@ -594,7 +648,7 @@ int he_read_state(he_handle h, void* K, void* V, void* codes, int32_t* occupancy
   if (rc != HE_OK) return rc;
   const size_t cache = (size_t)h->U * h->cfg.budget * h->cfg.head_dim * h->eb;
   if (K) HE_TRY(h, cudaMemcpy(K, h->K, cache, cudaMemcpyDeviceToHost));
-  if (V) HE_TRY(h, cudaMemcpy(V, h->V, cache, cudaMemcpyDeviceToHost));
+  if (V) HE_TRY(h, cudaMemcpy(V, h->V, h->vq ? cache / h->eb : cache, cudaMemcpyDeviceToHost));
   if (codes) {
     const size_t w = (size_t)h->cfg.budget * h->code_bytes;
     HE_TRY(h, cudaMemcpy2D(codes, w, h->codes, (size_t)h->code_stride, w, (size_t)h->U,
@@ -664,6 +718,19 @@ int he_read_scores(he_handle h, float* host_scores) {
   return HE_OK;
 }
 
+int he_read_vscales(he_handle h, float* host_scales) {
+  if (!h || !host_scales || !h->vq) return HE_EINVAL;
+  if (h->sticky) return h->sticky;
+  DeviceGuard g(h->device);
+  if (!g.ok) return fail_cuda(h, cudaErrorInvalidDevice);
+  const int rc = check_device_error(h);
+  if (rc != HE_OK) return rc;
+  const size_t w = (size_t)h->cfg.budget * sizeof(float);
+  HE_TRY(h, cudaMemcpy2D(host_scales, w, h->vs, (size_t)h->vs_stride * sizeof(float), w,
+                         (size_t)h->U, cudaMemcpyDeviceToHost));
+  return HE_OK;
+}
+
 int he_occupancy(he_handle h, int32_t* occupancy) {
   if (!h || !occupancy) return HE_EINVAL;
   *occupancy = h->occupancy;
@@ -675,8 +742,9 @@ int he_step_bytes(he_handle h, uint64_t* bytes) {
   const uint64_t U = (uint64_t)h->U, B = (uint64_t)h->cfg.budget, D = (uint64_t)h->cfg.head_dim;
   const uint64_t e = (uint64_t)h->eb, w = (uint64_t)h->code_bytes;
   const uint64_t Bt = (uint64_t)h->cfg.batch, H = (uint64_t)h->cfg.heads;
-  *bytes = U * B * (2 * D * e + w)        // retained K, V and codes read
-           + U * (2 * D * e + w)          // the overwritten slot
+  const uint64_t kv = h->vq ? D * e + D + 4 : 2 * D * e;  // bytes of one slot's key and value
+  *bytes = U * B * (kv + w)               // retained K, V and codes read
+           + U * (kv + w)                 // the overwritten slot
            + Bt * H * D * e + U * 2 * D * e  // q, k, v in
            + Bt * H * D * 4                // out
            + D * (uint64_t)h->cfg.bits * e;  // W

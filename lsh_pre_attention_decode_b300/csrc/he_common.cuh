@@ -58,6 +58,8 @@ struct StepParams {
   float tau;             // binarisation threshold: bit = (projection > tau)
   float decay;           // score memory gamma (with score != nullptr)
   float* score;          // per-slot scores [U][budget] (null: evict by the step's distances)
+  float* vs;             // int8 value cache: per-slot scales [U][vs_stride] (V holds int8 rows)
+  int32_t vs_stride;
   // bf16 pipeline: per-unit results, the parity of this step's eviction key,
   // and the slot the previous step of this cache wrote: 0 none (or not
   // tracked), s + 1 appended at slot s, -1 evicted (slot in the other key)

@@ -52,6 +52,9 @@ struct UnitOut {
   int32_t arrived;         // prep CTAs of the unit done (reset by the last one)
   int32_t pad[3];
   uint16_t vstar[128];     // the evicted slot's value row (bf16)
+  int8_t vqstar[128];      // int8 value cache: the evicted slot's row ...
+  float vsstar;            // ... and its scale
+  int32_t pad2[3];
 };
 
 // Partial record of one (stream CTA, unit): [m G][l G] padded to 4, acc [G][D].
@@ -82,7 +85,7 @@ struct PrepShape {
 // register use is higher.  One CTA per SM at most: a CTA takes the (unit, code chunk) items
 // blockIdx.x, blockIdx.x + gridDim.x, ... in turn, so that prep never crowds
 // the stream kernel's CTAs off an SM.
-template <int D, int G, bool MEM>
+template <int D, int G, bool MEM, bool VQ = false>
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, UnitOut* uo,
                                                             int splits, int first_of_step) {
   using S = PrepShape<D, G>;
@@ -253,7 +256,13 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
           a = warp_sum(a);
           if (lane == 0) uo[u].lstar[g] = a * p.qscale;
         }
-        for (int d = tid; d < D; d += kPrepThreads) uo[u].vstar[d] = __ldcg(Vrow + d);
+        if constexpr (VQ) {
+          const int8_t* Vq = reinterpret_cast<const int8_t*>(p.V) + ((size_t)u * p.budget + winner) * D;
+          for (int d = tid; d < D; d += kPrepThreads) uo[u].vqstar[d] = __ldcg(Vq + d);
+          if (tid == 0) uo[u].vsstar = __ldcg(p.vs + (size_t)u * p.vs_stride + winner);
+        } else {
+          for (int d = tid; d < D; d += kPrepThreads) uo[u].vstar[d] = __ldcg(Vrow + d);
+        }
         if (tid == 0) uo[u].arrived = 0;
       }
     }
@@ -263,6 +272,38 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
   // this grid completes only after stream has, so that merge's wait on this
   // grid covers stream's partials too
   if (tid == 0) pdl_wait();
+}
+
+// Quantisation of value rows into an int8 value cache (one warp per row): row r
+// of V_in [rows][D] (bf16) is slot r % n of unit r / n; s = max |v| / 127,
+// q = v / s rounded half to even (fp32 division), a zero row gives s = 0, q = 0.
+template <int D>
+__global__ void __launch_bounds__(256) vq_fill_kernel(const uint16_t* __restrict__ V_in,
+                                                      int64_t rows, int n, int budget,
+                                                      int8_t* Vq, float* vs, int vs_stride) {
+  constexpr int E = D / 32;
+  const int lane = threadIdx.x & 31;
+  for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows;
+       r += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+    const int64_t u = r / n, sl = r - u * n;
+    float v[E], m = 0.0f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      v[e] = __uint_as_float((uint32_t)V_in[r * D + lane * E + e] << 16);
+      m = fmaxf(m, fabsf(v[e]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+    const float sc = __fdiv_rn(m, 127.0f);
+    int8_t* dst = Vq + ((size_t)u * budget + sl) * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      float q = 0.0f;
+      if (sc > 0.0f) q = fminf(fmaxf(rintf(__fdiv_rn(v[e], sc)), -127.0f), 127.0f);
+      dst[e] = (int8_t)(int)q;
+    }
+    if (lane == 0) vs[(size_t)u * vs_stride + sl] = sc;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -283,7 +324,10 @@ constexpr int kDescFirst = 1;  // first tile of a segment: load q, reset the sta
 constexpr int kDescLast = 2;   // last tile of a segment: write the partial
 constexpr int kDescEnd = 4;    // no more tiles
 
-template <int D, int G, int NS>
+// VQ: the value cache holds int8 rows with one fp32 scale per slot (a stage is
+// the bf16 K tile, the int8 V tile and the tile's scales; each consumer warp
+// widens its 16 value rows to bf16 in a buffer of its own for the value MMA).
+template <int D, int G, int NS, bool VQ = false>
 struct StreamShape {
   static constexpr int NCW = 4;              // consumer warps
   static constexpr int NC = NCW * 32;        // consumer threads
@@ -292,7 +336,10 @@ struct StreamShape {
   static constexpr int NHALF = D / 64;       // 128-byte column boxes per row
   static constexpr int BOXB = TS * 128;      // bytes per TMA box
   static constexpr int TILEB = NHALF * BOXB; // bytes per K (or V) tile
-  static constexpr int STAGEB = 2 * TILEB;   // K + V
+  static constexpr int VQT = TS * D;         // VQ: bytes of the int8 V tile
+  static constexpr int SCB = TS * 4;         // VQ: bytes of the tile's scales
+  static constexpr int STAGEB = VQ ? (TILEB + VQT + SCB + 1023) / 1024 * 1024 : 2 * TILEB;
+  static constexpr int VWB = 16 * D * 2;     // VQ: one warp's bf16 value rows
   static constexpr int QB = G * D * 2;       // the unit's query rows (bf16)
   static constexpr int KS = D / 16;          // k-steps of the logit MMA
   static constexpr int MT = D / 16;          // d blocks of the value MMA
@@ -300,7 +347,8 @@ struct StreamShape {
   static constexpr int WACC = NCW * G * D;   // floats of the warp-merge area
   static constexpr int OFF_STAGE = 0;        // 1024-byte aligned (128B swizzle)
   static constexpr int OFF_Q = NS * STAGEB;  // [NS][QB]
-  static constexpr int OFF_WACC = OFF_Q + NS * QB;
+  static constexpr int OFF_VW = (OFF_Q + NS * QB + 1023) / 1024 * 1024;  // VQ: [NCW][VWB]
+  static constexpr int OFF_WACC = OFF_VW + (VQ ? NCW * VWB : 0);
   static constexpr int OFF_P = OFF_WACC + WACC * 4;
   static constexpr int OFF_WM = OFF_P + NCW * 2 * PB;
   static constexpr int OFF_DESC = OFF_WM + 2 * NCW * G * 4;  // int4 [NS]
@@ -326,11 +374,11 @@ __device__ __forceinline__ bool consumer_sync(uint64_t* bar, uint32_t& phase, in
   return ok;
 }
 
-template <int D, int G, int NS, bool PSPLIT>
-__global__ void __launch_bounds__(StreamShape<D, G, NS>::NT, 2)
+template <int D, int G, int NS, bool PSPLIT, bool VQ = false>
+__global__ void __launch_bounds__(StreamShape<D, G, NS, VQ>::NT, 2)
     stream_kernel(const StepParams p, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV) {
-  using S = StreamShape<D, G, NS>;
+  using S = StreamShape<D, G, NS, VQ>;
   using R = PRec<G, D>;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -364,8 +412,9 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS>::NT, 2)
     } else {
       unsigned char* dst = stage + st * S::STAGEB;
       const int y = u * p.budget + lt * S::TS;
+      constexpr uint32_t tile_bytes = VQ ? S::TILEB + S::VQT + S::SCB : 2 * S::TILEB;
       mbar_arrive_expect_tx(&full_bar[st],
-                            (uint32_t)(S::STAGEB + ((flags & kDescFirst) ? S::QB : 0)));
+                            tile_bytes + ((flags & kDescFirst) ? (uint32_t)S::QB : 0u));
       if (flags & kDescFirst)
         bulk_g2s(const_cast<unsigned char*>(qstage) + st * S::QB,
                  reinterpret_cast<const uint16_t*>(p.q) + (size_t)u * G * D, (uint32_t)S::QB,
@@ -373,9 +422,15 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS>::NT, 2)
 #pragma unroll
       for (int h = 0; h < S::NHALF; ++h)
         tma_load_2d(dst + h * S::BOXB, &tmK, 64 * h, y, &full_bar[st]);
+      if constexpr (VQ) {
+        tma_load_2d(dst + S::TILEB, &tmV, 0, y, &full_bar[st]);
+        bulk_g2s(dst + S::TILEB + S::VQT, p.vs + (size_t)u * p.vs_stride + (size_t)lt * S::TS,
+                 (uint32_t)S::SCB, &full_bar[st]);
+      } else {
 #pragma unroll
-      for (int h = 0; h < S::NHALF; ++h)
-        tma_load_2d(dst + S::TILEB + h * S::BOXB, &tmV, 64 * h, y, &full_bar[st]);
+        for (int h = 0; h < S::NHALF; ++h)
+          tma_load_2d(dst + S::TILEB + h * S::BOXB, &tmV, 64 * h, y, &full_bar[st]);
+      }
     }
     *v_issued = k + 1;
   };
@@ -496,7 +551,31 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS>::NT, 2)
       // slot, or the last appended one): stale in a tile fetched before the wait
       wslot = k < npre ? prew[k] : -1;
     }
-    if (k < npre && (unsigned)(wslot - slot_base) < 16u) {
+    if (VQ && k < npre && (unsigned)(wslot - slot_base) < 16u) {
+      // re-read the row written by the previous step (now visible) into the
+      // tile: its bf16 key (swizzled), int8 value row and scale
+      const int row = wslot - lt * S::TS;
+      constexpr int CK = D / 8, CV = D / 16;  // 16-byte chunks of the key and value rows
+      const size_t r = (size_t)u * p.budget + wslot;
+      unsigned char* Kd = const_cast<unsigned char*>(Ks);
+      if (lane < CK) {
+        const uint4 x = __ldcg(reinterpret_cast<const uint4*>(
+            reinterpret_cast<const uint16_t*>(p.K) + r * D + 8 * lane));
+        *reinterpret_cast<uint4*>(Kd + (lane >> 3) * S::BOXB + row * 128 +
+                                  (((lane & 7) ^ (row & 7)) << 4)) = x;
+      } else if (lane < CK + CV) {
+        const int c = lane - CK;
+        const uint4 x = __ldcg(reinterpret_cast<const uint4*>(
+            reinterpret_cast<const int8_t*>(p.V) + r * D + 16 * c));
+        *reinterpret_cast<uint4*>(Kd + S::TILEB + row * D + 16 * c) = x;
+      } else if (lane == CK + CV) {
+        *reinterpret_cast<float*>(Kd + S::TILEB + S::VQT + 4 * row) =
+            __ldcg(p.vs + (size_t)u * p.vs_stride + wslot);
+      }
+      fence_proxy_async_smem();  // the stage is refilled by TMA later
+      __syncwarp();
+    }
+    if (!VQ && k < npre && (unsigned)(wslot - slot_base) < 16u) {
       // re-read the row written by the previous step (now visible) into the tile
       const int row = wslot - lt * S::TS;
       constexpr int CH = D / 8;  // 16-byte chunks per row
@@ -554,20 +633,68 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS>::NT, 2)
       acc[mt][3] *= sc1;
     }
 
-    // P^T [8 heads][16 slots] in bf16 (hi, and the rounding remainder lo)
+    // P^T [8 heads][16 slots] in bf16 (hi, and the rounding remainder lo); with
+    // an int8 value cache each slot's weight carries the slot's value scale
     {
-      const __nv_bfloat16 a00 = __float2bfloat16_rn(p00), a01 = __float2bfloat16_rn(p01);
-      const __nv_bfloat16 a10 = __float2bfloat16_rn(p10), a11 = __float2bfloat16_rn(p11);
+      float w00 = p00, w01 = p01, w10 = p10, w11 = p11;
+      if constexpr (VQ) {
+        const float* scl = reinterpret_cast<const float*>(Ks + S::TILEB + S::VQT);
+        const float sa = scl[row0 + g8], sb = scl[row0 + g8 + 8];
+        w00 *= sa;
+        w01 *= sa;
+        w10 *= sb;
+        w11 *= sb;
+      }
+      const __nv_bfloat16 a00 = __float2bfloat16_rn(w00), a01 = __float2bfloat16_rn(w01);
+      const __nv_bfloat16 a10 = __float2bfloat16_rn(w10), a11 = __float2bfloat16_rn(w11);
       Phi[h0 * 16 + g8] = a00;
       Phi[h1 * 16 + g8] = a01;
       Phi[h0 * 16 + g8 + 8] = a10;
       Phi[h1 * 16 + g8 + 8] = a11;
       if (PSPLIT) {
-        Plo[h0 * 16 + g8] = __float2bfloat16_rn(p00 - __bfloat162float(a00));
-        Plo[h1 * 16 + g8] = __float2bfloat16_rn(p01 - __bfloat162float(a01));
-        Plo[h0 * 16 + g8 + 8] = __float2bfloat16_rn(p10 - __bfloat162float(a10));
-        Plo[h1 * 16 + g8 + 8] = __float2bfloat16_rn(p11 - __bfloat162float(a11));
+        Plo[h0 * 16 + g8] = __float2bfloat16_rn(w00 - __bfloat162float(a00));
+        Plo[h1 * 16 + g8] = __float2bfloat16_rn(w01 - __bfloat162float(a01));
+        Plo[h0 * 16 + g8 + 8] = __float2bfloat16_rn(w10 - __bfloat162float(a10));
+        Plo[h1 * 16 + g8 + 8] = __float2bfloat16_rn(w11 - __bfloat162float(a11));
       }
+    }
+    // VQ: this warp's 16 int8 value rows -> bf16 (exact), in the swizzled layout
+    // of a 16-row tile; the stage is then free
+    unsigned char* vw = smem + S::OFF_VW + cw * S::VWB;
+    if constexpr (VQ) {
+      const int lr = lane >> 1, hb = lane & 1;  // local row, half of the row
+      const int8_t* src = reinterpret_cast<const int8_t*>(Ks + S::TILEB) + (row0 + lr) * D +
+                          hb * (D / 2);
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(src + 16 * i);
+        const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          // byte b -> fp32 with exponent 2^23 holding b + 128 in its low mantissa
+          // bits (a byte permute), minus 2^23 + 128: b exactly; two at a time to bf16
+          const uint32_t u4 = wd[e] ^ 0x80808080u;
+          float f[4];
+#pragma unroll
+          for (int i2 = 0; i2 < 4; ++i2)
+            f[i2] = __uint_as_float(__byte_perm(u4, 0x4B000000u, 0x7540u + i2)) - 8388736.0f;
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(f[0], f[1]);
+          const __nv_bfloat162 hi = __floats2bfloat162_rn(f[2], f[3]);
+          o[2 * e] = *reinterpret_cast<const uint32_t*>(&lo);
+          o[2 * e + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+        }
+        const int cc = hb * (D / 16) + 2 * i;  // first 8-column chunk of these 16 values
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int c = cc + j;
+          *reinterpret_cast<uint4*>(vw + (c >> 3) * (16 * 128) + lr * 128 +
+                                    (((c & 7) ^ (lr & 7)) << 4)) =
+              make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[st]);  // stage free for refill
     }
     __syncwarp();
     const uint32_t* Phw = reinterpret_cast<const uint32_t*>(Phi);
@@ -579,16 +706,16 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS>::NT, 2)
     // values: O^T[d][head] += V^T[d][slots] P^T[slots][head]
 #pragma unroll
     for (int mt = 0; mt < S::MT; ++mt) {
-      const int row = row0 + (lane & 7) + ((lane >> 4) << 3);
+      const int row = (VQ ? 0 : row0) + (lane & 7) + ((lane >> 4) << 3);
       const int chunk = ((mt & 3) << 1) + ((lane >> 3) & 1);
       uint32_t a[4];
-      ldsm_x4_trans(a, smem_u32(Vs + (mt >> 2) * S::BOXB + row * 128 +
-                                ((chunk ^ (row & 7)) << 4)));
+      const unsigned char* vbase = VQ ? vw + (mt >> 2) * (16 * 128) : Vs + (mt >> 2) * S::BOXB;
+      ldsm_x4_trans(a, smem_u32(vbase + row * 128 + ((chunk ^ (row & 7)) << 4)));
       mma_bf16_16816(acc[mt], a, bh0, bh1);
       if (PSPLIT) mma_bf16_16816(acc[mt], a, bl0, bl1);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty_bar[st]);  // stage free for refill
+    if (!VQ && lane == 0) mbar_arrive(&empty_bar[st]);  // stage free for refill
 
     if (dsc.z & kDescLast) {
       // warp states -> shared memory -> the partial record of this segment
@@ -701,7 +828,7 @@ struct MergeShape {
 // fp32): per head the base-2 max, sum and accumulator -> xm, xl, xa [G][D].
 // Every warp of the CTA runs an online softmax over a strided share of the
 // slots (lane owns D/32 elements), then the warp states merge in a fixed order.
-template <int D, int G>
+template <int D, int G, bool VQ>
 __device__ void recompute_partial(const StepParams& p, int u, int lo, int hi, int skip,
                                   const float* qf, float* wstate, float* xm, float* xl,
                                   float* xa, int tid) {
@@ -710,7 +837,10 @@ __device__ void recompute_partial(const StepParams& p, int u, int lo, int hi, in
   const int lane = tid & 31, warp = tid >> 5;
   {
     const uint16_t* Kc = reinterpret_cast<const uint16_t*>(p.K) + (size_t)u * p.budget * D;
-    const uint16_t* Vc = reinterpret_cast<const uint16_t*>(p.V) + (size_t)u * p.budget * D;
+    // (the int8 value cache: bytes instead of bf16, one scale per slot)
+    const uint16_t* Vc = VQ ? reinterpret_cast<const uint16_t*>(reinterpret_cast<const int8_t*>(p.V) +
+                                                                (size_t)u * p.budget * D)
+                            : reinterpret_cast<const uint16_t*>(p.V) + (size_t)u * p.budget * D;
     float mr[G], lr[G], ar[G][E];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -725,7 +855,11 @@ __device__ void recompute_partial(const StepParams& p, int u, int lo, int hi, in
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         kx[e] = __uint_as_float((uint32_t)Kc[(size_t)s * D + lane * E + e] << 16);
-        vx[e] = __uint_as_float((uint32_t)Vc[(size_t)s * D + lane * E + e] << 16);
+        if constexpr (VQ)
+          vx[e] = (float)reinterpret_cast<const int8_t*>(Vc)[(size_t)s * D + lane * E + e] *
+                  __ldcg(p.vs + (size_t)u * p.vs_stride + s);
+        else
+          vx[e] = __uint_as_float((uint32_t)Vc[(size_t)s * D + lane * E + e] << 16);
       }
 #pragma unroll
       for (int g = 0; g < G; ++g) {
@@ -804,7 +938,7 @@ __device__ __forceinline__ void fold_one(float mc, float lc, float4 x, bool is_c
   mx = mn;
 }
 
-template <int D, int G>
+template <int D, int G, bool VQ = false>
 __global__ void __launch_bounds__(kMergeMaxThreads)
     merge_kernel(const StepParams p, UnitOut* uo, int stream_ctas) {
   using R = PRec<G, D>;
@@ -820,6 +954,7 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
   float* xl = xm + 8;                                               // [8]
   int* sflag = reinterpret_cast<int*>(xl + 8);                      // [4]
   float* wstate = reinterpret_cast<float*>(sflag + 4);              // recompute scratch
+  float* vqrow = wstate + (MT / 32) * G * (2 + D);                  // VQ: [D] new row, [32] maxima
   const int tid = threadIdx.x;
   const int u = blockIdx.x;
   const bool full = p.append_slot < 0;
@@ -880,10 +1015,37 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
   const int crel = (full && n > 0)
                        ? (int)((((int64_t)u * tps + winner / p.tile + 1) * NCT - 1) / TSS) - first
                        : -1;
-  const float4 vs = make_float4(__uint_as_float(vs2.x << 16), __uint_as_float(vs2.x & 0xFFFF0000u),
-                                __uint_as_float(vs2.y << 16), __uint_as_float(vs2.y & 0xFFFF0000u));
+  float4 vs = make_float4(__uint_as_float(vs2.x << 16), __uint_as_float(vs2.x & 0xFFFF0000u),
+                          __uint_as_float(vs2.y << 16), __uint_as_float(vs2.y & 0xFFFF0000u));
+  // int8 value cache: the evicted row as stored (q * s), and the new row's
+  // quantisation (s = max |v| / 127, q = v / s rounded half to even)
+  float vnew = 0.0f;
+  if constexpr (VQ) {
+    if (full) {
+      const int32_t w4 = __ldcg(reinterpret_cast<const int32_t*>(uo[u].vqstar + d0));
+      const float ss = __ldcg(&uo[u].vsstar);
+      vs = make_float4((float)(int8_t)(w4 & 0xFF) * ss, (float)(int8_t)((w4 >> 8) & 0xFF) * ss,
+                       (float)(int8_t)((w4 >> 16) & 0xFF) * ss, (float)(int8_t)(w4 >> 24) * ss);
+    }
+    vnew = __uint_as_float((uint32_t)vt1 << 16);
+    float m = tid < D ? fabsf(vnew) : 0.0f;
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o2));
+    if ((tid & 31) == 0 && tid < D) vqrow[D + (tid >> 5)] = m;
+  }
   if (tid == 0) sflag[0] = 0;
   __syncthreads();
+  float vscale = 0.0f;
+  if constexpr (VQ) {
+    float m = 0.0f;
+    for (int w2 = 0; w2 < D / 32; ++w2) m = fmaxf(m, vqrow[D + w2]);
+    vscale = __fdiv_rn(m, 127.0f);
+    if (tid < D) {
+      float r = 0.0f;
+      if (vscale > 0.0f) r = fminf(fmaxf(rintf(__fdiv_rn(vnew, vscale)), -127.0f), 127.0f);
+      vqrow[tid] = r;
+    }
+  }
 
   float mx = -1e30f, sum = 0.0f;
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -914,7 +1076,7 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
     const int tb = (int)((int64_t)c * TSS / NCT), te = (int)(((int64_t)c + 1) * TSS / NCT);
     const int lo = (max(tb, u * tps) - u * tps) * p.tile;
     const int hi = min((min(te, (u + 1) * tps) - u * tps) * p.tile, p.occ);
-    recompute_partial<D, G>(p, u, lo, hi, winner, qf, wstate, xm, xl, xa, tid);
+    recompute_partial<D, G, VQ>(p, u, lo, hi, winner, qf, wstate, xm, xl, xa, tid);
     mx = -1e30f;
     sum = 0.0f;
     a = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -952,21 +1114,30 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
     }
     const float wn = exp2f(ln - m2);
     const float inv = 1.0f / (l2 + wn);
+    float4 vt = make_float4(__uint_as_float(vt2.x << 16), __uint_as_float(vt2.x & 0xFFFF0000u),
+                            __uint_as_float(vt2.y << 16), __uint_as_float(vt2.y & 0xFFFF0000u));
+    if constexpr (VQ)  // the new token's value as stored
+      vt = make_float4(vqrow[d0] * vscale, vqrow[d0 + 1] * vscale, vqrow[d0 + 2] * vscale,
+                       vqrow[d0 + 3] * vscale);
     float4 r;
-    r.x = (s.x + wn * __uint_as_float(vt2.x << 16)) * inv;
-    r.y = (s.y + wn * __uint_as_float(vt2.x & 0xFFFF0000u)) * inv;
-    r.z = (s.z + wn * __uint_as_float(vt2.y << 16)) * inv;
-    r.w = (s.w + wn * __uint_as_float(vt2.y & 0xFFFF0000u)) * inv;
+    r.x = (s.x + wn * vt.x) * inv;
+    r.y = (s.y + wn * vt.y) * inv;
+    r.z = (s.z + wn * vt.z) * inv;
+    r.w = (s.w + wn * vt.w) * inv;
     reinterpret_cast<float4*>(p.out + ((size_t)b * p.kv_heads * G + (size_t)j * G) * D)[tid] = r;
   }
 
   // method step 5: the current token's key, value and code replace the slot
   uint16_t* Kw = reinterpret_cast<uint16_t*>(p.K) + ((size_t)u * p.budget + winner) * D;
-  uint16_t* Vw = reinterpret_cast<uint16_t*>(p.V) + ((size_t)u * p.budget + winner) * D;
   if (tid < D) {
     Kw[tid] = kt1;
-    Vw[tid] = vt1;
+    if constexpr (VQ)
+      reinterpret_cast<int8_t*>(p.V)[((size_t)u * p.budget + winner) * D + tid] =
+          (int8_t)(int)vqrow[tid];
+    else
+      reinterpret_cast<uint16_t*>(p.V)[((size_t)u * p.budget + winner) * D + tid] = vt1;
   }
+  if (VQ && tid == 0) p.vs[(size_t)u * p.vs_stride + winner] = vscale;
   if (tid == 0) {
     store_code(p.codes + (size_t)u * p.code_stride + (size_t)winner * (p.bits >> 3), p.bits,
                codek);
@@ -982,7 +1153,7 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
 template <int D, int G>
 constexpr int merge_smem_bytes(int threads) {
   return threads * (16 + 4 + 4) + (G * D + G * D + 8 + 8) * 4 + 16 +
-         (threads / 32) * G * (2 + D) * 4;
+         (threads / 32) * G * (2 + D) * 4 + (D + 32) * 4;
 }
 
 }  // namespace he

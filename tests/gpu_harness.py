@@ -42,20 +42,24 @@ class GpuRun:
     prof: dict | None = None   # summed kernel times of the library's timing mode
 
 
-def make_handle(w: synth.Workload, layer: int = 0, threshold: float = 0.0, decay: float = 0.0):
+def make_handle(w: synth.Workload, layer: int = 0, threshold: float = 0.0, decay: float = 0.0,
+                v_int8: bool = False):
     from lsh_pre_attention_decode_b300 import HashEvict
     return HashEvict(w.batch, w.heads, w.kv_heads, w.head_dim, w.bits, w.budget, w.dtype,
-                     seed=w.projection_seed(layer), threshold=threshold, decay=decay)
+                     seed=w.projection_seed(layer), threshold=threshold, decay=decay,
+                     v_int8=v_int8)
 
 
 def run_gpu(w: synth.Workload, fill_n: int, steps: int, out_steps=(), layer: int = 0,
             device_gen: bool = False, read_state: bool = False, chunk: int = 256,
-            profile: bool = False, threshold: float = 0.0, decay: float = 0.0) -> GpuRun:
+            profile: bool = False, threshold: float = 0.0, decay: float = 0.0,
+            v_int8: bool = False) -> GpuRun:
     """Fill with prompt tokens [0, fill_n), then stream tokens fill_n .. fill_n+steps-1.
-    With decay > 0 the returned state also holds the per-slot scores."""
+    With decay > 0 the returned state also holds the per-slot scores; with an
+    int8 value cache, V is int8 and the value scales follow."""
     import torch
     out_steps = set(out_steps)
-    he = make_handle(w, layer, threshold, decay)
+    he = make_handle(w, layer, threshold, decay, v_int8)
     try:
         if fill_n > 0:
             if device_gen:
@@ -91,8 +95,9 @@ def run_gpu(w: synth.Workload, fill_n: int, steps: int, out_steps=(), layer: int
                     outs[c0 + i] = out.cpu().numpy().copy()
         prof = he.profile_stop() if profile else None
         state = he.state() if read_state else None
-        if read_state and decay > 0.0:
-            state = state + (he.scores(),)
+        if read_state:
+            state = state + (he.scores() if decay > 0.0 else None,
+                             he.vscales() if v_int8 else None)
         return GpuRun(evicted, outs, state, prof)
     finally:
         he.close()
@@ -107,15 +112,18 @@ class OracleRun:
     V: np.ndarray
     occupancy: int
     score: np.ndarray | None = None  # per-slot scores (score memory only)
+    Vq: np.ndarray | None = None     # int8 value cache: rows ...
+    Vs: np.ndarray | None = None     # ... and scales
 
 
 def run_oracle_unit(w: synth.Workload, b: int, j: int, fill_n: int, steps: int, out_steps=(),
-                    layer: int = 0, threshold: float = 0.0, decay: float = 0.0) -> OracleRun:
+                    layer: int = 0, threshold: float = 0.0, decay: float = 0.0,
+                    v_int8: bool = False) -> OracleRun:
     o = oracle.load()
     W = o.projection(w.projection_seed(layer), w.head_dim, w.bits, w.dtype)
     Kin = synth.host_unit_kv(w, "key", b, j, 0, fill_n, layer)
     Vin = synth.host_unit_kv(w, "value", b, j, 0, fill_n, layer)
-    st = o.unit_fill(W, w.budget, Kin, Vin, tau=threshold, memory=decay > 0.0)
+    st = o.unit_fill(W, w.budget, Kin, Vin, tau=threshold, memory=decay > 0.0, vq=v_int8)
     q = synth.host_unit_queries(w, b, j, fill_n, steps, layer)
     k = synth.host_unit_kv(w, "key", b, j, fill_n, steps, layer)
     v = synth.host_unit_kv(w, "value", b, j, fill_n, steps, layer)
@@ -123,15 +131,16 @@ def run_oracle_unit(w: synth.Workload, b: int, j: int, fill_n: int, steps: int, 
     for s in out_steps:
         want[s] = 1
     r = o.unit_stream(st, q, k, v, want_out=want, decay=decay)
-    return OracleRun(r["evicted"], r["out"], st.codes, st.K, st.V, st.occupancy, st.score)
+    return OracleRun(r["evicted"], r["out"], st.codes, st.K, st.V, st.occupancy, st.score,
+                     st.Vq, st.Vs)
 
 
 def run_oracle_units(w, units, fill_n, steps, out_steps=(), layer=0, threads=8,
-                     threshold: float = 0.0, decay: float = 0.0):
+                     threshold: float = 0.0, decay: float = 0.0, v_int8: bool = False):
     """Oracle over several (b, j) units in parallel threads (ctypes releases the GIL)."""
     with cf.ThreadPoolExecutor(max_workers=threads) as ex:
         futs = {u: ex.submit(run_oracle_unit, w, u[0], u[1], fill_n, steps, out_steps, layer,
-                             threshold, decay)
+                             threshold, decay, v_int8)
                 for u in units}
         return {u: f.result() for u, f in futs.items()}
 
@@ -156,7 +165,12 @@ def compare(w: synth.Workload, g: GpuRun, orc: dict, out_steps=(), check_state: 
             K, V, codes, occ = g.state[:4]
             assert occ == r.occupancy
             assert np.array_equal(codes[b, j].astype(np.uint64), r.codes), f"codes ({b},{j})"
-            assert np.array_equal(K[b, j], r.K) and np.array_equal(V[b, j], r.V), f"K/V ({b},{j})"
+            assert np.array_equal(K[b, j], r.K), f"K ({b},{j})"
+            if r.Vq is not None:  # int8 value cache: rows and scales, exactly
+                assert np.array_equal(V[b, j], r.Vq), f"int8 V ({b},{j})"
+                assert np.array_equal(g.state[5][b, j], r.Vs), f"value scales ({b},{j})"
+            else:
+                assert np.array_equal(V[b, j], r.V), f"V ({b},{j})"
     assert worst_max <= MAX_ABS_TOL, f"max-abs error {worst_max}"
     assert worst_mean <= MEAN_ABS_TOL, f"mean-abs error {worst_mean}"
     return worst_max, worst_mean

@@ -51,7 +51,7 @@ def test_strerror(L):
 
 def cfg(**kw):
     d = dict(batch=1, heads=32, kv_heads=8, head_dim=128, bits=32, budget=256, dtype=0,
-             threshold=0.0, seed=1, decay=0.0, reserved=0)
+             threshold=0.0, seed=1, decay=0.0, v_format=0)
     d.update(kw)
     return pkg.HeCfg(**d)
 
@@ -59,7 +59,8 @@ def cfg(**kw):
 @pytest.mark.parametrize("bad", [dict(batch=0), dict(heads=30), dict(kv_heads=0), dict(bits=12),
                                  dict(bits=128), dict(budget=0), dict(budget=(1 << 24) + 1),
                                  dict(head_dim=96), dict(head_dim=256), dict(dtype=2),
-                                 dict(heads=64, kv_heads=4), dict(reserved=1),
+                                 dict(heads=64, kv_heads=4), dict(v_format=2),
+                                 dict(v_format=1, dtype=1),
                                  dict(batch=70000), dict(decay=-0.5), dict(decay=1.5),
                                  dict(decay=float("nan")), dict(threshold=float("inf")),
                                  dict(threshold=float("nan"))])
@@ -85,6 +86,7 @@ def test_null_arguments_are_rejected(L):
     assert L.he_launch_info(None, None, None, None, None) == -1
     assert L.he_recompute_count(None, None) == -1
     assert L.he_read_scores(None, None) == -1
+    assert L.he_read_vscales(None, None) == -1
 
 
 def test_python_errors_raise(L):
