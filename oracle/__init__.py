@@ -75,6 +75,7 @@ class UnitState:
     score: np.ndarray | None = None
     Vq: np.ndarray | None = None     # quantised value cache: int8 [budget][D] ...
     Vs: np.ndarray | None = None     # ... and one fp32 scale per row (then V is unused)
+    chunk: int = 1                   # chunk eviction: K, V, codes hold budget + chunk - 1 rows
 
 
 class Oracle:
@@ -108,6 +109,10 @@ class Oracle:
                                            _vp, _vp, _i32, _vp, _vp, _vp, ctypes.c_float,
                                            ctypes.c_float, _vp, _vp, _vp, _vp]
         lib.orc_unit_stream_vq.restype = None
+        lib.orc_unit_stream_chunk.argtypes = [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp,
+                                              _vp, _vp, _i32, _vp, _vp, _vp, ctypes.c_float, _vp,
+                                              _vp, _vp, _vp]
+        lib.orc_unit_stream_chunk.restype = None
         lib.orc_group_distance.argtypes = [_vp, _i32, _u64]
         lib.orc_group_distance.restype = _i32
         lib.orc_most_dissimilar.argtypes = [_vp, _i32]
@@ -194,6 +199,16 @@ class Oracle:
         return out
 
     # -- one (batch, KV head) unit -----------------------------------------
+    def unit_fill_chunk(self, W: np.ndarray, budget: int, chunk: int, Kin: np.ndarray,
+                        Vin: np.ndarray, tau: float = 0.0) -> UnitState:
+        """A unit for chunk eviction: room for budget + chunk - 1 rows."""
+        if budget % chunk:
+            raise ValueError("the budget must be a whole number of chunks")
+        st = self.unit_fill(W, budget + chunk - 1, Kin, Vin, tau=tau)
+        st.budget = budget
+        st.chunk = chunk
+        return st
+
     def unit_fill(self, W: np.ndarray, budget: int, Kin: np.ndarray, Vin: np.ndarray,
                   tau: float = 0.0, memory: bool = False, vq: bool = False) -> UnitState:
         """A unit filled with the rows of Kin, Vin.  ``memory``: keep per-slot
@@ -251,7 +266,15 @@ class Oracle:
         out = np.empty((n_out, G, D), np.float64)
         dl = np.empty((T, st.budget), np.int32) if dist_log else None
         occ = np.array([st.occupancy], np.int32)
-        if st.Vq is not None:
+        if st.chunk > 1:
+            if decay != 0.0 or st.score is not None or st.Vq is not None or dist_log:
+                raise ValueError("chunk eviction takes neither score memory nor int8 values")
+            self.lib.orc_unit_stream_chunk(_ptr(st.W), D, G, st.bits, _dtype_code(qc), st.budget,
+                                           st.chunk, _ptr(st.K), _ptr(st.V), _ptr(st.codes),
+                                           _ptr(occ), T, _ptr(qc), _ptr(kc), _ptr(vc),
+                                           float(st.tau), _ptr(evicted), _ptr(written), _ptr(wo),
+                                           _ptr(out))
+        elif st.Vq is not None:
             if st.score is None and decay != 0.0:
                 raise ValueError("score memory needs a unit filled with memory=True")
             self.lib.orc_unit_stream_vq(_ptr(st.W), D, G, st.bits, _dtype_code(qc), st.budget,

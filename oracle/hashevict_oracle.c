@@ -469,6 +469,76 @@ void orc_unit_stream_vq(const void* W, int32_t D, int32_t G, int32_t bits, int32
   free(code_q);
 }
 
+/* ------------------------------------------------------------------------- */
+/* Chunk eviction (the survey's chunk-granular row; ChunkKV page: chunks of   */
+/* 10 contiguous tokens).  Reading: the budget B is cut into B / c aligned    */
+/* chunks of c slots; while the cache is full, new tokens are staged in the   */
+/* c - 1 slots after the budget (and attended); the token that would fill the */
+/* stage evicts the chunk with the largest sum of its slots' group-summed     */
+/* distances (ties: lowest chunk), and the c - 1 staged tokens, in order,     */
+/* then the token itself take the chunk's slots.  c = 1 is the method.        */
+/* State: K, V [B + c - 1][D], codes [B + c - 1]; occupancy counts staged.    */
+/* ------------------------------------------------------------------------- */
+
+void orc_unit_stream_chunk(const void* W, int32_t D, int32_t G, int32_t bits, int32_t dtype,
+                           int32_t budget, int32_t chunk, void* K, void* V, uint64_t* codes,
+                           int32_t* occupancy, int32_t nsteps, const void* q, const void* k,
+                           const void* v, float tau, int32_t* evicted, int32_t* written,
+                           const uint8_t* want_out, double* out) {
+  size_t row = (size_t)D * elem_bytes(dtype);
+  const int32_t nch = budget / chunk;
+  int32_t* dsum = (int32_t*)malloc(sizeof(int32_t) * (size_t)(nch > 0 ? nch : 1));
+  uint64_t* code_q = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)G);
+  size_t n_out = 0;
+  for (int32_t t = 0; t < nsteps; ++t) {
+    const char* qt = (const char*)q + (size_t)t * (size_t)G * row;
+    const char* kt = (const char*)k + (size_t)t * row;
+    const char* vt = (const char*)v + (size_t)t * row;
+    int32_t slot;
+    if (*occupancy < budget + chunk - 1) {
+      /* a free slot of the budget, or a staging slot */
+      slot = *occupancy;
+      *occupancy += 1;
+      evicted[t] = -1;
+    } else {
+      for (int32_t g = 0; g < G; ++g)
+        code_q[g] = orc_code_tau(qt + (size_t)g * row, dtype, D, W, bits, tau);
+      for (int32_t i = 0; i < nch; ++i) {
+        dsum[i] = 0;
+        for (int32_t j = 0; j < chunk; ++j) {
+#if ORACLE_MUTANT == 15 /* planted: a chunk scores by its first slot only */
+          if (j > 0) break;
+#endif
+          dsum[i] += orc_group_distance(code_q, G, codes[i * chunk + j]);
+        }
+      }
+      const int32_t e = orc_most_dissimilar(dsum, nch);
+      /* the staged tokens, in order, then this token take the chunk's slots */
+      for (int32_t j = 0; j < chunk - 1; ++j) {
+#if ORACLE_MUTANT == 16 /* planted: the staged tokens land in reverse order */
+        const int32_t from = budget + chunk - 2 - j;
+#else
+        const int32_t from = budget + j;
+#endif
+        memcpy((char*)K + (size_t)(e * chunk + j) * row, (char*)K + (size_t)from * row, row);
+        memcpy((char*)V + (size_t)(e * chunk + j) * row, (char*)V + (size_t)from * row, row);
+        codes[e * chunk + j] = codes[from];
+      }
+      slot = e * chunk + chunk - 1;
+      *occupancy = budget;
+      evicted[t] = e * chunk;
+    }
+    written[t] = slot;
+    memcpy((char*)K + (size_t)slot * row, kt, row);
+    memcpy((char*)V + (size_t)slot * row, vt, row);
+    codes[slot] = orc_code_tau(kt, dtype, D, W, bits, tau);
+    if (!want_out || want_out[t])
+      orc_attend(qt, K, V, *occupancy, D, G, dtype, out + (n_out++) * (size_t)G * (size_t)D);
+  }
+  free(dsum);
+  free(code_q);
+}
+
 /* The method as described: threshold 0, the step's own distances. */
 void orc_unit_stream(const void* W, int32_t D, int32_t G, int32_t bits, int32_t dtype,
                      int32_t budget, void* K, void* V, uint64_t* codes, int32_t* occupancy,

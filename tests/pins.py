@@ -96,6 +96,24 @@ def read_decay_case():
     return c
 
 
+def read_chunk_case():
+    c = {"fill": [], "steps": [], "rows": []}
+    for tok in _lines("chunk_hand.txt"):
+        if tok[0] in ("budget", "chunk"):
+            c[tok[0]] = int(tok[1])
+        elif tok[0] == "fill":
+            c["fill"].append([float(t) for t in tok[1:]])
+        elif tok[0] == "row":
+            c["rows"].append([float(t) for t in tok[1:]])
+        elif tok[0] == "step":
+            i_k, i_e, i_s, i_c = (tok.index(w) for w in ("k", "expect", "slot", "codes"))
+            c["steps"].append({"q": [float(t) for t in tok[2:i_k]],
+                               "k": [float(t) for t in tok[i_k + 1:i_e]],
+                               "expect": int(tok[i_e + 1]), "slot": int(tok[i_s + 1]),
+                               "codes": [int(t) for t in tok[i_c + 1:]]})
+    return c
+
+
 def read_vquant_rows():
     rows = []
     for tok in _lines("vquant_hand.txt"):
@@ -500,11 +518,102 @@ def check_vquant_stream(o):
         assert np.allclose(rb["out"][-1], last, rtol=0, atol=1e-5)
 
 
+def check_chunk_hand(o):
+    """Chunk eviction (tests/golden/chunk_hand.txt): staged appends, the chunk
+    chosen, the slot written and the resident codes after every step, the rows
+    after the last step, and the last output = attention over those rows."""
+    c = read_chunk_case()
+    W = np.eye(4, dtype=np.float32)
+    fill = f32(c["fill"])
+    st = o.unit_fill_chunk(W, c["budget"], c["chunk"], fill, fill)
+    for s in c["steps"]:
+        r = o.unit_stream(st, f32([[s["q"]]]), f32([s["k"]]), f32([s["k"]]))
+        assert r["evicted"].tolist() == [s["expect"]], (s, r["evicted"])
+        assert r["written"].tolist() == [s["slot"]], (s, r["written"])
+        assert st.occupancy == len(s["codes"]), (s, st.occupancy)
+        assert st.codes[:st.occupancy].tolist() == s["codes"], (s, st.codes)
+    rows = f32(c["rows"])
+    assert np.array_equal(st.K[:st.occupancy], rows) and np.array_equal(st.V[:st.occupancy], rows)
+    last = c["steps"][-1]
+    assert np.array_equal(r["out"][0], o.attend(f32([last["q"]]), rows, rows))
+
+
+def check_chunk_one_is_method(o):
+    """Chunks of one slot are the method: the same evictions, cache and outputs
+    as the per-step path (random streams with ties and appends, both dtypes)."""
+    rng = np.random.default_rng(61)
+    for trial in range(6):
+        dtype = ("fp32", "bf16")[trial % 2]
+        cast = f32 if dtype == "fp32" else bf16_bits
+        D, bits, G, B, T = 16, 4 + 2 * trial, 2, 9, 14
+        W = o.projection(200 + trial, D, bits, dtype)
+        n0 = int(rng.integers(3, B + 1))
+        K0, V0 = cast(rng.standard_normal((n0, D))), cast(rng.standard_normal((n0, D)))
+        q, k, v = (cast(rng.standard_normal(sh)) for sh in ((T, G, D), (T, D), (T, D)))
+        a = o.unit_fill(W, B, K0, V0)
+        b = o.unit_fill_chunk(W, B, 1, K0, V0)
+        ra, rb = o.unit_stream(a, q, k, v), o.unit_stream(b, q, k, v)
+        assert ra["evicted"].tolist() == rb["evicted"].tolist()
+        assert ra["written"].tolist() == rb["written"].tolist()
+        assert np.array_equal(ra["out"], rb["out"]) and np.array_equal(a.codes, b.codes)
+        assert np.array_equal(a.K, b.K) and np.array_equal(a.V, b.V)
+
+
+def check_chunk_whole_budget(o):
+    """One chunk spanning the whole budget replaces the cache in blocks: after
+    every eviction the cache holds exactly the last B tokens in arrival order,
+    and between evictions the newest tokens sit in the stage after them."""
+    rng = np.random.default_rng(62)
+    D, bits, G, B = 8, 8, 2, 4
+    W = o.projection(9, D, bits, "fp32")
+    K0 = f32(rng.standard_normal((B, D)))
+    T = 3 * B + 2
+    q, k, v = (f32(rng.standard_normal(sh)) for sh in ((T, G, D), (T, D), (T, D)))
+    st = o.unit_fill_chunk(W, B, B, K0, K0)
+    allk = np.concatenate([K0, k])
+    for t in range(T):
+        r = o.unit_stream(st, q[t:t + 1], k[t:t + 1], v[t:t + 1])
+        n = B + t + 1                       # tokens seen so far (fill + stream)
+        staged = (t + 1) % B
+        assert st.occupancy == B + staged
+        assert r["evicted"].tolist() == [0 if staged == 0 else -1]
+        window = allk[n - staged - B:n - staged]
+        assert np.array_equal(st.K[:B], window)
+        assert np.array_equal(st.K[B:B + staged], allk[n - staged:n])
+
+
+def check_chunk_sums_brute(o):
+    """The chunk chosen at each eviction is the argmax (lowest on ties) of the
+    brute-force sum of the group-summed Hamming distances over its slots, with
+    codes and distances recomputed here from the stored rows by popcount."""
+    rng = np.random.default_rng(63)
+    for trial in range(4):
+        D, bits, G, c = 16, 6, 2, (2, 3, 4, 6)[trial]
+        B = 4 * c
+        W = o.projection(300 + trial, D, bits, "fp32")
+        K0 = f32(rng.standard_normal((B, D)))
+        st = o.unit_fill_chunk(W, B, c, K0, K0)
+        for t in range(5 * c):
+            qt = f32(rng.standard_normal((1, G, D)))
+            kt = f32(rng.standard_normal((1, D)))
+            full = st.occupancy == B + c - 1
+            before = st.codes[:B].copy()
+            r = o.unit_stream(st, qt, kt, kt)
+            if not full:
+                assert r["evicted"][0] == -1
+                continue
+            cq = [int(x) for x in o.code(qt[0], W)]
+            d = [sum(bin(int(x) ^ y).count("1") for y in cq) for x in before]
+            sums = [sum(d[i * c:(i + 1) * c]) for i in range(B // c)]
+            assert r["evicted"][0] == c * sums.index(max(sums)), (sums, r["evicted"])
+
+
 ALL_CHECKS = [
     check_codes_hand, check_codes_identity_sign, check_codes_invariances, check_projection_moments,
     check_distance_brute, check_argmax_ties, check_eviction_hand, check_special_cases,
     check_stream_invariants, check_attention_hand, check_attention_closed_forms,
     check_attention_bf16_elements, check_codes_tau_hand, check_codes_tau_monotone,
     check_decay_hand, check_decay_zero_is_per_step, check_vquant_hand, check_vquant_attention,
-    check_vquant_stream,
+    check_vquant_stream, check_chunk_hand, check_chunk_one_is_method, check_chunk_whole_budget,
+    check_chunk_sums_brute,
 ]

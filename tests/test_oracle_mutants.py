@@ -21,6 +21,8 @@ MUTANTS = {
     12: "score ties go to the highest slot",
     13: "value rows scaled by max / 128",
     14: "value rows rounded half away from zero",
+    15: "a chunk scores by its first slot only",
+    16: "staged tokens land in reverse order",
 }
 
 
