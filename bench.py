@@ -26,6 +26,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import re
 import subprocess
@@ -63,6 +64,8 @@ def parse_args():
                     help="score memory gamma (0: the step's own distances, the method)")
     ap.add_argument("--v-int8", action="store_true",
                     help="int8 value cache with one scale per slot (keys stay bf16)")
+    ap.add_argument("--chunk", type=int, default=1,
+                    help="chunk eviction: chunks of this many slots (1: the method)")
     ap.add_argument("--graph-ring", type=int, default=64,
                     help="tokens per layer in the captured step graph (even)")
     ap.add_argument("--e2e-steps", type=int, default=400)
@@ -173,12 +176,14 @@ def config_of(w: synth.Workload, args, extra=None):
     c = {"workload": f"{w.name}: {w.description}" + (
             f"; threshold {args.threshold}, score memory {args.decay}"
             if (args.threshold or args.decay) else "") + (
-            "; int8 value cache" if args.v_int8 else ""),
+            "; int8 value cache" if args.v_int8 else "") + (
+            f"; chunk eviction, chunks of {args.chunk} slots" if args.chunk > 1 else ""),
          "batch": w.batch, "heads": w.heads,
          "kv_heads": w.kv_heads, "head_dim": w.head_dim, "bits": w.bits, "budget": w.budget,
          "prompt": w.prompt, "dtype": w.dtype,
-         "cache_fill": "first `budget` prompt tokens; timed steps are streamed tokens "
-                       "(eviction on every step)"}
+         "cache_fill": "first `budget` prompt tokens; timed steps are streamed tokens " + (
+             "(eviction on every step)" if args.chunk <= 1 else
+             f"(one chunk eviction every {args.chunk} steps, tokens staged between)")}
     if extra:
         c.update(extra)
     return c
@@ -189,7 +194,8 @@ def config_of(w: synth.Workload, args, extra=None):
 # ---------------------------------------------------------------------------
 
 def run_cpu_baseline(w: synth.Workload, target_s: float, steps: int | None = None,
-                     threshold: float = 0.0, decay: float = 0.0, v_int8: bool = False):
+                     threshold: float = 0.0, decay: float = 0.0, v_int8: bool = False,
+                     chunk: int = 1):
     """Times the CPU oracle, as it stands, on a bounded sample of the workload.
 
     The unit of work is a unit-step: one streamed token through one (batch, KV
@@ -211,9 +217,11 @@ def run_cpu_baseline(w: synth.Workload, target_s: float, steps: int | None = Non
 
     def prep(u):
         b, j = u
-        return o.unit_fill(W, w.budget, synth.host_unit_kv(w, "key", b, j, 0, w.budget),
-                           synth.host_unit_kv(w, "value", b, j, 0, w.budget), tau=threshold,
-                           memory=decay > 0.0, vq=v_int8)
+        K0 = synth.host_unit_kv(w, "key", b, j, 0, w.budget)
+        V0 = synth.host_unit_kv(w, "value", b, j, 0, w.budget)
+        if chunk > 1:
+            return o.unit_fill_chunk(W, w.budget, chunk, K0, V0, tau=threshold)
+        return o.unit_fill(W, w.budget, K0, V0, tau=threshold, memory=decay > 0.0, vq=v_int8)
 
     def run(u, st, t0, n):
         b, j = u
@@ -279,7 +287,7 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     for layer in layers:
         he = HashEvict(w.batch, w.heads, w.kv_heads, w.head_dim, w.bits, w.budget, w.dtype,
                        seed=w.projection_seed(layer), threshold=args.threshold,
-                       decay=args.decay, v_int8=args.v_int8)
+                       decay=args.decay, v_int8=args.v_int8, chunk=args.chunk)
         K = synth.gpu_kv(w, "key", 0, w.budget, layer)
         V = synth.gpu_kv(w, "value", 0, w.budget, layer)
         he.fill(K, V)
@@ -334,8 +342,13 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     # layer, in the same round-robin order; an even count per cache keeps the
     # library's per-step double buffering in phase): the host issues one launch
     # per GS steps instead of three per step
+    # (with chunk eviction a whole number of staging cycles per cache too, so
+    # that every replay starts from the state the capture started from)
+    period = 2 * args.chunk // math.gcd(2, args.chunk) if args.chunk > 1 else 2
     Rg = min(args.graph_ring, R)
-    Rg -= Rg % 2
+    Rg -= Rg % period
+    if Rg == 0:
+        raise SystemExit(f"--graph-ring must hold at least {period} tokens per layer")
     GS = L * Rg
     cursor[0] = 0
     graph = torch.cuda.CUDAGraph()
@@ -424,12 +437,12 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     value = steps_total / (elapsed_ms / 1e3)
     peak, peak_kind = measured_peaks()
     eb = 2 if w.dtype == "bf16" else 4
-    occ = w.budget
+    occ = w.budget + (args.chunk - 1) / 2  # resident rows (chunk eviction: a cycle's mean)
     U = w.batch * w.kv_heads
     # K and V rows of every resident slot (int8 value rows and their scales with
     # an int8 value cache)
-    stream_bytes = U * occ * (w.head_dim * eb + (w.head_dim + 4 if args.v_int8
-                                                   else w.head_dim * eb))
+    stream_bytes = int(U * occ * (w.head_dim * eb + (w.head_dim + 4 if args.v_int8
+                                                       else w.head_dim * eb)))
     achieved = stream_bytes / (stream_ms / 1e3) / 1e9
     step_gbs = step_bytes / (elapsed_ms / K / 1e3) / 1e9
     launches_per_step = 3 if w.dtype == "bf16" else 1
@@ -497,7 +510,7 @@ def main():
         w = workload_from(args)
         val, cores, sample, el = run_cpu_baseline(w, args.ref_seconds, steps=args.steps,
                                                   threshold=args.threshold, decay=args.decay,
-                                                  v_int8=args.v_int8)
+                                                  v_int8=args.v_int8, chunk=args.chunk)
         res = {
             "metric": "HashEvict decode steps/s (hash+evict+attend); achieved HBM GB/s vs B300 peak",
             "impl": "reference", "value": val, "unit": "steps/s", "n_gpus": 0,
@@ -526,7 +539,7 @@ def main():
         if not args.no_cpu_baseline:
             val, cores, sample, el = run_cpu_baseline(w, args.cpu_seconds,
                                                       threshold=args.threshold, decay=args.decay,
-                                                      v_int8=args.v_int8)
+                                                      v_int8=args.v_int8, chunk=args.chunk)
             res["cpu_baseline"] = {"value": val, "unit": "steps/s", "cores": cores,
                                    "kind": "oracle", "sample": sample}
         print(json.dumps(res))

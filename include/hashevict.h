@@ -58,8 +58,12 @@ extern "C" {
 /* Handle configuration.  Supported: head_dim in {64, 128};
  * G = heads / kv_heads in {1, 2, 4, 8}; bits in {8, 16, 32, 64};
  * 1 <= budget <= 2^24; batch * kv_heads <= 2^16; dtype HE_DTYPE_*;
- * threshold finite; 0 <= decay <= 1; v_format HE_VFMT_*.  A zero-initialised
- * tail (threshold 0, decay 0, v_format 0) is the method as the paper describes it. */
+ * threshold finite; 0 <= decay <= 1; v_format HE_VFMT_*; 0 <= chunk <= 16
+ * (chunk >= 2: bf16, budget % chunk == 0, decay 0, v_format HE_VFMT_ELEM).
+ * A zero-initialised tail (threshold 0, decay 0, v_format 0, chunk 0) is the
+ * method as the paper describes it.
+ * Rows per (batch, KV head): R = budget + chunk - 1 with chunk >= 2, else
+ * R = budget; the state calls below return R rows per unit. */
 typedef struct {
   int32_t batch;
   int32_t heads;     /* query heads */
@@ -80,13 +84,22 @@ typedef struct {
   int32_t v_format;  /* HE_VFMT_ELEM, or HE_VFMT_INT8: each value row v is stored as
                         q = v / s rounded half to even with s = max|v| / 127 (fp32), and
                         attended as q * s; keys, codes and evictions are unchanged */
+  int32_t chunk;     /* chunk eviction c (the ChunkKV page's chunks of contiguous
+                        tokens applied to the method's scores): the budget is cut into
+                        budget / c aligned chunks of c slots, a chunk scores the sum of
+                        its slots' distances; once the cache is full, new tokens are
+                        staged (and attended) in the c - 1 rows after the budget, and
+                        the token that would overflow the stage evicts the chunk with
+                        the largest score (ties: lowest chunk): the staged tokens in
+                        arrival order, then that token, take the chunk's slots.
+                        0 or 1 = the method (one slot at a time) */
 } he_cfg;
 
 typedef struct he_ctx* he_handle;
 
 /* Creates a handle on the current CUDA device and allocates, in device memory
- * owned by the handle: the cache K, V [batch][kv_heads][budget][head_dim], the
- * codes [batch][kv_heads][budget] (bits/8-byte words), W [head_dim][bits] drawn
+ * owned by the handle: the cache K, V [batch][kv_heads][R][head_dim], the
+ * codes [batch][kv_heads][R] (bits/8-byte words), W [head_dim][bits] drawn
  * from cfg->seed (see he_get_projection) and the step's scratch.
  * Errors: HE_EINVAL (cfg or out NULL, unsupported sizes), HE_ENOMEM, HE_ECUDA. */
 int he_create(const he_cfg* cfg, he_handle* out);
@@ -115,15 +128,16 @@ int he_step_host(he_handle h, const void* q, const void* k, const void* v, float
 /* Frees everything the handle owns.  NULL-safe.  Synchronises the device. */
 int he_destroy(he_handle h);
 
-/* Slots written by the last step, host [batch][kv_heads]: the evicted slot, or
- * -1 when the token was appended to a cache not yet full.  Synchronises.
+/* Slots written by the last step, host [batch][kv_heads]: the evicted slot (with
+ * chunk eviction, the evicted chunk's first slot), or -1 when the token was
+ * appended to a cache not yet full (or staged).  Synchronises.
  * Also returns HE_EDEVICE if a kernel of this handle reported an internal error. */
 int he_last_evicted(he_handle h, int32_t* host_slots);
 
 /* Snapshot of the cache into host buffers (any may be NULL):
- * K, V [batch][kv_heads][budget][head_dim] (element type; V int8 with an int8
- * value cache), codes
- * [batch][kv_heads][budget] (bits/8-byte words), occupancy (one int).  Synchronises. */
+ * K, V [batch][kv_heads][R][head_dim] (element type; V int8 with an int8
+ * value cache), codes [batch][kv_heads][R] (bits/8-byte words), occupancy
+ * (one int: resident rows, staged ones included).  Synchronises. */
 int he_read_state(he_handle h, void* K, void* V, void* codes, int32_t* occupancy);
 
 /* The projection matrix W [head_dim][bits] (element type), host.  W[d][j] is a
@@ -141,7 +155,7 @@ int he_codes(he_handle h, const void* x, int32_t n, void* codes, void* stream);
 
 /* Group-summed Hamming distances of every resident slot to the step's query
  * (method step 3) without changing the cache: q device [batch][heads][head_dim],
- * dist device int32 [batch][kv_heads][budget] (slots >= occupancy get 0).
+ * dist device int32 [batch][kv_heads][R] (slots >= occupancy get 0).
  * Errors: HE_EINVAL, HE_ENOTFILLED, HE_ECUDA. */
 int he_scores(he_handle h, const void* q, int32_t* dist, void* stream);
 

@@ -20,7 +20,8 @@ _vp = ctypes.c_void_p
 class HeCfg(ctypes.Structure):
     _fields_ = [("batch", _i32), ("heads", _i32), ("kv_heads", _i32), ("head_dim", _i32),
                 ("bits", _i32), ("budget", _i32), ("dtype", _i32), ("threshold", ctypes.c_float),
-                ("seed", ctypes.c_uint64), ("decay", ctypes.c_float), ("v_format", _i32)]
+                ("seed", ctypes.c_uint64), ("decay", ctypes.c_float), ("v_format", _i32),
+                ("chunk", _i32)]
 
 
 class HashEvictError(RuntimeError):
@@ -209,13 +210,15 @@ class HashEvict:
 
     def __init__(self, batch: int, heads: int, kv_heads: int, head_dim: int, bits: int,
                  budget: int, dtype: str = "bf16", seed: int = 0, threshold: float = 0.0,
-                 decay: float = 0.0, v_int8: bool = False):
+                 decay: float = 0.0, v_int8: bool = False, chunk: int = 1):
         self.cfg = HeCfg(batch=batch, heads=heads, kv_heads=kv_heads, head_dim=head_dim,
                          bits=bits, budget=budget,
                          dtype=HE_DTYPE_FP32 if dtype == "fp32" else HE_DTYPE_BF16,
                          threshold=threshold, seed=seed, decay=decay,
-                         v_format=HE_VFMT_INT8 if v_int8 else HE_VFMT_ELEM)
+                         v_format=HE_VFMT_INT8 if v_int8 else HE_VFMT_ELEM, chunk=chunk)
         self.v_int8 = v_int8
+        # rows per unit: the budget, plus chunk - 1 staging rows with chunk eviction
+        self.rows = budget + max(chunk, 1) - 1
         self.dtype = dtype
         self.h = he_create(self.cfg)
 
@@ -261,15 +264,15 @@ class HashEvict:
         return a
 
     def state(self):
-        """Host snapshot: K, V [batch][kv][budget][D] (uint16 bf16 bits or float32),
-        codes [batch][kv][budget] (uint8/16/32/64), occupancy."""
+        """Host snapshot: K, V [batch][kv][rows][D] (uint16 bf16 bits or float32),
+        codes [batch][kv][rows] (uint8/16/32/64), occupancy."""
         import numpy as np
         c = self.cfg
         et = np.float32 if self.dtype == "fp32" else np.uint16
         ct = {8: np.uint8, 16: np.uint16, 32: np.uint32, 64: np.uint64}[c.bits]
-        K = np.empty((c.batch, c.kv_heads, c.budget, c.head_dim), et)
+        K = np.empty((c.batch, c.kv_heads, self.rows, c.head_dim), et)
         V = np.empty(K.shape, np.int8 if self.v_int8 else et)
-        codes = np.empty((c.batch, c.kv_heads, c.budget), ct)
+        codes = np.empty((c.batch, c.kv_heads, self.rows), ct)
         occ = np.zeros(1, np.int32)
         he_read_state(self.h, K, V, codes, occ)
         return K, V, codes, int(occ[0])
@@ -278,7 +281,7 @@ class HashEvict:
         """Per-slot value scales [batch][kv_heads][budget] (int8 value cache only)."""
         import numpy as np
         c = self.cfg
-        a = np.empty((c.batch, c.kv_heads, c.budget), np.float32)
+        a = np.empty((c.batch, c.kv_heads, self.rows), np.float32)
         he_read_vscales(self.h, a)
         return a
 
@@ -286,7 +289,7 @@ class HashEvict:
         """Per-slot eviction scores [batch][kv_heads][budget] (score memory only)."""
         import numpy as np
         c = self.cfg
-        a = np.empty((c.batch, c.kv_heads, c.budget), np.float32)
+        a = np.empty((c.batch, c.kv_heads, self.rows), np.float32)
         he_read_scores(self.h, a)
         return a
 

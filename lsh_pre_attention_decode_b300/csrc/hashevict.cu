@@ -43,6 +43,9 @@ struct Kernels {
   int rec_floats;
   bool tc;  // tensor-core pipeline (tensor maps, programmatic dependent launch)
   const void* vq_fill;  // int8 value cache: quantisation of filled value rows
+  const void* prep_chunk;   // bf16 pipeline with chunk eviction
+  const void* merge_chunk;
+  int chunk_floats;         // floats of the per-unit chunk record
 };
 
 template <int D, int G>
@@ -64,6 +67,11 @@ Kernels kernels_for() {
     k.prep_mem = reinterpret_cast<const void*>(&he::prep_kernel<D, G, true, VQ>);
     k.merge = reinterpret_cast<const void*>(&he::merge_kernel<D, G, VQ>);
     k.vq_fill = reinterpret_cast<const void*>(&he::vq_fill_kernel<D>);
+    if constexpr (!VQ) {
+      k.prep_chunk = reinterpret_cast<const void*>(&he::prep_kernel<D, G, false, false, true>);
+      k.merge_chunk = reinterpret_cast<const void*>(&he::merge_kernel<D, G, false, true>);
+      k.chunk_floats = he::ChunkRec<G, D>::FLOATS;
+    }
     k.step_smem = S::SMEM_ALLOC;
     k.step_threads = S::NT;
     k.prep_smem = he::PrepShape<D, G>::SMEM;
@@ -226,6 +234,10 @@ struct he_ctx {
   he::UnitOut* uo = nullptr;  // bf16 pipeline: per-unit results of prep
   int kpar = 0;               // parity of the next step's eviction key
   int prev_w1 = 0;            // the previous step's written slot (StepParams::prev_w1)
+  int chunk = 1;              // slots per evicted chunk (1: the method)
+  int rows = 0;               // rows per unit: budget + chunk - 1 (the stride of K, V, codes)
+  float* cstar = nullptr;     // chunk eviction: the evicted chunk's softmax parts, per unit
+  int nopre = 0;              // the previous step moved rows (StepParams::nopre)
   void* sq = nullptr;  // he_step_host staging
   void* sk = nullptr;
   void* sv = nullptr;
@@ -273,7 +285,7 @@ void free_profile(he_ctx* h) {
 void free_all(he_ctx* h) {
   free_profile(h);
   void* ptrs[] = {h->K, h->V, h->W, h->codes, h->evicted, h->counters, h->err, h->partials,
-                  h->score, h->vs,
+                  h->score, h->vs, h->cstar,
                   h->uo, h->sq, h->sk, h->sv, h->sout};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -291,14 +303,17 @@ StepParams base_params(const he_ctx* h) {
   p.err = h->err;
   p.U = h->U;
   p.kv_heads = h->cfg.kv_heads;
-  p.budget = h->cfg.budget;
+  p.budget = h->rows;
+  p.lbudget = h->cfg.budget;
+  p.chunk = h->chunk;
+  p.cstar = h->cstar;
   p.occ = h->occupancy;
   p.tile = h->kern.tile;
   p.tpu = (h->occupancy + p.tile - 1) / p.tile;
   p.total_tiles = h->U * p.tpu;
   p.bits = h->cfg.bits;
   p.code_stride = h->code_stride;
-  p.append_slot = h->occupancy < h->cfg.budget ? h->occupancy : -1;
+  p.append_slot = h->occupancy < h->rows ? h->occupancy : -1;  // (or staged)
   p.qscale = (float)(1.4426950408889634 / std::sqrt((double)h->cfg.head_dim));
   p.vs = h->vs;
   p.vs_stride = h->vs_stride;
@@ -351,14 +366,20 @@ int he_create(const he_cfg* cfg, he_handle* out) {
   if (c.v_format != HE_VFMT_ELEM && !(c.v_format == HE_VFMT_INT8 && c.dtype == HE_DTYPE_BF16))
     return HE_EINVAL;
   if (!std::isfinite(c.threshold) || !(c.decay >= 0.0f && c.decay <= 1.0f)) return HE_EINVAL;
+  if (c.chunk < 0 || c.chunk > he::kMaxChunk) return HE_EINVAL;
+  const int chunk = c.chunk > 1 ? c.chunk : 1;
+  if (chunk > 1 && (c.dtype != HE_DTYPE_BF16 || c.v_format != HE_VFMT_ELEM || c.decay != 0.0f ||
+                    c.budget % chunk != 0))
+    return HE_EINVAL;
+  const int rows = c.budget + chunk - 1;
   if ((int64_t)c.batch * c.kv_heads > 65536) return HE_EINVAL;
   const int G = c.heads / c.kv_heads;
   Kernels kern;
   const bool vq = c.v_format == HE_VFMT_INT8;
   if (!pick_kernels(c.dtype, c.head_dim, G, vq, &kern)) return HE_EINVAL;
   const int64_t U = (int64_t)c.batch * c.kv_heads;
-  if (U * ((c.budget + kern.tile - 1) / kern.tile) > INT32_MAX) return HE_EINVAL;
-  if (U * c.budget >= ((int64_t)1 << 31)) return HE_EINVAL;  // TMA row coordinate
+  if (U * ((rows + kern.tile - 1) / kern.tile) > INT32_MAX) return HE_EINVAL;
+  if (U * rows + kern.tile >= ((int64_t)1 << 31)) return HE_EINVAL;  // TMA row coordinate
 
   he_ctx* h = new (std::nothrow) he_ctx();
   if (!h) return HE_ENOMEM;
@@ -367,10 +388,12 @@ int he_create(const he_cfg* cfg, he_handle* out) {
   h->U = (int)U;
   h->eb = c.dtype == HE_DTYPE_FP32 ? 4 : 2;
   h->code_bytes = c.bits / 8;
-  h->code_stride = (int)(((int64_t)c.budget * h->code_bytes + 15) / 16 * 16);
+  h->code_stride = (int)(((int64_t)rows * h->code_bytes + 15) / 16 * 16);
   h->kern = kern;
   h->vq = vq;
-  h->vs_stride = (c.budget + 63) / 64 * 64;
+  h->chunk = chunk;
+  h->rows = rows;
+  h->vs_stride = (rows + 63) / 64 * 64;
   if (cudaGetDevice(&h->device) != cudaSuccess) {
     (void)cudaGetLastError();
     delete h;
@@ -382,6 +405,18 @@ int he_create(const he_cfg* cfg, he_handle* out) {
         cudaSuccess) { rc = HE_ECUDA; break; }
     if (cudaFuncSetAttribute(kern.step, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kern.step_smem) != cudaSuccess) { rc = HE_ECUDA; break; }
+    if (chunk > 1 &&
+        (cudaFuncSetAttribute(kern.prep_chunk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kern.prep_smem) != cudaSuccess ||
+         cudaFuncSetAttribute(kern.prep_chunk, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+         cudaFuncSetAttribute(kern.merge_chunk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kern.merge_smem) != cudaSuccess ||
+         cudaFuncSetAttribute(kern.merge_chunk, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)) {
+      rc = HE_ECUDA;
+      break;
+    }
     // the three kernels of the bf16 pipeline run side by side on an SM: give
     // them one L1/shared split so that none waits for the SM to reconfigure
     if (kern.tc &&
@@ -410,8 +445,8 @@ int he_create(const he_cfg* cfg, he_handle* out) {
     h->max_ctas = h->num_sms * h->ctas_per_sm;
     // one spare tile of rows after the last unit keeps every tile load in bounds;
     // the cache starts zeroed so rows no token has written are finite
-    const size_t cache = ((size_t)U * c.budget + kern.tile) * c.head_dim * h->eb;
-    const size_t vcache = vq ? ((size_t)U * c.budget + kern.tile) * c.head_dim : cache;
+    const size_t cache = ((size_t)U * rows + kern.tile) * c.head_dim * h->eb;
+    const size_t vcache = vq ? ((size_t)U * rows + kern.tile) * c.head_dim : cache;
     const size_t nrec = (size_t)h->max_ctas + (size_t)U;
     struct { void** p; size_t bytes; } allocs[] = {
         {&h->K, cache},
@@ -424,7 +459,8 @@ int he_create(const he_cfg* cfg, he_handle* out) {
         {(void**)&h->err, sizeof(int32_t)},
         {(void**)&h->partials, nrec * kern.rec_floats * sizeof(float)},
         {(void**)&h->uo, (size_t)U * sizeof(he::UnitOut)},
-        {(void**)&h->score, c.decay > 0.0f ? (size_t)U * c.budget * sizeof(float) : 0},
+        {(void**)&h->score, c.decay > 0.0f ? (size_t)U * rows * sizeof(float) : 0},
+        {(void**)&h->cstar, chunk > 1 ? (size_t)U * kern.chunk_floats * sizeof(float) : 0},
     };
     for (auto& a : allocs) {
       if (a.bytes == 0) continue;
@@ -445,10 +481,10 @@ int he_create(const he_cfg* cfg, he_handle* out) {
       rc = HE_ECUDA;
       break;
     }
-    const uint64_t rows = (uint64_t)U * c.budget + kern.tile;
-    if (kern.tc && (!encode_cache_map(&h->tmK, h->K, rows, c.head_dim, kern.tile) ||
-                     !(vq ? encode_vq_map(&h->tmV, h->V, rows, c.head_dim, kern.tile)
-                          : encode_cache_map(&h->tmV, h->V, rows, c.head_dim, kern.tile)))) {
+    const uint64_t mrows = (uint64_t)U * rows + kern.tile;
+    if (kern.tc && (!encode_cache_map(&h->tmK, h->K, mrows, c.head_dim, kern.tile) ||
+                     !(vq ? encode_vq_map(&h->tmV, h->V, mrows, c.head_dim, kern.tile)
+                          : encode_cache_map(&h->tmV, h->V, mrows, c.head_dim, kern.tile)))) {
       rc = HE_ECUDA;
       break;
     }
@@ -489,31 +525,32 @@ int he_fill(he_handle h, const void* K, const void* V, int32_t n, void* stream) 
   cudaStream_t s = (cudaStream_t)stream;
   const size_t row = (size_t)h->cfg.head_dim * h->eb;
   if (n > 0) {
-    HE_TRY(h, cudaMemcpy2DAsync(h->K, (size_t)h->cfg.budget * row, K, (size_t)n * row,
+    HE_TRY(h, cudaMemcpy2DAsync(h->K, (size_t)h->rows * row, K, (size_t)n * row,
                                 (size_t)n * row, (size_t)h->U, cudaMemcpyDeviceToDevice, s));
     if (h->vq) {  // value rows quantised into the int8 cache
       const int64_t rows = (int64_t)h->U * n;
       int64_t blocks = (rows + 7) / 8;
       if (blocks > (int64_t)h->num_sms * 16) blocks = (int64_t)h->num_sms * 16;
-      int nn = n, budget = h->cfg.budget, vstride = h->vs_stride;
+      int nn = n, budget = h->rows, vstride = h->vs_stride;
       int8_t* Vq = reinterpret_cast<int8_t*>(h->V);
       float* vs = h->vs;
       void* args[] = {(void*)&V, (void*)&rows, (void*)&nn, (void*)&budget, (void*)&Vq,
                       (void*)&vs, (void*)&vstride};
       HE_TRY(h, cudaLaunchKernel(h->kern.vq_fill, dim3((unsigned)blocks), dim3(256), args, 0, s));
     } else {
-      HE_TRY(h, cudaMemcpy2DAsync(h->V, (size_t)h->cfg.budget * row, V, (size_t)n * row,
+      HE_TRY(h, cudaMemcpy2DAsync(h->V, (size_t)h->rows * row, V, (size_t)n * row,
                                   (size_t)n * row, (size_t)h->U, cudaMemcpyDeviceToDevice, s));
     }
-    const int rc = launch_codes(h, h->K, (int64_t)h->U * n, n, h->cfg.budget, h->codes,
+    const int rc = launch_codes(h, h->K, (int64_t)h->U * n, n, h->rows, h->codes,
                                 h->code_stride, s);
     if (rc != HE_OK) return rc;
   }
   HE_TRY(h, cudaMemsetAsync(h->counters, 0, (size_t)h->U * sizeof(int32_t), s));
   if (h->uo) HE_TRY(h, cudaMemsetAsync(h->uo, 0, (size_t)h->U * sizeof(he::UnitOut), s));
   if (h->score)  // filled slots start with no accumulated score
-    HE_TRY(h, cudaMemsetAsync(h->score, 0, (size_t)h->U * h->cfg.budget * sizeof(float), s));
+    HE_TRY(h, cudaMemsetAsync(h->score, 0, (size_t)h->U * h->rows * sizeof(float), s));
   h->prev_w1 = 0;  // no step has written a slot of the filled cache
+  h->nopre = 0;
   h->occupancy = n;
   h->filled = true;
   return HE_OK;
@@ -553,12 +590,16 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
     }
   } else {
     const bool full = p.append_slot < 0;
-    int splits = full ? (p.occ + he::kPrepChunk - 1) / he::kPrepChunk : 1;
+    const bool ch = h->chunk > 1;
+    // prep items: code slots of the budget per CTA (the chunk path: whole chunks)
+    const int item = ch ? he::chunk_item_slots(h->chunk) : he::kPrepItem;
+    int splits = full ? (h->cfg.budget + item - 1) / item : 1;
     if (splits < 1) splits = 1;
     he::UnitOut* uo = h->uo;
     p.uo = uo;
     p.kpar = h->kpar;
     p.prev_w1 = h->prev_w1;
+    p.nopre = h->nopre;
     if (stream_ctas > 0) {
       void* sa[] = {(void*)&p, (void*)&h->tmK, (void*)&h->tmV};
       HE_TRY(h, launch_pdl(h->kern.step, dim3(stream_ctas), dim3(h->kern.step_threads),
@@ -568,7 +609,8 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
     int first_of_step = stream_ctas > 0 ? 0 : 1;
     void* pa[] = {(void*)&p, (void*)&uo, (void*)&splits, (void*)&first_of_step};
     const int prep_ctas = h->U * splits < h->num_sms ? h->U * splits : h->num_sms;
-    HE_TRY(h, launch_pdl(h->score ? h->kern.prep_mem : h->kern.prep, dim3(prep_ctas),
+    HE_TRY(h, launch_pdl(ch ? h->kern.prep_chunk : (h->score ? h->kern.prep_mem : h->kern.prep),
+                         dim3(prep_ctas),
                          dim3(he::kPrepThreads),
                          (size_t)h->kern.prep_smem, s, pa));
     if (ev) HE_TRY(h, cudaEventRecord(ev[2], s));
@@ -579,7 +621,8 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
     const int nmax = TT > 0 ? (int)(((int64_t)p.tpu * stream_ctas + TT - 1) / TT) + 1 : 0;
     int msmem = 0;
     const int mthreads = h->kern.merge_cfg(nmax, &msmem);
-    HE_TRY(h, launch_pdl(h->kern.merge, dim3(h->U), dim3(mthreads), (size_t)msmem, s, ma));
+    HE_TRY(h, launch_pdl(ch ? h->kern.merge_chunk : h->kern.merge, dim3(h->U), dim3(mthreads),
+                         (size_t)msmem, s, ma));
   }
   if (ev) {
     HE_TRY(h, cudaEventRecord(ev[3], s));
@@ -587,9 +630,14 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
   }
   if (h->kern.tc) {
     h->prev_w1 = p.append_slot >= 0 ? p.append_slot + 1 : -1;
+    h->nopre = h->chunk > 1 && p.append_slot < 0;  // a chunk eviction moved c rows
     h->kpar ^= 1;
   }
-  if (h->occupancy < h->cfg.budget) h->occupancy += 1;
+  // append (or stage); a chunk eviction returns the cache to its budget
+  if (h->occupancy < h->rows)
+    h->occupancy += 1;
+  else
+    h->occupancy = h->cfg.budget;
   return HE_OK;
 }
 
@@ -646,11 +694,11 @@ int he_read_state(he_handle h, void* K, void* V, void* codes, int32_t* occupancy
   DeviceGuard g(h->device);
   const int rc = check_device_error(h);
   if (rc != HE_OK) return rc;
-  const size_t cache = (size_t)h->U * h->cfg.budget * h->cfg.head_dim * h->eb;
+  const size_t cache = (size_t)h->U * h->rows * h->cfg.head_dim * h->eb;
   if (K) HE_TRY(h, cudaMemcpy(K, h->K, cache, cudaMemcpyDeviceToHost));
   if (V) HE_TRY(h, cudaMemcpy(V, h->V, h->vq ? cache / h->eb : cache, cudaMemcpyDeviceToHost));
   if (codes) {
-    const size_t w = (size_t)h->cfg.budget * h->code_bytes;
+    const size_t w = (size_t)h->rows * h->code_bytes;
     HE_TRY(h, cudaMemcpy2D(codes, w, h->codes, (size_t)h->code_stride, w, (size_t)h->U,
                            cudaMemcpyDeviceToHost));
   }
@@ -713,7 +761,7 @@ int he_read_scores(he_handle h, float* host_scores) {
   if (!g.ok) return fail_cuda(h, cudaErrorInvalidDevice);
   const int rc = check_device_error(h);
   if (rc != HE_OK) return rc;
-  HE_TRY(h, cudaMemcpy(host_scores, h->score, (size_t)h->U * h->cfg.budget * sizeof(float),
+  HE_TRY(h, cudaMemcpy(host_scores, h->score, (size_t)h->U * h->rows * sizeof(float),
                        cudaMemcpyDeviceToHost));
   return HE_OK;
 }
@@ -725,7 +773,7 @@ int he_read_vscales(he_handle h, float* host_scales) {
   if (!g.ok) return fail_cuda(h, cudaErrorInvalidDevice);
   const int rc = check_device_error(h);
   if (rc != HE_OK) return rc;
-  const size_t w = (size_t)h->cfg.budget * sizeof(float);
+  const size_t w = (size_t)h->rows * sizeof(float);
   HE_TRY(h, cudaMemcpy2D(host_scales, w, h->vs, (size_t)h->vs_stride * sizeof(float), w,
                          (size_t)h->U, cudaMemcpyDeviceToHost));
   return HE_OK;
@@ -743,8 +791,12 @@ int he_step_bytes(he_handle h, uint64_t* bytes) {
   const uint64_t e = (uint64_t)h->eb, w = (uint64_t)h->code_bytes;
   const uint64_t Bt = (uint64_t)h->cfg.batch, H = (uint64_t)h->cfg.heads;
   const uint64_t kv = h->vq ? D * e + D + 4 : 2 * D * e;  // bytes of one slot's key and value
-  *bytes = U * B * (kv + w)               // retained K, V and codes read
+  // chunk eviction: over a cycle of c steps the resident rows average
+  // B + (c - 1) / 2, and the c - 1 staged rows are read and written once more
+  const uint64_t c = (uint64_t)h->chunk;
+  *bytes = U * (2 * B + c - 1) / 2 * (kv + w)  // retained K, V and codes read
            + U * (kv + w)                 // the overwritten slot
+           + U * 2 * (c - 1) * (kv + w) / c  // staged rows moved into the evicted chunk
            + Bt * H * D * e + U * 2 * D * e  // q, k, v in
            + Bt * H * D * 4                // out
            + D * (uint64_t)h->cfg.bits * e;  // W

@@ -32,7 +32,7 @@ namespace he {
 struct UnitOut;  // bf16 pipeline: per-unit results of the codes/eviction kernel
 
 struct StepParams {
-  void* K;               // cache keys   [U][budget][D]
+  void* K;               // cache keys   [U][budget][D] (budget: rows per unit, the stride)
   void* V;               // cache values [U][budget][D]
   unsigned char* codes;  // [U][code_stride] words of bits/8 bytes
   const void* W;         // projection [D][bits]
@@ -66,6 +66,15 @@ struct StepParams {
   UnitOut* uo;
   int32_t kpar;
   int32_t prev_w1;
+  // chunk eviction (bf16 pipeline): chunk c > 1 evicts aligned chunks of c
+  // slots of the first lbudget (a multiple of c); the rows [lbudget, budget)
+  // stage the newest tokens; cstar holds the evicted chunk's logits and value
+  // rows (per unit); nopre: the previous step moved rows, so the stream kernel
+  // fetches no tile before it waits for that step
+  int32_t lbudget;
+  int32_t chunk;
+  int32_t nopre;
+  void* cstar;
 #ifdef HE_TIMELINE
   int32_t tl_step;       // diagnostic builds: step slot of the stamps
 #endif

@@ -3,7 +3,7 @@
 // critical path: it is computed concurrently with the attention, and the
 // evicted slot is taken out of the attention afterwards.
 //
-//   prep   (one CTA per unit and code chunk)  method steps 1-4: project the G
+//   prep   (one CTA per unit and code item)  method steps 1-4: project the G
 //          query heads and the new key onto W and binarise (the fixed-order
 //          fp32 chains of the specification), form the new token's attention
 //          logits, scan a chunk of the unit's packed codes (XOR + popcount,
@@ -57,6 +57,26 @@ struct UnitOut {
   int32_t pad2[3];
 };
 
+// Chunk eviction: what merge needs to take the evicted chunk out of the
+// attention, per unit.  The chunk's slots fall in at most two 64-slot tiles
+// (part 0: the tile of its first slot, part 1: the next one); per part and
+// query head, the base-2 softmax state of the part's slots alone: max m, sum
+// l = sum exp2(x - m), accumulator a[D] = sum exp2(x - m) v.  An empty part
+// has m = -1e30, l = 0, a = 0.  Layout (floats): m [2][8], l [2][8], a [2][G][D].
+constexpr int kMaxChunk = 16;
+template <int G, int D>
+struct ChunkRec {
+  static constexpr int M = 0, L = 16, A = 32;
+  static constexpr int FLOATS = A + 2 * G * D;
+};
+
+// Slots per prep item with chunks of c slots: a multiple of c and of 16 (so
+// that an item's codes start on a 16-byte boundary for the bulk copy).
+__host__ __device__ __forceinline__ int chunk_item_slots(int c) {
+  const int l = 16 * c / (c & -c);  // lcm(c, 16) for 1 <= c <= 16
+  return 4096 / l * l;
+}
+
 // Partial record of one (stream CTA, unit): [m G][l G] padded to 4, acc [G][D].
 template <int G, int D>
 struct PRec {
@@ -68,26 +88,29 @@ struct PRec {
 // prep
 // ---------------------------------------------------------------------------
 constexpr int kPrepThreads = 128;  // one warp per SM sub-partition: fits beside two stream CTAs
-constexpr int kPrepChunk = 4096;  // code slots scanned per CTA
+constexpr int kPrepItem = 4096;  // code slots scanned per CTA item
 
 template <int D, int G>
 struct PrepShape {
   static constexpr int OFF_W = 0;                         // [D][bits] bf16, <= 16 KiB
   static constexpr int OFF_X = OFF_W + D * 64 * 2;        // (G+1) vectors [D] bf16
-  static constexpr int OFF_C = OFF_X + ((G + 1) * D * 2 + 15) / 16 * 16;  // code chunk
-  static constexpr int OFF_BITS = OFF_C + kPrepChunk * 8;
+  static constexpr int OFF_C = OFF_X + ((G + 1) * D * 2 + 15) / 16 * 16;  // the item's codes
+  static constexpr int OFF_BITS = OFF_C + kPrepItem * 8;
   static constexpr int OFF_RED = OFF_BITS + ((G + 1) * 64 / 32) * 4;
   static constexpr int OFF_BAR = (OFF_RED + 8 * 8 + 16 + 15) / 16 * 16;
   static constexpr int SMEM = OFF_BAR + 16;
 };
 
 // MEM: score memory (p.score, p.decay), a separate instantiation because its
-// register use is higher.  One CTA per SM at most: a CTA takes the (unit, code chunk) items
+// register use is higher.  CH: chunk eviction (p.chunk slots per chunk; the
+// chunks of the first p.lbudget slots score the sum of their slots' distances).
+// One CTA per SM at most: a CTA takes the (unit, code item) items
 // blockIdx.x, blockIdx.x + gridDim.x, ... in turn, so that prep never crowds
 // the stream kernel's CTAs off an SM.
-template <int D, int G, bool MEM, bool VQ = false>
+template <int D, int G, bool MEM, bool VQ = false, bool CH = false>
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, UnitOut* uo,
                                                             int splits, int first_of_step) {
+  static_assert(!(CH && (MEM || VQ)), "chunk eviction takes neither option");
   using S = PrepShape<D, G>;
   extern __shared__ __align__(16) unsigned char smem_prep[];
   unsigned char* smem = smem_prep;
@@ -120,8 +143,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
   uint32_t phase = 0;
   for (int it = blockIdx.x; it < nitems; it += gridDim.x, phase ^= 1u) {
     const int u = it / splits, split = it - u * splits;
-    const int s0 = split * kPrepChunk;
-    const int s1 = full ? min(s0 + kPrepChunk, p.occ) : s0;
+    const int item = CH ? chunk_item_slots(p.chunk) : kPrepItem;
+    const int s0 = split * item;
+    const int s1 = full ? min(s0 + item, CH ? p.lbudget : p.occ) : s0;
     if (tid == 0) {
       const int b = u / p.kv_heads, j = u - b * p.kv_heads;
       const uint32_t wbytes = it == (int)blockIdx.x ? (uint32_t)(D * bits * 2) : 0u;
@@ -167,7 +191,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
       const uint32_t word = __ballot_sync(kFull, bit);
       if (lane == 0) sbits[t0 >> 5] = word;
     }
-    // the new token's logits (only the unit's first chunk publishes them)
+    // the new token's logits (only the unit's first item publishes them)
     if (split == 0) {
       for (int g = warp; g < G; g += kPrepThreads / 32) {
         float a = 0.0f;
@@ -182,7 +206,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
     if (split == 0 && tid == 0) uo[u].codek = code_from_bits(sbits, bits, G);
 
     if (full) {
-      // method steps 3-4 on this chunk: the largest group-summed distance, lowest slot
+      // method steps 3-4 on this item: the largest group-summed distance, lowest slot
       uint64_t cq[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) cq[g] = code_from_bits(sbits, bits, g);
@@ -196,7 +220,17 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
           default: return *reinterpret_cast<const uint64_t*>(c);
         }
       };
-      if constexpr (!MEM) {  // (the method: 32 registers, so prep fits beside two stream CTAs)
+      if constexpr (CH) {
+        // a chunk [s, s + c) scores the sum of its slots' distances; the key
+        // carries its first slot, so ties go to the lowest chunk
+        const int c = p.chunk;
+        for (int s = s0 + tid * c; s < s1; s += kPrepThreads * c) {
+          uint32_t sum = 0;
+          for (int i = 0; i < c; ++i) sum += group_distance<G>(cq, code_at(s + i));
+          const uint64_t key = evict_key(sum, (uint32_t)s);
+          best = key > best ? key : best;
+        }
+      } else if constexpr (!MEM) {  // (the method: 32 registers, so prep fits beside two stream CTAs)
         for (int s = s0 + tid; s < s1; s += kPrepThreads) {
           const uint64_t key = evict_key(group_distance<G>(cq, code_at(s)), (uint32_t)s);
           best = key > best ? key : best;
@@ -206,7 +240,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
         // The scores of a batch of this thread's slots are all loaded before any
         // is used (one memory round trip per batch).
         constexpr int NB = 16;
-        constexpr int IT = kPrepChunk / kPrepThreads;
+        constexpr int IT = kPrepItem / kPrepThreads;
         static_assert(IT % NB == 0, "score batches");
         float* sc = p.score + (size_t)u * p.budget;
         for (int i0 = 0; i0 < IT; i0 += NB) {
@@ -244,26 +278,113 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
         // the unit's eviction is decided: hand merge the evicted slot's logits
         // and value row, so that merge needs no dependent load
         const int winner = (int)evict_key_slot(__ldcg(&uo[u].key[p.kpar]));
-        const uint16_t* Krow =
-            reinterpret_cast<const uint16_t*>(p.K) + ((size_t)u * p.budget + winner) * D;
-        const uint16_t* Vrow =
-            reinterpret_cast<const uint16_t*>(p.V) + ((size_t)u * p.budget + winner) * D;
-        for (int g = warp; g < G; g += kPrepThreads / 32) {
-          float a = 0.0f;
-          for (int d = lane; d < D; d += 32)
-            a = fmaf(__uint_as_float((uint32_t)xs[g * D + d] << 16),
-                     __uint_as_float((uint32_t)__ldcg(Krow + d) << 16), a);
-          a = warp_sum(a);
-          if (lane == 0) uo[u].lstar[g] = a * p.qscale;
-        }
-        if constexpr (VQ) {
-          const int8_t* Vq = reinterpret_cast<const int8_t*>(p.V) + ((size_t)u * p.budget + winner) * D;
-          for (int d = tid; d < D; d += kPrepThreads) uo[u].vqstar[d] = __ldcg(Vq + d);
-          if (tid == 0) uo[u].vsstar = __ldcg(p.vs + (size_t)u * p.vs_stride + winner);
+        if constexpr (CH) {
+          // the chunk's softmax parts (see ChunkRec): every key and value row
+          // of the chunk loaded at once (rows i = warp, warp + 4, ...), the
+          // logits, then per part and head the max, the sum and the accumulator
+          using CR = ChunkRec<G, D>;
+          constexpr int E = D / 32;  // elements of a row per lane
+          float* co = reinterpret_cast<float*>(p.cstar) + (size_t)u * CR::FLOATS;
+          // (a chunk outside the budget cannot be chosen; merge reports it)
+          const int c = (winner >= 0 && winner + p.chunk <= p.lbudget) ? p.chunk : 0;
+          // the item's code buffer is free now: logits [16][8], maxima [2][8],
+          // weights [16][8] (fp32), value rows [16][D] (bf16)
+          float* sl = reinterpret_cast<float*>(smem + S::OFF_C);
+          float* sm = sl + kMaxChunk * 8;
+          float* sw = sm + 16;
+          uint16_t* sv = reinterpret_cast<uint16_t*>(sw + kMaxChunk * 8);
+          const size_t rb = ((size_t)u * p.budget + winner) * D + (size_t)lane * E;
+          uint32_t kr[kMaxChunk / 4][E / 2], vr[kMaxChunk / 4][E / 2];
+#pragma unroll
+          for (int r = 0; r < kMaxChunk / 4; ++r) {
+            const int i = warp + 4 * r;
+            if (i < c) {
+              const uint32_t* kp = reinterpret_cast<const uint32_t*>(
+                  reinterpret_cast<const uint16_t*>(p.K) + rb + (size_t)i * D);
+              const uint32_t* vp = reinterpret_cast<const uint32_t*>(
+                  reinterpret_cast<const uint16_t*>(p.V) + rb + (size_t)i * D);
+#pragma unroll
+              for (int e = 0; e < E / 2; ++e) {
+                kr[r][e] = __ldcg(kp + e);
+                vr[r][e] = __ldcg(vp + e);
+              }
+            }
+          }
+#pragma unroll
+          for (int r = 0; r < kMaxChunk / 4; ++r) {
+            const int i = warp + 4 * r;
+            if (i < c) {
+#pragma unroll
+              for (int g = 0; g < G; ++g) {
+                float a = 0.0f;
+#pragma unroll
+                for (int e = 0; e < E / 2; ++e) {
+                  a = fmaf(__uint_as_float((uint32_t)xs[g * D + lane * E + 2 * e] << 16),
+                           bf16_lo(kr[r][e]), a);
+                  a = fmaf(__uint_as_float((uint32_t)xs[g * D + lane * E + 2 * e + 1] << 16),
+                           bf16_hi(kr[r][e]), a);
+                }
+                a = warp_sum(a);
+                if (lane == 0) sl[i * 8 + g] = a * p.qscale;
+              }
+#pragma unroll
+              for (int e = 0; e < E / 2; ++e)
+                reinterpret_cast<uint32_t*>(sv + i * D + lane * E)[e] = vr[r][e];
+            }
+          }
+          __syncthreads();
+          const int t0 = winner / p.tile;
+          auto part_of = [&](int i) { return (winner + i) / p.tile != t0 ? 1 : 0; };
+          if (tid < 2 * G) {
+            const int part = tid / G, g = tid - part * G;
+            float m = -1e30f;
+            for (int i = 0; i < c; ++i)
+              if (part_of(i) == part) m = fmaxf(m, sl[i * 8 + g]);
+            float l = 0.0f;
+            for (int i = 0; i < c; ++i)
+              if (part_of(i) == part) l += exp2f(sl[i * 8 + g] - m);
+            sm[part * 8 + g] = m;
+            co[CR::M + part * 8 + g] = m;
+            co[CR::L + part * 8 + g] = l;
+          }
+          __syncthreads();
+          if (tid < c * G) {
+            const int i = tid / G, g = tid - i * G;
+            sw[i * 8 + g] = exp2f(sl[i * 8 + g] - sm[part_of(i) * 8 + g]);
+          }
+          __syncthreads();
+          for (int idx = tid; idx < 2 * G * D; idx += kPrepThreads) {
+            const int part = idx / (G * D), rem = idx - part * (G * D);
+            const int g = rem / D, d = rem - g * D;
+            float a = 0.0f;
+            for (int i = 0; i < c; ++i)
+              if (part_of(i) == part)
+                a = fmaf(sw[i * 8 + g], __uint_as_float((uint32_t)sv[i * D + d] << 16), a);
+            co[CR::A + idx] = a;
+          }
+          if (tid == 0) uo[u].arrived = 0;
         } else {
-          for (int d = tid; d < D; d += kPrepThreads) uo[u].vstar[d] = __ldcg(Vrow + d);
+          const uint16_t* Krow =
+              reinterpret_cast<const uint16_t*>(p.K) + ((size_t)u * p.budget + winner) * D;
+          const uint16_t* Vrow =
+              reinterpret_cast<const uint16_t*>(p.V) + ((size_t)u * p.budget + winner) * D;
+          for (int g = warp; g < G; g += kPrepThreads / 32) {
+            float a = 0.0f;
+            for (int d = lane; d < D; d += 32)
+              a = fmaf(__uint_as_float((uint32_t)xs[g * D + d] << 16),
+                       __uint_as_float((uint32_t)__ldcg(Krow + d) << 16), a);
+            a = warp_sum(a);
+            if (lane == 0) uo[u].lstar[g] = a * p.qscale;
+          }
+          if constexpr (VQ) {
+            const int8_t* Vq = reinterpret_cast<const int8_t*>(p.V) + ((size_t)u * p.budget + winner) * D;
+            for (int d = tid; d < D; d += kPrepThreads) uo[u].vqstar[d] = __ldcg(Vq + d);
+            if (tid == 0) uo[u].vsstar = __ldcg(p.vs + (size_t)u * p.vs_stride + winner);
+          } else {
+            for (int d = tid; d < D; d += kPrepThreads) uo[u].vstar[d] = __ldcg(Vrow + d);
+          }
+          if (tid == 0) uo[u].arrived = 0;
         }
-        if (tid == 0) uo[u].arrived = 0;
       }
     }
     __syncthreads();  // the staging buffers are reused by the next item
@@ -400,7 +521,8 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ>::NT, 2)
   const int64_t TSS = (int64_t)p.U * tps, NCTA = gridDim.x;
   const int sb = (int)((int64_t)blockIdx.x * TSS / NCTA);
   const int se = (int)(((int64_t)blockIdx.x + 1) * TSS / NCTA);
-  const int npre = se - sb < NS ? se - sb : NS;  // tiles fetched before the wait
+  // tiles fetched before the wait (none after a step that moved whole rows)
+  const int npre = p.nopre ? 0 : (se - sb < NS ? se - sb : NS);
 
   // one stage: its descriptor, then (unless it is the sentinel) K, V and, at a
   // segment's first tile, the unit's query rows, all on the stage's barrier
@@ -809,6 +931,11 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ>::NT, 2)
 constexpr int kMergeMaxThreads = 512;
 constexpr int kMergeMinThreads = 512;
 constexpr int kMergeRegs = 8;  // partials held in registers per thread (more are looped)
+// Chunk eviction: the chunk is subtracted from its partials unless its weight
+// exceeds this many times the weight that remains (every partial and the new
+// token, per head); the subtraction's rounding error is then at most about
+// (1 + this) times the partials' own relative error, else merge recomputes.
+constexpr float kChunkRemoveMax = 16.0f;
 
 template <int D, int G>
 struct MergeShape {
@@ -824,13 +951,14 @@ struct MergeShape {
   }
 };
 
-// Exact partial over slots [lo, hi) of unit u without slot `skip` (CUDA cores,
-// fp32): per head the base-2 max, sum and accumulator -> xm, xl, xa [G][D].
+// Exact partial over slots [lo, hi) of unit u without the slots [skip,
+// skip + nskip) (CUDA cores, fp32): per head the base-2 max, sum and
+// accumulator -> xm, xl, xa [G][D].
 // Every warp of the CTA runs an online softmax over a strided share of the
 // slots (lane owns D/32 elements), then the warp states merge in a fixed order.
 template <int D, int G, bool VQ>
 __device__ void recompute_partial(const StepParams& p, int u, int lo, int hi, int skip,
-                                  const float* qf, float* wstate, float* xm, float* xl,
+                                  int nskip, const float* qf, float* wstate, float* xm, float* xl,
                                   float* xa, int tid) {
   constexpr int E = D / 32;
   const int RW = (int)(blockDim.x >> 5);
@@ -850,7 +978,7 @@ __device__ void recompute_partial(const StepParams& p, int u, int lo, int hi, in
       for (int e = 0; e < E; ++e) ar[g][e] = 0.0f;
     }
     for (int s = lo + warp; s < hi; s += RW) {
-      if (s == skip) continue;
+      if ((unsigned)(s - skip) < (unsigned)nskip) continue;
       float kx[E], vx[E];
 #pragma unroll
       for (int e = 0; e < E; ++e) {
@@ -938,9 +1066,30 @@ __device__ __forceinline__ void fold_one(float mc, float lc, float4 x, bool is_c
   mx = mn;
 }
 
-template <int D, int G, bool VQ = false>
+// Chunk eviction: take part(s) of the evicted chunk (ChunkRec) out of a
+// partial (mc, lc, x); returns the weight taken out, which the caller compares
+// with half the partial's sum.
+__device__ __forceinline__ float take_part(float cm, float cl, const float4& ca, float mc,
+                                          float& lc, float4& x) {
+  const float sc = exp2f(cm - mc);
+  const float w = cl * sc;
+  lc -= w;
+  x.x -= ca.x * sc;
+  x.y -= ca.y * sc;
+  x.z -= ca.z * sc;
+  x.w -= ca.w * sc;
+  return w;
+}
+
+// CH: chunk eviction.  At a full step the key names the evicted chunk's first
+// slot; its c slots leave the (at most two) partials that hold them, the
+// staged rows [lbudget, lbudget + c - 1) move to the chunk's first c - 1
+// slots and the new token takes its last.  Other steps append (stage) the
+// token at p.append_slot, as the method does.
+template <int D, int G, bool VQ = false, bool CH = false>
 __global__ void __launch_bounds__(kMergeMaxThreads)
     merge_kernel(const StepParams p, UnitOut* uo, int stream_ctas) {
+  static_assert(!(CH && VQ), "chunk eviction keeps bf16 values");
   using R = PRec<G, D>;
   constexpr int GD4 = MergeShape<D, G>::GD4;
   const int MT = (int)blockDim.x, NQ = MT / GD4;
@@ -982,9 +1131,11 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
 
   // ---- loads, all independent ----
   const unsigned long long key = full ? __ldcg(&uo[u].key[p.kpar]) : 0ull;
-  const float lst = full ? __ldcg(&uo[u].lstar[g]) : 0.0f;
-  const uint2 vs2 = full ? __ldcg(reinterpret_cast<const uint2*>(uo[u].vstar + d0)) : make_uint2(0u, 0u);
+  const float lst = (full && !CH) ? __ldcg(&uo[u].lstar[g]) : 0.0f;
+  const uint2 vs2 = (full && !CH) ? __ldcg(reinterpret_cast<const uint2*>(uo[u].vstar + d0))
+                                  : make_uint2(0u, 0u);
   const float ln = __ldcg(&uo[u].lnew[g]);
+  const float lng = (CH && tid < G) ? __ldcg(&uo[u].lnew[tid]) : 0.0f;  // head tid's
   const unsigned long long codek = __ldcg(&uo[u].codek);
   const uint16_t* kt = reinterpret_cast<const uint16_t*>(p.k) + (size_t)u * D;
   const uint16_t* vtp = reinterpret_cast<const uint16_t*>(p.v) + (size_t)u * D;
@@ -992,6 +1143,37 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
   const uint16_t vt1 = tid < D ? __ldcg(vtp + tid) : (uint16_t)0;
   const uint2 vt2 = __ldcg(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(p.v) +
                                                           (size_t)u * D + d0));
+  // chunk eviction: the chunk's two softmax parts and the staged rows (one
+  // 16-byte piece per thread; their addresses do not depend on the decision)
+  float cm0 = -1e30f, cl0 = 0.0f, cm1 = -1e30f, cl1 = 0.0f;
+  float4 ca0 = make_float4(0.f, 0.f, 0.f, 0.f), ca1 = ca0;
+  uint4 srow = make_uint4(0u, 0u, 0u, 0u);
+  uint64_t scode = 0;
+  if constexpr (CH) {
+    if (full) {
+      using CR = ChunkRec<G, D>;
+      const float* cr = reinterpret_cast<const float*>(p.cstar) + (size_t)u * CR::FLOATS;
+      cm0 = __ldcg(cr + CR::M + g);
+      cl0 = __ldcg(cr + CR::L + g);
+      ca0 = __ldcg(reinterpret_cast<const float4*>(cr + CR::A) + o);
+      cm1 = __ldcg(cr + CR::M + 8 + g);
+      cl1 = __ldcg(cr + CR::L + 8 + g);
+      ca1 = __ldcg(reinterpret_cast<const float4*>(cr + CR::A + G * D) + o);
+      const int CH8 = D / 8, npc = (p.chunk - 1) * CH8;
+      if (tid < 2 * npc) {
+        const int arr = tid / npc, r = tid - arr * npc;
+        const uint16_t* base = reinterpret_cast<const uint16_t*>(arr ? p.V : p.K);
+        srow = __ldcg(reinterpret_cast<const uint4*>(
+                          base + ((size_t)u * p.budget + p.lbudget + r / CH8) * D) + r % CH8);
+      }
+      if (tid < p.chunk - 1) {
+        const int wb = p.bits >> 3;
+        const unsigned char* src =
+            p.codes + (size_t)u * p.code_stride + (size_t)(p.lbudget + tid) * wb;
+        for (int bb = 0; bb < wb; ++bb) scode |= (uint64_t)__ldcg(src + bb) << (8 * bb);
+      }
+    }
+  }
   float rm[kMergeRegs], rl[kMergeRegs];
   float4 rx[kMergeRegs];
 #pragma unroll
@@ -1006,15 +1188,23 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
   }
 
   const int winner = full ? (key ? (int)evict_key_slot(key) : -1) : p.append_slot;
-  if (winner < 0 || winner >= p.budget) {  // cannot happen: never write outside the cache
+  // slots evicted, and the end of the slots eviction may choose from
+  const int nev = (CH && full) ? p.chunk : 1;
+  const int wend = (CH && full) ? p.lbudget : p.budget;
+  if (winner < 0 || winner + nev > wend) {  // cannot happen: never write outside the cache
     if (tid == 0) atomicExch(p.err, 2);
     return;
   }
-  // the evicted slot's contributor: owner of tile winner / tile
-  // the evicted slot's contributor: the owner of tile winner / tile
+  // the evicted slot's contributor: the owner of tile winner / tile (with a
+  // chunk, crel .. crel_hi own its first and last slot)
   const int crel = (full && n > 0)
                        ? (int)((((int64_t)u * tps + winner / p.tile + 1) * NCT - 1) / TSS) - first
                        : -1;
+  const int crel_hi =
+      (CH && full && n > 0)
+          ? (int)((((int64_t)u * tps + (winner + nev - 1) / p.tile + 1) * NCT - 1) / TSS) - first
+          : crel;
+
   float4 vs = make_float4(__uint_as_float(vs2.x << 16), __uint_as_float(vs2.x & 0xFFFF0000u),
                           __uint_as_float(vs2.y << 16), __uint_as_float(vs2.y & 0xFFFF0000u));
   // int8 value cache: the evicted row as stored (q * s), and the new row's
@@ -1049,20 +1239,65 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
 
   float mx = -1e30f, sum = 0.0f;
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+  float rw = 0.0f;  // chunk eviction: the weight taken out, in the running max's frame
 #pragma unroll
   for (int i = 0; i < kMergeRegs; ++i) {
     const int c = q + i * NQ;
     if (c < n) {
-      if (c == crel && d0 == 0 && !(exp2f(lst - rm[i]) <= 0.5f * rl[i])) atomicExch(&sflag[0], 1);
-      fold_one<D, G>(rm[i], rl[i], rx[i], c == crel, lst, vs, mx, sum, a);
+      if constexpr (CH) {
+        if (full && (c == crel || c == crel_hi)) {
+          float w = 0.0f;
+          if (c == crel) w += take_part(cm0, cl0, ca0, rm[i], rl[i], rx[i]);
+          if (c == crel_hi) w += take_part(cm1, cl1, ca1, rm[i], rl[i], rx[i]);
+          const float mn = fmaxf(mx, rm[i]);
+          rw = rw * exp2f(mx - mn) + w * exp2f(rm[i] - mn);
+        }
+        fold_one<D, G>(rm[i], rl[i], rx[i], false, lst, vs, mx, sum, a);
+      } else {
+        if (c == crel && d0 == 0 && !(exp2f(lst - rm[i]) <= 0.5f * rl[i])) atomicExch(&sflag[0], 1);
+        fold_one<D, G>(rm[i], rl[i], rx[i], c == crel, lst, vs, mx, sum, a);
+      }
     }
   }
   for (int c = q + kMergeRegs * NQ; c < n; c += NQ) {
     const float* r = rec_of(c);
-    const float mc = __ldcg(r + g), lc = __ldcg(r + G + g);
-    const float4 x = __ldcg(reinterpret_cast<const float4*>(r + R::HDR) + o);
-    if (c == crel && d0 == 0 && !(exp2f(lst - mc) <= 0.5f * lc)) atomicExch(&sflag[0], 1);
-    fold_one<D, G>(mc, lc, x, c == crel, lst, vs, mx, sum, a);
+    const float mc = __ldcg(r + g);
+    float lc = __ldcg(r + G + g);
+    float4 x = __ldcg(reinterpret_cast<const float4*>(r + R::HDR) + o);
+    if constexpr (CH) {
+      if (full && (c == crel || c == crel_hi)) {
+        float w = 0.0f;
+        if (c == crel) w += take_part(cm0, cl0, ca0, mc, lc, x);
+        if (c == crel_hi) w += take_part(cm1, cl1, ca1, mc, lc, x);
+        const float mn = fmaxf(mx, mc);
+        rw = rw * exp2f(mx - mn) + w * exp2f(mc - mn);
+      }
+      fold_one<D, G>(mc, lc, x, false, lst, vs, mx, sum, a);
+    } else {
+      if (c == crel && d0 == 0 && !(exp2f(lst - mc) <= 0.5f * lc)) atomicExch(&sflag[0], 1);
+      fold_one<D, G>(mc, lc, x, c == crel, lst, vs, mx, sum, a);
+    }
+  }
+  if constexpr (CH) {
+    if (full) {
+      // the weight taken out against the weight that remains, per head
+      smax[tid] = mx;
+      ssum[tid] = sum;
+      wstate[tid] = rw;
+      __syncthreads();
+      if (tid < G) {
+        const int og = tid * (D / 4);  // head tid's first output group
+        float M = lng;
+        for (int q2 = 0; q2 < NQ; ++q2) M = fmaxf(M, smax[q2 * GD4 + og]);
+        float rem = exp2f(lng - M), out_w = 0.0f;
+        for (int q2 = 0; q2 < NQ; ++q2) {
+          const float f = exp2f(smax[q2 * GD4 + og] - M);
+          rem += ssum[q2 * GD4 + og] * f;
+          out_w += wstate[q2 * GD4 + og] * f;
+        }
+        if (!(out_w <= kChunkRemoveMax * rem)) atomicExch(&sflag[0], 1);
+      }
+    }
   }
   __syncthreads();
   const bool recomputed = sflag[0] != 0;
@@ -1071,16 +1306,17 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
     const uint16_t* qg = reinterpret_cast<const uint16_t*>(p.q) + (size_t)(b * p.kv_heads + j) * G * D;
     for (int i2 = tid; i2 < G * D; i2 += MT) qf[i2] = __uint_as_float((uint32_t)qg[i2] << 16);
     __syncthreads();
-    // the slots of that contributor
-    const int c = first + crel;
-    const int tb = (int)((int64_t)c * TSS / NCT), te = (int)(((int64_t)c + 1) * TSS / NCT);
+    // the slots of that contributor (with a chunk: of contributors crel .. crel_hi)
+    const int c = first + crel, ch = first + crel_hi;
+    const int tb = (int)((int64_t)c * TSS / NCT), te = (int)(((int64_t)ch + 1) * TSS / NCT);
     const int lo = (max(tb, u * tps) - u * tps) * p.tile;
     const int hi = min((min(te, (u + 1) * tps) - u * tps) * p.tile, p.occ);
-    recompute_partial<D, G, VQ>(p, u, lo, hi, winner, qf, wstate, xm, xl, xa, tid);
+    recompute_partial<D, G, VQ>(p, u, lo, hi, winner, nev, qf, wstate, xm, xl, xa, tid);
     mx = -1e30f;
     sum = 0.0f;
     a = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int c2 = q; c2 < n; c2 += NQ) {
+      if (c2 > crel && c2 <= crel_hi) continue;  // (a chunk's second contributor: in the first)
       if (c2 == crel) {
         fold_one<D, G>(xm[g], xl[g], reinterpret_cast<const float4*>(xa)[o], false, lst, vs, mx,
                        sum, a);
@@ -1127,19 +1363,42 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
     reinterpret_cast<float4*>(p.out + ((size_t)b * p.kv_heads * G + (size_t)j * G) * D)[tid] = r;
   }
 
+  // chunk eviction: the staged rows, keys, values and codes, in arrival order
+  // take the chunk's first c - 1 slots (rows of the stage are only read here)
+  int wslot = winner;
+  if constexpr (CH) {
+    if (full) {
+      const int c = nev, CH8 = D / 8, npc = (c - 1) * CH8;  // 16-byte pieces per array
+      const size_t ub = (size_t)u * p.budget;
+      for (int t = tid; t < 2 * npc; t += MT) {
+        const int arr = t / npc, r = t - arr * npc;
+        const int i = r / CH8, w = r - i * CH8;
+        uint16_t* base = reinterpret_cast<uint16_t*>(arr ? p.V : p.K);
+        // (the piece of this thread was loaded up front; more threads than pieces)
+        const uint4 x = t == tid ? srow
+                                 : __ldcg(reinterpret_cast<const uint4*>(
+                                              base + (ub + p.lbudget + i) * D) + w);
+        reinterpret_cast<uint4*>(base + (ub + winner + i) * D)[w] = x;
+      }
+      if (tid < c - 1)
+        store_code(p.codes + (size_t)u * p.code_stride + (size_t)(winner + tid) * (p.bits >> 3),
+                   p.bits, scode);
+      wslot = winner + c - 1;
+    }
+  }
   // method step 5: the current token's key, value and code replace the slot
-  uint16_t* Kw = reinterpret_cast<uint16_t*>(p.K) + ((size_t)u * p.budget + winner) * D;
+  uint16_t* Kw = reinterpret_cast<uint16_t*>(p.K) + ((size_t)u * p.budget + wslot) * D;
   if (tid < D) {
     Kw[tid] = kt1;
     if constexpr (VQ)
       reinterpret_cast<int8_t*>(p.V)[((size_t)u * p.budget + winner) * D + tid] =
           (int8_t)(int)vqrow[tid];
     else
-      reinterpret_cast<uint16_t*>(p.V)[((size_t)u * p.budget + winner) * D + tid] = vt1;
+      reinterpret_cast<uint16_t*>(p.V)[((size_t)u * p.budget + wslot) * D + tid] = vt1;
   }
   if (VQ && tid == 0) p.vs[(size_t)u * p.vs_stride + winner] = vscale;
   if (tid == 0) {
-    store_code(p.codes + (size_t)u * p.code_stride + (size_t)winner * (p.bits >> 3), p.bits,
+    store_code(p.codes + (size_t)u * p.code_stride + (size_t)wslot * (p.bits >> 3), p.bits,
                codek);
     p.evicted[u] = full ? winner : -1;
     if (p.score != nullptr) p.score[(size_t)u * p.budget + winner] = 0.0f;  // not scored yet

@@ -43,23 +43,24 @@ class GpuRun:
 
 
 def make_handle(w: synth.Workload, layer: int = 0, threshold: float = 0.0, decay: float = 0.0,
-                v_int8: bool = False):
+                v_int8: bool = False, chunk: int = 1):
     from lsh_pre_attention_decode_b300 import HashEvict
     return HashEvict(w.batch, w.heads, w.kv_heads, w.head_dim, w.bits, w.budget, w.dtype,
                      seed=w.projection_seed(layer), threshold=threshold, decay=decay,
-                     v_int8=v_int8)
+                     v_int8=v_int8, chunk=chunk)
 
 
 def run_gpu(w: synth.Workload, fill_n: int, steps: int, out_steps=(), layer: int = 0,
-            device_gen: bool = False, read_state: bool = False, chunk: int = 256,
+            device_gen: bool = False, read_state: bool = False, batch_tokens: int = 256,
             profile: bool = False, threshold: float = 0.0, decay: float = 0.0,
-            v_int8: bool = False) -> GpuRun:
-    """Fill with prompt tokens [0, fill_n), then stream tokens fill_n .. fill_n+steps-1.
-    With decay > 0 the returned state also holds the per-slot scores; with an
-    int8 value cache, V is int8 and the value scales follow."""
+            v_int8: bool = False, chunk: int = 1) -> GpuRun:
+    """Fill with prompt tokens [0, fill_n), then stream tokens fill_n .. fill_n+steps-1
+    (generated batch_tokens at a time).  With decay > 0 the returned state also
+    holds the per-slot scores; with an int8 value cache, V is int8 and the value
+    scales follow; chunk > 1: chunk eviction (state rows budget + chunk - 1)."""
     import torch
     out_steps = set(out_steps)
-    he = make_handle(w, layer, threshold, decay, v_int8)
+    he = make_handle(w, layer, threshold, decay, v_int8, chunk)
     try:
         if fill_n > 0:
             if device_gen:
@@ -77,8 +78,8 @@ def run_gpu(w: synth.Workload, fill_n: int, steps: int, out_steps=(), layer: int
         evicted = np.empty((steps, w.batch, w.kv_heads), np.int32)
         outs = {}
         out = torch.empty((w.batch, w.heads, w.head_dim), dtype=torch.float32, device="cuda")
-        for c0 in range(0, steps, chunk):
-            n = min(chunk, steps - c0)
+        for c0 in range(0, steps, batch_tokens):
+            n = min(batch_tokens, steps - c0)
             t0 = fill_n + c0
             if device_gen:
                 q = synth.gpu_queries(w, t0, n, layer)
@@ -118,12 +119,15 @@ class OracleRun:
 
 def run_oracle_unit(w: synth.Workload, b: int, j: int, fill_n: int, steps: int, out_steps=(),
                     layer: int = 0, threshold: float = 0.0, decay: float = 0.0,
-                    v_int8: bool = False) -> OracleRun:
+                    v_int8: bool = False, chunk: int = 1) -> OracleRun:
     o = oracle.load()
     W = o.projection(w.projection_seed(layer), w.head_dim, w.bits, w.dtype)
     Kin = synth.host_unit_kv(w, "key", b, j, 0, fill_n, layer)
     Vin = synth.host_unit_kv(w, "value", b, j, 0, fill_n, layer)
-    st = o.unit_fill(W, w.budget, Kin, Vin, tau=threshold, memory=decay > 0.0, vq=v_int8)
+    if chunk > 1:
+        st = o.unit_fill_chunk(W, w.budget, chunk, Kin, Vin, tau=threshold)
+    else:
+        st = o.unit_fill(W, w.budget, Kin, Vin, tau=threshold, memory=decay > 0.0, vq=v_int8)
     q = synth.host_unit_queries(w, b, j, fill_n, steps, layer)
     k = synth.host_unit_kv(w, "key", b, j, fill_n, steps, layer)
     v = synth.host_unit_kv(w, "value", b, j, fill_n, steps, layer)
@@ -136,11 +140,12 @@ def run_oracle_unit(w: synth.Workload, b: int, j: int, fill_n: int, steps: int, 
 
 
 def run_oracle_units(w, units, fill_n, steps, out_steps=(), layer=0, threads=8,
-                     threshold: float = 0.0, decay: float = 0.0, v_int8: bool = False):
+                     threshold: float = 0.0, decay: float = 0.0, v_int8: bool = False,
+                     chunk: int = 1):
     """Oracle over several (b, j) units in parallel threads (ctypes releases the GIL)."""
     with cf.ThreadPoolExecutor(max_workers=threads) as ex:
         futs = {u: ex.submit(run_oracle_unit, w, u[0], u[1], fill_n, steps, out_steps, layer,
-                             threshold, decay, v_int8)
+                             threshold, decay, v_int8, chunk)
                 for u in units}
         return {u: f.result() for u, f in futs.items()}
 

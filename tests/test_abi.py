@@ -51,7 +51,7 @@ def test_strerror(L):
 
 def cfg(**kw):
     d = dict(batch=1, heads=32, kv_heads=8, head_dim=128, bits=32, budget=256, dtype=0,
-             threshold=0.0, seed=1, decay=0.0, v_format=0)
+             threshold=0.0, seed=1, decay=0.0, v_format=0, chunk=0)
     d.update(kw)
     return pkg.HeCfg(**d)
 
@@ -63,7 +63,9 @@ def cfg(**kw):
                                  dict(v_format=1, dtype=1),
                                  dict(batch=70000), dict(decay=-0.5), dict(decay=1.5),
                                  dict(decay=float("nan")), dict(threshold=float("inf")),
-                                 dict(threshold=float("nan"))])
+                                 dict(threshold=float("nan")), dict(chunk=-1), dict(chunk=17),
+                                 dict(chunk=3), dict(chunk=2, dtype=1),
+                                 dict(chunk=2, v_format=1), dict(chunk=2, decay=0.5)])
 def test_create_rejects_bad_configs(L, bad):
     h = ctypes.c_void_p()
     assert L.he_create(ctypes.byref(cfg(**bad)), ctypes.byref(h)) == -1
