@@ -54,6 +54,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--bits", type=int, default=None, help="override the code length")
+    ap.add_argument("--budget", type=int, default=None,
+                    help="override the cache budget (e.g. a multiple of --chunk)")
     ap.add_argument("--layers", type=int, default=None,
                     help="independent layer caches rotated (default: the workload's own "
                          "layer count if above 1, else 4)")
@@ -169,6 +171,8 @@ def workload_from(args) -> synth.Workload:
     w = synth.WORKLOADS[args.workload]
     if args.bits:
         w = w.with_(bits=args.bits)
+    if args.budget:
+        w = w.with_(budget=args.budget, prompt=max(w.prompt, args.budget + 64))
     return w
 
 
@@ -177,7 +181,8 @@ def config_of(w: synth.Workload, args, extra=None):
             f"; threshold {args.threshold}, score memory {args.decay}"
             if (args.threshold or args.decay) else "") + (
             "; int8 value cache" if args.v_int8 else "") + (
-            f"; chunk eviction, chunks of {args.chunk} slots" if args.chunk > 1 else ""),
+            f"; chunk eviction, chunks of {args.chunk} slots" if args.chunk > 1 else "") + (
+            f"; budget set to {w.budget}" if args.budget else ""),
          "batch": w.batch, "heads": w.heads,
          "kv_heads": w.kv_heads, "head_dim": w.head_dim, "bits": w.bits, "budget": w.budget,
          "prompt": w.prompt, "dtype": w.dtype,
@@ -403,6 +408,28 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     merge_ms = prof["merge_ms"] / n_prof
     serial_step_ms = prof["step_ms"] / n_prof
 
+    # chunk eviction: the same timing mode step by step on layer 0's cache,
+    # split into evicting steps (the stage is full) and staging steps
+    by_type = None
+    if args.chunk > 1:
+        he0 = handles[0]
+        acc = {"evict": [0.0, 0.0, 0.0, 0], "stage": [0.0, 0.0, 0.0, 0]}
+        for t in range(8 * args.chunk):
+            kind = "evict" if he0.occupancy == he0.rows else "stage"
+            he0.profile_start(1)
+            rc = he_step_raw(hs[0], qp[0][t % R], kp[0][t % R], vp[0][t % R], op[0],
+                             stream.cuda_stream)
+            if rc:
+                raise HashEvictError("he_step", rc)
+            r = he0.profile_stop()
+            a = acc[kind]
+            a[0] += r["stream_ms"]
+            a[1] += r["prep_ms"]
+            a[2] += r["merge_ms"]
+            a[3] += 1
+        by_type = {k: {"steps": a[3], "stream_ms": a[0] / a[3], "prep_ms": a[1] / a[3],
+                       "merge_ms": a[2] / a[3]} for k, a in acc.items() if a[3]}
+
     step_bytes = handles[0].step_bytes
     info = handles[0].launch_info()
 
@@ -485,6 +512,7 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
                      "other_kernels_ms": {"prep (codes + eviction)": prep_ms,
                                           "merge (LSE merge + overwrite)": merge_ms,
                                           "serialised step": serial_step_ms},
+                     "by_step_type": by_type,
                      "step": {"algorithmic_bytes": step_bytes, "achieved": step_gbs,
                               "frac": step_gbs / peak,
                               "note": "he_step_bytes / ms_per_step of the timed region "

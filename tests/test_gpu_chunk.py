@@ -35,7 +35,7 @@ def _stream(w, fill_n, steps, out_every, chunk, threshold=0.0, units=None):
     return g, orc
 
 
-@pytest.mark.parametrize("chunk", [2, 3, 8, 16])
+@pytest.mark.parametrize("chunk", [2, 3, 8, 10, 16])
 @pytest.mark.parametrize("D,bits,heads", [(128, 32, 32), (64, 8, 8), (128, 64, 64)])
 def test_chunk_stream(chunk, D, bits, heads):
     """Appends below the budget, staging, several eviction cycles; ragged
