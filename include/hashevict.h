@@ -201,9 +201,25 @@ int he_profile_stop(he_handle h, float* ms, int32_t* steps);
 
 /* Number of times, since he_fill, that the attention partial holding the
  * evicted slot was recomputed exactly instead of having the slot's weight
- * subtracted (the slot carried more than half of that partial's softmax mass).
- * Always 0 for fp32 handles.  Synchronises. */
+ * subtracted (the slot carried more than half of that partial's softmax mass;
+ * with chunk eviction: the chunk outweighed 16 times the weight that remains in
+ * the unit).  Always 0 for fp32 handles.  Synchronises. */
 int he_recompute_count(he_handle h, int64_t* total);
+
+/* Checks of the failure paths.
+ * he_set_alloc_limit: a process-wide cap, in bytes, on the device memory one
+ * he_create may allocate (0 = no cap, the default).  A handle that would need
+ * more fails with HE_ENOMEM before allocating anything, as on an exhausted
+ * device.  Always returns HE_OK.
+ * he_wait_probe: launches on `stream` one kernel that waits on a barrier that
+ * nothing completes, through the same bounded wait as every kernel of the
+ * library, giving up after limit_us microseconds (1 .. 1,000,000).  On giving
+ * up it records the handle's device error flag and exits, as a step kernel
+ * does: the next synchronising call on the handle returns HE_EDEVICE and the
+ * handle refuses further work; other handles and the CUDA context stay usable.
+ * Errors: HE_EINVAL (NULL handle, limit out of range), HE_ECUDA. */
+int he_set_alloc_limit(uint64_t bytes);
+int he_wait_probe(he_handle h, uint32_t limit_us, void* stream);
 
 /* Allocation-free decode attention.  This entry point has no counterpart in
  * the method's description: it is an integration aid for callers that cannot

@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
         L.he_attend_noalloc.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp]
         L.he_read_scores.argtypes = [_vp, _vp]
         L.he_read_vscales.argtypes = [_vp, _vp]
+        L.he_set_alloc_limit.argtypes = [ctypes.c_uint64]
+        L.he_wait_probe.argtypes = [_vp, ctypes.c_uint32, _vp]
         L.he_profile_start.argtypes = [_vp, _i32]
         L.he_profile_stop.argtypes = [_vp, P(ctypes.c_float), P(_i32)]
         L.he_strerror.argtypes = [ctypes.c_int]
@@ -71,7 +73,7 @@ def lib() -> ctypes.CDLL:
                   "he_last_evicted", "he_read_state", "he_get_projection", "he_codes", "he_scores",
                   "he_occupancy", "he_step_bytes", "he_launch_info", "he_recompute_count",
                   "he_attend_noalloc", "he_profile_start", "he_profile_stop", "he_read_scores",
-                  "he_read_vscales"):
+                  "he_read_vscales", "he_set_alloc_limit", "he_wait_probe"):
             getattr(L, n).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -156,6 +158,14 @@ def he_occupancy(h: int) -> int:
     o = _i32()
     _check("he_occupancy", lib().he_occupancy(h, ctypes.byref(o)))
     return o.value
+
+
+def he_set_alloc_limit(nbytes: int) -> None:
+    _check("he_set_alloc_limit", lib().he_set_alloc_limit(nbytes))
+
+
+def he_wait_probe(h: int, limit_us: int, stream=None) -> None:
+    _check("he_wait_probe", lib().he_wait_probe(h, limit_us, _stream(stream)))
 
 
 def he_read_vscales(h: int, host_scales) -> None:

@@ -183,6 +183,22 @@ bool encode_vq_map(CUtensorMap* map, void* base, uint64_t rows, int D, int box_r
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Device memory cap of one he_create (0: none), see he_set_alloc_limit.
+uint64_t g_alloc_limit = 0;
+
+// One thread waits on a barrier that nothing completes, through the library's
+// bounded wait; when the wait gives up it records the error flag, as the step
+// kernels do.
+__global__ void wait_probe_kernel(int32_t* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    he::mbar_init(&bar, 1);
+    he::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !he::mbar_wait_bounded(&bar, 0u, limit_ns)) atomicExch(err, 1);
+}
+
 // Keeps the caller's current device and switches to the handle's for the call.
 struct DeviceGuard {
   int prev = -1;
@@ -462,6 +478,12 @@ int he_create(const he_cfg* cfg, he_handle* out) {
         {(void**)&h->score, c.decay > 0.0f ? (size_t)U * rows * sizeof(float) : 0},
         {(void**)&h->cstar, chunk > 1 ? (size_t)U * kern.chunk_floats * sizeof(float) : 0},
     };
+    uint64_t total = 0;
+    for (auto& a : allocs) total += a.bytes;
+    if (g_alloc_limit != 0 && total > g_alloc_limit) {
+      rc = HE_ENOMEM;
+      break;
+    }
     for (auto& a : allocs) {
       if (a.bytes == 0) continue;
       if (cudaMalloc(a.p, a.bytes) != cudaSuccess) {
@@ -751,6 +773,21 @@ int he_recompute_count(he_handle h, int64_t* total) {
     for (int i = 0; i < h->U; ++i) *total += host[i];
   delete[] host;
   if (e != cudaSuccess) return fail_cuda(h, e);
+  return HE_OK;
+}
+
+int he_set_alloc_limit(uint64_t bytes) {
+  g_alloc_limit = bytes;
+  return HE_OK;
+}
+
+int he_wait_probe(he_handle h, uint32_t limit_us, void* stream) {
+  if (!h || limit_us < 1 || limit_us > 1000000) return HE_EINVAL;
+  if (h->sticky) return h->sticky;
+  DeviceGuard g(h->device);
+  if (!g.ok) return fail_cuda(h, cudaErrorInvalidDevice);
+  wait_probe_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(h->err, (uint64_t)limit_us * 1000u);
+  HE_TRY(h, cudaGetLastError());
   return HE_OK;
 }
 

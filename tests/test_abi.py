@@ -89,6 +89,8 @@ def test_null_arguments_are_rejected(L):
     assert L.he_recompute_count(None, None) == -1
     assert L.he_read_scores(None, None) == -1
     assert L.he_read_vscales(None, None) == -1
+    assert L.he_wait_probe(None, 1000, None) == -1
+    assert L.he_set_alloc_limit(0) == 0
 
 
 def test_python_errors_raise(L):
