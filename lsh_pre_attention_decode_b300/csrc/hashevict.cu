@@ -3,6 +3,7 @@
 // Every step of the decode path runs in the kernels of he_step.cuh.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -26,6 +27,10 @@ using he::StepParams;
 constexpr int kSimtStages = 4;    // CUDA-core engine (fp32 caches): 32-slot tiles
 constexpr int kTcStages = 2;      // tensor-core pipeline (bf16 caches): 64-slot tiles
 constexpr bool kPSplit = true;    // attention weights as bf16 hi + lo parts
+// Stream CTAs that start behind the previous step's merge CTAs (a 512-thread
+// merge CTA leaves no room for a stream CTA on its SM) take this many tiles
+// fewer than the others.
+constexpr double kLateTiles = 2.0;
 
 struct Kernels {
   const void* step;    // fp32: the fused step; bf16: the stream kernel
@@ -622,6 +627,22 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
     p.kpar = h->kpar;
     p.prev_w1 = h->prev_w1;
     p.nopre = h->nopre;
+    // two-group stream-K split (he::TileSplit): when every CTA slot is used,
+    // the CTAs placed on SMs free of the previous step's merge CTAs (one per
+    // unit, at most one per SM) start first and take more tiles
+    const int64_t TT = p.total_tiles;
+    if (stream_ctas == h->max_ctas && TT > stream_ctas) {
+      const int merge_sms = h->U < h->num_sms ? h->U : h->num_sms;
+      const int64_t E = (int64_t)h->ctas_per_sm * (h->num_sms - merge_sms);
+      if (E > 0 && E < stream_ctas) {
+        const double per = ((double)TT + (double)(stream_ctas - E) * kLateTiles) / stream_ctas;
+        int64_t T1 = (int64_t)std::llround(per * (double)E);
+        if (T1 > TT - (stream_ctas - E)) T1 = TT - (stream_ctas - E);  // a tile per late CTA
+        if (T1 < E) T1 = E;
+        p.split_e = (int32_t)E;
+        p.split_t1 = (int32_t)T1;
+      }
+    }
     if (stream_ctas > 0) {
       void* sa[] = {(void*)&p, (void*)&h->tmK, (void*)&h->tmV};
       HE_TRY(h, launch_pdl(h->kern.step, dim3(stream_ctas), dim3(h->kern.step_threads),
@@ -638,9 +659,16 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
     if (ev) HE_TRY(h, cudaEventRecord(ev[2], s));
     int sc = stream_ctas;
     void* ma[] = {(void*)&p, (void*)&uo, (void*)&sc};
-    // partials per unit: at most ceil(tiles per unit * CTAs / tiles) + 1
-    const int64_t TT = p.total_tiles;
-    const int nmax = TT > 0 ? (int)(((int64_t)p.tpu * stream_ctas + TT - 1) / TT) + 1 : 0;
+    // partials per unit: at most ceil(tiles per unit / fewest tiles of a CTA) + 1
+    int nmax = 0;
+    if (TT > 0 && stream_ctas > 0) {
+      const he::TileSplit sp{TT, stream_ctas, p.split_e, p.split_t1};
+      int64_t fewest = TT;
+      for (int64_t c : {(int64_t)0, (int64_t)stream_ctas - 1})
+        fewest = std::min(fewest, sp.begin(c + 1) - sp.begin(c));
+      if (p.split_e > 0) fewest = std::min(fewest, sp.begin(p.split_e) - sp.begin(p.split_e - 1));
+      nmax = (int)((p.tpu + fewest - 1) / fewest) + 1;
+    }
     int msmem = 0;
     const int mthreads = h->kern.merge_cfg(nmax, &msmem);
     HE_TRY(h, launch_pdl(ch ? h->kern.merge_chunk : h->kern.merge, dim3(h->U), dim3(mthreads),

@@ -75,6 +75,10 @@ struct StepParams {
   int32_t chunk;
   int32_t nopre;
   void* cstar;
+  // bf16 pipeline: stream-K split of the tiles in two groups (TileSplit);
+  // split_e = split_t1 = 0 is the even split
+  int32_t split_e;
+  int32_t split_t1;
 #ifdef HE_TIMELINE
   int32_t tl_step;       // diagnostic builds: step slot of the stamps
 #endif

@@ -77,6 +77,25 @@ __host__ __device__ __forceinline__ int chunk_item_slots(int c) {
   return 4096 / l * l;
 }
 
+// Stream-K split of a step's TT tiles over NC stream CTAs, in two groups: the
+// first E CTAs take tiles [0, T1) and the others [T1, TT), each group split
+// evenly (CTA c of a group of n over T tiles: [c T / n, (c + 1) T / n)).  The
+// host gives the first group more tiles when the others start later (they wait
+// for SMs that the previous step's merge CTAs hold); E = T1 = 0 is the even
+// split.  Every CTA holds at least one tile, so the CTAs holding a unit's
+// tiles are consecutive and each writes a partial.
+struct TileSplit {
+  int64_t TT, NC, E, T1;
+  __host__ __device__ int64_t begin(int64_t c) const {  // first tile of CTA c (c <= NC)
+    if (c <= E) return E > 0 ? c * T1 / E : 0;
+    return T1 + (c - E) * (TT - T1) / (NC - E);
+  }
+  __host__ __device__ int64_t owner(int64_t t) const {  // the CTA whose range holds tile t
+    if (t < T1) return ((t + 1) * E - 1) / T1;
+    return E + ((t - T1 + 1) * (NC - E) - 1) / (TT - T1);
+  }
+};
+
 // Partial record of one (stream CTA, unit): [m G][l G] padded to 4, acc [G][D].
 template <int G, int D>
 struct PRec {
@@ -518,9 +537,9 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ>::NT, 2)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tps = p.tpu;
-  const int64_t TSS = (int64_t)p.U * tps, NCTA = gridDim.x;
-  const int sb = (int)((int64_t)blockIdx.x * TSS / NCTA);
-  const int se = (int)(((int64_t)blockIdx.x + 1) * TSS / NCTA);
+  const TileSplit split{(int64_t)p.U * tps, (int64_t)gridDim.x, p.split_e, p.split_t1};
+  const int sb = (int)split.begin(blockIdx.x);
+  const int se = (int)split.begin((int64_t)blockIdx.x + 1);
   // tiles fetched before the wait (none after a step that moved whole rows)
   const int npre = p.nopre ? 0 : (se - sb < NS ? se - sb : NS);
 
@@ -930,7 +949,7 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ>::NT, 2)
 // where a unit has dozens of partials (long contexts).
 constexpr int kMergeMaxThreads = 512;
 constexpr int kMergeMinThreads = 512;
-constexpr int kMergeRegs = 8;  // partials held in registers per thread (more are looped)
+constexpr int kMergeRegs = 12;  // partials held in registers per thread (more are looped)
 // Chunk eviction: the chunk is subtracted from its partials unless its weight
 // exceeds this many times the weight that remains (every partial and the new
 // token, per head); the subtraction's rounding error is then at most about
@@ -1116,10 +1135,11 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
   // contributors: the CTAs whose ranges cover the unit's tiles (records first+u ..)
   const int tps = p.tpu;
   const int64_t TSS = (int64_t)p.U * tps, NCT = stream_ctas;
+  const TileSplit split{TSS, NCT, p.split_e, p.split_t1};
   int first = 0, n = 0;
   if (TSS > 0 && NCT > 0) {
-    first = (int)((((int64_t)u * tps + 1) * NCT - 1) / TSS);
-    const int last = (int)((((int64_t)u * tps + tps) * NCT - 1) / TSS);
+    first = (int)split.owner((int64_t)u * tps);
+    const int last = (int)split.owner((int64_t)u * tps + tps - 1);
     n = last - first + 1;
   }
   const float* recs = p.partials + (size_t)(first + u) * R::FLOATS;
@@ -1198,11 +1218,11 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
   // the evicted slot's contributor: the owner of tile winner / tile (with a
   // chunk, crel .. crel_hi own its first and last slot)
   const int crel = (full && n > 0)
-                       ? (int)((((int64_t)u * tps + winner / p.tile + 1) * NCT - 1) / TSS) - first
+                       ? (int)split.owner((int64_t)u * tps + winner / p.tile) - first
                        : -1;
   const int crel_hi =
       (CH && full && n > 0)
-          ? (int)((((int64_t)u * tps + (winner + nev - 1) / p.tile + 1) * NCT - 1) / TSS) - first
+          ? (int)split.owner((int64_t)u * tps + (winner + nev - 1) / p.tile) - first
           : crel;
 
   float4 vs = make_float4(__uint_as_float(vs2.x << 16), __uint_as_float(vs2.x & 0xFFFF0000u),
@@ -1308,7 +1328,7 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
     __syncthreads();
     // the slots of that contributor (with a chunk: of contributors crel .. crel_hi)
     const int c = first + crel, ch = first + crel_hi;
-    const int tb = (int)((int64_t)c * TSS / NCT), te = (int)(((int64_t)ch + 1) * TSS / NCT);
+    const int tb = (int)split.begin(c), te = (int)split.begin((int64_t)ch + 1);
     const int lo = (max(tb, u * tps) - u * tps) * p.tile;
     const int hi = min((min(te, (u + 1) * tps) - u * tps) * p.tile, p.occ);
     recompute_partial<D, G, VQ>(p, u, lo, hi, winner, nev, qf, wstate, xm, xl, xa, tid);
