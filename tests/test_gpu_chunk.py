@@ -188,3 +188,19 @@ def test_heavy_chunk_is_subtracted():
         he.close()
     err = np.abs(got - r_or["out"][-1])
     assert err.max() <= MAX_ABS_TOL and err.mean() <= MEAN_ABS_TOL, (err.max(), err.mean())
+
+
+def test_chunk_full_llama8b_b8_sampled():
+    """The benchmark's workload (batch 8, 32/8 heads, budget 4096) with c = 16
+    in the launch configuration the benchmark times (296 stream CTAs, the
+    two-group tile split): 40 steps (two and a half staging cycles) on sampled
+    units: every eviction, outputs at the evicting steps, and the final cache."""
+    w = synth.WORKLOADS["llama8b_b8"]
+    steps = 40
+    out_steps = [0, 14, 15, 16, 31, 39]
+    g = run_gpu(w, w.budget, steps, out_steps, read_state=True, chunk=16, device_gen=True)
+    units = [(0, 0), (3, 5), (7, 7)]
+    orc = run_oracle_units(w, units, w.budget, steps, out_steps, chunk=16)
+    compare(w, g, orc, out_steps, check_state=True)
+    assert (g.evicted[15] >= 0).all() and (g.evicted[31] >= 0).all()
+    assert (g.evicted[:15] == -1).all()
