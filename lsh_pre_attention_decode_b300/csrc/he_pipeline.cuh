@@ -545,6 +545,10 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ>::NT, 2)
 
   // one stage: its descriptor, then (unless it is the sentinel) K, V and, at a
   // segment's first tile, the unit's query rows, all on the stage's barrier
+  // the K/V tiles are read once per step: evict them from L2 first, so that
+  // the small data re-read within the step (partial records, prep's results,
+  // codes) stays resident for merge and prep
+  const uint64_t l2pol = l2_evict_first_policy();
   auto put = [&](int k, int u, int lt, int flags, int rec) {
     const int st = k % NS;
     desc[st] = make_int4(u, lt, flags, rec);
@@ -562,15 +566,15 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ>::NT, 2)
                  &full_bar[st]);
 #pragma unroll
       for (int h = 0; h < S::NHALF; ++h)
-        tma_load_2d(dst + h * S::BOXB, &tmK, 64 * h, y, &full_bar[st]);
+        tma_load_2d_hint(dst + h * S::BOXB, &tmK, 64 * h, y, &full_bar[st], l2pol);
       if constexpr (VQ) {
-        tma_load_2d(dst + S::TILEB, &tmV, 0, y, &full_bar[st]);
+        tma_load_2d_hint(dst + S::TILEB, &tmV, 0, y, &full_bar[st], l2pol);
         bulk_g2s(dst + S::TILEB + S::VQT, p.vs + (size_t)u * p.vs_stride + (size_t)lt * S::TS,
                  (uint32_t)S::SCB, &full_bar[st]);
       } else {
 #pragma unroll
         for (int h = 0; h < S::NHALF; ++h)
-          tma_load_2d(dst + S::TILEB + h * S::BOXB, &tmV, 64 * h, y, &full_bar[st]);
+          tma_load_2d_hint(dst + S::TILEB + h * S::BOXB, &tmV, 64 * h, y, &full_bar[st], l2pol);
       }
     }
     *v_issued = k + 1;
