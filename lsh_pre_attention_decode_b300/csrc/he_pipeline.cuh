@@ -1000,30 +1000,61 @@ __device__ void recompute_partial(const StepParams& p, int u, int lo, int hi, in
 #pragma unroll
       for (int e = 0; e < E; ++e) ar[g][e] = 0.0f;
     }
-    for (int s = lo + warp; s < hi; s += RW) {
-      if ((unsigned)(s - skip) < (unsigned)nskip) continue;
-      float kx[E], vx[E];
+    // a warp takes RU consecutive slots at a time, every row of the group
+    // loaded before any is used (one memory round trip per group); lane l
+    // holds elements [l E, l E + E) of each row
+    constexpr int RU = 4;
+    for (int s0 = lo + warp * RU; s0 < hi; s0 += RW * RU) {
+      float kx[RU][E], vx[RU][E];
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        kx[e] = __uint_as_float((uint32_t)Kc[(size_t)s * D + lane * E + e] << 16);
-        if constexpr (VQ)
-          vx[e] = (float)reinterpret_cast<const int8_t*>(Vc)[(size_t)s * D + lane * E + e] *
-                  __ldcg(p.vs + (size_t)u * p.vs_stride + s);
-        else
-          vx[e] = __uint_as_float((uint32_t)Vc[(size_t)s * D + lane * E + e] << 16);
+      for (int r = 0; r < RU; ++r) {
+        const int s = s0 + r < hi ? s0 + r : hi - 1;  // (a slot past the range is not folded)
+        const size_t at = (size_t)s * D + lane * E;
+        if constexpr (E == 4) {
+          const uint2 kw = __ldcg(reinterpret_cast<const uint2*>(Kc + at));
+          kx[r][0] = bf16_lo(kw.x);
+          kx[r][1] = bf16_hi(kw.x);
+          kx[r][2] = bf16_lo(kw.y);
+          kx[r][3] = bf16_hi(kw.y);
+        } else {
+          const uint32_t kw = __ldcg(reinterpret_cast<const uint32_t*>(Kc + at));
+          kx[r][0] = bf16_lo(kw);
+          kx[r][1] = bf16_hi(kw);
+        }
+        if constexpr (VQ) {
+          const int8_t* vb = reinterpret_cast<const int8_t*>(Vc) + at;
+          const float sc = __ldcg(p.vs + (size_t)u * p.vs_stride + s);
+#pragma unroll
+          for (int e = 0; e < E; ++e) vx[r][e] = (float)__ldcg(vb + e) * sc;
+        } else if constexpr (E == 4) {
+          const uint2 vw = __ldcg(reinterpret_cast<const uint2*>(Vc + at));
+          vx[r][0] = bf16_lo(vw.x);
+          vx[r][1] = bf16_hi(vw.x);
+          vx[r][2] = bf16_lo(vw.y);
+          vx[r][3] = bf16_hi(vw.y);
+        } else {
+          const uint32_t vw = __ldcg(reinterpret_cast<const uint32_t*>(Vc + at));
+          vx[r][0] = bf16_lo(vw);
+          vx[r][1] = bf16_hi(vw);
+        }
       }
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float dot = 0.0f;
+      for (int r = 0; r < RU; ++r) {
+        const int s = s0 + r;
+        if (s >= hi || (unsigned)(s - skip) < (unsigned)nskip) continue;
 #pragma unroll
-        for (int e = 0; e < E; ++e) dot = fmaf(qf[g * D + lane * E + e], kx[e], dot);
-        const float x = warp_sum(dot) * p.qscale;
-        const float mn = fmaxf(mr[g], x);
-        const float so = exp2f(mr[g] - mn), sn = exp2f(x - mn);
-        lr[g] = lr[g] * so + sn;
+        for (int g = 0; g < G; ++g) {
+          float dot = 0.0f;
 #pragma unroll
-        for (int e = 0; e < E; ++e) ar[g][e] = ar[g][e] * so + sn * vx[e];
-        mr[g] = mn;
+          for (int e = 0; e < E; ++e) dot = fmaf(qf[g * D + lane * E + e], kx[r][e], dot);
+          const float x = warp_sum(dot) * p.qscale;
+          const float mn = fmaxf(mr[g], x);
+          const float so = exp2f(mr[g] - mn), sn = exp2f(x - mn);
+          lr[g] = lr[g] * so + sn;
+#pragma unroll
+          for (int e = 0; e < E; ++e) ar[g][e] = ar[g][e] * so + sn * vx[r][e];
+          mr[g] = mn;
+        }
       }
     }
     // warp state -> wstate [warp][G][2 + D]
