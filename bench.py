@@ -93,12 +93,18 @@ def measured_peaks():
 
 
 def kernel_source_sha() -> str:
+    """Hash of the kernel sources with comments and whitespace removed: an edit
+    of the code (not of its comments) invalidates a committed ncu summary."""
     csrc = os.path.join(ROOT, "lsh_pre_attention_decode_b300", "csrc")
     h = hashlib.sha256()
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+                src = fh.read()
+            src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+            src = re.sub(r"//[^\n]*", " ", src)
+            h.update(f.encode())
+            h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -946,11 +946,9 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ>::NT, 2)
 // merge
 // ---------------------------------------------------------------------------
 // A merge CTA has GD4 * NQ threads: NQ contributor groups of GD4 = G * D / 4
-// threads (one float4 of the unit's output each).  The host picks NQ from the
-// number of partials per unit: small CTAs (128 threads) where units have few
-// partials, so that one fits on an SM beside two stream CTAs and the next
-// step's stream CTAs launch everywhere while merge runs; up to 512 threads
-// where a unit has dozens of partials (long contexts).
+// threads (one float4 of the unit's output each).  Every shape runs 512
+// threads: smaller CTAs (which could sit beside two stream CTAs) made the
+// merge itself slower by more than their earlier start gained.
 constexpr int kMergeMaxThreads = 512;
 constexpr int kMergeMinThreads = 512;
 constexpr int kMergeRegs = 12;  // partials held in registers per thread (more are looped)

@@ -15,17 +15,6 @@ __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" :::);
 }
 
-// 2-D tensor TMA load (global -> shared), completion on an mbarrier.  x is the
-// innermost (element) coordinate: a multiple of 64 here, so 16-byte aligned.
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
@@ -66,6 +55,9 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return pol;
 }
 
+// 2-D tensor TMA load (global -> shared) with an L2 cache policy, completion on
+// an mbarrier.  x is the innermost (element) coordinate: a multiple of 64 here
+// (or 0 for whole-row boxes), so 16-byte aligned.
 __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, int x, int y,
                                                  uint64_t* bar, uint64_t policy) {
   asm volatile(
