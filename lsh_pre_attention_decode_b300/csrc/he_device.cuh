@@ -130,6 +130,20 @@ __device__ __forceinline__ uint64_t code_from_bits(const uint32_t* s_bits, int b
 
 __device__ __forceinline__ int popc64(uint64_t x) { return __popcll(x); }
 
+// Bounds checks of the debug build (-DHE_DEBUG; compute-sanitizer is not
+// available): a failed check records error 3 in the handle's flag, which the
+// host reports as HE_EDEVICE, and the caller skips the access.  Without
+// HE_DEBUG every check is the constant true and costs nothing.
+#ifdef HE_DEBUG
+__device__ __forceinline__ bool debug_check(bool ok, int32_t* err) {
+  if (!ok) atomicExch(err, 3);
+  return ok;
+}
+#define HE_CHECK(cond, err) (he::debug_check((cond), (err)))
+#else
+#define HE_CHECK(cond, err) true
+#endif
+
 // Packed eviction key: larger distance wins, then the lower slot.
 __device__ __forceinline__ uint64_t evict_key(uint32_t dist, uint32_t slot) {
   return ((uint64_t)dist << 32) | (uint64_t)(0xFFFFFFFFu - slot);

@@ -169,7 +169,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
       const int b = u / p.kv_heads, j = u - b * p.kv_heads;
       const uint32_t wbytes = it == (int)blockIdx.x ? (uint32_t)(D * bits * 2) : 0u;
       const uint32_t qbytes = (uint32_t)(G * D * 2), kbytes = (uint32_t)(D * 2);
-      const uint32_t cbytes = s1 > s0 ? (uint32_t)(((s1 - s0) * wb + 15) & ~15) : 0u;
+      uint32_t cbytes = s1 > s0 ? (uint32_t)(((s1 - s0) * wb + 15) & ~15) : 0u;
+      if (!HE_CHECK((int64_t)s0 * wb + cbytes <= p.code_stride, p.err)) cbytes = 0;
       mbar_arrive_expect_tx(bar, wbytes + qbytes + kbytes + cbytes);
       if (wbytes) bulk_g2s(smem + S::OFF_W, p.W, wbytes, bar);
       bulk_g2s(smem + S::OFF_X,
@@ -552,11 +553,15 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ>::NT, 2)
   auto put = [&](int k, int u, int lt, int flags, int rec) {
     const int st = k % NS;
     desc[st] = make_int4(u, lt, flags, rec);
-    if (flags & kDescEnd) {
-      mbar_arrive(&full_bar[st]);
+    const int y = u * p.budget + lt * S::TS;
+    if ((flags & kDescEnd) ||
+        !HE_CHECK(u >= 0 && u < p.U && lt >= 0 &&
+                      (int64_t)y + S::TS <= (int64_t)p.U * p.budget + S::TS &&
+                      (!VQ || (lt + 1) * S::TS <= p.vs_stride),
+                  p.err)) {
+      mbar_arrive(&full_bar[st]);  // (a failed check: the stage is left as it was)
     } else {
       unsigned char* dst = stage + st * S::STAGEB;
-      const int y = u * p.budget + lt * S::TS;
       constexpr uint32_t tile_bytes = VQ ? S::TILEB + S::VQT + S::SCB : 2 * S::TILEB;
       mbar_arrive_expect_tx(&full_bar[st],
                             tile_bytes + ((flags & kDescFirst) ? (uint32_t)S::QB : 0u));
@@ -696,7 +701,8 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ>::NT, 2)
       // slot, or the last appended one): stale in a tile fetched before the wait
       wslot = k < npre ? prew[k] : -1;
     }
-    if (VQ && k < npre && (unsigned)(wslot - slot_base) < 16u) {
+    if (VQ && k < npre && (unsigned)(wslot - slot_base) < 16u &&
+        HE_CHECK(wslot < p.budget, p.err)) {
       // re-read the row written by the previous step (now visible) into the
       // tile: its bf16 key (swizzled), int8 value row and scale
       const int row = wslot - lt * S::TS;
@@ -720,7 +726,8 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ>::NT, 2)
       fence_proxy_async_smem();  // the stage is refilled by TMA later
       __syncwarp();
     }
-    if (!VQ && k < npre && (unsigned)(wslot - slot_base) < 16u) {
+    if (!VQ && k < npre && (unsigned)(wslot - slot_base) < 16u &&
+        HE_CHECK(wslot < p.budget, p.err)) {
       // re-read the row written by the previous step (now visible) into the tile
       const int row = wslot - lt * S::TS;
       constexpr int CH = D / 8;  // 16-byte chunks per row
@@ -898,7 +905,9 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ>::NT, 2)
         aborted = true;
         break;
       }
-      float* rec = p.partials + (size_t)dsc.w * R::FLOATS;
+      float* rec = p.partials +
+                   (size_t)(HE_CHECK(dsc.w >= 0 && dsc.w < (int)gridDim.x + p.U, p.err) ? dsc.w : 0) *
+                       R::FLOATS;
       for (int idx = tid; idx < G * D; idx += S::NC) {
         const int g = idx / D, d = idx - g * D;
         float mx = -1e30f;
@@ -1175,6 +1184,7 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
     const int last = (int)split.owner((int64_t)u * tps + tps - 1);
     n = last - first + 1;
   }
+  if (!HE_CHECK(first + u + n <= stream_ctas + p.U, p.err)) n = 0;
   const float* recs = p.partials + (size_t)(first + u) * R::FLOATS;
   auto rec_of = [&](int c) { return recs + (size_t)c * R::FLOATS; };
   const int b = u / p.kv_heads, j = u - b * p.kv_heads;
@@ -1364,7 +1374,9 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
     const int tb = (int)split.begin(c), te = (int)split.begin((int64_t)ch + 1);
     const int lo = (max(tb, u * tps) - u * tps) * p.tile;
     const int hi = min((min(te, (u + 1) * tps) - u * tps) * p.tile, p.occ);
-    recompute_partial<D, G, VQ>(p, u, lo, hi, winner, nev, qf, wstate, xm, xl, xa, tid);
+    recompute_partial<D, G, VQ>(p, u, lo,
+                                HE_CHECK(0 <= lo && lo <= hi && hi <= p.budget, p.err) ? hi : lo,
+                                winner, nev, qf, wstate, xm, xl, xa, tid);
     mx = -1e30f;
     sum = 0.0f;
     a = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1440,6 +1452,10 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
     }
   }
   // method step 5: the current token's key, value and code replace the slot
+  if (!HE_CHECK(wslot >= 0 && wslot < p.budget &&
+                    (!(CH && full) || p.lbudget + nev - 1 <= p.budget),
+                p.err))
+    return;
   uint16_t* Kw = reinterpret_cast<uint16_t*>(p.K) + ((size_t)u * p.budget + wslot) * D;
   if (tid < D) {
     Kw[tid] = kt1;
