@@ -461,6 +461,7 @@ __global__ void __launch_bounds__(256) vq_fill_kernel(const uint16_t* __restrict
 // on a global load).  A sentinel descriptor ends the stream.  Consumer-wide
 // synchronisation uses mbarriers with bounded waits, so a wait that gives up
 // unwinds every warp without a hang.
+constexpr int kL2PrefetchTiles = 1;  // tiles of the range prefetched into L2 before the wait
 constexpr int kDescFirst = 1;  // first tile of a segment: load q, reset the state
 constexpr int kDescLast = 2;   // last tile of a segment: write the partial
 constexpr int kDescEnd = 4;    // no more tiles
@@ -612,6 +613,22 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ>::NT, 2)
     v_prod_done[0] = 0;
     fence_mbar_init();
     for (int k = 0; k < npre; ++k) put_static(k);
+    // the next tile of the range into L2 as well, while the previous step's
+    // merge (latency bound, little DRAM traffic) finishes: a stale copy of the
+    // one row that merge overwrites is harmless, L2 sees merge's write
+    const int pfe =
+        p.nopre ? 0 : (se - sb < npre + kL2PrefetchTiles ? se - sb : npre + kL2PrefetchTiles);
+    for (int k = npre; k < pfe; ++k) {
+      const int t = sb + k;
+      const int u = t / tps, lt = t - u * tps;
+      const int y = u * p.budget + lt * S::TS;
+#pragma unroll
+      for (int h = 0; h < S::NHALF; ++h) {
+        tma_prefetch_2d(&tmK, 64 * h, y);
+        if constexpr (!VQ) tma_prefetch_2d(&tmV, 64 * h, y);
+      }
+      if constexpr (VQ) tma_prefetch_2d(&tmV, 0, y);
+    }
   }
   if (tid < npre) {
     const int u = (sb + tid) / tps;  // the unit of tile tid

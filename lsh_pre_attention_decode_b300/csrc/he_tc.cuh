@@ -55,6 +55,14 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return pol;
 }
 
+// L2 prefetch of a 2-D tensor box (no shared-memory destination, no barrier).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // 2-D tensor TMA load (global -> shared) with an L2 cache policy, completion on
 // an mbarrier.  x is the innermost (element) coordinate: a multiple of 64 here
 // (or 0 for whole-row boxes), so 16-byte aligned.
