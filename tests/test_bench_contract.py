@@ -1,0 +1,45 @@
+"""bench.py's reference arm (the CPU oracle timed on a bounded sample) on the
+CPU: one JSON line with the benchmark's keys, the metric and unit of the GPU
+arm, "impl": "reference", a cpu_baseline that describes the run and an e2e
+with no host<->device bytes; under a multi-rank launch only rank 0 prints."""
+import json
+import os
+import subprocess
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+ARGS = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2",
+        "--warmup", "1", "--ref-seconds", "1"]
+
+
+def _env(**kw):
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    env.update(kw)
+    return env
+
+
+def test_reference_arm_prints_one_line_with_the_contract_keys():
+    r = subprocess.run(ARGS, cwd=ROOT, env=_env(), capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [x for x in r.stdout.splitlines() if x.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["unit"] == "steps/s" and d["value"] > 0
+    assert d["higher_is_better"] is True and d["steps"] == 2 and d["warmup"] == 1
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
+    assert cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "steps/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"].startswith("llama8b_b8")
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    r = subprocess.run(ARGS, cwd=ROOT, env=_env(RANK="1", WORLD_SIZE="2", LOCAL_RANK="1"),
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == ""
