@@ -831,12 +831,15 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ>::NT, 2)
     // of a 16-row tile; the stage is then free
     unsigned char* vw = smem + S::OFF_VW + cw * S::VWB;
     if constexpr (VQ) {
-      const int lr = lane >> 1, hb = lane & 1;  // local row, half of the row
-      const int8_t* src = reinterpret_cast<const int8_t*>(Ks + S::TILEB) + (row0 + lr) * D +
-                          hb * (D / 2);
+      // (each load of the warp covers 512 contiguous bytes of the unswizzled
+      // int8 tile, lane l taking 16-byte piece i * 32 + l of the warp's rows:
+      // no two lanes of a load share a bank)
+      constexpr int CPR = D / 16;  // 16-byte pieces per value row
+      const int8_t* src = reinterpret_cast<const int8_t*>(Ks + S::TILEB) + row0 * D;
 #pragma unroll
       for (int i = 0; i < D / 32; ++i) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(src + 16 * i);
+        const int pc = i * 32 + lane, lr = pc / CPR, c16 = pc - lr * CPR;
+        const uint4 raw = *reinterpret_cast<const uint4*>(src + lr * D + 16 * c16);
         const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
         uint32_t o[8];
 #pragma unroll
@@ -853,7 +856,7 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ>::NT, 2)
           o[2 * e] = *reinterpret_cast<const uint32_t*>(&lo);
           o[2 * e + 1] = *reinterpret_cast<const uint32_t*>(&hi);
         }
-        const int cc = hb * (D / 16) + 2 * i;  // first 8-column chunk of these 16 values
+        const int cc = 2 * c16;  // first 8-column chunk of these 16 values
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           const int c = cc + j;
