@@ -32,6 +32,9 @@
  *     take a stream are asynchronous on it; calls that take host buffers
  *     synchronise the handle's last-used stream first.
  *   - A handle is not thread-safe; use one handle per layer and per thread.
+ *   - libhashevict_debug.so exports the same entry points with device-side
+ *     bounds checks on every computed global access of the step kernels; a
+ *     failed check is returned as HE_EDEVICE by the next synchronising call.
  */
 #ifndef HASHEVICT_H
 #define HASHEVICT_H
