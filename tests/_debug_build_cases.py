@@ -19,6 +19,33 @@ def case(w, fill_n, steps, units, **kw):
     compare(w, g, orc, out_steps, check_state=True)
 
 
+def noalloc_case():
+    """The allocation-free attention entry point (same stream kernel) on the
+    cache the step leaves, against the step's own output."""
+    import torch
+    from gpu_harness import MAX_ABS_TOL, MEAN_ABS_TOL, make_handle, torch_from_host
+    w = synth.WORKLOADS["llama8b_b8"].with_(batch=2, budget=300, prompt=600)
+    he = make_handle(w)
+    try:
+        he.fill(torch_from_host(synth.host_kv(w, "key", 0, w.budget)),
+                torch_from_host(synth.host_kv(w, "value", 0, w.budget)))
+        q = torch_from_host(synth.host_queries(w, w.budget, 1))[0]
+        k = torch_from_host(synth.host_kv(w, "key", w.budget, 1, token_major=True))[0]
+        v = torch_from_host(synth.host_kv(w, "value", w.budget, 1, token_major=True))[0]
+        ref = he.step(q, k, v)
+        K, V, _, occ = he.state()
+        out = torch.full_like(ref, float("nan"))
+        binding.he_attend_noalloc(w.batch, w.heads, w.kv_heads, w.head_dim, w.budget, occ,
+                                  torch_from_host(K), torch_from_host(V), q, out)
+        torch.cuda.synchronize()
+        err = (out - ref).abs()
+        assert torch.isfinite(out).all()
+        assert err.max().item() <= MAX_ABS_TOL and err.mean().item() <= MEAN_ABS_TOL
+        he.last_evicted()  # HE_EDEVICE here if a check failed
+    finally:
+        he.close()
+
+
 def main():
     base = synth.WORKLOADS["llama8b_b8"]
     cases = [
@@ -34,6 +61,8 @@ def main():
         units = [(b, j) for b in range(w.batch) for j in (0, w.kv_heads - 1)]
         case(w, fill_n, steps, units, **kw)
         print("ok", name, flush=True)
+    noalloc_case()
+    print("ok allocation-free attention", flush=True)
     assert binding.lib()._name == _build.DEBUG_LIB
 
 

@@ -1,7 +1,8 @@
 """The bounds-checked debug build of the library (-DHE_DEBUG: each computed
 global access of the step kernels is checked, a failed check records an error
 the host returns as HE_EDEVICE) runs the parity cases of several shapes and
-options clean: no check fails and every result matches the oracle.  It stands
+options, and the allocation-free attention entry point, clean: no check fails
+and every result matches the oracle (or, for the entry point, the step).  It stands
 in for compute-sanitizer, which this pool does not offer."""
 import os
 import subprocess
@@ -23,4 +24,4 @@ def test_debug_build_runs_clean():
     r = subprocess.run([sys.executable, os.path.join(HERE, "_debug_build_cases.py")], cwd=ROOT,
                        env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
-    assert r.stdout.count("ok ") == 6, r.stdout
+    assert r.stdout.count("ok ") == 7, r.stdout
