@@ -76,6 +76,7 @@ class UnitState:
     Vq: np.ndarray | None = None     # quantised value cache: int8 [budget][D] ...
     Vs: np.ndarray | None = None     # ... and one fp32 scale per row (then V is unused)
     chunk: int = 1                   # chunk eviction: K, V, codes hold budget + chunk - 1 rows
+    chunked: bool = False            # filled by unit_fill_chunk: streams run the chunk routine
 
 
 class Oracle:
@@ -207,6 +208,7 @@ class Oracle:
         st = self.unit_fill(W, budget + chunk - 1, Kin, Vin, tau=tau)
         st.budget = budget
         st.chunk = chunk
+        st.chunked = True  # (c = 1 too: then the chunk routine must give the method)
         return st
 
     def unit_fill(self, W: np.ndarray, budget: int, Kin: np.ndarray, Vin: np.ndarray,
@@ -266,7 +268,7 @@ class Oracle:
         out = np.empty((n_out, G, D), np.float64)
         dl = np.empty((T, st.budget), np.int32) if dist_log else None
         occ = np.array([st.occupancy], np.int32)
-        if st.chunk > 1:
+        if st.chunked:
             if decay != 0.0 or st.score is not None or st.Vq is not None or dist_log:
                 raise ValueError("chunk eviction takes neither score memory nor int8 values")
             self.lib.orc_unit_stream_chunk(_ptr(st.W), D, G, st.bits, _dtype_code(qc), st.budget,

@@ -509,7 +509,11 @@ void orc_unit_stream_chunk(const void* W, int32_t D, int32_t G, int32_t bits, in
 #if ORACLE_MUTANT == 15 /* planted: a chunk scores by its first slot only */
           if (j > 0) break;
 #endif
+#if ORACLE_MUTANT == 17 /* planted: a chunk scores its slots shifted by one */
+          dsum[i] += orc_group_distance(code_q, G, codes[(i * chunk + j + 1) % budget]);
+#else
           dsum[i] += orc_group_distance(code_q, G, codes[i * chunk + j]);
+#endif
         }
       }
       const int32_t e = orc_most_dissimilar(dsum, nch);

@@ -559,6 +559,24 @@ def check_chunk_one_is_method(o):
         assert np.array_equal(a.K, b.K) and np.array_equal(a.V, b.V)
 
 
+def check_chunk_one_with_threshold_is_method(o):
+    """Chunks of one slot under a binarisation threshold tau equal the method's
+    path with the same tau (codes, evictions, cache and outputs)."""
+    rng = np.random.default_rng(64)
+    for tau in (-0.5, 0.4, 1.2):
+        D, bits, G, B, T = 16, 8, 2, 9, 14
+        W = o.projection(410, D, bits, "fp32")
+        K0, V0 = f32(rng.standard_normal((6, D))), f32(rng.standard_normal((6, D)))
+        q, k, v = (f32(rng.standard_normal(sh)) for sh in ((T, G, D), (T, D), (T, D)))
+        a = o.unit_fill(W, B, K0, V0, tau=tau)
+        b = o.unit_fill_chunk(W, B, 1, K0, V0, tau=tau)
+        ra, rb = o.unit_stream(a, q, k, v), o.unit_stream(b, q, k, v)
+        assert ra["evicted"].tolist() == rb["evicted"].tolist()
+        assert np.array_equal(ra["out"], rb["out"]) and np.array_equal(a.codes, b.codes)
+        # the threshold changes the codes (the case is not vacuous)
+        assert not np.array_equal(a.codes, o.unit_fill(W, B, K0, V0).codes)
+
+
 def check_chunk_whole_budget(o):
     """One chunk spanning the whole budget replaces the cache in blocks: after
     every eviction the cache holds exactly the last B tokens in arrival order,
@@ -615,5 +633,5 @@ ALL_CHECKS = [
     check_attention_bf16_elements, check_codes_tau_hand, check_codes_tau_monotone,
     check_decay_hand, check_decay_zero_is_per_step, check_vquant_hand, check_vquant_attention,
     check_vquant_stream, check_chunk_hand, check_chunk_one_is_method, check_chunk_whole_budget,
-    check_chunk_sums_brute,
+    check_chunk_sums_brute, check_chunk_one_with_threshold_is_method,
 ]

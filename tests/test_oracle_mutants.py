@@ -23,6 +23,7 @@ MUTANTS = {
     14: "value rows rounded half away from zero",
     15: "a chunk scores by its first slot only",
     16: "staged tokens land in reverse order",
+    17: "a chunk scores its slots shifted by one",
 }
 
 
