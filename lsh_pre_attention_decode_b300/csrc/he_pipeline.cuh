@@ -857,13 +857,18 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ>::NT, 2)
           o[2 * e + 1] = *reinterpret_cast<const uint32_t*>(&hi);
         }
         const int cc = 2 * c16;  // first 8-column chunk of these 16 values
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int c = cc + j;
-          *reinterpret_cast<uint4*>(vw + (c >> 3) * (16 * 128) + lr * 128 +
-                                    (((c & 7) ^ (lr & 7)) << 4)) =
-              make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-        }
+        // (the lanes of a row's upper half store their two chunks in the other
+        // order, so that the eight lanes of each 128-bit store phase fall in
+        // eight different bank groups)
+        const bool swap = c16 >= CPR / 2;
+        const uint4 w0 = make_uint4(o[0], o[1], o[2], o[3]);
+        const uint4 w1 = make_uint4(o[4], o[5], o[6], o[7]);
+        const uint4 first = swap ? w1 : w0, second = swap ? w0 : w1;
+        const int ca = cc + (swap ? 1 : 0), cb = cc + (swap ? 0 : 1);
+        *reinterpret_cast<uint4*>(vw + (ca >> 3) * (16 * 128) + lr * 128 +
+                                  (((ca & 7) ^ (lr & 7)) << 4)) = first;
+        *reinterpret_cast<uint4*>(vw + (cb >> 3) * (16 * 128) + lr * 128 +
+                                  (((cb & 7) ^ (lr & 7)) << 4)) = second;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[st]);  // stage free for refill
