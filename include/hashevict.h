@@ -209,6 +209,29 @@ int he_profile_stop(he_handle h, float* ms, int32_t* steps);
  * the unit).  Always 0 for fp32 handles.  Synchronises. */
 int he_recompute_count(he_handle h, int64_t* total);
 
+/* Test export: a per-step eviction log kept on the device.  After
+ * he_set_evict_log(h, log, count, capacity), each later step writes, for every
+ * unit u = b * kv_heads + j, the slot it wrote (as he_last_evicted reports it)
+ * to log[count[u]][u] and then increments count[u]; entries beyond `capacity`
+ * are counted but not stored.  log: device int32 [capacity][batch * kv_heads];
+ * count: device int32 [batch * kv_heads], set by the caller (normally to 0).
+ * The writes happen on the device in step order, so steps issued back to back
+ * on a stream, or replayed from a captured CUDA graph, are logged without any
+ * host synchronisation; a graph records the log pointers it was captured with.
+ * log = NULL turns the log off.  The buffers stay owned by the caller and must
+ * outlive every step that logs into them.
+ * Errors: HE_EINVAL (NULL handle; log without count or with capacity < 1). */
+int he_set_evict_log(he_handle h, int32_t* log, int32_t* count, int32_t capacity);
+
+/* Test export: the distances the step itself computes (method step 3).  After
+ * he_set_dist_log(h, dist), each later step that scores a full cache writes the
+ * group-summed Hamming distance of every slot it scores to dist[b][j][s]
+ * (device int32 [batch][kv_heads][R]); with chunk eviction that is every slot
+ * of the budget, the chunks' sums being built from them.  Steps that append
+ * write nothing.  NULL turns it off.  Caller-owned, as for the eviction log.
+ * Errors: HE_EINVAL (NULL handle). */
+int he_set_dist_log(he_handle h, int32_t* dist);
+
 /* Checks of the failure paths.
  * he_set_alloc_limit: a process-wide cap, in bytes, on the device memory one
  * he_create may allocate (0 = no cap, the default).  A handle that would need
@@ -226,9 +249,9 @@ int he_wait_probe(he_handle h, uint32_t limit_us, void* stream);
 
 /* Allocation-free decode attention.  This entry point has no counterpart in
  * the method's description: it is an integration aid for callers that cannot
- * let a library allocate device memory — code that runs while a CUDA graph is
- * being captured, runtimes whose device memory is owned by their own pool or
- * arena, deployments that fix every byte of device memory up front.
+ * let a library allocate device memory — runtimes whose device memory is owned
+ * by their own pool or arena (a second allocator would fragment it or break
+ * its accounting), deployments that fix every byte of device memory up front.
  *   out[b][h][:] = sum_{s < n} softmax_s(q[b][h] . K[b][kv][s] / sqrt(head_dim))
  *                  V[b][kv][s],   kv = h / (heads / kv_heads)
  * K, V: device bf16 [batch][kv_heads][budget][head_dim] (rows s >= n of each
@@ -241,10 +264,14 @@ int he_wait_probe(he_handle h, uint32_t limit_us, void* stream);
  * ceil(2G / 4) + G * head_dim) bytes per partial record (G = heads / kv_heads),
  * (C + batch * kv_heads) * R + 256 <= HE_NOALLOC_SCRATCH_BYTES, else HE_EINVAL.
  * The first call on each device does a one-off set-up (the array's device
- * address, kernel attributes) on the current device: make it before any stream
- * capture.  Every call uses the same array, so calls that overlap on the GPU
- * race: order them (one stream, or events).  No part of the array needs to
- * start at zero.  Not thread-safe on a device's first call.
+ * address, kernel attributes) on the current device; make that first call
+ * before any stream capture.  Not thread-safe on a device's first call.  Every
+ * call uses the same array, so calls that overlap on the GPU race: order them
+ * (one stream, or events).  Each call clears the array's error word itself
+ * (an asynchronous memset on `stream`); nothing else in the array needs to
+ * start at zero.  No cudaMalloc or cudaFree is called.
+ * Device-side failure: if a kernel of the call gives up a bounded wait, the
+ * call's whole output is NaN (the call has already returned HE_OK by then).
  * Errors: HE_EINVAL (sizes, NULL or misaligned pointers, scratch too small),
  * HE_ECUDA. */
 #define HE_NOALLOC_SCRATCH_BYTES (8u << 20)

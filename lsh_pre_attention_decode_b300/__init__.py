@@ -15,7 +15,7 @@ from ._binding import (  # noqa: F401
     he_attend_noalloc, he_codes, he_create, he_destroy, he_fill, he_get_projection,
     he_last_evicted, he_launch_info, he_occupancy, he_profile_start, he_profile_stop,
     he_read_scores, he_read_state, he_read_vscales, he_recompute_count, he_scores,
-    he_set_alloc_limit, he_step, he_step_bytes, he_step_host, he_strerror, he_wait_probe, lib,
-    lib_path,
+    he_set_alloc_limit, he_set_dist_log, he_set_evict_log, he_step, he_step_bytes, he_step_host,
+    he_strerror, he_wait_probe, lib, lib_path,
 )
 from .shard import layer_shard, max_over_ranks  # noqa: F401

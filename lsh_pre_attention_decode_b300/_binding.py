@@ -67,13 +67,16 @@ def lib() -> ctypes.CDLL:
         L.he_wait_probe.argtypes = [_vp, ctypes.c_uint32, _vp]
         L.he_profile_start.argtypes = [_vp, _i32]
         L.he_profile_stop.argtypes = [_vp, P(ctypes.c_float), P(_i32)]
+        L.he_set_evict_log.argtypes = [_vp, _vp, _vp, _i32]
+        L.he_set_dist_log.argtypes = [_vp, _vp]
         L.he_strerror.argtypes = [ctypes.c_int]
         L.he_strerror.restype = ctypes.c_char_p
         for n in ("he_create", "he_fill", "he_step", "he_step_host", "he_destroy",
                   "he_last_evicted", "he_read_state", "he_get_projection", "he_codes", "he_scores",
                   "he_occupancy", "he_step_bytes", "he_launch_info", "he_recompute_count",
                   "he_attend_noalloc", "he_profile_start", "he_profile_stop", "he_read_scores",
-                  "he_read_vscales", "he_set_alloc_limit", "he_wait_probe"):
+                  "he_read_vscales", "he_set_alloc_limit", "he_wait_probe", "he_set_evict_log",
+                  "he_set_dist_log"):
             getattr(L, n).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -206,6 +209,14 @@ def he_attend_noalloc(batch: int, heads: int, kv_heads: int, head_dim: int, budg
     _check("he_attend_noalloc",
            lib().he_attend_noalloc(batch, heads, kv_heads, head_dim, budget, n, _ptr(K), _ptr(V),
                                    _ptr(q), _ptr(out), _stream(stream)))
+
+
+def he_set_evict_log(h: int, log, count, capacity: int) -> None:
+    _check("he_set_evict_log", lib().he_set_evict_log(h, _ptr(log), _ptr(count), capacity))
+
+
+def he_set_dist_log(h: int, dist) -> None:
+    _check("he_set_dist_log", lib().he_set_dist_log(h, _ptr(dist)))
 
 
 def he_launch_info(h: int) -> dict:

@@ -259,6 +259,10 @@ struct he_ctx {
   int rows = 0;               // rows per unit: budget + chunk - 1 (the stride of K, V, codes)
   float* cstar = nullptr;     // chunk eviction: the evicted chunk's softmax parts, per unit
   int nopre = 0;              // the previous step moved rows (StepParams::nopre)
+  int32_t* evlog = nullptr;   // test exports (caller-owned device buffers, or null)
+  int32_t* evcnt = nullptr;
+  int32_t evcap = 0;
+  int32_t* dist = nullptr;
   void* sq = nullptr;  // he_step_host staging
   void* sk = nullptr;
   void* sv = nullptr;
@@ -341,6 +345,10 @@ StepParams base_params(const he_ctx* h) {
   p.tau = h->cfg.threshold;
   p.decay = h->cfg.decay;
   p.score = h->score;
+  p.evlog = h->evlog;
+  p.evcnt = h->evcnt;
+  p.evcap = h->evcap;
+  p.dist = h->dist;
   return p;
 }
 
@@ -576,8 +584,13 @@ int he_fill(he_handle h, const void* K, const void* V, int32_t n, void* stream) 
   if (h->uo) HE_TRY(h, cudaMemsetAsync(h->uo, 0, (size_t)h->U * sizeof(he::UnitOut), s));
   if (h->score)  // filled slots start with no accumulated score
     HE_TRY(h, cudaMemsetAsync(h->score, 0, (size_t)h->U * h->rows * sizeof(float), s));
-  h->prev_w1 = 0;  // no step has written a slot of the filled cache
-  h->nopre = 0;
+  // The first step after a fill reads the (zeroed) eviction key for the slot
+  // the step before it wrote, and with chunk eviction fetches no tile before it
+  // waits: the same parameters a step gets after an evicting step, so that a
+  // step sequence captured from here (whole eviction cycles, an even number
+  // of steps) replays on the cache state it leaves.
+  h->prev_w1 = -1;
+  h->nopre = h->chunk > 1 ? 1 : 0;
   h->occupancy = n;
   h->filled = true;
   return HE_OK;
@@ -910,6 +923,21 @@ int he_profile_stop(he_handle h, float* ms, int32_t* steps) {
   for (int k = 0; k < 4; ++k) ms[k] = (float)sum[k];
   *steps = n;
   free_profile(h);
+  return HE_OK;
+}
+
+int he_set_evict_log(he_handle h, int32_t* log, int32_t* count, int32_t capacity) {
+  if (!h) return HE_EINVAL;
+  if (log != nullptr && (count == nullptr || capacity < 1)) return HE_EINVAL;
+  h->evlog = log;
+  h->evcnt = log ? count : nullptr;
+  h->evcap = log ? capacity : 0;
+  return HE_OK;
+}
+
+int he_set_dist_log(he_handle h, int32_t* dist) {
+  if (!h) return HE_EINVAL;
+  h->dist = dist;
   return HE_OK;
 }
 

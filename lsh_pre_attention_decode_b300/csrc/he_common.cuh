@@ -79,6 +79,13 @@ struct StepParams {
   // split_e = split_t1 = 0 is the even split
   int32_t split_e;
   int32_t split_t1;
+  // test exports (null: off): a per-step eviction log written on the device
+  // (evlog [evcap][U], evcnt [U] entries written per unit) and the group-summed
+  // distance of every slot scored by a full-cache step (dist [U][budget])
+  int32_t* evlog;
+  int32_t* evcnt;
+  int32_t evcap;
+  int32_t* dist;
 #ifdef HE_TIMELINE
   int32_t tl_step;       // diagnostic builds: step slot of the stamps
 #endif
@@ -133,6 +140,16 @@ __device__ __forceinline__ void store_code(unsigned char* dst, int bits, uint64_
     case 32: *reinterpret_cast<uint32_t*>(dst) = (uint32_t)code; break;
     default: *reinterpret_cast<uint64_t*>(dst) = code; break;
   }
+}
+
+// Test export: appends the slot a step wrote in unit u to the device eviction
+// log.  Steps of one cache are ordered on the device (each waits for the
+// previous one), so the per-unit count needs no atomic.
+__device__ __forceinline__ void log_eviction(const StepParams& p, int u, int32_t slot) {
+  if (p.evlog == nullptr) return;
+  const int32_t i = p.evcnt[u];
+  if (i < p.evcap) p.evlog[(size_t)i * p.U + u] = slot;
+  p.evcnt[u] = i + 1;
 }
 
 // Method step 3: group-summed Hamming distance of one cached code.
@@ -262,8 +279,8 @@ __device__ __forceinline__ void local_candidate(const StepParams& p, int u, int 
 #pragma unroll
   for (int g = 0; g < G; ++g) cq[g] = m.cq[g];
   uint64_t best = scan_codes<G>(p.codes + (size_t)u * p.code_stride, p.bits, lo, hi, cq, tid, NT,
-                                nullptr, p.score ? p.score + (size_t)u * p.budget : nullptr,
-                                p.decay);
+                                p.dist ? p.dist + (size_t)u * p.budget : nullptr,
+                                p.score ? p.score + (size_t)u * p.budget : nullptr, p.decay);
   best = warp_max_u64(best);
   if (lane == 0) m.red64[warp] = best;
   group_sync<NT, BAR>();
@@ -449,6 +466,7 @@ __device__ void combine_unit(const StepParams& p, int u, int first, int n, Misc&
     if (p.score) p.score[(size_t)u * p.budget + winner] = 0.0f;  // not scored yet
     p.evicted[u] = full ? winner : -1;
     p.counters[u] = 0;
+    log_eviction(p, u, full ? winner : -1);
   }
 }
 

@@ -1,19 +1,20 @@
 // he_noalloc.cu — he_attend_noalloc: decode attention over a caller-owned bf16
 // cache that allocates no device memory.
 //
-// Some callers cannot let a library call cudaMalloc: code that runs while a
-// CUDA graph is being captured (allocation is not a capturable operation),
-// runtimes whose device memory is entirely owned by their own pool or arena,
-// and deployments that must fix every byte of device memory up front.  For
-// them this entry point runs the same split-K attention kernel as he_step
-// (tensor-core stream over 64-slot tiles, then a log-sum-exp merge) with its
-// partial results in a file-scope static device array instead of in
-// handle-owned memory.  The caller passes the cache, the queries and the output.
+// Some callers cannot let a library call cudaMalloc: runtimes whose device
+// memory is entirely owned by their own pool or arena (a second allocator
+// would fragment it or break its accounting), and deployments that must fix
+// every byte of device memory up front.  For them this entry point runs the
+// same split-K attention kernel as he_step (tensor-core stream over 64-slot
+// tiles, then a log-sum-exp merge) with its partial results in a file-scope
+// static device array instead of in handle-owned memory.  The caller passes
+// the cache, the queries and the output.
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "hashevict.h"
 #include "he_pipeline.cuh"
@@ -48,7 +49,9 @@ const void* stream_fn() {
 constexpr int kAttendMergeThreads = 512;
 constexpr int kStreamThreads = he::StreamShape<128, 4, kStages>::NT;  // the same for every shape
 
-// Log-sum-exp merge of a unit's partials (no eviction, no new token).
+// Log-sum-exp merge of a unit's partials (no eviction, no new token).  If a
+// stream CTA of this call gave up a bounded wait (the flag word of the array
+// is set), its partials are missing: the unit's output is written as NaN.
 template <int D, int G>
 __global__ void __launch_bounds__(kAttendMergeThreads) attend_merge_kernel(const he::StepParams p,
                                                                        int stream_ctas) {
@@ -100,7 +103,7 @@ __global__ void __launch_bounds__(kAttendMergeThreads) attend_merge_kernel(const
       s.z += y.z * w;
       s.w += y.w * w;
     }
-    const float inv = 1.0f / l2;
+    const float inv = __ldcg(p.err) != 0 ? __int_as_float(0x7fc00000) : 1.0f / l2;
     const int b = u / p.kv_heads, j = u - b * p.kv_heads;
     reinterpret_cast<float4*>(p.out + ((size_t)b * p.kv_heads * G + (size_t)j * G) * D)[tid] =
         make_float4(s.x * inv, s.y * inv, s.z * inv, s.w * inv);
@@ -201,17 +204,23 @@ int setup_device(int dev) {
   return HE_OK;
 }
 
+// The driver's tensor-map encoder, resolved once per process (thread-safe).
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
 bool encode_map(CUtensorMap* map, const void* base, uint64_t rows, int D) {
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  if (!encode) {
+  std::call_once(g_encode_once, [] {
     cudaDriverEntryPointQueryResult q;
     void* fn = nullptr;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || !fn)
-      return false;
-    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess && fn)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    else
+      (void)cudaGetLastError();
+  });
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = g_encode;
+  if (!encode) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
   const cuuint32_t box[2] = {64, 64};
@@ -280,6 +289,11 @@ extern "C" int he_attend_noalloc(int32_t batch, int32_t heads, int32_t kv_heads,
   p.qscale = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
 
   cudaStream_t st = (cudaStream_t)stream;
+  // the flag word starts each call at zero (a kernel that gives up a wait sets it)
+  if (cudaMemsetAsync(s.scratch, 0, sizeof(int32_t), st) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return HE_ECUDA;
+  }
   void* sa[] = {(void*)&p, (void*)&tmK, (void*)&tmV};
   if (cudaLaunchKernel(pick_stream(head_dim, G), dim3(ctas), dim3(kStreamThreads), sa,
                        (size_t)stream_smem(head_dim, G), st) != cudaSuccess) {

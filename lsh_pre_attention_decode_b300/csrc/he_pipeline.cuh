@@ -246,13 +246,19 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
         const int c = p.chunk;
         for (int s = s0 + tid * c; s < s1; s += kPrepThreads * c) {
           uint32_t sum = 0;
-          for (int i = 0; i < c; ++i) sum += group_distance<G>(cq, code_at(s + i));
+          for (int i = 0; i < c; ++i) {
+            const uint32_t d = group_distance<G>(cq, code_at(s + i));
+            if (p.dist != nullptr) p.dist[(size_t)u * p.budget + s + i] = (int32_t)d;
+            sum += d;
+          }
           const uint64_t key = evict_key(sum, (uint32_t)s);
           best = key > best ? key : best;
         }
       } else if constexpr (!MEM) {  // (the method: 32 registers, so prep fits beside two stream CTAs)
         for (int s = s0 + tid; s < s1; s += kPrepThreads) {
-          const uint64_t key = evict_key(group_distance<G>(cq, code_at(s)), (uint32_t)s);
+          const uint32_t d = group_distance<G>(cq, code_at(s));
+          if (p.dist != nullptr) p.dist[(size_t)u * p.budget + s] = (int32_t)d;
+          const uint64_t key = evict_key(d, (uint32_t)s);
           best = key > best ? key : best;
         }
       } else {
@@ -274,7 +280,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
           for (int i = 0; i < NB; ++i) {
             const int s = s0 + tid + (i0 + i) * kPrepThreads;
             if (s < s1) {
-              const float v = __fmaf_rn(p.decay, a[i], (float)group_distance<G>(cq, code_at(s)));
+              const uint32_t d = group_distance<G>(cq, code_at(s));
+              if (p.dist != nullptr) p.dist[(size_t)u * p.budget + s] = (int32_t)d;
+              const float v = __fmaf_rn(p.decay, a[i], (float)d);
               sc[s] = v;
               const uint64_t key = evict_key(__float_as_uint(v), (uint32_t)s);
               best = key > best ? key : best;
@@ -1495,6 +1503,7 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
     store_code(p.codes + (size_t)u * p.code_stride + (size_t)wslot * (p.bits >> 3), p.bits,
                codek);
     p.evicted[u] = full ? winner : -1;
+    log_eviction(p, u, full ? winner : -1);
     if (p.score != nullptr) p.score[(size_t)u * p.budget + winner] = 0.0f;  // not scored yet
     uo[u].key[p.kpar ^ 1] = 0;  // ready for the next step's atomicMax
     if (recomputed) atomicAdd(p.counters + u, 1);  // how often the exact path ran

@@ -21,7 +21,9 @@ def case(w, fill_n, steps, units, **kw):
 
 def noalloc_case():
     """The allocation-free attention entry point (same stream kernel) on the
-    cache the step leaves, against the step's own output."""
+    cache the step leaves, against the step's own output.  A failed bounds
+    check inside its kernels sets the scratch array's error word, which turns
+    the whole output into NaN: the finiteness check below catches it."""
     import torch
     from gpu_harness import MAX_ABS_TOL, MEAN_ABS_TOL, make_handle, torch_from_host
     w = synth.WORKLOADS["llama8b_b8"].with_(batch=2, budget=300, prompt=600)
@@ -41,7 +43,7 @@ def noalloc_case():
         err = (out - ref).abs()
         assert torch.isfinite(out).all()
         assert err.max().item() <= MAX_ABS_TOL and err.mean().item() <= MEAN_ABS_TOL
-        he.last_evicted()  # HE_EDEVICE here if a check failed
+        he.last_evicted()  # HE_EDEVICE here if a check of the step's own kernels failed
     finally:
         he.close()
 

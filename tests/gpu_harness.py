@@ -179,3 +179,188 @@ def compare(w: synth.Workload, g: GpuRun, orc: dict, out_steps=(), check_state: 
     assert worst_max <= MAX_ABS_TOL, f"max-abs error {worst_max}"
     assert worst_mean <= MEAN_ABS_TOL, f"mean-abs error {worst_mean}"
     return worst_max, worst_mean
+
+
+# ---------------------------------------------------------------------------
+# steps issued back to back (no host synchronisation between them), as a
+# serving loop and the benchmark issue them
+# ---------------------------------------------------------------------------
+
+@dataclass
+class B2BRun:
+    evicted: dict   # layer -> [total steps][batch][kv_heads] from the device eviction log
+    outs: dict      # (layer, step) -> out [batch][heads][D] float32
+    states: dict    # layer -> (K, V, codes, occupancy, vscales or None, scores or None)
+    tokens: list    # per layer step -> token index (the stream each layer saw)
+
+
+def run_gpu_b2b(w: synth.Workload, fill_n: int, tokens: int, out_steps=(), layers: int = 1,
+                graph: bool = False, replays: int = 2, warm: int = 0, threshold: float = 0.0,
+                decay: float = 0.0, v_int8: bool = False, chunk: int = 1,
+                hold_ms: float = 20.0) -> B2BRun:
+    """Fill `layers` independent caches with prompt tokens [0, fill_n), then
+    issue steps round robin over the layers (layer 0 token t, layer 1 token t,
+    ...) with no host synchronisation, each step writing the slots it wrote to
+    a device eviction log.
+
+    Eager (graph=False): `tokens` tokens per layer, fill_n .. fill_n + tokens - 1.
+    Graph: `warm` eager tokens per layer first, then a CUDA graph of the next
+    `tokens` tokens per layer is captured and replayed `replays` times back to
+    back, so each layer sees warm tokens, then its `tokens` captured tokens
+    `replays` times over (the inputs of a replay are the captured ones).
+
+    Before the first step a sleep kernel holds the stream for `hold_ms`, so that
+    every launch is queued before any runs.  out_steps are indices into a
+    layer's step sequence whose output is kept (each in its own buffer; in
+    graph mode only those of the last replay survive, so pass those).  The
+    host reads anything back only once, after the last step."""
+    import ctypes
+    import torch
+    from lsh_pre_attention_decode_b300 import he_set_evict_log, lib
+    L = layers
+    U = w.batch * w.kv_heads
+    n_steps = warm + tokens * replays if graph else tokens
+    tok_of = ([fill_n + t for t in range(warm)] +
+              [fill_n + warm + t for _ in range(replays) for t in range(tokens)]) if graph else \
+        [fill_n + t for t in range(tokens)]
+    out_set = set(out_steps)
+    handles, logs, ins, outs, scratch = [], [], [], [], []
+    he_step_raw = lib().he_step
+    try:
+        for layer in range(L):
+            he = make_handle(w, layer, threshold, decay, v_int8, chunk)
+            handles.append(he)
+            if fill_n > 0:
+                he.fill(synth.gpu_kv(w, "key", 0, fill_n, layer),
+                        synth.gpu_kv(w, "value", 0, fill_n, layer))
+            else:
+                he.fill(None, None)
+            n_in = warm + tokens if graph else tokens
+            q = synth.gpu_queries(w, fill_n, n_in, layer)
+            k = synth.gpu_kv(w, "key", fill_n, n_in, layer, token_major=True)
+            v = synth.gpu_kv(w, "value", fill_n, n_in, layer, token_major=True)
+            ins.append((q, k, v))
+            log = torch.full((n_steps, U), -7, dtype=torch.int32, device="cuda")
+            cnt = torch.zeros(U, dtype=torch.int32, device="cuda")
+            he_set_evict_log(he.h, log, cnt, n_steps)
+            logs.append((log, cnt))
+            outs.append({s: torch.full((w.batch, w.heads, w.head_dim), float("nan"),
+                                       dtype=torch.float32, device="cuda") for s in out_set})
+            scratch.append(torch.empty((w.batch, w.heads, w.head_dim), dtype=torch.float32,
+                                       device="cuda"))
+        torch.cuda.synchronize()
+
+        def issue(step_idx, inp_idx, stream_ptr):
+            for layer in range(L):
+                q, k, v = ins[layer]
+                o = outs[layer].get(step_idx, scratch[layer])
+                rc = he_step_raw(handles[layer].h, ctypes.c_void_p(q[inp_idx].data_ptr()),
+                                 ctypes.c_void_p(k[inp_idx].data_ptr()),
+                                 ctypes.c_void_p(v[inp_idx].data_ptr()),
+                                 ctypes.c_void_p(o.data_ptr()), ctypes.c_void_p(stream_ptr))
+                assert rc == 0, rc
+
+        cur = torch.cuda.current_stream()
+        cycles = int(hold_ms * 1e-3 * 2.0e9)
+        if not graph:
+            torch.cuda._sleep(cycles)
+            for t in range(tokens):
+                issue(t, t, cur.cuda_stream)
+        else:
+            torch.cuda._sleep(cycles)
+            for t in range(warm):
+                issue(t, t, cur.cuda_stream)
+            g = torch.cuda.CUDAGraph()
+            # capture: the output buffers of the steps of the last replay
+            last0 = warm + (replays - 1) * tokens
+            with torch.cuda.graph(g):
+                cs = torch.cuda.current_stream().cuda_stream
+                for t in range(tokens):
+                    issue(last0 + t, warm + t, cs)
+            torch.cuda._sleep(cycles)
+            for _ in range(replays):
+                g.replay()
+        torch.cuda.synchronize()
+        evicted, res_outs, states = {}, {}, {}
+        for layer in range(L):
+            log, cnt = logs[layer]
+            c = cnt.cpu().numpy()
+            assert (c == n_steps).all(), f"layer {layer}: {c.min()}..{c.max()} logged, {n_steps} steps"
+            evicted[layer] = log.cpu().numpy().reshape(n_steps, w.batch, w.kv_heads)
+            for s, o in outs[layer].items():
+                res_outs[(layer, s)] = o.cpu().numpy()
+            he = handles[layer]
+            st = he.state()
+            states[layer] = st + (he.vscales() if v_int8 else None,
+                                  he.scores() if decay > 0.0 else None)
+        return B2BRun(evicted, res_outs, states, tok_of)
+    finally:
+        for he in handles:
+            he.close()
+
+
+def oracle_b2b(w: synth.Workload, units, fill_n: int, tok_of, out_steps=(), layer: int = 0,
+               threshold: float = 0.0, decay: float = 0.0, v_int8: bool = False,
+               chunk: int = 1, threads: int = 8) -> dict:
+    """The oracle over the token sequence tok_of (token indices, repeats
+    allowed) for the given (b, j) units of one layer."""
+    o = oracle.load()
+    W = o.projection(w.projection_seed(layer), w.head_dim, w.bits, w.dtype)
+    lo, hi = min(tok_of), max(tok_of) + 1
+    sel = np.asarray(tok_of) - lo
+    want = np.zeros(len(tok_of), np.uint8)
+    for s in out_steps:
+        want[s] = 1
+
+    def one(u):
+        b, j = u
+        Kin = synth.host_unit_kv(w, "key", b, j, 0, fill_n, layer)
+        Vin = synth.host_unit_kv(w, "value", b, j, 0, fill_n, layer)
+        if chunk > 1:
+            st = o.unit_fill_chunk(W, w.budget, chunk, Kin, Vin, tau=threshold)
+        else:
+            st = o.unit_fill(W, w.budget, Kin, Vin, tau=threshold, memory=decay > 0.0,
+                             vq=v_int8)
+        q = synth.host_unit_queries(w, b, j, lo, hi - lo, layer)[sel]
+        k = synth.host_unit_kv(w, "key", b, j, lo, hi - lo, layer)[sel]
+        v = synth.host_unit_kv(w, "value", b, j, lo, hi - lo, layer)[sel]
+        r = o.unit_stream(st, q, k, v, want_out=want, decay=decay)
+        return OracleRun(r["evicted"], r["out"], st.codes, st.K, st.V, st.occupancy, st.score,
+                         st.Vq, st.Vs)
+
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        futs = {u: ex.submit(one, u) for u in units}
+        return {u: f.result() for u, f in futs.items()}
+
+
+def compare_b2b(w: synth.Workload, g: B2BRun, layer: int, orc: dict, out_steps=()):
+    """Every logged eviction bit-exact, the final cache state of each unit
+    byte-exact, kept outputs within the tolerance."""
+    out_steps = sorted(out_steps)
+    K, V, codes, occ, vs, sc = g.states[layer]
+    worst_max = worst_mean = 0.0
+    for (b, j), r in orc.items():
+        ge = g.evicted[layer][:, b, j]
+        if not np.array_equal(ge, r.evicted):
+            bad = np.nonzero(ge != r.evicted)[0]
+            raise AssertionError(f"layer {layer} unit ({b},{j}): evictions differ first at step "
+                                 f"{bad[0]}: gpu {ge[bad[0]]} oracle {r.evicted[bad[0]]} "
+                                 f"({len(bad)} of {len(ge)} steps differ)")
+        assert occ == r.occupancy
+        assert np.array_equal(codes[b, j].astype(np.uint64), r.codes), f"codes ({b},{j})"
+        assert np.array_equal(K[b, j], r.K), f"K ({b},{j})"
+        if r.Vq is not None:
+            assert np.array_equal(V[b, j], r.Vq), f"int8 V ({b},{j})"
+            assert np.array_equal(vs[b, j], r.Vs), f"value scales ({b},{j})"
+        else:
+            assert np.array_equal(V[b, j], r.V), f"V ({b},{j})"
+        if r.score is not None:
+            assert np.array_equal(sc[b, j], r.score), f"scores ({b},{j})"
+        for i, s in enumerate(out_steps):
+            got = g.outs[(layer, s)][b, j * w.group:(j + 1) * w.group].astype(np.float64)
+            err = np.abs(got - r.outs[i])
+            worst_max = max(worst_max, float(err.max()))
+            worst_mean = max(worst_mean, float(err.mean()))
+    assert worst_max <= MAX_ABS_TOL, f"max-abs error {worst_max}"
+    assert worst_mean <= MEAN_ABS_TOL, f"mean-abs error {worst_mean}"
+    return worst_max, worst_mean

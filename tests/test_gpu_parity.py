@@ -103,6 +103,79 @@ def test_scores_bit_exact():
             assert got[b, j].tolist() == want
 
 
+@pytest.mark.parametrize("bits,budget,opt", [(32, 4096, {}), (8, 4096, {}), (64, 4096, {}),
+                                              (16, 9000, {}), (32, 5000, {"decay": 0.5}),
+                                              (32, 4096, {"threshold": 0.5}),
+                                              (32, 4096, {"v_int8": True})])
+def test_step_distances_bit_exact(bits, budget, opt):
+    """The group-summed Hamming distances that the step's own scan computes
+    (method step 3, the codes/eviction kernel of every step), logged on the
+    device for three steps issued back to back, against the oracle's distances
+    on the same token stream: Llama-3-8B-shaped units (32/8 heads, head_dim 128),
+    one and several scan items per unit (budget 9000), the options."""
+    import torch
+    from lsh_pre_attention_decode_b300 import he_set_dist_log
+    w = small("llama8b_b8", batch=2, bits=bits, budget=budget, prompt=budget + 64)
+    decay, tau, vq = opt.get("decay", 0.0), opt.get("threshold", 0.0), opt.get("v_int8", False)
+    steps = 3
+    with make_handle(w, threshold=tau, decay=decay, v_int8=vq) as he:
+        he.fill(synth.gpu_kv(w, "key", 0, w.budget), synth.gpu_kv(w, "value", 0, w.budget))
+        q = synth.gpu_queries(w, w.budget, steps)
+        k = synth.gpu_kv(w, "key", w.budget, steps, token_major=True)
+        v = synth.gpu_kv(w, "value", w.budget, steps, token_major=True)
+        dist = torch.full((steps, w.batch, w.kv_heads, w.budget), -1, dtype=torch.int32,
+                          device="cuda")
+        out = torch.empty((w.batch, w.heads, w.head_dim), dtype=torch.float32, device="cuda")
+        for t in range(steps):
+            he_set_dist_log(he.h, dist[t])
+            he.step(q[t], k[t], v[t], out)
+        he_set_dist_log(he.h, None)
+        got = dist.cpu().numpy()
+    o = oracle.load()
+    W = o.projection(w.projection_seed(), w.head_dim, bits, w.dtype)
+    for b in range(w.batch):
+        for j in range(w.kv_heads):
+            st = o.unit_fill(W, w.budget, synth.host_unit_kv(w, "key", b, j, 0, w.budget),
+                             synth.host_unit_kv(w, "value", b, j, 0, w.budget), tau=tau,
+                             memory=decay > 0.0)
+            r = o.unit_stream(st, synth.host_unit_queries(w, b, j, w.budget, steps),
+                              synth.host_unit_kv(w, "key", b, j, w.budget, steps),
+                              synth.host_unit_kv(w, "value", b, j, w.budget, steps),
+                              dist_log=True, decay=decay)
+            assert np.array_equal(got[:, b, j], r["dist"]), (b, j)
+
+
+def test_chunk_step_distances_bit_exact():
+    """With chunk eviction the scan logs every slot's own distance (the chunks'
+    sums are built from them): compared with the brute-force group distances
+    of the cache before the step."""
+    import torch
+    from lsh_pre_attention_decode_b300 import he_set_dist_log
+    w = small("llama8b_b8", batch=2, budget=4800, prompt=4900)
+    c = 16
+    o = oracle.load()
+    with make_handle(w, chunk=c) as he:
+        K = synth.host_kv(w, "key", 0, w.budget)
+        he.fill(torch_from_host(K), torch_from_host(synth.host_kv(w, "value", 0, w.budget)))
+        q = synth.host_queries(w, w.budget, c)
+        k = synth.host_kv(w, "key", w.budget, c, token_major=True)
+        v = synth.host_kv(w, "value", w.budget, c, token_major=True)
+        dist = torch.full((w.batch, w.kv_heads, he.rows), -1, dtype=torch.int32, device="cuda")
+        for t in range(c):  # c - 1 staged tokens, then the evicting step
+            if t == c - 1:
+                he_set_dist_log(he.h, dist)
+            he.step(torch_from_host(q[t]), torch_from_host(k[t]), torch_from_host(v[t]))
+        got = dist.cpu().numpy()
+        W = he.projection()
+    for b in range(w.batch):
+        for j in range(w.kv_heads):
+            cq = o.code(q[c - 1, b, j * w.group:(j + 1) * w.group], W)
+            ck = o.code(K[b, j], W)
+            want = [o.group_distance(cq, int(x)) for x in ck]
+            assert got[b, j, :w.budget].tolist() == want
+            assert (got[b, j, w.budget:] == -1).all()
+
+
 # ---------------------------------------------------------------------------
 # whole streams: method steps 1-5 + attention
 # ---------------------------------------------------------------------------

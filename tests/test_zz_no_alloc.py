@@ -1,19 +1,21 @@
 """he_attend_noalloc — decode attention that allocates no device memory.
 
-It serves callers that cannot let a library allocate: work recorded under CUDA
-graph capture (allocation cannot be captured), runtimes whose device memory is
-owned by their own pool or arena, and deployments that fix every byte of device
-memory up front.  It runs the same split-K attention kernel as he_step with its
-scratch in a static device array.
+It serves callers that cannot let a library allocate: runtimes whose device
+memory is owned by their own pool or arena, and deployments that fix every byte
+of device memory up front.  It runs the same split-K attention kernel as he_step
+with its scratch in a static device array that every call shares.
 
-he_step attends over the cache as it stands after the step, so he_attend_noalloc
-on that cache with the same queries must give he_step's output, within the
-tolerance of the parity tests.  This file is collected last on purpose.
+Checked here: against the CPU oracle's fp64 attention on the identical cache
+(stream CTAs that hold several tiles of several units, n below the budget,
+head_dim 64 and 128, G = 1, 2, 4 and 8), two calls in a row each time; and
+against he_step's own output on the cache the step leaves.  This file is
+collected last on purpose.
 """
 import numpy as np
 import pytest
 
 import lsh_pre_attention_decode_b300 as pkg
+import oracle
 import synth
 from gpu_harness import MAX_ABS_TOL, MEAN_ABS_TOL, make_handle, torch_from_host
 
@@ -28,11 +30,51 @@ def test_rejects_bad_arguments_without_touching_the_device():
     assert L.he_attend_noalloc(1, 32, 8, 128, 64, 64, None, None, None, None, None) == -1
 
 
-@pytest.mark.gpu
-def test_matches_the_step_on_two_calls_in_a_row():
+def _cuda():
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
+    pkg.lib()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("batch,heads,kv,D,budget,n", [
+    (8, 32, 8, 128, 4096, 4000),   # 64 units x 63 tiles: every CTA holds several tiles
+    (2, 64, 8, 64, 1000, 777),     # G = 8, head_dim 64, ragged n
+    (3, 8, 8, 128, 300, 300),      # G = 1
+    (1, 8, 4, 64, 9000, 8999),     # G = 2, long units over many CTAs
+])
+def test_matches_the_oracle_on_two_calls_in_a_row(batch, heads, kv, D, budget, n):
+    import torch
+    _cuda()
+    w = synth.WORKLOADS["llama8b_b8"].with_(batch=batch, heads=heads, kv_heads=kv, head_dim=D,
+                                            budget=budget, prompt=budget + 8)
+    K = synth.host_kv(w, "key", 0, budget)
+    V = synth.host_kv(w, "value", 0, budget)
+    Q = synth.host_queries(w, budget, 2)
+    Kd, Vd, Qd = torch_from_host(K), torch_from_host(V), torch_from_host(Q)
+    o = oracle.load()
+    G = heads // kv
+    for call in range(2):
+        out = torch.full((batch, heads, D), float("nan"), dtype=torch.float32, device="cuda")
+        pkg.he_attend_noalloc(batch, heads, kv, D, budget, n, Kd, Vd, Qd[call], out)
+        got = out.cpu().numpy().astype(np.float64)
+        assert np.isfinite(got).all()
+        worst_max = worst_mean = 0.0
+        for b in range(batch):
+            for j in range(kv):
+                want = o.attend(Q[call, b, j * G:(j + 1) * G], K[b, j, :n], V[b, j, :n])
+                err = np.abs(got[b, j * G:(j + 1) * G] - want)
+                worst_max = max(worst_max, float(err.max()))
+                worst_mean = max(worst_mean, float(err.mean()))
+        assert worst_max <= MAX_ABS_TOL and worst_mean <= MEAN_ABS_TOL, (call, worst_max,
+                                                                          worst_mean)
+
+
+@pytest.mark.gpu
+def test_matches_the_step_on_two_calls_in_a_row():
+    import torch
+    _cuda()
     w = synth.WORKLOADS["llama8b_b8"].with_(batch=2, budget=300, prompt=600)
     he = make_handle(w)
     try:
@@ -60,8 +102,7 @@ def test_matches_the_step_on_two_calls_in_a_row():
 @pytest.mark.gpu
 def test_rejects_sizes_beyond_the_scratch():
     import torch
-    if not torch.cuda.is_available():
-        pytest.skip("no CUDA device")
+    _cuda()
     buf = torch.zeros(1024, dtype=torch.bfloat16, device="cuda")
     out = torch.zeros(1024, dtype=torch.float32, device="cuda")
     # 4096 (batch, KV head) units of partial records do not fit 8 MiB
