@@ -36,7 +36,7 @@ def test_reference_arm_prints_one_line_with_the_contract_keys():
     assert cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "steps/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
-    assert d["config"]["workload"].startswith("llama8b_b8")
+    assert d["config"]["workload"].startswith("llama8b_32layer")
 
 
 def test_reference_arm_other_ranks_exit_without_work():
