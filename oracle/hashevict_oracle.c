@@ -17,7 +17,7 @@
  * Decode attention over the retained cache follows (TTKV page, introduction:
  * every decode step attends the whole cache).
  *
- * Readings taken where the pages are silent (each is listed in the design notes):
+ * Readings taken where the pages are silent:
  *   - projection W[d][j] ~ N(0,1) (Irwin-Hall(12) counter-based draw, below),
  *     shared by the query and the keys; no normalisation;
  *   - the projection sum is fp32, fused multiply-add, d = 0..D-1 in order,
@@ -347,8 +347,8 @@ void orc_unit_stream_ext(const void* W, int32_t D, int32_t G, int32_t bits, int3
 
 /* ------------------------------------------------------------------------- */
 /* Quantised value cache (int8 rows with one fp32 scale per row).             */
-/* Reading (the survey's "quantised V with bf16 K"; the value-compression     */
-/* remarks of the DASH-KV and TTKV pages): s = max_d |v_d| / 127 in fp32,     */
+/* Reading (DASH-KV page: values tolerate coarser compression than keys; TTKV */
+/* page: keys get more bits than values): s = max_d |v_d| / 127 in fp32,      */
 /* q_d = v_d / s (fp32 division) rounded half to even, clamped to [-127, 127];*/
 /* a zero row has s = 0 and q = 0.  The stored value is q_d * s.  Keys stay   */
 /* in the element type: codes and logits are those of the method.            */
@@ -470,13 +470,14 @@ void orc_unit_stream_vq(const void* W, int32_t D, int32_t G, int32_t bits, int32
 }
 
 /* ------------------------------------------------------------------------- */
-/* Chunk eviction (the survey's chunk-granular row; ChunkKV page: chunks of   */
-/* 10 contiguous tokens).  Reading: the budget B is cut into B / c aligned    */
-/* chunks of c slots; while the cache is full, new tokens are staged in the   */
-/* c - 1 slots after the budget (and attended); the token that would fill the */
-/* stage evicts the chunk with the largest sum of its slots' group-summed     */
-/* distances (ties: lowest chunk), and the c - 1 staged tokens, in order,     */
-/* then the token itself take the chunk's slots.  c = 1 is the method.        */
+/* Chunk eviction (ChunkKV page: chunks of about 10 contiguous tokens, here  */
+/* scored by the method's distances).  Reading: the budget B is cut into     */
+/* B / c aligned chunks of c slots; while the cache is full, new tokens are  */
+/* staged in the c - 1 slots after the budget (and attended); the token that */
+/* would fill the stage evicts the chunk with the largest sum of its slots'  */
+/* group-summed distances (ties: lowest chunk), and the c - 1 staged tokens, */
+/* in order, then the token itself take the chunk's slots.  c = 1 is the     */
+/* method.                                                                   */
 /* State: K, V [B + c - 1][D], codes [B + c - 1]; occupancy counts staged.    */
 /* ------------------------------------------------------------------------- */
 
