@@ -80,6 +80,8 @@ def parse_args(argv=None):
                     help="int8 value cache with one scale per slot (keys stay bf16)")
     ap.add_argument("--chunk", type=int, default=1,
                     help="chunk eviction: chunks of this many slots (1: the method)")
+    ap.add_argument("--engine", choices=["pipeline", "fused"], default="pipeline",
+                    help="bf16 step engine: three kernels (default) or one kernel")
     ap.add_argument("--graph-ring", type=int, default=64,
                     help="tokens per layer in the captured step graph (even)")
     ap.add_argument("--e2e-steps", type=int, default=8, help="decode steps of the e2e pass")
@@ -210,6 +212,7 @@ def config_of(w: synth.Workload, opts: dict, extra=None):
             if (opts.get("threshold") or opts.get("decay")) else "") + (
             "; int8 value cache" if opts.get("v_int8") else "") + (
             f"; chunk eviction, chunks of {chunk} slots" if chunk > 1 else "") + (
+            "; single-kernel engine" if opts.get("engine") == "fused" else "") + (
             f"; code length {w.bits}" if w.bits != synth.WORKLOADS[w.name].bits else "") + (
             f"; budget set to {w.budget}" if w.budget != synth.WORKLOADS[w.name].budget else ""),
          "batch": w.batch, "heads": w.heads, "kv_heads": w.kv_heads, "head_dim": w.head_dim,
@@ -346,7 +349,7 @@ def measure(w: synth.Workload, opts: dict, L: int, min_s: float, min_steps: int,
         he = HashEvict(w.batch, w.heads, w.kv_heads, w.head_dim, w.bits, w.budget, w.dtype,
                        seed=w.projection_seed(layer), threshold=opts.get("threshold", 0.0),
                        decay=opts.get("decay", 0.0), v_int8=opts.get("v_int8", False),
-                       chunk=chunk)
+                       chunk=chunk, engine=opts.get("engine", "pipeline"))
         K = synth.gpu_kv(w, "key", 0, w.budget, layer)
         V = synth.gpu_kv(w, "value", 0, w.budget, layer)
         he.fill(K, V)
@@ -586,7 +589,7 @@ def measure(w: synth.Workload, opts: dict, L: int, min_s: float, min_steps: int,
 def run_ours(args, rank: int, world: int, dist_on: bool):
     w = make_workload(args.workload, args.bits, args.budget)
     opts = {"threshold": args.threshold, "decay": args.decay, "v_int8": args.v_int8,
-            "chunk": args.chunk}
+            "chunk": args.chunk, "engine": args.engine}
     L = args.layers if args.layers else (w.layers if w.layers > 1 else 4)
     if w.layers > 1 and L != w.layers:
         w = w.with_(layers=L)
@@ -611,12 +614,14 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
         per = {}
         for name, bits, layers in PER_CONFIG:
             wc = make_workload(name, bits)
-            if (wc.name, wc.bits) == (w.name, w.bits) and not any(opts.values()):
+            copts = {"engine": args.engine}
+            if (wc.name, wc.bits) == (w.name, w.bits) and not any(
+                    v for k, v in opts.items() if k != "engine"):
                 continue
             key = name if bits is None else f"{name}_b{bits}"
-            r = measure(wc, {}, layers, args.config_seconds, 0, args.warmup, args.graph_ring, rank,
+            r = measure(wc, copts, layers, args.config_seconds, 0, args.warmup, args.graph_ring, rank,
                         world, dist_on)
-            per[key] = {"config": config_of(wc, {}, {"layers_rotated": layers,
+            per[key] = {"config": config_of(wc, copts, {"layers_rotated": layers,
                                                      "timed_region": r.pop("timed_region")}),
                         **{k: r[k] for k in ("value", "unit", "ms_per_step", "layer_steps_per_s",
                                              "tokens_per_s", "steps", "timed_s", "roofline",
@@ -665,7 +670,8 @@ def main(argv=None):
     res, w, opts, per_meta = run_ours(args, rank, world, dist_on)
     if rank == 0:
         if not args.no_cpu_baseline:
-            res["cpu_baseline"] = cpu_baselines(w, args.cpu_seconds, **opts)
+            res["cpu_baseline"] = cpu_baselines(
+                w, args.cpu_seconds, **{k: v for k, v in opts.items() if k != "engine"})
             for key, wc in per_meta:
                 res["per_config"][key]["cpu_baseline"] = cpu_baselines(wc, 3.0)
         print(json.dumps(res))

@@ -62,7 +62,9 @@ extern "C" {
  * G = heads / kv_heads in {1, 2, 4, 8}; bits in {8, 16, 32, 64};
  * 1 <= budget <= 2^24; batch * kv_heads <= 2^16; dtype HE_DTYPE_*;
  * threshold finite; 0 <= decay <= 1; v_format HE_VFMT_*; 0 <= chunk <= 16
- * (chunk >= 2: bf16, budget % chunk == 0, decay 0, v_format HE_VFMT_ELEM).
+ * (chunk >= 2: bf16, budget % chunk == 0, decay 0, v_format HE_VFMT_ELEM);
+ * engine HE_ENGINE_* (HE_ENGINE_FUSED: bf16, decay 0, v_format HE_VFMT_ELEM,
+ * chunk <= 1).
  * A zero-initialised tail (threshold 0, decay 0, v_format 0, chunk 0) is the
  * method as the paper describes it.
  * Rows per (batch, KV head): R = budget + chunk - 1 with chunk >= 2, else
@@ -96,7 +98,16 @@ typedef struct {
                         the largest score (ties: lowest chunk): the staged tokens in
                         arrival order, then that token, take the chunk's slots.
                         0 or 1 = the method (one slot at a time) */
+  int32_t engine;    /* bf16 handles: HE_ENGINE_PIPELINE (0) runs a step as three
+                        kernels (attention stream; codes and eviction alongside it;
+                        merge and overwrite); HE_ENGINE_FUSED (1) runs it as one
+                        kernel (a hash warp per CTA, and the last CTA of each (batch,
+                        KV head) merges it; the method only: threshold allowed, no
+                        score memory, int8 values or chunks).  Same results. */
 } he_cfg;
+
+#define HE_ENGINE_PIPELINE 0
+#define HE_ENGINE_FUSED 1
 
 typedef struct he_ctx* he_handle;
 
@@ -116,7 +127,11 @@ int he_fill(he_handle h, const void* K, const void* V, int32_t n, void* stream);
 /* One decode step (method steps 1-5, then attention).  bf16 handles launch
  * three kernels on `stream` (attention partials over the cache, codes and
  * eviction, then merge and overwrite), chained by programmatic dependent
- * launch; fp32 handles launch one fused kernel.
+ * launch, or one kernel with HE_ENGINE_FUSED; fp32 handles launch one fused
+ * kernel.  The step's kernels may start before the preceding work on `stream`
+ * has finished and read q, k, v (and fetch cache tiles) before they wait for
+ * it: q, k and v must be complete when he_step is called, or be written by
+ * work that does not let dependent launches start early.
  * q: device [batch][heads][head_dim]; k, v: device [batch][kv_heads][head_dim];
  * out: device fp32 [batch][heads][head_dim].  Updates the cache in place.
  * Errors: HE_EINVAL (NULL handle or pointer, misalignment), HE_ENOTFILLED, HE_ECUDA. */

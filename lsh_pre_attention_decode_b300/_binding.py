@@ -12,6 +12,8 @@ HE_DTYPE_BF16 = 0
 HE_DTYPE_FP32 = 1
 HE_VFMT_ELEM = 0
 HE_VFMT_INT8 = 1
+HE_ENGINE_PIPELINE = 0
+HE_ENGINE_FUSED = 1
 
 _i32 = ctypes.c_int32
 _vp = ctypes.c_void_p
@@ -21,7 +23,7 @@ class HeCfg(ctypes.Structure):
     _fields_ = [("batch", _i32), ("heads", _i32), ("kv_heads", _i32), ("head_dim", _i32),
                 ("bits", _i32), ("budget", _i32), ("dtype", _i32), ("threshold", ctypes.c_float),
                 ("seed", ctypes.c_uint64), ("decay", ctypes.c_float), ("v_format", _i32),
-                ("chunk", _i32)]
+                ("chunk", _i32), ("engine", _i32)]
 
 
 class HashEvictError(RuntimeError):
@@ -231,12 +233,15 @@ class HashEvict:
 
     def __init__(self, batch: int, heads: int, kv_heads: int, head_dim: int, bits: int,
                  budget: int, dtype: str = "bf16", seed: int = 0, threshold: float = 0.0,
-                 decay: float = 0.0, v_int8: bool = False, chunk: int = 1):
+                 decay: float = 0.0, v_int8: bool = False, chunk: int = 1,
+                 engine: str = "pipeline"):
         self.cfg = HeCfg(batch=batch, heads=heads, kv_heads=kv_heads, head_dim=head_dim,
                          bits=bits, budget=budget,
                          dtype=HE_DTYPE_FP32 if dtype == "fp32" else HE_DTYPE_BF16,
                          threshold=threshold, seed=seed, decay=decay,
-                         v_format=HE_VFMT_INT8 if v_int8 else HE_VFMT_ELEM, chunk=chunk)
+                         v_format=HE_VFMT_INT8 if v_int8 else HE_VFMT_ELEM, chunk=chunk,
+                         engine={"pipeline": HE_ENGINE_PIPELINE,
+                                 "fused": HE_ENGINE_FUSED}[engine])
         self.v_int8 = v_int8
         # rows per unit: the budget, plus chunk - 1 staging rows with chunk eviction
         self.rows = budget + max(chunk, 1) - 1

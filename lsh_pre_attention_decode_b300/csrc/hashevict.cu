@@ -31,6 +31,9 @@ constexpr bool kPSplit = true;    // attention weights as bf16 hi + lo parts
 // merge CTA leaves no room for a stream CTA on its SM) take this many tiles
 // fewer than the others.
 constexpr double kLateTiles = 2.0;
+// The same for the fused step: the CTAs that start behind the previous step's
+// merging CTAs (its last contributors, one per unit at most).
+constexpr double kLateTilesFused = 0.0;
 
 struct Kernels {
   const void* step;    // fp32: the fused step; bf16: the stream kernel
@@ -51,7 +54,19 @@ struct Kernels {
   const void* prep_chunk;   // bf16 pipeline with chunk eviction
   const void* merge_chunk;
   int chunk_floats;         // floats of the per-unit chunk record
+  const void* fused;        // bf16, the method: the whole step in one kernel
+  int fused_smem;
+  int fused_threads;
+  int fused_rec_floats;
+  int fused_stages;
 };
+
+// Ring stages of the fused step: two (with the hash warp's copy of W, a third
+// stage would leave one CTA per SM).
+template <int D, int G>
+constexpr int fused_stages() {
+  return 2 * (he::StreamShape<D, G, 3, false, true>::SMEM_ALLOC + 1024) <= 233472 ? 3 : 2;
+}
 
 template <int D, int G>
 int merge_cfg(int n, int* smem) {
@@ -73,6 +88,13 @@ Kernels kernels_for() {
     k.merge = reinterpret_cast<const void*>(&he::merge_kernel<D, G, VQ>);
     k.vq_fill = reinterpret_cast<const void*>(&he::vq_fill_kernel<D>);
     if constexpr (!VQ) {
+      constexpr int NSF = fused_stages<D, G>();
+      using SF = he::StreamShape<D, G, NSF, false, true>;
+      k.fused = reinterpret_cast<const void*>(&he::stream_kernel<D, G, NSF, kPSplit, false, true>);
+      k.fused_smem = SF::SMEM_ALLOC;
+      k.fused_threads = SF::NT;
+      k.fused_rec_floats = he::FRec<G, D>::FLOATS;
+      k.fused_stages = NSF;
       k.prep_chunk = reinterpret_cast<const void*>(&he::prep_kernel<D, G, false, false, true>);
       k.merge_chunk = reinterpret_cast<const void*>(&he::merge_kernel<D, G, false, true>);
       k.chunk_floats = he::ChunkRec<G, D>::FLOATS;
@@ -259,6 +281,11 @@ struct he_ctx {
   int rows = 0;               // rows per unit: budget + chunk - 1 (the stride of K, V, codes)
   float* cstar = nullptr;     // chunk eviction: the evicted chunk's softmax parts, per unit
   int nopre = 0;              // the previous step moved rows (StepParams::nopre)
+  bool fused = false;         // the method on bf16: one kernel per step
+  int prev_tpu = 0;           // fused: the split of the previous step (StepParams::prev_*)
+  int prev_nc = 0;
+  int prev_e = 0;
+  int prev_t1 = 0;
   int32_t* evlog = nullptr;   // test exports (caller-owned device buffers, or null)
   int32_t* evcnt = nullptr;
   int32_t evcap = 0;
@@ -396,6 +423,10 @@ int he_create(const he_cfg* cfg, he_handle* out) {
     return HE_EINVAL;
   if (!std::isfinite(c.threshold) || !(c.decay >= 0.0f && c.decay <= 1.0f)) return HE_EINVAL;
   if (c.chunk < 0 || c.chunk > he::kMaxChunk) return HE_EINVAL;
+  if (c.engine != HE_ENGINE_PIPELINE &&
+      !(c.engine == HE_ENGINE_FUSED && c.dtype == HE_DTYPE_BF16 && c.decay == 0.0f &&
+        c.v_format == HE_VFMT_ELEM && c.chunk <= 1))
+    return HE_EINVAL;
   const int chunk = c.chunk > 1 ? c.chunk : 1;
   if (chunk > 1 && (c.dtype != HE_DTYPE_BF16 || c.v_format != HE_VFMT_ELEM || c.decay != 0.0f ||
                     c.budget % chunk != 0))
@@ -467,8 +498,19 @@ int he_create(const he_cfg* cfg, he_handle* out) {
       break;
     }
 
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&h->ctas_per_sm, kern.step,
-                                                      kern.step_threads, kern.step_smem) !=
+    h->fused = c.engine == HE_ENGINE_FUSED && kern.fused != nullptr;
+    if (h->fused &&
+        (cudaFuncSetAttribute(kern.fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kern.fused_smem) != cudaSuccess ||
+         cudaFuncSetAttribute(kern.fused, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)) {
+      rc = HE_ECUDA;
+      break;
+    }
+    if ((h->fused ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                        &h->ctas_per_sm, kern.fused, kern.fused_threads, kern.fused_smem)
+                  : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                        &h->ctas_per_sm, kern.step, kern.step_threads, kern.step_smem)) !=
             cudaSuccess ||
         h->ctas_per_sm < 1) { rc = HE_ECUDA; break; }
     h->max_ctas = h->num_sms * h->ctas_per_sm;
@@ -486,7 +528,8 @@ int he_create(const he_cfg* cfg, he_handle* out) {
         {(void**)&h->evicted, (size_t)U * sizeof(int32_t)},
         {(void**)&h->counters, (size_t)U * sizeof(int32_t)},
         {(void**)&h->err, sizeof(int32_t)},
-        {(void**)&h->partials, nrec * kern.rec_floats * sizeof(float)},
+        {(void**)&h->partials,
+         nrec * (h->fused ? kern.fused_rec_floats : kern.rec_floats) * sizeof(float)},
         {(void**)&h->uo, (size_t)U * sizeof(he::UnitOut)},
         {(void**)&h->score, c.decay > 0.0f ? (size_t)U * rows * sizeof(float) : 0},
         {(void**)&h->cstar, chunk > 1 ? (size_t)U * kern.chunk_floats * sizeof(float) : 0},
@@ -591,6 +634,7 @@ int he_fill(he_handle h, const void* K, const void* V, int32_t n, void* stream) 
   // of steps) replays on the cache state it leaves.
   h->prev_w1 = -1;
   h->nopre = h->chunk > 1 ? 1 : 0;
+  h->prev_tpu = h->prev_nc = h->prev_e = h->prev_t1 = 0;  // no hash warp folds a key
   h->occupancy = n;
   h->filled = true;
   return HE_OK;
@@ -619,7 +663,44 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
   const int stream_ctas = p.total_tiles == 0
                               ? 0
                               : (p.total_tiles < h->max_ctas ? p.total_tiles : h->max_ctas);
-  if (!h->kern.tc) {
+  if (h->fused) {
+    // the whole step in one kernel (he_fused.cuh); an empty cache runs one CTA per unit
+    p.uo = h->uo;
+    p.kpar = h->kpar;
+    p.prev_w1 = h->prev_w1;
+    p.nopre = 0;
+    p.prev_tpu = h->prev_tpu;
+    p.prev_nc = h->prev_nc;
+    p.prev_e = h->prev_e;
+    p.prev_t1 = h->prev_t1;
+    // every CTA of the step passes its dependency wait at about the same time
+    // (the previous step's CTAs all finish before it returns): an even split
+    const int64_t TT = p.total_tiles;
+    if (kLateTilesFused > 0.0 && stream_ctas == h->max_ctas && TT > stream_ctas) {
+      const int64_t late = h->U < h->max_ctas ? h->U : h->max_ctas;
+      const int64_t E = (int64_t)h->max_ctas - late;
+      if (E > 0 && E < stream_ctas) {
+        const double per = ((double)TT + (double)(stream_ctas - E) * kLateTilesFused) / stream_ctas;
+        int64_t T1 = (int64_t)std::llround(per * (double)E);
+        if (T1 > TT - (stream_ctas - E)) T1 = TT - (stream_ctas - E);  // a tile per late CTA
+        if (T1 < E) T1 = E;
+        p.split_e = (int32_t)E;
+        p.split_t1 = (int32_t)T1;
+      }
+    }
+    const int grid = stream_ctas == 0 ? h->U : stream_ctas;
+    void* sa[] = {(void*)&p, (void*)&h->tmK, (void*)&h->tmV};
+    HE_TRY(h, launch_pdl(h->kern.fused, dim3(grid), dim3(h->kern.fused_threads),
+                         (size_t)h->kern.fused_smem, s, sa));
+    if (ev) {
+      HE_TRY(h, cudaEventRecord(ev[1], s));
+      HE_TRY(h, cudaEventRecord(ev[2], s));
+    }
+    h->prev_tpu = p.tpu;
+    h->prev_nc = stream_ctas;
+    h->prev_e = p.split_e;
+    h->prev_t1 = p.split_t1;
+  } else if (!h->kern.tc) {
     const int grid = stream_ctas == 0 ? h->U : stream_ctas;
     void* args[] = {(void*)&p};
     HE_TRY(h, cudaLaunchKernel(h->kern.step, dim3(grid), dim3(h->kern.step_threads), args,
@@ -949,7 +1030,7 @@ int he_launch_info(he_handle h, int32_t* ctas, int32_t* ctas_per_sm, int32_t* ti
   if (ctas) *ctas = T == 0 ? h->U : (T < h->max_ctas ? T : h->max_ctas);
   if (ctas_per_sm) *ctas_per_sm = h->ctas_per_sm;
   if (tiles) *tiles = T;
-  if (stages) *stages = h->kern.tc ? kTcStages : kSimtStages;
+  if (stages) *stages = h->fused ? h->kern.fused_stages : h->kern.tc ? kTcStages : kSimtStages;
   return HE_OK;
 }
 

@@ -79,6 +79,13 @@ struct StepParams {
   // split_e = split_t1 = 0 is the even split
   int32_t split_e;
   int32_t split_t1;
+  // fused step: the split of this cache's previous step (prev_tpu tiles per
+  // unit over prev_nc CTAs, prev_e / prev_t1 as split_e / split_t1; prev_nc = 0:
+  // no CTA), which fixes how many hash warps fold that step's eviction key
+  int32_t prev_tpu;
+  int32_t prev_nc;
+  int32_t prev_e;
+  int32_t prev_t1;
   // test exports (null: off): a per-step eviction log written on the device
   // (evlog [evcap][U], evcnt [U] entries written per unit) and the group-summed
   // distance of every slot scored by a full-cache step (dist [U][budget])

@@ -209,7 +209,17 @@ struct PhaseTimer {
   if (threadIdx.x == 0 && he::g_he_timeline && blockIdx.x < 4096)                  \
     he::g_he_timeline[(((size_t)p.tl_step * 3 + (r)) * 4096 + blockIdx.x) * 8 + (k)] = \
         (int64_t)he::global_ns();
+// The same for any thread that passes `c`, and a stored value instead of the time.
+#define HE_STAMP_IF(c, r, k)                                                         \
+  if ((c) && he::g_he_timeline && blockIdx.x < 4096)                                 \
+    he::g_he_timeline[(((size_t)p.tl_step * 3 + (r)) * 4096 + blockIdx.x) * 8 + (k)] = \
+        (int64_t)he::global_ns();
+#define HE_STAMP_VAL(c, r, k, v)                                                     \
+  if ((c) && he::g_he_timeline && blockIdx.x < 4096)                                 \
+    he::g_he_timeline[(((size_t)p.tl_step * 3 + (r)) * 4096 + blockIdx.x) * 8 + (k)] = (v);
 #else
+#define HE_STAMP_IF(c, r, k)
+#define HE_STAMP_VAL(c, r, k, v)
 #define HE_TL_FIELDS
 #define HE_TL_INIT(m)
 #define HE_TL_MARK(m, k)

@@ -35,73 +35,14 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "he_common.cuh"
+#include "he_fused.cuh"
+#include "he_layout.cuh"
 #include "he_tc.cuh"
 
 namespace he {
-
-// Per-unit results of prep, read by merge.
-struct UnitOut {
-  // eviction key (distance << 32 | ~slot) of the steps of parity 0 and 1: a
-  // step folds into key[kpar] while the next step's stream kernel may still
-  // read key[kpar ^ 1] (the previous step's decision); merge zeroes key[kpar ^ 1]
-  unsigned long long key[2];
-  unsigned long long codek;
-  float lnew[8];           // the new token's base-2 logits, per query head
-  float lstar[8];          // the evicted slot's base-2 logits, per query head
-  int32_t arrived;         // prep CTAs of the unit done (reset by the last one)
-  int32_t pad[3];
-  uint16_t vstar[128];     // the evicted slot's value row (bf16)
-  int8_t vqstar[128];      // int8 value cache: the evicted slot's row ...
-  float vsstar;            // ... and its scale
-  int32_t pad2[3];
-};
-
-// Chunk eviction: what merge needs to take the evicted chunk out of the
-// attention, per unit.  The chunk's slots fall in at most two 64-slot tiles
-// (part 0: the tile of its first slot, part 1: the next one); per part and
-// query head, the base-2 softmax state of the part's slots alone: max m, sum
-// l = sum exp2(x - m), accumulator a[D] = sum exp2(x - m) v.  An empty part
-// has m = -1e30, l = 0, a = 0.  Layout (floats): m [2][8], l [2][8], a [2][G][D].
-constexpr int kMaxChunk = 16;
-template <int G, int D>
-struct ChunkRec {
-  static constexpr int M = 0, L = 16, A = 32;
-  static constexpr int FLOATS = A + 2 * G * D;
-};
-
-// Slots per prep item with chunks of c slots: a multiple of c and of 16 (so
-// that an item's codes start on a 16-byte boundary for the bulk copy).
-__host__ __device__ __forceinline__ int chunk_item_slots(int c) {
-  const int l = 16 * c / (c & -c);  // lcm(c, 16) for 1 <= c <= 16
-  return 4096 / l * l;
-}
-
-// Stream-K split of a step's TT tiles over NC stream CTAs, in two groups: the
-// first E CTAs take tiles [0, T1) and the others [T1, TT), each group split
-// evenly (CTA c of a group of n over T tiles: [c T / n, (c + 1) T / n)).  The
-// host gives the first group more tiles when the others start later (they wait
-// for SMs that the previous step's merge CTAs hold); E = T1 = 0 is the even
-// split.  Every CTA holds at least one tile, so the CTAs holding a unit's
-// tiles are consecutive and each writes a partial.
-struct TileSplit {
-  int64_t TT, NC, E, T1;
-  __host__ __device__ int64_t begin(int64_t c) const {  // first tile of CTA c (c <= NC)
-    if (c <= E) return E > 0 ? c * T1 / E : 0;
-    return T1 + (c - E) * (TT - T1) / (NC - E);
-  }
-  __host__ __device__ int64_t owner(int64_t t) const {  // the CTA whose range holds tile t
-    if (t < T1) return ((t + 1) * E - 1) / T1;
-    return E + ((t - T1 + 1) * (NC - E) - 1) / (TT - T1);
-  }
-};
-
-// Partial record of one (stream CTA, unit): [m G][l G] padded to 4, acc [G][D].
-template <int G, int D>
-struct PRec {
-  static constexpr int HDR = (2 * G + 3) / 4 * 4;
-  static constexpr int FLOATS = HDR + G * D;
-};
 
 // ---------------------------------------------------------------------------
 // prep
@@ -477,11 +418,13 @@ constexpr int kDescEnd = 4;    // no more tiles
 // VQ: the value cache holds int8 rows with one fp32 scale per slot (a stage is
 // the bf16 K tile, the int8 V tile and the tile's scales; each consumer warp
 // widens its 16 value rows to bf16 in a buffer of its own for the value MMA).
-template <int D, int G, int NS, bool VQ = false>
+// FUSED: the whole step in this kernel (he_fused.cuh): a hash warp after the
+// producer warp, and the last CTA of each unit merges it.
+template <int D, int G, int NS, bool VQ = false, bool FUSED = false>
 struct StreamShape {
   static constexpr int NCW = 4;              // consumer warps
   static constexpr int NC = NCW * 32;        // consumer threads
-  static constexpr int NT = NC + 32;         // + the producer warp
+  static constexpr int NT = NC + 32 + (FUSED ? 32 : 0);  // + the producer (and hash) warp
   static constexpr int TS = 16 * NCW;        // slots per tile
   static constexpr int NHALF = D / 64;       // 128-byte column boxes per row
   static constexpr int BOXB = TS * 128;      // bytes per TMA box
@@ -494,7 +437,8 @@ struct StreamShape {
   static constexpr int KS = D / 16;          // k-steps of the logit MMA
   static constexpr int MT = D / 16;          // d blocks of the value MMA
   static constexpr int PB = 8 * 16 * 2;      // bytes of one P^T block [8 heads][16 slots] bf16
-  static constexpr int WACC = NCW * G * D;   // floats of the warp-merge area
+  // floats of the warp-merge area (FUSED: also the merge's recompute scratch)
+  static constexpr int WACC = NCW * G * (D + (FUSED ? 2 : 0));
   static constexpr int OFF_STAGE = 0;        // 1024-byte aligned (128B swizzle)
   static constexpr int OFF_Q = NS * STAGEB;  // [NS][QB]
   static constexpr int OFF_VW = (OFF_Q + NS * QB + 1023) / 1024 * 1024;  // VQ: [NCW][VWB]
@@ -502,34 +446,34 @@ struct StreamShape {
   static constexpr int OFF_P = OFF_WACC + WACC * 4;
   static constexpr int OFF_WM = OFF_P + NCW * 2 * PB;
   static constexpr int OFF_DESC = OFF_WM + 2 * NCW * G * 4;  // int4 [NS]
-  static constexpr int OFF_FLAG = OFF_DESC + 16 * NS;       // abort, issued, producer done, pad
-  static constexpr int OFF_BAR = OFF_FLAG + 16;             // full[NS], empty[NS], sync[2]
-  static constexpr int OFF_PREW = OFF_BAR + (2 * NS + 2) * 8;  // int [NS]
-  static constexpr int SMEM = OFF_PREW + 16;
+  // abort, issued, producer done, hash done, merge flag, last contributor, pad[2]
+  static constexpr int OFF_FLAG = OFF_DESC + 16 * NS;
+  static constexpr int OFF_BAR = OFF_FLAG + 32;             // full[NS], empty[NS], sync[3]
+  static constexpr int OFF_PREW = OFF_BAR + (2 * NS + 3) * 8;  // int [NS]
+  // FUSED: the hash warp's copy of W (up to 64 bits; a bulk-copy destination,
+  // so 16-byte aligned) and its barrier
+  static constexpr int OFF_W = (OFF_PREW + 16 + 127) / 128 * 128;
+  static constexpr int WB = FUSED ? D * 64 * 2 : 0;
+  static constexpr int OFF_WBAR = OFF_W + WB;
+  static constexpr int OFF_XS = OFF_WBAR + 16;  // FUSED: the hash warp's rows, fp32 [G + 1][D]
+  static constexpr int SMEM = FUSED ? OFF_XS + (G + 1) * D * 4 : OFF_WBAR;
+  static_assert(OFF_Q % 16 == 0 && OFF_DESC % 16 == 0 && OFF_BAR % 8 == 0 && OFF_W % 16 == 0 &&
+                    OFF_WBAR % 8 == 0 && OFF_P % 16 == 0 && OFF_WACC % 16 == 0 &&
+                    OFF_XS % 16 == 0,
+                "shared-memory alignment (bulk copies 16 bytes, mbarriers 8)");
   static_assert(NS <= 4, "written-slot table");
   static constexpr int SMEM_ALLOC = SMEM + 1024;  // slack to align the base to 1024
   static_assert(D % 64 == 0 && G >= 1 && G <= 8 && (G & (G - 1)) == 0, "shape");
   static_assert(STAGEB % 1024 == 0 && BOXB % 1024 == 0 && QB % 16 == 0, "alignment");
 };
 
-// Bounded barrier of the four consumer warps on an mbarrier of count NCW
-// (lane 0 of each warp arrives); false if the wait gave up.
-template <int NCW>
-__device__ __forceinline__ bool consumer_sync(uint64_t* bar, uint32_t& phase, int lane) {
-  __syncwarp();
-  if (lane == 0) mbar_arrive(bar);
-  const bool ok = mbar_wait_bounded(bar, phase & 1u);
-  ++phase;
-  __syncwarp();
-  return ok;
-}
-
-template <int D, int G, int NS, bool PSPLIT, bool VQ = false>
-__global__ void __launch_bounds__(StreamShape<D, G, NS, VQ>::NT, 2)
+template <int D, int G, int NS, bool PSPLIT, bool VQ = false, bool FUSED = false>
+__global__ void __launch_bounds__(StreamShape<D, G, NS, VQ, FUSED>::NT, 2)
     stream_kernel(const StepParams p, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV) {
-  using S = StreamShape<D, G, NS, VQ>;
-  using R = PRec<G, D>;
+  static_assert(!(FUSED && VQ), "the fused step keeps bf16 values");
+  using S = StreamShape<D, G, NS, VQ, FUSED>;
+  using R = std::conditional_t<FUSED, FRec<G, D>, PRec<G, D>>;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   unsigned char* stage = smem + S::OFF_STAGE;
@@ -541,6 +485,9 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ>::NT, 2)
   volatile int32_t* v_abort = reinterpret_cast<int32_t*>(smem + S::OFF_FLAG);
   volatile int32_t* v_issued = v_abort + 1;   // stages issued (descriptors written)
   volatile int32_t* v_prod_done = v_abort + 2;
+  volatile int32_t* v_hash_done = v_abort + 3;  // FUSED: segments the hash warp finished
+  int* s_flag = const_cast<int*>(reinterpret_cast<volatile int*>(v_abort + 4));
+  volatile int32_t* v_last = v_abort + 5;  // FUSED: this CTA is the unit's last contributor
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + S::OFF_BAR);
   uint64_t* empty_bar = full_bar + NS;
   uint64_t* sync_bar = empty_bar + NS;
@@ -616,10 +563,28 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ>::NT, 2)
     }
     mbar_init(&sync_bar[0], S::NCW);
     mbar_init(&sync_bar[1], S::NCW);
+    mbar_init(&sync_bar[2], S::NCW);
     v_abort[0] = 0;
     v_issued[0] = 0;
     v_prod_done[0] = 0;
+    v_hash_done[0] = 0;
+    v_abort[4] = 0;
+    v_abort[5] = 0;
+    if constexpr (FUSED) mbar_init(reinterpret_cast<uint64_t*>(smem + S::OFF_WBAR), 1);
     fence_mbar_init();
+  }
+  if constexpr (FUSED) {
+    // the barriers and flags are set up; the hash warp goes its own way (it
+    // does its own dependency wait once its work before the wait is done)
+    __syncthreads();
+    if (warp == S::NCW + 1) {
+      hash_warp<D, G>(p, sb, se, v_hash_done, lane, reinterpret_cast<uint16_t*>(smem + S::OFF_W),
+                      reinterpret_cast<uint64_t*>(smem + S::OFF_WBAR),
+                      reinterpret_cast<float*>(smem + S::OFF_XS));
+      return;
+    }
+  }
+  if (warp == S::NCW && lane == 0) {
     for (int k = 0; k < npre; ++k) put_static(k);
     // the next tile of the range into L2 as well, while the previous step's
     // merge (latency bound, little DRAM traffic) finishes: a stale copy of the
@@ -644,13 +609,25 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ>::NT, 2)
     if (p.prev_w1 > 0) {
       w = p.prev_w1 - 1;  // the previous step appended here
     } else if (p.prev_w1 < 0 && p.uo != nullptr) {
-      const unsigned long long key = __ldcg(&p.uo[u].key[p.kpar ^ 1]);
-      w = key ? (int)evict_key_slot(key) : -1;
+      if constexpr (FUSED) {
+        // the previous step's key is final once all its hash warps counted in
+        // (they do so early in that step); if not yet, read the slot after the wait
+        if (ld_acquire_gpu(&p.uo[u].hcnt[p.kpar ^ 1]) == prev_hash_count(p, u)) {
+          const unsigned long long key = __ldcg(&p.uo[u].key[p.kpar ^ 1]);
+          w = key ? (int)evict_key_slot(key) : -1;
+        } else {
+          w = -2;
+        }
+      } else {
+        const unsigned long long key = __ldcg(&p.uo[u].key[p.kpar ^ 1]);
+        w = key ? (int)evict_key_slot(key) : -1;
+      }
     }
     prew[tid] = w;
   }
-  __syncthreads();
+  group_sync<S::NC + 32, FUSED ? 1 : 0>();  // (FUSED: the hash warp has gone its own way)
   pdl_wait();     // the previous step is complete: the cache is final
+  HE_STAMP_IF(FUSED && tid == 0, 1, 2);
   pdl_trigger();  // prep may launch now: its CTAs take the room stream leaves
 
   // ---------------- producer warp ----------------
@@ -691,7 +668,9 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ>::NT, 2)
   float mrun0 = -1e30f, mrun1 = -1e30f, lrun0 = 0.0f, lrun1 = 0.0f;
   float acc[S::MT][4];
   int wslot = -1;
-  uint32_t sync_phase[2] = {0u, 0u};
+  uint32_t sync_phase[3] = {0u, 0u, 0u};
+  int seg = 0;     // FUSED: segments finished by this CTA
+  int merges = 0;  // FUSED: units this CTA merged
   int k = 0;
   bool aborted = false;
   for (;; ++k) {
@@ -725,6 +704,7 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ>::NT, 2)
       // the slot the previous step of this cache wrote in unit u (the evicted
       // slot, or the last appended one): stale in a tile fetched before the wait
       wslot = k < npre ? prew[k] : -1;
+      if (FUSED && wslot == -2) wslot = __ldcg(&p.evicted[u]);  // (final after the wait)
     }
     if (VQ && k < npre && (unsigned)(wslot - slot_base) < 16u &&
         HE_CHECK(wslot < p.budget, p.err)) {
@@ -968,6 +948,73 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ>::NT, 2)
         *v_abort = 1;
         aborted = true;
         break;
+      }
+      if constexpr (FUSED) {
+        // the segment's state is written: the next tile starts a segment, so
+        // these hold nothing while this CTA counts in and perhaps merges
+        mrun0 = mrun1 = -1e30f;
+        lrun0 = lrun1 = 0.0f;
+#pragma unroll
+        for (int mt = 0; mt < S::MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
+#pragma unroll
+        for (int ks = 0; ks < S::KS; ++ks) qb[ks][0] = qb[ks][1] = 0u;
+        // count in once the hash warp has stored this segment's candidate; the
+        // unit's last contributor merges it
+        int first, n;
+        unit_contributors(split, u, tps, first, n);
+        if (tid == 0) {
+          *v_last = 0;
+          const uint64_t t0 = global_ns();
+          HE_STAMP_IF(true, 1, 3);
+          while (*v_hash_done <= seg && global_ns() - t0 < 2000000000ull) {
+          }
+          HE_STAMP_IF(true, 1, 4);
+          if (*v_hash_done <= seg) {
+            atomicExch(p.err, 1);
+            *v_abort = 1;
+          } else {
+            const int prev = atom_add_acq_rel_gpu(&p.uo[u].arrived, 1);
+            *v_last = prev == n - 1 ? 1 : 0;
+          }
+          HE_STAMP_IF(true, 1, 5);
+        }
+        if (!consumer_sync<S::NCW>(&sync_bar[2], sync_phase[2], lane) || *v_abort) {
+          atomicExch(p.err, 1);
+          *v_abort = 1;
+          aborted = true;
+          break;
+        }
+        if (*v_last &&
+            !fused_merge<D, G, S::NCW>(p, split, u, first, n, wacc, s_flag, ++merges, tid,
+                                       &sync_bar[2], sync_phase[2])) {
+          atomicExch(p.err, 1);
+          *v_abort = 1;
+          aborted = true;
+          break;
+        }
+        HE_STAMP_IF(tid == 0 && *v_last, 1, 6);
+        ++seg;
+      }
+    }
+  }
+  if constexpr (FUSED) {
+    // an empty cache (no tiles; CTA u per unit): the new token alone
+    if (!aborted && p.tpu == 0) {
+      if (tid == 0) {
+        const uint64_t t0 = global_ns();
+        while (*v_hash_done < 1 && global_ns() - t0 < 2000000000ull) {
+        }
+        if (*v_hash_done < 1) {
+          atomicExch(p.err, 1);
+          *v_abort = 1;
+        }
+      }
+      if (!consumer_sync<S::NCW>(&sync_bar[2], sync_phase[2], lane) || *v_abort ||
+          !fused_merge<D, G, S::NCW>(p, split, (int)blockIdx.x, 0, 0, wacc, s_flag, ++merges,
+                                     tid, &sync_bar[2], sync_phase[2])) {
+        atomicExch(p.err, 1);
+        *v_abort = 1;
+        aborted = true;
       }
     }
   }

@@ -19,6 +19,18 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Bounded barrier of NCW warps (the consumer warps of a step kernel) on an mbarrier of count NCW
+// (lane 0 of each warp arrives); false if the wait gave up.
+template <int NCW>
+__device__ __forceinline__ bool consumer_sync(uint64_t* bar, uint32_t& phase, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+  const bool ok = mbar_wait_bounded(bar, phase & 1u);
+  ++phase;
+  __syncwarp();
+  return ok;
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) accesses of the same bytes.
 __device__ __forceinline__ void fence_proxy_async_smem() {

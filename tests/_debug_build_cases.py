@@ -12,9 +12,9 @@ import synth  # noqa: E402
 from gpu_harness import compare, run_gpu, run_oracle_units  # noqa: E402
 
 
-def case(w, fill_n, steps, units, **kw):
+def case(w, fill_n, steps, units, engine="pipeline", **kw):
     out_steps = sorted({0, steps // 2, steps - 1})
-    g = run_gpu(w, fill_n, steps, out_steps, read_state=True, **kw)
+    g = run_gpu(w, fill_n, steps, out_steps, read_state=True, engine=engine, **kw)
     orc = run_oracle_units(w, units, fill_n, steps, out_steps, **kw)
     compare(w, g, orc, out_steps, check_state=True)
 
@@ -58,6 +58,8 @@ def main():
         ("score memory", base.with_(batch=2, budget=333, prompt=700), 320, 30, {"decay": 0.5}),
         ("G = 8, D = 64", base.with_(batch=2, heads=64, head_dim=64, bits=16, budget=200,
                                      prompt=400), 200, 20, {}),
+        ("single-kernel engine", base.with_(batch=2, budget=3000, prompt=3100), 2990, 20,
+         {"engine": "fused"}),
     ]
     for name, w, fill_n, steps, kw in cases:
         units = [(b, j) for b in range(w.batch) for j in (0, w.kv_heads - 1)]

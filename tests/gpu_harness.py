@@ -43,24 +43,24 @@ class GpuRun:
 
 
 def make_handle(w: synth.Workload, layer: int = 0, threshold: float = 0.0, decay: float = 0.0,
-                v_int8: bool = False, chunk: int = 1):
+                v_int8: bool = False, chunk: int = 1, engine: str = "pipeline"):
     from lsh_pre_attention_decode_b300 import HashEvict
     return HashEvict(w.batch, w.heads, w.kv_heads, w.head_dim, w.bits, w.budget, w.dtype,
                      seed=w.projection_seed(layer), threshold=threshold, decay=decay,
-                     v_int8=v_int8, chunk=chunk)
+                     v_int8=v_int8, chunk=chunk, engine=engine)
 
 
 def run_gpu(w: synth.Workload, fill_n: int, steps: int, out_steps=(), layer: int = 0,
             device_gen: bool = False, read_state: bool = False, batch_tokens: int = 256,
             profile: bool = False, threshold: float = 0.0, decay: float = 0.0,
-            v_int8: bool = False, chunk: int = 1) -> GpuRun:
+            v_int8: bool = False, chunk: int = 1, engine: str = "pipeline") -> GpuRun:
     """Fill with prompt tokens [0, fill_n), then stream tokens fill_n .. fill_n+steps-1
     (generated batch_tokens at a time).  With decay > 0 the returned state also
     holds the per-slot scores; with an int8 value cache, V is int8 and the value
     scales follow; chunk > 1: chunk eviction (state rows budget + chunk - 1)."""
     import torch
     out_steps = set(out_steps)
-    he = make_handle(w, layer, threshold, decay, v_int8, chunk)
+    he = make_handle(w, layer, threshold, decay, v_int8, chunk, engine)
     try:
         if fill_n > 0:
             if device_gen:
@@ -197,7 +197,7 @@ class B2BRun:
 def run_gpu_b2b(w: synth.Workload, fill_n: int, tokens: int, out_steps=(), layers: int = 1,
                 graph: bool = False, replays: int = 2, warm: int = 0, threshold: float = 0.0,
                 decay: float = 0.0, v_int8: bool = False, chunk: int = 1,
-                hold_ms: float = 20.0) -> B2BRun:
+                hold_ms: float = 20.0, engine: str = "pipeline") -> B2BRun:
     """Fill `layers` independent caches with prompt tokens [0, fill_n), then
     issue steps round robin over the layers (layer 0 token t, layer 1 token t,
     ...) with no host synchronisation, each step writing the slots it wrote to
@@ -228,7 +228,7 @@ def run_gpu_b2b(w: synth.Workload, fill_n: int, tokens: int, out_steps=(), layer
     he_step_raw = lib().he_step
     try:
         for layer in range(L):
-            he = make_handle(w, layer, threshold, decay, v_int8, chunk)
+            he = make_handle(w, layer, threshold, decay, v_int8, chunk, engine)
             handles.append(he)
             if fill_n > 0:
                 he.fill(synth.gpu_kv(w, "key", 0, fill_n, layer),

@@ -65,7 +65,10 @@ def cfg(**kw):
                                  dict(decay=float("nan")), dict(threshold=float("inf")),
                                  dict(threshold=float("nan")), dict(chunk=-1), dict(chunk=17),
                                  dict(chunk=3), dict(chunk=2, dtype=1),
-                                 dict(chunk=2, v_format=1), dict(chunk=2, decay=0.5)])
+                                 dict(chunk=2, v_format=1), dict(chunk=2, decay=0.5),
+                                 dict(engine=2), dict(engine=-1), dict(engine=1, dtype=1),
+                                 dict(engine=1, decay=0.5), dict(engine=1, v_format=1),
+                                 dict(engine=1, chunk=4, budget=256)])
 def test_create_rejects_bad_configs(L, bad):
     h = ctypes.c_void_p()
     assert L.he_create(ctypes.byref(cfg(**bad)), ctypes.byref(h)) == -1
@@ -90,6 +93,8 @@ def test_null_arguments_are_rejected(L):
     assert L.he_read_scores(None, None) == -1
     assert L.he_read_vscales(None, None) == -1
     assert L.he_wait_probe(None, 1000, None) == -1
+    assert L.he_set_evict_log(None, None, None, 0) == -1
+    assert L.he_set_dist_log(None, None) == -1
     assert L.he_set_alloc_limit(0) == 0
 
 

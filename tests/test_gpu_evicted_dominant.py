@@ -2,7 +2,8 @@
 
 The bf16 step takes the evicted slot out of the attention partial that holds it;
 when the slot carries more than half of that partial's mass it recomputes the
-partial exactly instead of subtracting.  Here a key is built to be both the most
+partial exactly instead of subtracting (both engines: the three-kernel pipeline
+and the single fused kernel).  Here a key is built to be both the most
 Hamming-dissimilar to the query (all code bits flipped: evicted) and the key
 with by far the largest logit, so the exact path must run, and the result must
 still equal the oracle's (which never attends to the evicted slot).
@@ -29,8 +30,9 @@ def to_f64(h):
 # (bits, budget, slot): one unit of 4 tiles, and one of 375 tiles spread over
 # every stream CTA, with the slot (tile 340) inside one CTA's range (32-bit
 # codes there: no random key of 24000 ties the constructed distance).
+@pytest.mark.parametrize("engine", ["pipeline", "fused"])
 @pytest.mark.parametrize("bits,budget,slot", [(8, 256, 77), (16, 256, 77), (32, 24000, 21773)])
-def test_dominant_evicted_slot_is_recomputed(bits, budget, slot):
+def test_dominant_evicted_slot_is_recomputed(bits, budget, slot, engine):
     import torch
     w = synth.WORKLOADS["llama8b_b8"].with_(batch=1, heads=4, kv_heads=1, budget=budget,
                                             bits=bits, prompt=2 * budget)
@@ -67,7 +69,7 @@ def test_dominant_evicted_slot_is_recomputed(bits, budget, slot):
     r_or = o.unit_stream(st, q[None], knew[None], vnew[None])
     assert r_or["evicted"].tolist() == [slot]
 
-    he = make_handle(w)
+    he = make_handle(w, engine=engine)
     try:
         he.fill(torch_from_host(K[None, None]), torch_from_host(V[None, None]))
         out = he.step(torch_from_host(q[None]), torch_from_host(knew[None, None]),
