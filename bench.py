@@ -85,6 +85,8 @@ def parse_args(argv=None):
     ap.add_argument("--graph-ring", type=int, default=64,
                     help="tokens per layer in the captured step graph (even)")
     ap.add_argument("--e2e-steps", type=int, default=8, help="decode steps of the e2e pass")
+    ap.add_argument("--eager-steps", type=int, default=8,
+                    help="decode steps of the eager (one call per layer-step) pass")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU work of the headline's all-core oracle sample")
     ap.add_argument("--ref-seconds", type=float, default=60.0,
@@ -324,7 +326,7 @@ def cpu_baselines(w: synth.Workload, target_s: float, **opts) -> dict:
 # ---------------------------------------------------------------------------
 
 def measure(w: synth.Workload, opts: dict, L: int, min_s: float, min_steps: int, warmup: int,
-            graph_ring: int, rank: int, world: int, dist_on: bool, eager: bool = False,
+            graph_ring: int, rank: int, world: int, dist_on: bool, eager_steps: int = 0,
             e2e_steps: int = 0) -> dict:
     """Times `w` with L layer caches (this rank's shard), as a CUDA graph of
     captured he_step calls replayed back to back.  Returns the measurement."""
@@ -387,9 +389,9 @@ def measure(w: synth.Workload, opts: dict, L: int, min_s: float, min_steps: int,
         issue(i, stream.cuda_stream)
     torch.cuda.synchronize()
     res = {}
-    if eager:
+    if eager_steps > 0:
         # one he_step call per layer-step from this thread, no graph
-        n_eager = Ln * max(8, min(64, 2048 // Ln))
+        n_eager = Ln * max(eager_steps, period)
         n_eager -= n_eager % (Ln * period)
         ee0 = torch.cuda.Event(enable_timing=True)
         ee1 = torch.cuda.Event(enable_timing=True)
@@ -594,7 +596,7 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     if w.layers > 1 and L != w.layers:
         w = w.with_(layers=L)
     head = measure(w, opts, L, args.min_seconds, args.steps, args.warmup, args.graph_ring, rank,
-                   world, dist_on, eager=True, e2e_steps=args.e2e_steps)
+                   world, dist_on, eager_steps=args.eager_steps, e2e_steps=args.e2e_steps)
     res = {"metric": METRIC, "value": head.pop("value"), "unit": "steps/s", "n_gpus": world,
            "steps": head.pop("steps"), "steps_requested": args.steps,
            "warmup": max(args.warmup, 3), "ms_per_step": head.pop("ms_per_step"),
