@@ -40,13 +40,16 @@ struct Kernels {
   const void* prep;    // bf16 pipeline
   const void* prep_mem;  // bf16 pipeline with score memory
   const void* merge;   // bf16 pipeline
+  const void* merge_mu;  // bf16 pipeline, several units per merge CTA
   const void* score;
   const void* code;
   int step_smem;
   int step_threads;
   int prep_smem;
   int merge_smem;                  // dynamic shared memory of the largest merge CTA
-  int (*merge_cfg)(int, int*);     // merge threads (and smem) for n partials per unit
+  // merge launch shape for U units of at most n partials: threads per CTA
+  // (and nq, units per CTA, smem)
+  int (*merge_cfg)(int n, int U, bool multi, int* nq, int* upc, int* smem);
   int tile;
   int rec_floats;
   bool tc;  // tensor-core pipeline (tensor maps, programmatic dependent launch)
@@ -69,8 +72,9 @@ constexpr int fused_stages() {
 }
 
 template <int D, int G>
-int merge_cfg(int n, int* smem) {
-  const int t = he::MergeShape<D, G>::threads(n);
+int merge_cfg(int n, int U, bool multi, int* nq, int* upc, int* smem) {
+  he::MergeShape<D, G>::config(n, U, multi, nq, upc);
+  const int t = *nq * *upc * he::MergeShape<D, G>::GD4;
   *smem = he::merge_smem_bytes<D, G>(t);
   return t;
 }
@@ -86,6 +90,8 @@ Kernels kernels_for() {
     k.prep = reinterpret_cast<const void*>(&he::prep_kernel<D, G, false, VQ>);
     k.prep_mem = reinterpret_cast<const void*>(&he::prep_kernel<D, G, true, VQ>);
     k.merge = reinterpret_cast<const void*>(&he::merge_kernel<D, G, VQ>);
+    if constexpr (!VQ)
+      k.merge_mu = reinterpret_cast<const void*>(&he::merge_kernel<D, G, false, false, true>);
     k.vq_fill = reinterpret_cast<const void*>(&he::vq_fill_kernel<D>);
     if constexpr (!VQ) {
       constexpr int NSF = fused_stages<D, G>();
@@ -281,6 +287,7 @@ struct he_ctx {
   int rows = 0;               // rows per unit: budget + chunk - 1 (the stride of K, V, codes)
   float* cstar = nullptr;     // chunk eviction: the evicted chunk's softmax parts, per unit
   int nopre = 0;              // the previous step moved rows (StepParams::nopre)
+  int merge_ctas = 0;         // merge CTAs of the previous step (each holds an SM)
   bool fused = false;         // the method on bf16: one kernel per step
   int prev_tpu = 0;           // fused: the split of the previous step (StepParams::prev_*)
   int prev_nc = 0;
@@ -493,7 +500,12 @@ int he_create(const he_cfg* cfg, he_handle* out) {
          cudaFuncSetAttribute(kern.prep_mem, cudaFuncAttributePreferredSharedMemoryCarveout,
                               (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
          cudaFuncSetAttribute(kern.merge, cudaFuncAttributePreferredSharedMemoryCarveout,
-                              (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)) {
+                              (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+         (kern.merge_mu != nullptr &&
+          (cudaFuncSetAttribute(kern.merge_mu, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kern.merge_smem) != cudaSuccess ||
+           cudaFuncSetAttribute(kern.merge_mu, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)))) {
       rc = HE_ECUDA;
       break;
     }
@@ -726,7 +738,8 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
     // unit, at most one per SM) start first and take more tiles
     const int64_t TT = p.total_tiles;
     if (stream_ctas == h->max_ctas && TT > stream_ctas) {
-      const int merge_sms = h->U < h->num_sms ? h->U : h->num_sms;
+      const int mc = h->merge_ctas > 0 ? h->merge_ctas : h->U;
+      const int merge_sms = mc < h->num_sms ? mc : h->num_sms;
       const int64_t E = (int64_t)h->ctas_per_sm * (h->num_sms - merge_sms);
       if (E > 0 && E < stream_ctas) {
         const double per = ((double)TT + (double)(stream_ctas - E) * kLateTiles) / stream_ctas;
@@ -752,7 +765,6 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
                          (size_t)h->kern.prep_smem, s, pa));
     if (ev) HE_TRY(h, cudaEventRecord(ev[2], s));
     int sc = stream_ctas;
-    void* ma[] = {(void*)&p, (void*)&uo, (void*)&sc};
     // partials per unit: at most ceil(tiles per unit / fewest tiles of a CTA) + 1
     int nmax = 0;
     if (TT > 0 && stream_ctas > 0) {
@@ -763,10 +775,15 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
       if (p.split_e > 0) fewest = std::min(fewest, sp.begin(p.split_e) - sp.begin(p.split_e - 1));
       nmax = (int)((p.tpu + fewest - 1) / fewest) + 1;
     }
-    int msmem = 0;
-    const int mthreads = h->kern.merge_cfg(nmax, &msmem);
-    HE_TRY(h, launch_pdl(ch ? h->kern.merge_chunk : h->kern.merge, dim3(h->U), dim3(mthreads),
-                         (size_t)msmem, s, ma));
+    // several units per merge CTA only when the units outnumber the SMs (one
+    // wave of merge CTAs instead of several); else one unit per CTA
+    int msmem = 0, nq = 1, upc = 1;
+    const bool multi = !ch && !h->vq && h->U > h->num_sms;
+    const int mthreads = h->kern.merge_cfg(nmax, h->U, multi, &nq, &upc, &msmem);
+    void* ma[] = {(void*)&p, (void*)&uo, (void*)&sc, (void*)&nq};
+    HE_TRY(h, launch_pdl(ch ? h->kern.merge_chunk : (upc > 1 ? h->kern.merge_mu : h->kern.merge),
+                         dim3(h->U / upc), dim3(mthreads), (size_t)msmem, s, ma));
+    h->merge_ctas = h->U / upc;
   }
   if (ev) {
     HE_TRY(h, cudaEventRecord(ev[3], s));

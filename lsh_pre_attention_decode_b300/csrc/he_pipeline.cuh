@@ -1059,6 +1059,29 @@ struct MergeShape {
     nq = nq < NQ_MIN ? NQ_MIN : (nq > NQ_MAX ? NQ_MAX : nq);
     return GD4 * nq;
   }
+  // Launch shape for U units with at most n partials each: nq groups of GD4
+  // threads per unit and upc units per CTA.  With `multi` (no chunks, no int8
+  // values) a CTA takes up to four units of ceil(n / kMergeRegs) groups each
+  // (and at least D threads) when U is a multiple of that count; else one unit
+  // of threads(n) threads.
+  static void config(int n, int U, bool multi, int* nq, int* upc) {
+    // (at least D threads per unit: they write the new token's key and value rows)
+    constexpr int QMIN = (D + GD4 - 1) / GD4;
+    int q = (n + kMergeRegs - 1) / kMergeRegs;
+    q = q < QMIN ? QMIN : (q > NQ_MAX ? NQ_MAX : q);
+    if (multi) {
+      int up = kMergeMaxThreads / (q * GD4);
+      up = up >= 4 ? 4 : up;
+      while (up > 1 && U % up != 0) --up;
+      if (up > 1) {
+        *nq = q;
+        *upc = up;
+        return;
+      }
+    }
+    *nq = threads(n) / GD4;
+    *upc = 1;
+  }
 };
 
 // Exact partial over slots [lo, hi) of unit u without the slots [skip,
@@ -1227,13 +1250,17 @@ __device__ __forceinline__ float take_part(float cm, float cl, const float4& ca,
 // staged rows [lbudget, lbudget + c - 1) move to the chunk's first c - 1
 // slots and the new token takes its last.  Other steps append (stage) the
 // token at p.append_slot, as the method does.
-template <int D, int G, bool VQ = false, bool CH = false>
+// MU: a CTA merges MT / (nq * GD4) units, one group of nq * GD4 threads each
+// (without chunks and int8 values, for steps with more units than SMs: the
+// merge CTAs then run in one wave instead of several); else one unit per CTA.
+template <int D, int G, bool VQ = false, bool CH = false, bool MU = false>
 __global__ void __launch_bounds__(kMergeMaxThreads)
-    merge_kernel(const StepParams p, UnitOut* uo, int stream_ctas) {
+    merge_kernel(const StepParams p, UnitOut* uo, int stream_ctas, int nq) {
   static_assert(!(CH && VQ), "chunk eviction keeps bf16 values");
+  static_assert(!(MU && (CH || VQ)), "several units per CTA: the method's values only");
   using R = PRec<G, D>;
   constexpr int GD4 = MergeShape<D, G>::GD4;
-  const int MT = (int)blockDim.x, NQ = MT / GD4;
+  const int MT = (int)blockDim.x, NQ = MU ? nq : MT / GD4, GT = NQ * GD4, UPC = MU ? MT / GT : 1;
   extern __shared__ __align__(16) unsigned char smem_merge[];
   float4* sacc = reinterpret_cast<float4*>(smem_merge);  // [MT]
   float* smax = reinterpret_cast<float*>(sacc + MT);      // [MT]
@@ -1242,11 +1269,14 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
   float* xa = qf + G * D;                                           // [G][D] recomputed partial
   float* xm = xa + G * D;                                           // [8]
   float* xl = xm + 8;                                               // [8]
-  int* sflag = reinterpret_cast<int*>(xl + 8);                      // [4]
-  float* wstate = reinterpret_cast<float*>(sflag + 4);              // recompute scratch
+  int* sflag = reinterpret_cast<int*>(xl + 8);                      // [4] per group
+  int* rparam = sflag + 4;                                          // [4][4] per group
+  float* wstate = reinterpret_cast<float*>(rparam + 16);            // recompute scratch
   float* vqrow = wstate + (MT / 32) * G * (2 + D);                  // VQ: [D] new row, [32] maxima
-  const int tid = threadIdx.x;
-  const int u = blockIdx.x;
+  const int ctid = threadIdx.x;              // thread of the CTA
+  const int grp = MU ? ctid / GT : 0;        // the unit group
+  const int tid = ctid - grp * GT;           // thread of the group
+  const int u = blockIdx.x * UPC + grp;
   const bool full = p.append_slot < 0;
 
   HE_STAMP(2, 0);
@@ -1330,13 +1360,17 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
     }
   }
 
-  const int winner = full ? (key ? (int)evict_key_slot(key) : -1) : p.append_slot;
+  int winner = full ? (key ? (int)evict_key_slot(key) : -1) : p.append_slot;
   // slots evicted, and the end of the slots eviction may choose from
   const int nev = (CH && full) ? p.chunk : 1;
   const int wend = (CH && full) ? p.lbudget : p.budget;
-  if (winner < 0 || winner + nev > wend) {  // cannot happen: never write outside the cache
+  // (cannot happen: never write outside the cache; the group writes nothing
+  // but still takes part in the CTA's barriers)
+  const bool bad = winner < 0 || winner + nev > wend;
+  if (bad) {
     if (tid == 0) atomicExch(p.err, 2);
-    return;
+    if (!MU) return;
+    winner = 0;
   }
   // the evicted slot's contributor: the owner of tile winner / tile (with a
   // chunk, crel .. crel_hi own its first and last slot)
@@ -1366,7 +1400,7 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
     for (int o2 = 16; o2 > 0; o2 >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o2));
     if ((tid & 31) == 0 && tid < D) vqrow[D + (tid >> 5)] = m;
   }
-  if (tid == 0) sflag[0] = 0;
+  if (tid == 0) sflag[grp] = 0;
   __syncthreads();
   float vscale = 0.0f;
   if constexpr (VQ) {
@@ -1397,7 +1431,7 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
         }
         fold_one<D, G>(rm[i], rl[i], rx[i], false, lst, vs, mx, sum, a);
       } else {
-        if (c == crel && d0 == 0 && !(exp2f(lst - rm[i]) <= 0.5f * rl[i])) atomicExch(&sflag[0], 1);
+        if (c == crel && d0 == 0 && !(exp2f(lst - rm[i]) <= 0.5f * rl[i])) atomicExch(&sflag[grp], 1);
         fold_one<D, G>(rm[i], rl[i], rx[i], c == crel, lst, vs, mx, sum, a);
       }
     }
@@ -1417,13 +1451,14 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
       }
       fold_one<D, G>(mc, lc, x, false, lst, vs, mx, sum, a);
     } else {
-      if (c == crel && d0 == 0 && !(exp2f(lst - mc) <= 0.5f * lc)) atomicExch(&sflag[0], 1);
+      if (c == crel && d0 == 0 && !(exp2f(lst - mc) <= 0.5f * lc)) atomicExch(&sflag[grp], 1);
       fold_one<D, G>(mc, lc, x, c == crel, lst, vs, mx, sum, a);
     }
   }
   if constexpr (CH) {
     if (full) {
       // the weight taken out against the weight that remains, per head
+      // (one unit per CTA with chunks: ctid == tid)
       smax[tid] = mx;
       ssum[tid] = sum;
       wstate[tid] = rw;
@@ -1442,52 +1477,109 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
       }
     }
   }
-  __syncthreads();
-  const bool recomputed = sflag[0] != 0;
-  if (recomputed) {
-    // the evicted slot dominates its partial: recompute that partial without it
-    const uint16_t* qg = reinterpret_cast<const uint16_t*>(p.q) + (size_t)(b * p.kv_heads + j) * G * D;
-    for (int i2 = tid; i2 < G * D; i2 += MT) qf[i2] = __uint_as_float((uint32_t)qg[i2] << 16);
+  bool recomputed;
+  if constexpr (!MU) {
     __syncthreads();
-    // the slots of that contributor (with a chunk: of contributors crel .. crel_hi)
-    const int c = first + crel, ch = first + crel_hi;
-    const int tb = (int)split.begin(c), te = (int)split.begin((int64_t)ch + 1);
-    const int lo = (max(tb, u * tps) - u * tps) * p.tile;
-    const int hi = min((min(te, (u + 1) * tps) - u * tps) * p.tile, p.occ);
-    recompute_partial<D, G, VQ>(p, u, lo,
-                                HE_CHECK(0 <= lo && lo <= hi && hi <= p.budget, p.err) ? hi : lo,
-                                winner, nev, qf, wstate, xm, xl, xa, tid);
-    mx = -1e30f;
-    sum = 0.0f;
-    a = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c2 = q; c2 < n; c2 += NQ) {
-      if (c2 > crel && c2 <= crel_hi) continue;  // (a chunk's second contributor: in the first)
-      if (c2 == crel) {
-        fold_one<D, G>(xm[g], xl[g], reinterpret_cast<const float4*>(xa)[o], false, lst, vs, mx,
-                       sum, a);
-      } else {
-        const float* r = rec_of(c2);
-        fold_one<D, G>(__ldcg(r + g), __ldcg(r + G + g),
-                       __ldcg(reinterpret_cast<const float4*>(r + R::HDR) + o), false, lst, vs,
-                       mx, sum, a);
+    recomputed = sflag[0] != 0;
+    if (recomputed) {
+      // the evicted slot dominates its partial: recompute that partial without it
+      const uint16_t* qg =
+          reinterpret_cast<const uint16_t*>(p.q) + (size_t)(b * p.kv_heads + j) * G * D;
+      for (int i2 = tid; i2 < G * D; i2 += MT) qf[i2] = __uint_as_float((uint32_t)qg[i2] << 16);
+      __syncthreads();
+      // the slots of that contributor (with a chunk: of contributors crel .. crel_hi)
+      const int c = first + crel, ch = first + crel_hi;
+      const int tb = (int)split.begin(c), te = (int)split.begin((int64_t)ch + 1);
+      const int lo = (max(tb, u * tps) - u * tps) * p.tile;
+      const int hi = min((min(te, (u + 1) * tps) - u * tps) * p.tile, p.occ);
+      recompute_partial<D, G, VQ>(p, u, lo,
+                                  HE_CHECK(0 <= lo && lo <= hi && hi <= p.budget, p.err) ? hi : lo,
+                                  winner, nev, qf, wstate, xm, xl, xa, tid);
+      mx = -1e30f;
+      sum = 0.0f;
+      a = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int c2 = q; c2 < n; c2 += NQ) {
+        if (c2 > crel && c2 <= crel_hi) continue;  // (a chunk's second contributor: in the first)
+        if (c2 == crel) {
+          fold_one<D, G>(xm[g], xl[g], reinterpret_cast<const float4*>(xa)[o], false, lst, vs, mx,
+                         sum, a);
+        } else {
+          const float* r = rec_of(c2);
+          fold_one<D, G>(__ldcg(r + g), __ldcg(r + G + g),
+                         __ldcg(reinterpret_cast<const float4*>(r + R::HDR) + o), false, lst, vs,
+                         mx, sum, a);
+        }
       }
     }
+  } else {
+    // the slots an exact recompute would cover (contributor crel .. crel_hi's
+    // part of the unit), for whichever thread of the CTA runs it
+    if (tid == 0) {
+      const int c = first + crel, ch = first + crel_hi;
+      int lo = 0, hi = 0;
+      if (full && n > 0) {
+        const int tb = (int)split.begin(c), te = (int)split.begin((int64_t)ch + 1);
+        lo = (max(tb, u * tps) - u * tps) * p.tile;
+        hi = min((min(te, (u + 1) * tps) - u * tps) * p.tile, p.occ);
+      }
+      rparam[grp * 4 + 0] = lo;
+      rparam[grp * 4 + 1] = hi;
+      rparam[grp * 4 + 2] = winner;
+      rparam[grp * 4 + 3] = nev;
+    }
+    __syncthreads();
+    const bool recomputed_mu = sflag[grp] != 0;
+    // a unit whose evicted slot dominates its partial: the whole CTA recomputes
+    // that partial without it, then the unit's group folds again (one unit at a
+    // time; the loop is the same for every thread)
+    for (int gi = 0; gi < UPC; ++gi) {
+      if (sflag[gi] == 0) continue;
+      const int ug = blockIdx.x * UPC + gi;
+      const uint16_t* qg = reinterpret_cast<const uint16_t*>(p.q) + (size_t)ug * G * D;
+      for (int i2 = ctid; i2 < G * D; i2 += MT) qf[i2] = __uint_as_float((uint32_t)qg[i2] << 16);
+      __syncthreads();
+      const int lo = rparam[gi * 4 + 0], hi = rparam[gi * 4 + 1];
+      recompute_partial<D, G, VQ>(p, ug, lo,
+                                  HE_CHECK(0 <= lo && lo <= hi && hi <= p.budget, p.err) ? hi : lo,
+                                  rparam[gi * 4 + 2], rparam[gi * 4 + 3], qf, wstate, xm, xl, xa,
+                                  ctid);
+      if (grp == gi) {
+        mx = -1e30f;
+        sum = 0.0f;
+        a = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c2 = q; c2 < n; c2 += NQ) {
+          if (c2 > crel && c2 <= crel_hi) continue;  // (a chunk's second contributor: in the first)
+          if (c2 == crel) {
+            fold_one<D, G>(xm[g], xl[g], reinterpret_cast<const float4*>(xa)[o], false, lst, vs, mx,
+                           sum, a);
+          } else {
+            const float* r = rec_of(c2);
+            fold_one<D, G>(__ldcg(r + g), __ldcg(r + G + g),
+                           __ldcg(reinterpret_cast<const float4*>(r + R::HDR) + o), false, lst, vs,
+                           mx, sum, a);
+          }
+        }
+      }
+      __syncthreads();  // (qf, xa and the scratch serve the next unit)
+    }
+    recomputed = recomputed_mu;
   }
-  sacc[tid] = a;
-  smax[tid] = mx;
-  ssum[tid] = sum;
+  sacc[ctid] = a;
+  smax[ctid] = mx;
+  ssum[ctid] = sum;
   __syncthreads();
 
-  if (tid < GD4) {
+  const int gb = grp * GT;  // the group's first thread
+  if (tid < GD4 && !bad) {
     // fold the groups in order, then the new token
     float m2 = ln;
-    for (int q2 = 0; q2 < NQ; ++q2) m2 = fmaxf(m2, smax[q2 * GD4 + tid]);
+    for (int q2 = 0; q2 < NQ; ++q2) m2 = fmaxf(m2, smax[gb + q2 * GD4 + tid]);
     float l2 = 0.0f;
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int q2 = 0; q2 < NQ; ++q2) {
-      const float w = exp2f(smax[q2 * GD4 + tid] - m2);
-      const float4 y = sacc[q2 * GD4 + tid];
-      l2 += ssum[q2 * GD4 + tid] * w;
+      const float w = exp2f(smax[gb + q2 * GD4 + tid] - m2);
+      const float4 y = sacc[gb + q2 * GD4 + tid];
+      l2 += ssum[gb + q2 * GD4 + tid] * w;
       s.x += y.x * w;
       s.y += y.y * w;
       s.z += y.z * w;
@@ -1512,7 +1604,7 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
   // take the chunk's first c - 1 slots (rows of the stage are only read here)
   int wslot = winner;
   if constexpr (CH) {
-    if (full) {
+    if (full && !bad) {
       const int c = nev, CH8 = D / 8, npc = (c - 1) * CH8;  // 16-byte pieces per array
       const size_t ub = (size_t)u * p.budget;
       for (int t = tid; t < 2 * npc; t += MT) {
@@ -1532,6 +1624,7 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
     }
   }
   // method step 5: the current token's key, value and code replace the slot
+  if (bad) return;
   if (!HE_CHECK(wslot >= 0 && wslot < p.budget &&
                     (!(CH && full) || p.lbudget + nev - 1 <= p.budget),
                 p.err))
@@ -1561,7 +1654,7 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
 // Dynamic shared memory of merge.
 template <int D, int G>
 constexpr int merge_smem_bytes(int threads) {
-  return threads * (16 + 4 + 4) + (G * D + G * D + 8 + 8) * 4 + 16 +
+  return threads * (16 + 4 + 4) + (G * D + G * D + 8 + 8) * 4 + 16 + 64 +
          (threads / 32) * G * (2 + D) * 4 + (D + 32) * 4;
 }
 

@@ -81,3 +81,55 @@ def test_dominant_evicted_slot_is_recomputed(bits, budget, slot, engine):
         he.close()
     err = np.abs(got - r_or["out"][0])
     assert err.max() <= MAX_ABS_TOL and err.mean() <= MEAN_ABS_TOL, (err.max(), err.mean())
+
+
+def test_dominant_slot_with_several_units_per_merge_cta():
+    """More units than SMs (160 units of one KV head, 4 tiles each): the merge
+    CTAs take several units each; one unit's evicted slot dominates its
+    partial, so that CTA recomputes it while its other units merge normally."""
+    import torch
+    from gpu_harness import compare, run_oracle_units  # noqa: F401
+    bits, budget, slot, ud = 16, 256, 77, 77
+    w = synth.WORKLOADS["llama8b_b8"].with_(batch=160, heads=4, kv_heads=1, budget=budget,
+                                            bits=bits, prompt=2 * budget)
+    D, B, G = w.head_dim, w.budget, w.group
+    o = oracle.load()
+    rng = np.random.default_rng(5)
+    W = o.projection(w.projection_seed(), D, bits, "bf16")
+    Wf = to_f64(W)
+    q0 = to_f64(bf16_bits(rng.standard_normal(D)))
+    s = np.sign(Wf.T @ q0)
+    P = np.eye(D) - np.outer(q0, q0) / (q0 @ q0)
+    A = (P @ Wf).T
+    alpha = 30.0 * np.sqrt(D) / (q0 @ q0) / np.log2(np.e)
+    b = -alpha * (Wf.T @ q0) - s * 40.0
+    r = A.T @ np.linalg.solve(A @ A.T, b)
+    kstar = bf16_bits(alpha * q0 + r)
+    K = bf16_bits(rng.standard_normal((w.batch, 1, B, D)) * 0.5)
+    V = bf16_bits(rng.standard_normal((w.batch, 1, B, D)))
+    K[ud, 0, slot] = kstar
+    q = bf16_bits(rng.standard_normal((w.batch, G, D)))
+    q[ud] = np.broadcast_to(bf16_bits(q0), (G, D))
+    knew = bf16_bits(rng.standard_normal((w.batch, 1, D)))
+    vnew = bf16_bits(rng.standard_normal((w.batch, 1, D)))
+
+    he = make_handle(w)
+    try:
+        he.fill(torch_from_host(K), torch_from_host(V))
+        out = he.step(torch_from_host(q), torch_from_host(knew), torch_from_host(vnew))
+        ev = he.last_evicted()
+        got = out.cpu().numpy().astype(np.float64)
+        assert he.recompute_count == 1
+        state = he.state()
+    finally:
+        he.close()
+    assert ev[ud, 0] == slot
+    worst = 0.0
+    for u in [0, 1, 75, 76, 77, 78, 79, 80, 159]:  # the dominant unit and its merge CTA's others
+        st = o.unit_fill(W, B, K[u, 0], V[u, 0])
+        r_or = o.unit_stream(st, q[u][None], knew[u, 0][None], vnew[u, 0][None])
+        assert ev[u, 0] == r_or["evicted"][0], u
+        err = np.abs(got[u] - r_or["out"][0])
+        assert err.max() <= MAX_ABS_TOL and err.mean() <= MEAN_ABS_TOL, (u, err.max(), err.mean())
+        assert np.array_equal(state[0][u, 0], st.K) and np.array_equal(state[1][u, 0], st.V), u
+        worst = max(worst, float(err.max()))
