@@ -450,7 +450,7 @@ def measure(w: synth.Workload, opts: dict, L: int, min_s: float, min_steps: int,
     # (CUDA events on the launching stream before the cache-streaming kernel and
     # after each kernel of the step; the events serialise the three kernels)
     nk = min(layer_steps, max(256, 8 * Ln))
-    nk -= nk % (Ln * period)
+    nk = max(Ln * period, nk - nk % (Ln * period))  # whole cycles, at least one
     for he in handles:
         he.profile_start(nk // Ln + 1)
     for i in range(nk):
