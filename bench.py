@@ -565,8 +565,10 @@ def measure(w: synth.Workload, opts: dict, L: int, min_s: float, min_steps: int,
             "peak_source": (f"{peak_kind}: MEASURED_PEAKS.json hbm_gbs (of measured)"
                             if peak_kind == "measured" else "fallback 6.4 TB/s (of fallback)"),
             "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+            # (the committed summaries are of the method's three-kernel stream kernel)
             "traffic": profiled_traffic(w.name) if w.bits == synth.WORKLOADS[w.name].bits
-            and not opts.get("v_int8") and chunk <= 1 else None,
+            and not opts.get("v_int8") and chunk <= 1 and not opts.get("decay")
+            and opts.get("engine", "pipeline") == "pipeline" else None,
             "kernel": "he::stream_kernel (cache-streaming attention partials)",
             "algorithmic_bytes_per_launch": stream_bytes,
             "kernel_ms": stream_ms,
