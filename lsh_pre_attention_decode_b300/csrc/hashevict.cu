@@ -41,6 +41,7 @@ struct Kernels {
   const void* prep_mem;  // bf16 pipeline with score memory
   const void* merge;   // bf16 pipeline
   const void* merge_mu;  // bf16 pipeline, several units per merge CTA
+  const void* merge_chunk_mu;
   const void* score;
   const void* code;
   int step_smem;
@@ -90,8 +91,7 @@ Kernels kernels_for() {
     k.prep = reinterpret_cast<const void*>(&he::prep_kernel<D, G, false, VQ>);
     k.prep_mem = reinterpret_cast<const void*>(&he::prep_kernel<D, G, true, VQ>);
     k.merge = reinterpret_cast<const void*>(&he::merge_kernel<D, G, VQ>);
-    if constexpr (!VQ)
-      k.merge_mu = reinterpret_cast<const void*>(&he::merge_kernel<D, G, false, false, true>);
+    k.merge_mu = reinterpret_cast<const void*>(&he::merge_kernel<D, G, VQ, false, true>);
     k.vq_fill = reinterpret_cast<const void*>(&he::vq_fill_kernel<D>);
     if constexpr (!VQ) {
       constexpr int NSF = fused_stages<D, G>();
@@ -103,6 +103,7 @@ Kernels kernels_for() {
       k.fused_stages = NSF;
       k.prep_chunk = reinterpret_cast<const void*>(&he::prep_kernel<D, G, false, false, true>);
       k.merge_chunk = reinterpret_cast<const void*>(&he::merge_kernel<D, G, false, true>);
+      k.merge_chunk_mu = reinterpret_cast<const void*>(&he::merge_kernel<D, G, false, true, true>);
       k.chunk_floats = he::ChunkRec<G, D>::FLOATS;
     }
     k.step_smem = S::SMEM_ALLOC;
@@ -480,6 +481,10 @@ int he_create(const he_cfg* cfg, he_handle* out) {
          cudaFuncSetAttribute(kern.merge_chunk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kern.merge_smem) != cudaSuccess ||
          cudaFuncSetAttribute(kern.merge_chunk, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+         cudaFuncSetAttribute(kern.merge_chunk_mu, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kern.merge_smem) != cudaSuccess ||
+         cudaFuncSetAttribute(kern.merge_chunk_mu, cudaFuncAttributePreferredSharedMemoryCarveout,
                               (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)) {
       rc = HE_ECUDA;
       break;
@@ -778,11 +783,12 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
     // several units per merge CTA only when the units outnumber the SMs (one
     // wave of merge CTAs instead of several); else one unit per CTA
     int msmem = 0, nq = 1, upc = 1;
-    const bool multi = !ch && !h->vq && h->U > h->num_sms;
+    const bool multi = h->U > h->num_sms;
     const int mthreads = h->kern.merge_cfg(nmax, h->U, multi, &nq, &upc, &msmem);
     void* ma[] = {(void*)&p, (void*)&uo, (void*)&sc, (void*)&nq};
-    HE_TRY(h, launch_pdl(ch ? h->kern.merge_chunk : (upc > 1 ? h->kern.merge_mu : h->kern.merge),
-                         dim3(h->U / upc), dim3(mthreads), (size_t)msmem, s, ma));
+    const void* mfn = ch ? (upc > 1 ? h->kern.merge_chunk_mu : h->kern.merge_chunk)
+                         : (upc > 1 ? h->kern.merge_mu : h->kern.merge);
+    HE_TRY(h, launch_pdl(mfn, dim3(h->U / upc), dim3(mthreads), (size_t)msmem, s, ma));
     h->merge_ctas = h->U / upc;
   }
   if (ev) {

@@ -1060,10 +1060,9 @@ struct MergeShape {
     return GD4 * nq;
   }
   // Launch shape for U units with at most n partials each: nq groups of GD4
-  // threads per unit and upc units per CTA.  With `multi` (no chunks, no int8
-  // values) a CTA takes up to four units of ceil(n / kMergeRegs) groups each
-  // (and at least D threads) when U is a multiple of that count; else one unit
-  // of threads(n) threads.
+  // threads per unit and upc units per CTA.  With `multi` a CTA takes up to
+  // four units of ceil(n / kMergeRegs) groups each (and at least D threads)
+  // when U is a multiple of that count; else one unit of threads(n) threads.
   static void config(int n, int U, bool multi, int* nq, int* upc) {
     // (at least D threads per unit: they write the new token's key and value rows)
     constexpr int QMIN = (D + GD4 - 1) / GD4;
@@ -1251,13 +1250,12 @@ __device__ __forceinline__ float take_part(float cm, float cl, const float4& ca,
 // slots and the new token takes its last.  Other steps append (stage) the
 // token at p.append_slot, as the method does.
 // MU: a CTA merges MT / (nq * GD4) units, one group of nq * GD4 threads each
-// (without chunks and int8 values, for steps with more units than SMs: the
-// merge CTAs then run in one wave instead of several); else one unit per CTA.
+// (for steps with more units than SMs: the merge CTAs then run in one wave
+// instead of several); else one unit per CTA.
 template <int D, int G, bool VQ = false, bool CH = false, bool MU = false>
 __global__ void __launch_bounds__(kMergeMaxThreads)
     merge_kernel(const StepParams p, UnitOut* uo, int stream_ctas, int nq) {
   static_assert(!(CH && VQ), "chunk eviction keeps bf16 values");
-  static_assert(!(MU && (CH || VQ)), "several units per CTA: the method's values only");
   using R = PRec<G, D>;
   constexpr int GD4 = MergeShape<D, G>::GD4;
   const int MT = (int)blockDim.x, NQ = MU ? nq : MT / GD4, GT = NQ * GD4, UPC = MU ? MT / GT : 1;
@@ -1272,10 +1270,11 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
   int* sflag = reinterpret_cast<int*>(xl + 8);                      // [4] per group
   int* rparam = sflag + 4;                                          // [4][4] per group
   float* wstate = reinterpret_cast<float*>(rparam + 16);            // recompute scratch
-  float* vqrow = wstate + (MT / 32) * G * (2 + D);                  // VQ: [D] new row, [32] maxima
   const int ctid = threadIdx.x;              // thread of the CTA
   const int grp = MU ? ctid / GT : 0;        // the unit group
   const int tid = ctid - grp * GT;           // thread of the group
+  // VQ, per group: [D] the new row, [32] maxima
+  float* vqrow = wstate + (MT / 32) * G * (2 + D) + grp * (D + 32);
   const int u = blockIdx.x * UPC + grp;
   const bool full = p.append_slot < 0;
 
@@ -1459,21 +1458,21 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
     if (full) {
       // the weight taken out against the weight that remains, per head
       // (one unit per CTA with chunks: ctid == tid)
-      smax[tid] = mx;
-      ssum[tid] = sum;
-      wstate[tid] = rw;
+      smax[ctid] = mx;
+      ssum[ctid] = sum;
+      wstate[ctid] = rw;
       __syncthreads();
       if (tid < G) {
         const int og = tid * (D / 4);  // head tid's first output group
         float M = lng;
-        for (int q2 = 0; q2 < NQ; ++q2) M = fmaxf(M, smax[q2 * GD4 + og]);
+        for (int q2 = 0; q2 < NQ; ++q2) M = fmaxf(M, smax[grp * GT + q2 * GD4 + og]);
         float rem = exp2f(lng - M), out_w = 0.0f;
         for (int q2 = 0; q2 < NQ; ++q2) {
-          const float f = exp2f(smax[q2 * GD4 + og] - M);
-          rem += ssum[q2 * GD4 + og] * f;
-          out_w += wstate[q2 * GD4 + og] * f;
+          const float f = exp2f(smax[grp * GT + q2 * GD4 + og] - M);
+          rem += ssum[grp * GT + q2 * GD4 + og] * f;
+          out_w += wstate[grp * GT + q2 * GD4 + og] * f;
         }
-        if (!(out_w <= kChunkRemoveMax * rem)) atomicExch(&sflag[0], 1);
+        if (!(out_w <= kChunkRemoveMax * rem)) atomicExch(&sflag[grp], 1);
       }
     }
   }
@@ -1607,7 +1606,7 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
     if (full && !bad) {
       const int c = nev, CH8 = D / 8, npc = (c - 1) * CH8;  // 16-byte pieces per array
       const size_t ub = (size_t)u * p.budget;
-      for (int t = tid; t < 2 * npc; t += MT) {
+      for (int t = tid; t < 2 * npc; t += GT) {
         const int arr = t / npc, r = t - arr * npc;
         const int i = r / CH8, w = r - i * CH8;
         uint16_t* base = reinterpret_cast<uint16_t*>(arr ? p.V : p.K);
@@ -1655,7 +1654,7 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
 template <int D, int G>
 constexpr int merge_smem_bytes(int threads) {
   return threads * (16 + 4 + 4) + (G * D + G * D + 8 + 8) * 4 + 16 + 64 +
-         (threads / 32) * G * (2 + D) * 4 + (D + 32) * 4;
+         (threads / 32) * G * (2 + D) * 4 + 4 * (D + 32) * 4;
 }
 
 }  // namespace he

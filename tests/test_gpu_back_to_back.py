@@ -130,3 +130,10 @@ def test_other_shapes_back_to_back():
     check(w, w.budget, 64, all_units(w), layers=2, graph=True, replays=2, out_steps=[64, 127])
     w = small(batch=2, heads=8, kv_heads=8, bits=64, budget=300, prompt=700, decode=8)
     check(w, w.budget, 60, all_units(w), out_steps=[0, 59])
+
+
+def test_more_units_than_sms_back_to_back():
+    """320 units (several per merge CTA), a graph replayed twice."""
+    w = small(batch=40, budget=200, prompt=500, decode=8)
+    check(w, w.budget, 32, [(0, 0), (13, 4), (39, 7)], graph=True, replays=2,
+          out_steps=[32, 63])

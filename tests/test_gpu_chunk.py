@@ -204,3 +204,13 @@ def test_chunk_full_llama8b_b8_sampled():
     compare(w, g, orc, out_steps, check_state=True)
     assert (g.evicted[15] >= 0).all() and (g.evicted[31] >= 0).all()
     assert (g.evicted[:15] == -1).all()
+
+
+@pytest.mark.parametrize("chunk", [4, 16])
+def test_chunk_more_units_than_sms(chunk):
+    """Batch 40 x 8 KV heads = 320 units: the merge CTAs take several units
+    each through staging and chunk evictions."""
+    budget = 8 * chunk
+    w = small(batch=40, budget=budget, prompt=4 * budget, decode=8)
+    units = [(0, 0), (7, 3), (19, 7), (20, 0), (33, 5), (39, 7)]
+    _stream(w, budget - 3, 3 * chunk + 6, 4, chunk, units=units)

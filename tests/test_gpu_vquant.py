@@ -104,3 +104,10 @@ def test_dominant_evicted_slot_is_recomputed():
         he.close()
     err = np.abs(got - r_or["out"][0])
     assert err.max() <= MAX_ABS_TOL and err.mean() <= MEAN_ABS_TOL, (err.max(), err.mean())
+
+
+def test_more_units_than_sms():
+    """Batch 40 x 8 KV heads = 320 units: the merge CTAs take several units
+    each; every unit's rows, scales and evictions are checked."""
+    w = small("serving_b64", batch=40, budget=96, prompt=300, decode=8)
+    _stream(w, 90, 40, 13)
