@@ -55,6 +55,14 @@ def _dtype_code(a: np.ndarray) -> int:
     raise TypeError(f"oracle tensors are uint16 (bf16 bits) or float32, got {a.dtype}")
 
 
+def _vfmt(fmt: str) -> int:
+    """Byte format code of a quantised value cache: 1 int8, 2 fp8 (E4M3)."""
+    try:
+        return {"int8": 1, "fp8": 2}[fmt]
+    except KeyError:
+        raise ValueError(f"value format is 'int8' or 'fp8', got {fmt!r}") from None
+
+
 def _ptr(a: np.ndarray | None):
     return None if a is None else a.ctypes.data_as(_vp)
 
@@ -73,8 +81,9 @@ class UnitState:
     occupancy: int
     tau: float = 0.0
     score: np.ndarray | None = None
-    Vq: np.ndarray | None = None     # quantised value cache: int8 [budget][D] ...
-    Vs: np.ndarray | None = None     # ... and one fp32 scale per row (then V is unused)
+    Vq: np.ndarray | None = None     # quantised value cache: bytes [budget][D] (int8, or
+    Vs: np.ndarray | None = None     # E4M3 codes as uint8) and one fp32 scale per row
+                                     # (then V is unused)
     chunk: int = 1                   # chunk eviction: K, V, codes hold budget + chunk - 1 rows
     chunked: bool = False            # filled by unit_fill_chunk: streams run the chunk routine
 
@@ -99,16 +108,20 @@ class Oracle:
                                             _vp, _vp, _i32, _vp, _vp, _vp, ctypes.c_float,
                                             ctypes.c_float, _vp, _vp, _vp, _vp, _vp]
         lib.orc_unit_stream_ext.restype = None
-        lib.orc_quantize_row.argtypes = [_vp, _i32, _i32, _vp, _vp]
+        lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.orc_e4m3_decode.restype = ctypes.c_double
+        lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.orc_e4m3_encode.restype = ctypes.c_uint8
+        lib.orc_quantize_row.argtypes = [_vp, _i32, _i32, _i32, _vp, _vp]
         lib.orc_quantize_row.restype = None
-        lib.orc_attend_vq.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp]
+        lib.orc_attend_vq.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp]
         lib.orc_attend_vq.restype = None
         lib.orc_unit_fill_vq.argtypes = [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _i32,
-                                         ctypes.c_float, _vp, _vp, _vp, _vp, _vp]
+                                         ctypes.c_float, _i32, _vp, _vp, _vp, _vp, _vp]
         lib.orc_unit_fill_vq.restype = None
-        lib.orc_unit_stream_vq.argtypes = [_vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp,
-                                           _vp, _vp, _i32, _vp, _vp, _vp, ctypes.c_float,
-                                           ctypes.c_float, _vp, _vp, _vp, _vp]
+        lib.orc_unit_stream_vq.argtypes = [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp,
+                                           _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp,
+                                           ctypes.c_float, ctypes.c_float, _vp, _vp, _vp, _vp]
         lib.orc_unit_stream_vq.restype = None
         lib.orc_unit_stream_chunk.argtypes = [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp,
                                               _vp, _vp, _i32, _vp, _vp, _vp, ctypes.c_float, _vp,
@@ -165,26 +178,46 @@ class Oracle:
         return int(self.lib.orc_most_dissimilar_score(_ptr(a), a.size))
 
     # -- quantised values ----------------------------------------------------
-    def quantize_rows(self, v: np.ndarray):
-        """int8 rows and fp32 scales of v [n][D] (bf16 bits or fp32)."""
+    def e4m3_decode(self, c) -> np.ndarray:
+        """The values of E4M3 codes (fp64, exact)."""
+        c2 = np.asarray(c, np.uint8)
+        return np.array([self.lib.orc_e4m3_decode(int(x)) for x in c2.ravel()],
+                        np.float64).reshape(c2.shape)
+
+    def e4m3_encode(self, x) -> np.ndarray:
+        """The E4M3 codes nearest to fp32 values x (ties to even, saturating)."""
+        x2 = np.asarray(x, np.float32)
+        return np.array([self.lib.orc_e4m3_encode(float(v)) for v in x2.ravel()],
+                        np.uint8).reshape(x2.shape)
+
+    def quantize_rows(self, v: np.ndarray, fmt: str = "int8"):
+        """Byte rows and fp32 scales of v [n][D] (bf16 bits or fp32): int8
+        values (numpy int8) or E4M3 codes (``fmt="fp8"``, numpy uint8)."""
+        f = _vfmt(fmt)
         v2 = np.ascontiguousarray(v.reshape(-1, v.shape[-1]))
         n, D = v2.shape
-        q = np.empty((n, D), np.int8)
+        q = np.empty((n, D), np.uint8 if f == 2 else np.int8)
         sc = np.empty(n, np.float32)
         row = D * v2.itemsize
         for i in range(n):
             self.lib.orc_quantize_row(ctypes.c_void_p(v2.ctypes.data + i * row), _dtype_code(v2), D,
-                                      ctypes.c_void_p(q.ctypes.data + i * D),
+                                      f, ctypes.c_void_p(q.ctypes.data + i * D),
                                       ctypes.c_void_p(sc.ctypes.data + 4 * i))
         return q, sc
 
+    def dequantize_rows(self, q: np.ndarray, sc: np.ndarray) -> np.ndarray:
+        """fp64 values decode(q) * s of byte rows from ``quantize_rows``."""
+        deq = self.e4m3_decode(q) if q.dtype == np.uint8 else q.astype(np.float64)
+        return deq * np.asarray(sc, np.float64)[..., None]
+
     def attend_vq(self, q: np.ndarray, K: np.ndarray, Vq: np.ndarray, Vs: np.ndarray) -> np.ndarray:
+        """Attention over byte rows Vq (int8 values, or E4M3 codes as uint8)."""
         q2 = np.ascontiguousarray(q.reshape(-1, q.shape[-1]))
         K2, Vq2, Vs2 = (np.ascontiguousarray(a) for a in (K, Vq, Vs))
         G, D = q2.shape
         out = np.empty((G, D), np.float64)
         self.lib.orc_attend_vq(_ptr(q2), _ptr(K2), _ptr(Vq2), _ptr(Vs2), K2.shape[0], D, G,
-                               _dtype_code(q2), _ptr(out))
+                               _dtype_code(q2), 2 if Vq2.dtype == np.uint8 else 1, _ptr(out))
         return out
 
     # -- attention -----------------------------------------------------------
@@ -212,22 +245,24 @@ class Oracle:
         return st
 
     def unit_fill(self, W: np.ndarray, budget: int, Kin: np.ndarray, Vin: np.ndarray,
-                  tau: float = 0.0, memory: bool = False, vq: bool = False) -> UnitState:
+                  tau: float = 0.0, memory: bool = False, vq=False) -> UnitState:
         """A unit filled with the rows of Kin, Vin.  ``memory``: keep per-slot
         scores (zero after the fill) for streams with score memory.  ``vq``:
-        a quantised value cache (int8 rows, one fp32 scale per row)."""
+        a quantised value cache, one byte per value and one fp32 scale per row:
+        ``True`` or ``"int8"`` (int8 values), ``"fp8"`` (E4M3 codes)."""
         n, D = Kin.shape
         if n > budget:
             raise ValueError("more fill tokens than the budget")
         if vq:
+            f = _vfmt("int8" if vq is True else vq)
             K = np.zeros((budget, D), Kin.dtype)
-            Vq = np.zeros((budget, D), np.int8)
+            Vq = np.zeros((budget, D), np.uint8 if f == 2 else np.int8)
             Vs = np.zeros(budget, np.float32)
             codes = np.zeros(budget, np.uint64)
             occ = np.zeros(1, np.int32)
             Kc, Vc, Wc = (np.ascontiguousarray(a) for a in (Kin, Vin, W))
             self.lib.orc_unit_fill_vq(_ptr(Wc), D, Wc.shape[1], _dtype_code(Kc), budget, _ptr(Kc),
-                                      _ptr(Vc), n, float(tau), _ptr(K), _ptr(Vq), _ptr(Vs),
+                                      _ptr(Vc), n, float(tau), f, _ptr(K), _ptr(Vq), _ptr(Vs),
                                       _ptr(codes), _ptr(occ))
             score = np.zeros(budget, np.float32) if memory else None
             return UnitState(Wc, Wc.shape[1], budget, K, None, codes, int(occ[0]), float(tau),
@@ -280,7 +315,7 @@ class Oracle:
             if st.score is None and decay != 0.0:
                 raise ValueError("score memory needs a unit filled with memory=True")
             self.lib.orc_unit_stream_vq(_ptr(st.W), D, G, st.bits, _dtype_code(qc), st.budget,
-                                        _ptr(st.K), _ptr(st.Vq), _ptr(st.Vs), _ptr(st.codes),
+                                        2 if st.Vq.dtype == np.uint8 else 1, _ptr(st.K), _ptr(st.Vq), _ptr(st.Vs), _ptr(st.codes),
                                         _ptr(st.score), _ptr(occ), T, _ptr(qc), _ptr(kc),
                                         _ptr(vc), float(st.tau), float(decay), _ptr(evicted),
                                         _ptr(written), _ptr(wo), _ptr(out))

@@ -346,46 +346,124 @@ void orc_unit_stream_ext(const void* W, int32_t D, int32_t G, int32_t bits, int3
 }
 
 /* ------------------------------------------------------------------------- */
-/* Quantised value cache (int8 rows with one fp32 scale per row).             */
-/* Reading (DASH-KV page: values tolerate coarser compression than keys; TTKV */
-/* page: keys get more bits than values): s = max_d |v_d| / 127 in fp32,      */
-/* q_d = v_d / s (fp32 division) rounded half to even, clamped to [-127, 127];*/
-/* a zero row has s = 0 and q = 0.  The stored value is q_d * s.  Keys stay   */
-/* in the element type: codes and logits are those of the method.            */
+/* Quantised value cache: one byte per value element with one fp32 scale per  */
+/* row.  Reading (DASH-KV page: values tolerate coarser compression than      */
+/* keys; TTKV page: keys get more bits than values): the row is stored in one */
+/* of two byte formats, fmt:                                                 */
+/*   1 (int8): s = max_d |v_d| / 127 in fp32, q_d = v_d / s (fp32 division)   */
+/*     rounded half to even, clamped to [-127, 127]; stored value q_d * s;    */
+/*   2 (fp8, the E4M3 format of the OCP 8-bit floating point specification): */
+/*     s = max_d |v_d| / 448 in fp32 (448 is the format's largest finite      */
+/*     magnitude), c_d = E4M3 nearest to v_d / s (fp32 division), ties to the */
+/*     even mantissa, magnitudes beyond 448 saturating to 448; stored value   */
+/*     e4m3(c_d) * s.                                                         */
+/* A zero row has s = 0 and every code 0.  Keys stay in the element type:    */
+/* codes and logits are those of the method.                                 */
 /* ------------------------------------------------------------------------- */
 
-void orc_quantize_row(const void* v, int32_t dtype, int32_t D, int8_t* q, float* scale) {
+/* E4M3: sign bit, 4 exponent bits (bias 7), 3 mantissa bits.  Exponent field 0
+ * holds the subnormals m/8 * 2^-6; field 1..15 the normals (1 + m/8) * 2^(e-7);
+ * S.1111.111 is NaN (the format has no infinities), so the largest finite
+ * magnitude is 1.75 * 2^8 = 448. */
+double orc_e4m3_decode(uint8_t c) {
+  const int sgn = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return NAN;
+  double a;
+#if ORACLE_MUTANT == 20 /* planted: subnormals decoded with the implicit leading bit */
+  a = ldexp((double)(8 + m), (e == 0 ? 1 : e) - 10);
+  if (e == 0 && m == 0) a = 0.0;
+#else
+  if (e == 0)
+    a = ldexp((double)m, -9);
+  else
+    a = ldexp((double)(8 + m), e - 10);
+#endif
+  return sgn ? -a : a;
+}
+
+/* The E4M3 code nearest to x: ties to the even mantissa (the even multiple of
+ * the binade's step), magnitudes beyond 448 saturate to 448, the sign is kept
+ * (a negative x that rounds to zero gives -0, code 0x80), NaN gives 0x7F. */
+uint8_t orc_e4m3_encode(float x) {
+  if (isnan(x)) return 0x7F;
+  const uint8_t sgn = signbit(x) ? 0x80 : 0x00;
+  const double a = fabs((double)x);
+  if (a >= 448.0) return sgn | 0x7E;
+  /* the binade [2^e, 2^(e+1)) holds 8 values 2^(e-3) apart; below 2^-6 the
+   * subnormals are 2^-9 apart */
+  int e;
+  (void)frexp(a, &e); /* a = f 2^e with f in [0.5, 1) */
+  e -= 1;
+  if (e < -6) e = -6;
+  const double step = ldexp(1.0, e - 3);
+#if ORACLE_MUTANT == 18 /* planted: ties rounded away from zero */
+  const double n = round(a / step);
+#else
+  const double n = nearbyint(a / step); /* a / step is exact; half to even */
+#endif
+  const double r = n * step; /* (n = 16 carries into the next binade) */
+  if (r == 0.0) return sgn;
+  int er;
+  (void)frexp(r, &er);
+  er -= 1;
+  if (er < -6) return sgn | (uint8_t)(r / ldexp(1.0, -9)); /* subnormal: m = r / 2^-9 */
+  const int m = (int)(r / ldexp(1.0, er - 3)) - 8;
+  return sgn | (uint8_t)(((er + 7) << 3) | m);
+}
+
+/* The value a stored byte stands for before its row's scale. */
+double orc_value_decode(int32_t fmt, uint8_t c) {
+  return fmt == 2 ? orc_e4m3_decode(c) : (double)(int8_t)c;
+}
+
+void orc_quantize_row(const void* v, int32_t dtype, int32_t D, int32_t fmt, uint8_t* q,
+                      float* scale) {
   float m = 0.0f;
   for (int32_t d = 0; d < D; ++d) {
     float a = fabsf(elem(v, dtype, (size_t)d));
     if (a > m) m = a;
   }
-#if ORACLE_MUTANT == 13 /* planted: scale by 128 */
-  float s = m / 128.0f;
+  float s;
+  if (fmt == 2) {
+#if ORACLE_MUTANT == 19 /* planted: fp8 rows scaled by max / 256 */
+    s = m / 256.0f;
 #else
-  float s = m / 127.0f;
+    s = m / 448.0f;
 #endif
+  } else {
+#if ORACLE_MUTANT == 13 /* planted: scale by 128 */
+    s = m / 128.0f;
+#else
+    s = m / 127.0f;
+#endif
+  }
   *scale = s;
   for (int32_t d = 0; d < D; ++d) {
-    float r = 0.0f;
-    if (s > 0.0f) {
-      float x = elem(v, dtype, (size_t)d) / s;
-#if ORACLE_MUTANT == 14 /* planted: rounds half away from zero */
-      r = roundf(x);
-#else
-      r = nearbyintf(x); /* round half to even (default rounding mode) */
-#endif
-      if (r > 127.0f) r = 127.0f;
-      if (r < -127.0f) r = -127.0f;
+    if (!(s > 0.0f)) {
+      q[d] = 0;
+      continue;
     }
-    q[d] = (int8_t)r;
+    float x = elem(v, dtype, (size_t)d) / s;
+    if (fmt == 2) {
+      q[d] = orc_e4m3_encode(x);
+      continue;
+    }
+    float r;
+#if ORACLE_MUTANT == 14 /* planted: rounds half away from zero */
+    r = roundf(x);
+#else
+    r = nearbyintf(x); /* round half to even (default rounding mode) */
+#endif
+    if (r > 127.0f) r = 127.0f;
+    if (r < -127.0f) r = -127.0f;
+    q[d] = (uint8_t)(int8_t)r;
   }
 }
 
 /* Attention of G query heads over n rows with keys K (element type) and
- * values q[s][d] * scale[s], in fp64. */
-void orc_attend_vq(const void* qv, const void* K, const int8_t* Vq, const float* Vs, int32_t n,
-                   int32_t D, int32_t G, int32_t dtype, double* out) {
+ * values decode(q[s][d]) * scale[s] (format fmt), in fp64. */
+void orc_attend_vq(const void* qv, const void* K, const uint8_t* Vq, const float* Vs, int32_t n,
+                   int32_t D, int32_t G, int32_t dtype, int32_t fmt, double* out) {
   double* logit = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
   const double scale = 1.0 / sqrt((double)D);
   for (int32_t g = 0; g < G; ++g) {
@@ -403,32 +481,35 @@ void orc_attend_vq(const void* qv, const void* K, const int8_t* Vq, const float*
     for (int32_t d = 0; d < D; ++d) {
       double num = 0.0;
       for (int32_t s = 0; s < n; ++s)
-        num += exp(logit[s] - m) * (double)Vq[(size_t)s * D + d] * (double)Vs[s];
+        num += exp(logit[s] - m) * orc_value_decode(fmt, Vq[(size_t)s * D + d]) * (double)Vs[s];
       out[(size_t)g * D + d] = n > 0 ? num / den : 0.0;
     }
   }
   free(logit);
 }
 
-/* Fill of a unit with a quantised value cache: K copied, V quantised row by row. */
+/* Fill of a unit with a quantised value cache (format fmt): K copied, V
+ * quantised row by row. */
 void orc_unit_fill_vq(const void* W, int32_t D, int32_t bits, int32_t dtype, int32_t budget,
-                      const void* Kin, const void* Vin, int32_t n, float tau, void* K,
-                      int8_t* Vq, float* Vs, uint64_t* codes, int32_t* occupancy) {
+                      const void* Kin, const void* Vin, int32_t n, float tau, int32_t fmt,
+                      void* K, uint8_t* Vq, float* Vs, uint64_t* codes, int32_t* occupancy) {
   size_t row = (size_t)D * elem_bytes(dtype);
   (void)budget;
   memcpy(K, Kin, row * (size_t)n);
   for (int32_t s = 0; s < n; ++s) {
-    orc_quantize_row((const char*)Vin + (size_t)s * row, dtype, D, Vq + (size_t)s * D, Vs + s);
+    orc_quantize_row((const char*)Vin + (size_t)s * row, dtype, D, fmt, Vq + (size_t)s * D,
+                     Vs + s);
     codes[s] = orc_code_tau((const char*)Kin + (size_t)s * row, dtype, D, W, bits, tau);
   }
   *occupancy = n;
 }
 
-/* The step with a quantised value cache: as orc_unit_stream_ext, but the new
- * token's value is quantised when written and attention reads q * scale. */
+/* The step with a quantised value cache (format fmt): as orc_unit_stream_ext,
+ * but the new token's value is quantised when written and attention reads the
+ * stored values decode(q) * scale. */
 void orc_unit_stream_vq(const void* W, int32_t D, int32_t G, int32_t bits, int32_t dtype,
-                        int32_t budget, void* K, int8_t* Vq, float* Vs, uint64_t* codes,
-                        float* score, int32_t* occupancy, int32_t nsteps, const void* q,
+                        int32_t budget, int32_t fmt, void* K, uint8_t* Vq, float* Vs,
+                        uint64_t* codes, float* score, int32_t* occupancy, int32_t nsteps, const void* q,
                         const void* k, const void* v, float tau, float decay, int32_t* evicted,
                         int32_t* written, const uint8_t* want_out, double* out) {
   size_t row = (size_t)D * elem_bytes(dtype);
@@ -458,11 +539,11 @@ void orc_unit_stream_vq(const void* W, int32_t D, int32_t G, int32_t bits, int32
     }
     written[t] = slot;
     memcpy((char*)K + (size_t)slot * row, kt, row);
-    orc_quantize_row(vt, dtype, D, Vq + (size_t)slot * D, Vs + slot);
+    orc_quantize_row(vt, dtype, D, fmt, Vq + (size_t)slot * D, Vs + slot);
     codes[slot] = orc_code_tau(kt, dtype, D, W, bits, tau);
     if (score) score[slot] = 0.0f;
     if (!want_out || want_out[t])
-      orc_attend_vq(qt, K, Vq, Vs, *occupancy, D, G, dtype,
+      orc_attend_vq(qt, K, Vq, Vs, *occupancy, D, G, dtype, fmt,
                     out + (n_out++) * (size_t)G * (size_t)D);
   }
   free(dist);

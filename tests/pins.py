@@ -124,6 +124,16 @@ def read_vquant_rows():
     return rows
 
 
+def read_vquant_fp8_rows():
+    rows = []
+    for tok in _lines("vquant_fp8_hand.txt"):
+        if tok[0] == "row":
+            i_s, i_c, i_v = tok.index("scale"), tok.index("codes"), tok.index("values")
+            rows.append(([float(t) for t in tok[1:i_s]], float(tok[i_s + 1]),
+                         [int(t) for t in tok[i_c + 1:i_v]], [float(t) for t in tok[i_v + 1:]]))
+    return rows
+
+
 def read_attention_cases():
     cases, cur = [], None
     for tok in _lines("attention_hand.txt"):
@@ -474,48 +484,127 @@ def check_vquant_hand(o):
         assert float(ss[0]) == scale and qq[0].tolist() == q, (v, ss, qq)
 
 
+def check_vquant_fp8_hand(o):
+    """fp8 (E4M3) value rows (tests/golden/vquant_fp8_hand.txt): scales, codes
+    (ties to the even mantissa, subnormals, signed zero) and stored values."""
+    for v, scale, codes, values in read_vquant_fp8_rows():
+        qq, ss = o.quantize_rows(f32([v]), "fp8")
+        assert float(ss[0]) == scale and qq[0].tolist() == codes, (v, ss, qq)
+        deq = o.dequantize_rows(qq, ss)[0]
+        assert deq.tolist() == values and np.array_equal(np.signbit(deq), np.signbit(values))
+
+
+def check_e4m3_table(o):
+    """E4M3 values against the format's table (OCP 8-bit floating point
+    specification): zero and negative zero, the smallest subnormal 2^-9, the
+    largest subnormal 0.875 * 2^-6, the smallest normal 2^-6, 1.0 at 0x38, the
+    largest normal 448 at 0x7E, NaN at 0x7F / 0xFF; the 126 positive finite
+    codes increase strictly, eight per binade, each binade's step doubling the
+    previous one; negative codes mirror them."""
+    d = o.e4m3_decode(np.arange(256))
+    assert d[0x00] == 0 and not np.signbit(d[0x00]) and d[0x80] == 0 and np.signbit(d[0x80])
+    anchors = {0x01: 2.0 ** -9, 0x07: 0.875 * 2.0 ** -6, 0x08: 2.0 ** -6, 0x38: 1.0,
+               0x7E: 448.0, 0x7D: 416.0, 0x78: 256.0, 0x70: 128.0, 0x3C: 1.5}
+    for c, x in anchors.items():
+        assert d[c] == x and d[c | 0x80] == -x, (hex(c), d[c])
+    assert np.isnan(d[0x7F]) and np.isnan(d[0xFF])
+    pos = d[1:0x7F]
+    steps = np.diff(d[0:0x7F])
+    assert np.all(steps > 0)
+    # subnormals and the first binade share the step 2^-9; then it doubles per binade
+    assert np.all(steps[:16] == 2.0 ** -9)
+    for e in range(2, 16):
+        blk = steps[8 * e:8 * e + 8]
+        assert np.all(blk == 2.0 * steps[8 * e - 1]), e
+    assert np.array_equal(d[0x81:0xFF], -pos)
+
+
+def check_e4m3_encode_brute(o):
+    """The encoder against brute force over the decoded table: for random fp32
+    values, every representable value, every midpoint between neighbours and
+    the fp32 values just beside each midpoint, the code is the nearest finite
+    E4M3 value; a midpoint takes the code with the even mantissa; magnitudes
+    beyond 448 saturate to 448; the sign is kept."""
+    d = o.e4m3_decode(np.arange(0x7F))            # 0 .. 448
+    mids = (d[:-1] + d[1:]) / 2
+    rng = np.random.default_rng(46)
+    xs = np.concatenate([
+        d, mids, np.nextafter(f32(mids), f32(0)), np.nextafter(f32(mids), f32(1e9)),
+        f32(rng.uniform(0, 500, 3000)), f32(np.exp2(rng.uniform(-14, 9, 3000))),
+        f32([448.0, 463.9, 464.0, 480.0, 1e6, 3e38, 2.0 ** -10, 2.0 ** -11, 1e-30, 0.0])])
+    xs = f32(xs)
+    for sign in (1.0, -1.0):
+        x = f32(sign * xs)
+        got = o.e4m3_encode(x)
+        a = np.abs(x.astype(np.float64))
+        err = np.abs(a[:, None] - d[None, :])
+        best = err.min(axis=1)
+        for i in range(x.size):
+            if a[i] > 448:
+                want = 0x7E
+            else:
+                cands = np.flatnonzero(err[i] == best[i])
+                even = [c for c in cands if c % 2 == 0]
+                assert cands.size == 1 or len(even) == 1, (float(x[i]), cands)
+                want = cands[0] if cands.size == 1 else even[0]
+            if sign < 0 or np.signbit(x[i]):
+                want |= 0x80
+            assert got[i] == want, (float(x[i]), hex(got[i]), hex(want))
+
+
 def check_vquant_attention(o):
-    """Attention over a quantised value cache equals fp64 attention over the
-    dequantised rows q * s (uniform logits: their mean; random: the pinned fp64
-    attention on fp32 rows q * s, to fp32 rounding)."""
+    """Attention over a quantised value cache (int8 and fp8 rows) equals fp64
+    attention over the stored values decode(q) * s (uniform logits: their
+    mean; random: the pinned fp64 attention on the fp32 stored rows, to fp32
+    rounding)."""
     rng = np.random.default_rng(44)
     D, n, G = 16, 11, 2
     v = f32(rng.standard_normal((n, D)) * 3)
-    q8, sc = o.quantize_rows(v)
-    deq = q8.astype(np.float64) * sc.astype(np.float64)[:, None]
     K = f32(rng.standard_normal((n, D)))
-    out = o.attend_vq(f32(np.zeros((G, D))), K, q8, sc)
-    assert np.allclose(out, deq.mean(0)[None].repeat(G, 0), rtol=0, atol=1e-12)
     qv = f32(rng.standard_normal((G, D)))
-    ref = o.attend(qv, K, f32(deq))
-    assert np.allclose(o.attend_vq(qv, K, q8, sc), ref, rtol=0, atol=1e-5)
-    # every stored value is within half a step of the input, and the row maximum is exact
-    assert np.all(np.abs(deq - v) <= 0.5 * sc[:, None] * (1 + 1e-6))
+    for fmt in ("int8", "fp8"):
+        q8, sc = o.quantize_rows(v, fmt)
+        deq = o.dequantize_rows(q8, sc)
+        out = o.attend_vq(f32(np.zeros((G, D))), K, q8, sc)
+        assert np.allclose(out, deq.mean(0)[None].repeat(G, 0), rtol=0, atol=1e-12)
+        ref = o.attend(qv, K, f32(deq))
+        assert np.allclose(o.attend_vq(qv, K, q8, sc), ref, rtol=0, atol=1e-5)
+        if fmt == "int8":
+            # every stored value within half a step of the input
+            assert np.all(np.abs(deq - v) <= 0.5 * sc[:, None] * (1 + 1e-6))
+        else:
+            # within half an E4M3 step (relative 2^-4 above 2^-6 s, absolute
+            # 2^-10 s below), and each row's largest magnitude stored as 448 s
+            tol = np.maximum(np.abs(v) * 2.0 ** -4, 2.0 ** -10 * sc[:, None])
+            assert np.all(np.abs(deq - v) <= tol * (1 + 1e-6))
+            assert np.all((q8 & 0x7F).max(axis=1) == 0x7E)
 
 
 def check_vquant_stream(o):
-    """A quantised value cache evicts exactly as the method (codes come from
-    the keys) and attends over the retained keys with q * s values."""
+    """A quantised value cache (int8 or fp8) evicts exactly as the method
+    (codes come from the keys) and attends over the retained keys with the
+    stored values decode(q) * s."""
     rng = np.random.default_rng(45)
-    for dtype in ("fp32", "bf16"):
-        D, bits, G, B, T = 16, 8, 2, 7, 14
-        W = o.projection(7, D, bits, dtype)
-        cast = f32 if dtype == "fp32" else bf16_bits
-        K0, V0 = cast(rng.standard_normal((5, D))), cast(rng.standard_normal((5, D)))
-        q, k, v = (cast(rng.standard_normal(sh)) for sh in ((T, G, D), (T, D), (T, D)))
-        a = o.unit_fill(W, B, K0, V0)
-        b = o.unit_fill(W, B, K0, V0, vq=True)
-        ra = o.unit_stream(a, q, k, v)
-        rb = o.unit_stream(b, q, k, v)
-        assert ra["evicted"].tolist() == rb["evicted"].tolist()
-        assert np.array_equal(a.codes, b.codes) and np.array_equal(a.K, b.K)
-        qa, sa = o.quantize_rows(a.V)
-        assert np.array_equal(qa[:a.occupancy], b.Vq[:b.occupancy])
-        assert np.array_equal(sa[:a.occupancy], b.Vs[:b.occupancy])
-        deq = f32(qa.astype(np.float64) * sa.astype(np.float64)[:, None])
-        exact = (lambda x: x) if dtype == "fp32" else (lambda x: f32(bf16_to_f64(x)))
-        last = o.attend(exact(q[-1]), exact(a.K[:a.occupancy]), deq[:a.occupancy])
-        assert np.allclose(rb["out"][-1], last, rtol=0, atol=1e-5)
+    for fmt in ("int8", "fp8"):
+        for dtype in ("fp32", "bf16"):
+            D, bits, G, B, T = 16, 8, 2, 7, 14
+            W = o.projection(7, D, bits, dtype)
+            cast = f32 if dtype == "fp32" else bf16_bits
+            K0, V0 = cast(rng.standard_normal((5, D))), cast(rng.standard_normal((5, D)))
+            q, k, v = (cast(rng.standard_normal(sh)) for sh in ((T, G, D), (T, D), (T, D)))
+            a = o.unit_fill(W, B, K0, V0)
+            b = o.unit_fill(W, B, K0, V0, vq=fmt)
+            ra = o.unit_stream(a, q, k, v)
+            rb = o.unit_stream(b, q, k, v)
+            assert ra["evicted"].tolist() == rb["evicted"].tolist()
+            assert np.array_equal(a.codes, b.codes) and np.array_equal(a.K, b.K)
+            qa, sa = o.quantize_rows(a.V, fmt)
+            assert np.array_equal(qa[:a.occupancy], b.Vq[:b.occupancy])
+            assert np.array_equal(sa[:a.occupancy], b.Vs[:b.occupancy])
+            deq = f32(o.dequantize_rows(qa, sa))
+            exact = (lambda x: x) if dtype == "fp32" else (lambda x: f32(bf16_to_f64(x)))
+            last = o.attend(exact(q[-1]), exact(a.K[:a.occupancy]), deq[:a.occupancy])
+            assert np.allclose(rb["out"][-1], last, rtol=0, atol=1e-5)
 
 
 def check_chunk_hand(o):
@@ -631,7 +720,7 @@ ALL_CHECKS = [
     check_distance_brute, check_argmax_ties, check_eviction_hand, check_special_cases,
     check_stream_invariants, check_attention_hand, check_attention_closed_forms,
     check_attention_bf16_elements, check_codes_tau_hand, check_codes_tau_monotone,
-    check_decay_hand, check_decay_zero_is_per_step, check_vquant_hand, check_vquant_attention,
-    check_vquant_stream, check_chunk_hand, check_chunk_one_is_method, check_chunk_whole_budget,
+    check_decay_hand, check_decay_zero_is_per_step, check_vquant_hand, check_vquant_fp8_hand,
+    check_e4m3_table, check_e4m3_encode_brute, check_vquant_attention, check_vquant_stream, check_chunk_hand, check_chunk_one_is_method, check_chunk_whole_budget,
     check_chunk_sums_brute, check_chunk_one_with_threshold_is_method,
 ]

@@ -24,6 +24,9 @@ MUTANTS = {
     15: "a chunk scores by its first slot only",
     16: "staged tokens land in reverse order",
     17: "a chunk scores its slots shifted by one",
+    18: "fp8 values: ties rounded away from zero",
+    19: "fp8 value rows scaled by max / 256",
+    20: "fp8 subnormals decoded with the implicit leading bit",
 }
 
 
