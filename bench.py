@@ -76,8 +76,9 @@ def parse_args(argv=None):
                     help="binarisation threshold tau (0: the sign test of the method)")
     ap.add_argument("--decay", type=float, default=0.0,
                     help="score memory gamma (0: the step's own distances, the method)")
-    ap.add_argument("--v-int8", action="store_true",
-                    help="int8 value cache with one scale per slot (keys stay bf16)")
+    ap.add_argument("--v-format", choices=["elem", "int8", "fp8"], default="elem",
+                    help="value cache rows: bf16 (elem), or int8 / fp8 (E4M3) bytes with one "
+                         "scale per slot (keys stay bf16)")
     ap.add_argument("--chunk", type=int, default=1,
                     help="chunk eviction: chunks of this many slots (1: the method)")
     ap.add_argument("--engine", choices=["pipeline", "fused"], default="pipeline",
@@ -212,7 +213,8 @@ def config_of(w: synth.Workload, opts: dict, extra=None):
     c = {"workload": f"{w.name}: {w.description}" + (
             f"; threshold {opts.get('threshold')}, score memory {opts.get('decay')}"
             if (opts.get("threshold") or opts.get("decay")) else "") + (
-            "; int8 value cache" if opts.get("v_int8") else "") + (
+            f"; {opts.get('v_format')} value cache"
+            if opts.get("v_format", "elem") != "elem" else "") + (
             f"; chunk eviction, chunks of {chunk} slots" if chunk > 1 else "") + (
             "; single-kernel engine" if opts.get("engine") == "fused" else "") + (
             f"; code length {w.bits}" if w.bits != synth.WORKLOADS[w.name].bits else "") + (
@@ -234,7 +236,7 @@ def config_of(w: synth.Workload, opts: dict, extra=None):
 
 def run_cpu_baseline(w: synth.Workload, target_s: float, steps: int | None = None,
                      threads: int | None = None, threshold: float = 0.0, decay: float = 0.0,
-                     v_int8: bool = False, chunk: int = 1):
+                     v_format: str = "elem", chunk: int = 1):
     """Times the CPU oracle, as it stands, on a bounded sample of the workload.
 
     The unit of work is a unit-step: one streamed token through one (batch, KV
@@ -262,7 +264,8 @@ def run_cpu_baseline(w: synth.Workload, target_s: float, steps: int | None = Non
         V0 = synth.host_unit_kv(w, "value", b, j, 0, w.budget)
         if chunk > 1:
             return o.unit_fill_chunk(W, w.budget, chunk, K0, V0, tau=threshold)
-        return o.unit_fill(W, w.budget, K0, V0, tau=threshold, memory=decay > 0.0, vq=v_int8)
+        return o.unit_fill(W, w.budget, K0, V0, tau=threshold, memory=decay > 0.0,
+                           vq=False if v_format == "elem" else v_format)
 
     def run(u, st, t0, n):
         b, j = u
@@ -350,7 +353,7 @@ def measure(w: synth.Workload, opts: dict, L: int, min_s: float, min_steps: int,
     for layer in layers:
         he = HashEvict(w.batch, w.heads, w.kv_heads, w.head_dim, w.bits, w.budget, w.dtype,
                        seed=w.projection_seed(layer), threshold=opts.get("threshold", 0.0),
-                       decay=opts.get("decay", 0.0), v_int8=opts.get("v_int8", False),
+                       decay=opts.get("decay", 0.0), v_format=opts.get("v_format", "elem"),
                        chunk=chunk, engine=opts.get("engine", "pipeline"))
         K = synth.gpu_kv(w, "key", 0, w.budget, layer)
         V = synth.gpu_kv(w, "value", 0, w.budget, layer)
@@ -539,9 +542,10 @@ def measure(w: synth.Workload, opts: dict, L: int, min_s: float, min_steps: int,
     eb = 2 if w.dtype == "bf16" else 4
     occ = w.budget + (chunk - 1) / 2  # resident rows (chunk eviction: a cycle's mean)
     U = w.batch * w.kv_heads
-    # K and V rows of every resident slot (int8 value rows and their scales with
-    # an int8 value cache)
-    stream_bytes = int(U * occ * (w.head_dim * eb + (w.head_dim + 4 if opts.get("v_int8")
+    # K and V rows of every resident slot (byte value rows and their scales with
+    # a quantised value cache)
+    vq = opts.get("v_format", "elem") != "elem"
+    stream_bytes = int(U * occ * (w.head_dim * eb + (w.head_dim + 4 if vq
                                                        else w.head_dim * eb)))
     stream_ms = prof["stream_ms"] / n_prof
     achieved = stream_bytes / (stream_ms / 1e3) / 1e9
@@ -567,7 +571,7 @@ def measure(w: synth.Workload, opts: dict, L: int, min_s: float, min_steps: int,
             "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
             # (the committed summaries are of the method's three-kernel stream kernel)
             "traffic": profiled_traffic(w.name) if w.bits == synth.WORKLOADS[w.name].bits
-            and not opts.get("v_int8") and chunk <= 1 and not opts.get("decay")
+            and not vq and chunk <= 1 and not opts.get("decay")
             and opts.get("engine", "pipeline") == "pipeline" else None,
             "kernel": "he::stream_kernel (cache-streaming attention partials)",
             "algorithmic_bytes_per_launch": stream_bytes,
@@ -590,9 +594,15 @@ def measure(w: synth.Workload, opts: dict, L: int, min_s: float, min_steps: int,
     return res
 
 
+def is_method(opts: dict) -> bool:
+    """The options are those of the method as the pages describe it."""
+    return (not opts.get("threshold") and not opts.get("decay") and opts.get("chunk", 1) <= 1
+            and opts.get("v_format", "elem") == "elem")
+
+
 def run_ours(args, rank: int, world: int, dist_on: bool):
     w = make_workload(args.workload, args.bits, args.budget)
-    opts = {"threshold": args.threshold, "decay": args.decay, "v_int8": args.v_int8,
+    opts = {"threshold": args.threshold, "decay": args.decay, "v_format": args.v_format,
             "chunk": args.chunk, "engine": args.engine}
     L = args.layers if args.layers else (w.layers if w.layers > 1 else 4)
     if w.layers > 1 and L != w.layers:
@@ -619,8 +629,7 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
         for name, bits, layers in PER_CONFIG:
             wc = make_workload(name, bits)
             copts = {"engine": args.engine}
-            if (wc.name, wc.bits) == (w.name, w.bits) and not any(
-                    v for k, v in opts.items() if k != "engine"):
+            if (wc.name, wc.bits) == (w.name, w.bits) and is_method(opts):
                 continue
             key = name if bits is None else f"{name}_b{bits}"
             r = measure(wc, copts, layers, args.config_seconds, 0, args.warmup, args.graph_ring, rank,
@@ -640,7 +649,7 @@ def main(argv=None):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    opts = {"threshold": args.threshold, "decay": args.decay, "v_int8": args.v_int8,
+    opts = {"threshold": args.threshold, "decay": args.decay, "v_format": args.v_format,
             "chunk": args.chunk}
 
     if args.impl == "reference":

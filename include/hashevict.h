@@ -57,6 +57,7 @@ extern "C" {
 
 #define HE_VFMT_ELEM 0  /* values stored in the element type */
 #define HE_VFMT_INT8 1  /* values stored as int8 rows with one fp32 scale per slot (bf16 only) */
+#define HE_VFMT_FP8 2   /* values stored as fp8 E4M3 rows with one fp32 scale per slot (bf16 only) */
 
 /* Handle configuration.  Supported: head_dim in {64, 128};
  * G = heads / kv_heads in {1, 2, 4, 8}; bits in {8, 16, 32, 64};
@@ -86,9 +87,15 @@ typedef struct {
                         (d its group-summed Hamming distance); the largest A is
                         evicted (ties: lowest slot); a written or filled slot starts
                         at A = 0.  0 = the step's own distances (the paper's method) */
-  int32_t v_format;  /* HE_VFMT_ELEM, or HE_VFMT_INT8: each value row v is stored as
+  int32_t v_format;  /* HE_VFMT_ELEM; HE_VFMT_INT8: each value row v is stored as
                         q = v / s rounded half to even with s = max|v| / 127 (fp32), and
-                        attended as q * s; keys, codes and evictions are unchanged */
+                        attended as q * s; HE_VFMT_FP8: stored as c = the E4M3 value
+                        (OCP 8-bit floating point format: 4 exponent bits, bias 7,
+                        3 mantissa bits, subnormals, largest finite 448) nearest to
+                        v / s, ties to the even mantissa, with s = max|v| / 448 (fp32),
+                        and attended as c * s.  Keys, codes and evictions are unchanged
+                        (the DASH-KV page's value compression; the TTKV page's keys
+                        with more bits than values) */
   int32_t chunk;     /* chunk eviction c (the ChunkKV page's chunks of contiguous
                         tokens applied to the method's scores): the budget is cut into
                         budget / c aligned chunks of c slots, a chunk scores the sum of
@@ -103,7 +110,7 @@ typedef struct {
                         merge and overwrite); HE_ENGINE_FUSED (1) runs it as one
                         kernel (a hash warp per CTA, and the last CTA of each (batch,
                         KV head) merges it; the method only: threshold allowed, no
-                        score memory, int8 values or chunks).  Same results. */
+                        score memory, quantised values or chunks).  Same results. */
 } he_cfg;
 
 #define HE_ENGINE_PIPELINE 0
@@ -153,8 +160,8 @@ int he_destroy(he_handle h);
 int he_last_evicted(he_handle h, int32_t* host_slots);
 
 /* Snapshot of the cache into host buffers (any may be NULL):
- * K, V [batch][kv_heads][R][head_dim] (element type; V int8 with an int8
- * value cache), codes [batch][kv_heads][R] (bits/8-byte words), occupancy
+ * K, V [batch][kv_heads][R][head_dim] (element type; V bytes with a
+ * quantised value cache), codes [batch][kv_heads][R] (bits/8-byte words), occupancy
  * (one int: resident rows, staged ones included).  Synchronises. */
 int he_read_state(he_handle h, void* K, void* V, void* codes, int32_t* occupancy);
 
@@ -177,9 +184,10 @@ int he_codes(he_handle h, const void* x, int32_t n, void* codes, void* stream);
  * Errors: HE_EINVAL, HE_ENOTFILLED, HE_ECUDA. */
 int he_scores(he_handle h, const void* q, int32_t* dist, void* stream);
 
-/* Per-slot value scales of a handle with an int8 value cache (v_format
- * HE_VFMT_INT8), host fp32 [batch][kv_heads][budget]; he_read_state then
- * returns the value rows as int8 [batch][kv_heads][budget][head_dim].
+/* Per-slot value scales of a handle with a quantised value cache (v_format
+ * HE_VFMT_INT8 or HE_VFMT_FP8), host fp32 [batch][kv_heads][budget]; he_read_state
+ * then returns the value rows as bytes [batch][kv_heads][budget][head_dim] (int8
+ * values, or E4M3 codes).
  * Synchronises.  Errors: HE_EINVAL (NULL arguments, or another value format). */
 int he_read_vscales(he_handle h, float* host_scales);
 

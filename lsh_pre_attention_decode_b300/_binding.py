@@ -12,6 +12,7 @@ HE_DTYPE_BF16 = 0
 HE_DTYPE_FP32 = 1
 HE_VFMT_ELEM = 0
 HE_VFMT_INT8 = 1
+HE_VFMT_FP8 = 2
 HE_ENGINE_PIPELINE = 0
 HE_ENGINE_FUSED = 1
 
@@ -233,16 +234,17 @@ class HashEvict:
 
     def __init__(self, batch: int, heads: int, kv_heads: int, head_dim: int, bits: int,
                  budget: int, dtype: str = "bf16", seed: int = 0, threshold: float = 0.0,
-                 decay: float = 0.0, v_int8: bool = False, chunk: int = 1,
+                 decay: float = 0.0, v_format: str = "elem", chunk: int = 1,
                  engine: str = "pipeline"):
         self.cfg = HeCfg(batch=batch, heads=heads, kv_heads=kv_heads, head_dim=head_dim,
                          bits=bits, budget=budget,
                          dtype=HE_DTYPE_FP32 if dtype == "fp32" else HE_DTYPE_BF16,
                          threshold=threshold, seed=seed, decay=decay,
-                         v_format=HE_VFMT_INT8 if v_int8 else HE_VFMT_ELEM, chunk=chunk,
+                         v_format={"elem": HE_VFMT_ELEM, "int8": HE_VFMT_INT8,
+                                   "fp8": HE_VFMT_FP8}[v_format], chunk=chunk,
                          engine={"pipeline": HE_ENGINE_PIPELINE,
                                  "fused": HE_ENGINE_FUSED}[engine])
-        self.v_int8 = v_int8
+        self.v_format = v_format
         # rows per unit: the budget, plus chunk - 1 staging rows with chunk eviction
         self.rows = budget + max(chunk, 1) - 1
         self.dtype = dtype
@@ -290,21 +292,22 @@ class HashEvict:
         return a
 
     def state(self):
-        """Host snapshot: K, V [batch][kv][rows][D] (uint16 bf16 bits or float32),
-        codes [batch][kv][rows] (uint8/16/32/64), occupancy."""
+        """Host snapshot: K, V [batch][kv][rows][D] (uint16 bf16 bits or float32;
+        V int8 or uint8 E4M3 codes with a quantised value cache), codes
+        [batch][kv][rows] (uint8/16/32/64), occupancy."""
         import numpy as np
         c = self.cfg
         et = np.float32 if self.dtype == "fp32" else np.uint16
         ct = {8: np.uint8, 16: np.uint16, 32: np.uint32, 64: np.uint64}[c.bits]
         K = np.empty((c.batch, c.kv_heads, self.rows, c.head_dim), et)
-        V = np.empty(K.shape, np.int8 if self.v_int8 else et)
+        V = np.empty(K.shape, {"int8": np.int8, "fp8": np.uint8}.get(self.v_format, et))
         codes = np.empty((c.batch, c.kv_heads, self.rows), ct)
         occ = np.zeros(1, np.int32)
         he_read_state(self.h, K, V, codes, occ)
         return K, V, codes, int(occ[0])
 
     def vscales(self):
-        """Per-slot value scales [batch][kv_heads][budget] (int8 value cache only)."""
+        """Per-slot value scales [batch][kv_heads][budget] (quantised value cache only)."""
         import numpy as np
         c = self.cfg
         a = np.empty((c.batch, c.kv_heads, self.rows), np.float32)

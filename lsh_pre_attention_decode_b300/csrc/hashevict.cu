@@ -54,7 +54,7 @@ struct Kernels {
   int tile;
   int rec_floats;
   bool tc;  // tensor-core pipeline (tensor maps, programmatic dependent launch)
-  const void* vq_fill;  // int8 value cache: quantisation of filled value rows
+  const void* vq_fill;  // quantised value cache: quantisation of filled value rows
   const void* prep_chunk;   // bf16 pipeline with chunk eviction
   const void* merge_chunk;
   int chunk_floats;         // floats of the per-unit chunk record
@@ -80,7 +80,7 @@ int merge_cfg(int n, int U, bool multi, int* nq, int* upc, int* smem) {
   return t;
 }
 
-template <typename T, int D, int G, bool VQ = false>
+template <typename T, int D, int G, int VQ = 0>
 Kernels kernels_for() {
   Kernels k{};
   k.score = reinterpret_cast<const void*>(&he::score_kernel<T, D, G>);
@@ -92,7 +92,8 @@ Kernels kernels_for() {
     k.prep_mem = reinterpret_cast<const void*>(&he::prep_kernel<D, G, true, VQ>);
     k.merge = reinterpret_cast<const void*>(&he::merge_kernel<D, G, VQ>);
     k.merge_mu = reinterpret_cast<const void*>(&he::merge_kernel<D, G, VQ, false, true>);
-    k.vq_fill = reinterpret_cast<const void*>(&he::vq_fill_kernel<D>);
+    k.vq_fill = VQ ? reinterpret_cast<const void*>(&he::vq_fill_kernel<D, VQ ? VQ : he::kVqInt8>)
+                   : nullptr;
     if constexpr (!VQ) {
       constexpr int NSF = fused_stages<D, G>();
       using SF = he::StreamShape<D, G, NSF, false, true>;
@@ -144,7 +145,7 @@ cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaS
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-template <typename T, int D, bool VQ = false>
+template <typename T, int D, int VQ = 0>
 bool pick_g(int G, Kernels* k) {
   switch (G) {
     case 1: *k = kernels_for<T, D, 1, VQ>(); return true;
@@ -155,14 +156,18 @@ bool pick_g(int G, Kernels* k) {
   }
 }
 
-bool pick_kernels(int dtype, int D, int G, bool vq, Kernels* k) {
-  if (dtype == HE_DTYPE_BF16 && vq) {
-    if (D == 64) return pick_g<bf16_t, 64, true>(G, k);
-    if (D == 128) return pick_g<bf16_t, 128, true>(G, k);
-  } else if (dtype == HE_DTYPE_BF16) {
+// vq: 0, he::kVqInt8 or he::kVqFp8 (the value cache's byte format)
+bool pick_kernels(int dtype, int D, int G, int vq, Kernels* k) {
+  if (dtype == HE_DTYPE_BF16 && vq == he::kVqInt8) {
+    if (D == 64) return pick_g<bf16_t, 64, he::kVqInt8>(G, k);
+    if (D == 128) return pick_g<bf16_t, 128, he::kVqInt8>(G, k);
+  } else if (dtype == HE_DTYPE_BF16 && vq == he::kVqFp8) {
+    if (D == 64) return pick_g<bf16_t, 64, he::kVqFp8>(G, k);
+    if (D == 128) return pick_g<bf16_t, 128, he::kVqFp8>(G, k);
+  } else if (dtype == HE_DTYPE_BF16 && vq == 0) {
     if (D == 64) return pick_g<bf16_t, 64>(G, k);
     if (D == 128) return pick_g<bf16_t, 128>(G, k);
-  } else if (dtype == HE_DTYPE_FP32 && !vq) {
+  } else if (dtype == HE_DTYPE_FP32 && vq == 0) {
     if (D == 64) return pick_g<float, 64>(G, k);
     if (D == 128) return pick_g<float, 128>(G, k);
   }
@@ -192,7 +197,7 @@ bool encode_cache_map(CUtensorMap* map, void* base, uint64_t rows, int D, int bo
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D tensor map over an int8 value cache viewed as [rows][D] bytes; boxes of
+// 2-D tensor map over a quantised value cache viewed as [rows][D] bytes; boxes of
 // one whole row (D bytes) x `box_rows` rows, no swizzle.
 bool encode_vq_map(CUtensorMap* map, void* base, uint64_t rows, int D, int box_rows) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
@@ -275,7 +280,8 @@ struct he_ctx {
   unsigned char* codes = nullptr;
   int32_t* evicted = nullptr;
   float* score = nullptr;  // per-slot scores with score memory (decay > 0), else null
-  bool vq = false;         // int8 value cache: V holds int8 rows, vs their scales
+  bool vq = false;         // quantised value cache: V holds byte rows (int8 or E4M3 codes),
+                           // vs their scales
   float* vs = nullptr;     // [U][vs_stride]
   int vs_stride = 0;       // budget rounded up to whole 64-slot tiles
   int32_t* counters = nullptr;
@@ -427,7 +433,8 @@ int he_create(const he_cfg* cfg, he_handle* out) {
   if (c.batch < 1 || c.heads < 1 || c.kv_heads < 1 || c.heads % c.kv_heads != 0) return HE_EINVAL;
   if (c.bits != 8 && c.bits != 16 && c.bits != 32 && c.bits != 64) return HE_EINVAL;
   if (c.budget < 1 || c.budget > (1 << 24)) return HE_EINVAL;
-  if (c.v_format != HE_VFMT_ELEM && !(c.v_format == HE_VFMT_INT8 && c.dtype == HE_DTYPE_BF16))
+  if (c.v_format != HE_VFMT_ELEM &&
+      !((c.v_format == HE_VFMT_INT8 || c.v_format == HE_VFMT_FP8) && c.dtype == HE_DTYPE_BF16))
     return HE_EINVAL;
   if (!std::isfinite(c.threshold) || !(c.decay >= 0.0f && c.decay <= 1.0f)) return HE_EINVAL;
   if (c.chunk < 0 || c.chunk > he::kMaxChunk) return HE_EINVAL;
@@ -443,8 +450,11 @@ int he_create(const he_cfg* cfg, he_handle* out) {
   if ((int64_t)c.batch * c.kv_heads > 65536) return HE_EINVAL;
   const int G = c.heads / c.kv_heads;
   Kernels kern;
-  const bool vq = c.v_format == HE_VFMT_INT8;
-  if (!pick_kernels(c.dtype, c.head_dim, G, vq, &kern)) return HE_EINVAL;
+  const int vfmt = c.v_format == HE_VFMT_INT8 ? he::kVqInt8
+                   : c.v_format == HE_VFMT_FP8 ? he::kVqFp8
+                                               : 0;
+  const bool vq = vfmt != 0;
+  if (!pick_kernels(c.dtype, c.head_dim, G, vfmt, &kern)) return HE_EINVAL;
   const int64_t U = (int64_t)c.batch * c.kv_heads;
   if (U * ((rows + kern.tile - 1) / kern.tile) > INT32_MAX) return HE_EINVAL;
   if (U * rows + kern.tile >= ((int64_t)1 << 31)) return HE_EINVAL;  // TMA row coordinate
@@ -622,12 +632,12 @@ int he_fill(he_handle h, const void* K, const void* V, int32_t n, void* stream) 
   if (n > 0) {
     HE_TRY(h, cudaMemcpy2DAsync(h->K, (size_t)h->rows * row, K, (size_t)n * row,
                                 (size_t)n * row, (size_t)h->U, cudaMemcpyDeviceToDevice, s));
-    if (h->vq) {  // value rows quantised into the int8 cache
+    if (h->vq) {  // value rows quantised into the byte cache
       const int64_t rows = (int64_t)h->U * n;
       int64_t blocks = (rows + 7) / 8;
       if (blocks > (int64_t)h->num_sms * 16) blocks = (int64_t)h->num_sms * 16;
       int nn = n, budget = h->rows, vstride = h->vs_stride;
-      int8_t* Vq = reinterpret_cast<int8_t*>(h->V);
+      uint8_t* Vq = reinterpret_cast<uint8_t*>(h->V);
       float* vs = h->vs;
       void* args[] = {(void*)&V, (void*)&rows, (void*)&nn, (void*)&budget, (void*)&Vq,
                       (void*)&vs, (void*)&vstride};

@@ -21,7 +21,7 @@ struct UnitOut {
   int32_t hcnt[2];         // fused step: hash warps of the unit done, per key parity
   int32_t pad;
   uint16_t vstar[128];     // the evicted slot's value row (bf16)
-  int8_t vqstar[128];      // int8 value cache: the evicted slot's row ...
+  uint8_t vqstar[128];     // quantised value cache: the evicted slot's byte row ...
   float vsstar;            // ... and its scale
   int32_t cready[2];       // fused step: cq[parity] published (1), reset by the unit's merge
   int32_t pad2;

@@ -34,6 +34,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <type_traits>
 
@@ -43,6 +44,79 @@
 #include "he_tc.cuh"
 
 namespace he {
+
+// ---------------------------------------------------------------------------
+// Quantised value cache (template argument VQ of the bf16 kernels): 0 = value
+// rows in bf16; else one byte per value and one fp32 scale s per slot, the row
+// stored as codes of v / s with s = max |v| / range:
+//   kVqInt8: int8, v / s rounded half to even (range 127);
+//   kVqFp8:  E4M3 (OCP 8-bit floating point), v / s rounded to the nearest
+//            value, ties to the even mantissa, saturating at 448 (range 448).
+// ---------------------------------------------------------------------------
+constexpr int kVqInt8 = 1;
+constexpr int kVqFp8 = 2;
+
+template <int VQ>
+__device__ __forceinline__ float vq_range() {
+  return VQ == kVqFp8 ? 448.0f : 127.0f;
+}
+
+// The stored byte of x = v / s (s > 0).
+template <int VQ>
+__device__ __forceinline__ uint8_t vq_encode(float x) {
+  if constexpr (VQ == kVqFp8) {
+    uint16_t r;  // (the second operand lands in the low byte)
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(x));
+    return (uint8_t)(r & 0xFF);
+  } else {
+    return (uint8_t)(int8_t)(int)fminf(fmaxf(rintf(x), -127.0f), 127.0f);
+  }
+}
+
+// The value a stored byte stands for before its slot's scale (exact in fp32).
+template <int VQ>
+__device__ __forceinline__ float vq_decode(uint8_t c) {
+  if constexpr (VQ == kVqFp8) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)c));
+    return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+  } else {
+    return (float)(int8_t)c;
+  }
+}
+
+// Four stored bytes (byte i = element i) -> bf16 pairs, exact: lo holds
+// elements 0 and 1, hi elements 2 and 3 (the lower element in the lower half).
+template <int VQ>
+__device__ __forceinline__ void vq_widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  if constexpr (VQ == kVqFp8) {
+    // E4M3 -> f16 is exact (every E4M3 value is an f16 normal), f16 -> fp32
+    // exact, and the fp32 values have at most 4 significant bits: exact in bf16
+    uint32_t h01, h23;
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(h01), "=r"(h23)
+        : "r"(w));
+    const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+    const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+    const __nv_bfloat162 b01 = __floats2bfloat162_rn(f01.x, f01.y);
+    const __nv_bfloat162 b23 = __floats2bfloat162_rn(f23.x, f23.y);
+    lo = *reinterpret_cast<const uint32_t*>(&b01);
+    hi = *reinterpret_cast<const uint32_t*>(&b23);
+  } else {
+    // byte b -> fp32 with exponent 2^23 holding b + 128 in its low mantissa
+    // bits (a byte permute), minus 2^23 + 128: b exactly; two at a time to bf16
+    const uint32_t u4 = w ^ 0x80808080u;
+    float f[4];
+#pragma unroll
+    for (int i2 = 0; i2 < 4; ++i2)
+      f[i2] = __uint_as_float(__byte_perm(u4, 0x4B000000u, 0x7540u + i2)) - 8388736.0f;
+    const __nv_bfloat162 b01 = __floats2bfloat162_rn(f[0], f[1]);
+    const __nv_bfloat162 b23 = __floats2bfloat162_rn(f[2], f[3]);
+    lo = *reinterpret_cast<const uint32_t*>(&b01);
+    hi = *reinterpret_cast<const uint32_t*>(&b23);
+  }
+}
 
 // ---------------------------------------------------------------------------
 // prep
@@ -67,7 +141,7 @@ struct PrepShape {
 // One CTA per SM at most: a CTA takes the (unit, code item) items
 // blockIdx.x, blockIdx.x + gridDim.x, ... in turn, so that prep never crowds
 // the stream kernel's CTAs off an SM.
-template <int D, int G, bool MEM, bool VQ = false, bool CH = false>
+template <int D, int G, bool MEM, int VQ = 0, bool CH = false>
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, UnitOut* uo,
                                                             int splits, int first_of_step) {
   static_assert(!(CH && (MEM || VQ)), "chunk eviction takes neither option");
@@ -346,7 +420,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
             if (lane == 0) uo[u].lstar[g] = a * p.qscale;
           }
           if constexpr (VQ) {
-            const int8_t* Vq = reinterpret_cast<const int8_t*>(p.V) + ((size_t)u * p.budget + winner) * D;
+            const uint8_t* Vq = reinterpret_cast<const uint8_t*>(p.V) + ((size_t)u * p.budget + winner) * D;
             for (int d = tid; d < D; d += kPrepThreads) uo[u].vqstar[d] = __ldcg(Vq + d);
             if (tid == 0) uo[u].vsstar = __ldcg(p.vs + (size_t)u * p.vs_stride + winner);
           } else {
@@ -364,13 +438,15 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
   if (tid == 0) pdl_wait();
 }
 
-// Quantisation of value rows into an int8 value cache (one warp per row): row r
-// of V_in [rows][D] (bf16) is slot r % n of unit r / n; s = max |v| / 127,
-// q = v / s rounded half to even (fp32 division), a zero row gives s = 0, q = 0.
-template <int D>
+// Quantisation of value rows into a quantised value cache (one warp per row):
+// row r of V_in [rows][D] (bf16) is slot r % n of unit r / n; s = max |v| /
+// range (fp32 division), byte d = the code of v_d / s (fp32 division); a zero
+// row gives s = 0 and codes 0.
+template <int D, int VQ>
 __global__ void __launch_bounds__(256) vq_fill_kernel(const uint16_t* __restrict__ V_in,
                                                       int64_t rows, int n, int budget,
-                                                      int8_t* Vq, float* vs, int vs_stride) {
+                                                      uint8_t* Vq, float* vs, int vs_stride) {
+  static_assert(VQ == kVqInt8 || VQ == kVqFp8, "a byte format");
   constexpr int E = D / 32;
   const int lane = threadIdx.x & 31;
   for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows;
@@ -384,14 +460,10 @@ __global__ void __launch_bounds__(256) vq_fill_kernel(const uint16_t* __restrict
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-    const float sc = __fdiv_rn(m, 127.0f);
-    int8_t* dst = Vq + ((size_t)u * budget + sl) * D + lane * E;
+    const float sc = __fdiv_rn(m, vq_range<VQ>());
+    uint8_t* dst = Vq + ((size_t)u * budget + sl) * D + lane * E;
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      float q = 0.0f;
-      if (sc > 0.0f) q = fminf(fmaxf(rintf(__fdiv_rn(v[e], sc)), -127.0f), 127.0f);
-      dst[e] = (int8_t)(int)q;
-    }
+    for (int e = 0; e < E; ++e) dst[e] = sc > 0.0f ? vq_encode<VQ>(__fdiv_rn(v[e], sc)) : 0;
     if (lane == 0) vs[(size_t)u * vs_stride + sl] = sc;
   }
 }
@@ -415,12 +487,12 @@ constexpr int kDescFirst = 1;  // first tile of a segment: load q, reset the sta
 constexpr int kDescLast = 2;   // last tile of a segment: write the partial
 constexpr int kDescEnd = 4;    // no more tiles
 
-// VQ: the value cache holds int8 rows with one fp32 scale per slot (a stage is
-// the bf16 K tile, the int8 V tile and the tile's scales; each consumer warp
+// VQ: the value cache holds byte rows with one fp32 scale per slot (a stage is
+// the bf16 K tile, the byte V tile and the tile's scales; each consumer warp
 // widens its 16 value rows to bf16 in a buffer of its own for the value MMA).
 // FUSED: the whole step in this kernel (he_fused.cuh): a hash warp after the
 // producer warp, and the last CTA of each unit merges it.
-template <int D, int G, int NS, bool VQ = false, bool FUSED = false>
+template <int D, int G, int NS, int VQ = 0, bool FUSED = false>
 struct StreamShape {
   static constexpr int NCW = 4;              // consumer warps
   static constexpr int NC = NCW * 32;        // consumer threads
@@ -429,7 +501,7 @@ struct StreamShape {
   static constexpr int NHALF = D / 64;       // 128-byte column boxes per row
   static constexpr int BOXB = TS * 128;      // bytes per TMA box
   static constexpr int TILEB = NHALF * BOXB; // bytes per K (or V) tile
-  static constexpr int VQT = TS * D;         // VQ: bytes of the int8 V tile
+  static constexpr int VQT = TS * D;         // VQ: bytes of the V tile
   static constexpr int SCB = TS * 4;         // VQ: bytes of the tile's scales
   static constexpr int STAGEB = VQ ? (TILEB + VQT + SCB + 1023) / 1024 * 1024 : 2 * TILEB;
   static constexpr int VWB = 16 * D * 2;     // VQ: one warp's bf16 value rows
@@ -467,7 +539,7 @@ struct StreamShape {
   static_assert(STAGEB % 1024 == 0 && BOXB % 1024 == 0 && QB % 16 == 0, "alignment");
 };
 
-template <int D, int G, int NS, bool PSPLIT, bool VQ = false, bool FUSED = false>
+template <int D, int G, int NS, bool PSPLIT, int VQ = 0, bool FUSED = false>
 __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ, FUSED>::NT, 2)
     stream_kernel(const StepParams p, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV) {
@@ -709,7 +781,7 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ, FUSED>::NT, 2)
     if (VQ && k < npre && (unsigned)(wslot - slot_base) < 16u &&
         HE_CHECK(wslot < p.budget, p.err)) {
       // re-read the row written by the previous step (now visible) into the
-      // tile: its bf16 key (swizzled), int8 value row and scale
+      // tile: its bf16 key (swizzled), byte value row and scale
       const int row = wslot - lt * S::TS;
       constexpr int CK = D / 8, CV = D / 16;  // 16-byte chunks of the key and value rows
       const size_t r = (size_t)u * p.budget + wslot;
@@ -722,7 +794,7 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ, FUSED>::NT, 2)
       } else if (lane < CK + CV) {
         const int c = lane - CK;
         const uint4 x = __ldcg(reinterpret_cast<const uint4*>(
-            reinterpret_cast<const int8_t*>(p.V) + r * D + 16 * c));
+            reinterpret_cast<const uint8_t*>(p.V) + r * D + 16 * c));
         *reinterpret_cast<uint4*>(Kd + S::TILEB + row * D + 16 * c) = x;
       } else if (lane == CK + CV) {
         *reinterpret_cast<float*>(Kd + S::TILEB + S::VQT + 4 * row) =
@@ -791,7 +863,7 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ, FUSED>::NT, 2)
     }
 
     // P^T [8 heads][16 slots] in bf16 (hi, and the rounding remainder lo); with
-    // an int8 value cache each slot's weight carries the slot's value scale
+    // a quantised value cache each slot's weight carries the slot's value scale
     {
       float w00 = p00, w01 = p01, w10 = p10, w11 = p11;
       if constexpr (VQ) {
@@ -815,12 +887,12 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ, FUSED>::NT, 2)
         Plo[h1 * 16 + g8 + 8] = __float2bfloat16_rn(w11 - __bfloat162float(a11));
       }
     }
-    // VQ: this warp's 16 int8 value rows -> bf16 (exact), in the swizzled layout
+    // VQ: this warp's 16 value rows (bytes) -> bf16 (exact), in the swizzled layout
     // of a 16-row tile; the stage is then free
     unsigned char* vw = smem + S::OFF_VW + cw * S::VWB;
     if constexpr (VQ) {
       // (each load of the warp covers 512 contiguous bytes of the unswizzled
-      // int8 tile, lane l taking 16-byte piece i * 32 + l of the warp's rows:
+      // byte tile, lane l taking 16-byte piece i * 32 + l of the warp's rows:
       // no two lanes of a load share a bank)
       constexpr int CPR = D / 16;  // 16-byte pieces per value row
       const int8_t* src = reinterpret_cast<const int8_t*>(Ks + S::TILEB) + row0 * D;
@@ -831,19 +903,7 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ, FUSED>::NT, 2)
         const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
         uint32_t o[8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          // byte b -> fp32 with exponent 2^23 holding b + 128 in its low mantissa
-          // bits (a byte permute), minus 2^23 + 128: b exactly; two at a time to bf16
-          const uint32_t u4 = wd[e] ^ 0x80808080u;
-          float f[4];
-#pragma unroll
-          for (int i2 = 0; i2 < 4; ++i2)
-            f[i2] = __uint_as_float(__byte_perm(u4, 0x4B000000u, 0x7540u + i2)) - 8388736.0f;
-          const __nv_bfloat162 lo = __floats2bfloat162_rn(f[0], f[1]);
-          const __nv_bfloat162 hi = __floats2bfloat162_rn(f[2], f[3]);
-          o[2 * e] = *reinterpret_cast<const uint32_t*>(&lo);
-          o[2 * e + 1] = *reinterpret_cast<const uint32_t*>(&hi);
-        }
+        for (int e = 0; e < 4; ++e) vq_widen4<VQ>(wd[e], o[2 * e], o[2 * e + 1]);
         const int cc = 2 * c16;  // first 8-column chunk of these 16 values
         // (the lanes of a row's upper half store their two chunks in the other
         // order, so that the eight lanes of each 128-bit store phase fall in
@@ -1088,7 +1148,7 @@ struct MergeShape {
 // accumulator -> xm, xl, xa [G][D].
 // Every warp of the CTA runs an online softmax over a strided share of the
 // slots (lane owns D/32 elements), then the warp states merge in a fixed order.
-template <int D, int G, bool VQ>
+template <int D, int G, int VQ>
 __device__ void recompute_partial(const StepParams& p, int u, int lo, int hi, int skip,
                                   int nskip, const float* qf, float* wstate, float* xm, float* xl,
                                   float* xa, int tid) {
@@ -1097,7 +1157,7 @@ __device__ void recompute_partial(const StepParams& p, int u, int lo, int hi, in
   const int lane = tid & 31, warp = tid >> 5;
   {
     const uint16_t* Kc = reinterpret_cast<const uint16_t*>(p.K) + (size_t)u * p.budget * D;
-    // (the int8 value cache: bytes instead of bf16, one scale per slot)
+    // (a quantised value cache: bytes instead of bf16, one scale per slot)
     const uint16_t* Vc = VQ ? reinterpret_cast<const uint16_t*>(reinterpret_cast<const int8_t*>(p.V) +
                                                                 (size_t)u * p.budget * D)
                             : reinterpret_cast<const uint16_t*>(p.V) + (size_t)u * p.budget * D;
@@ -1134,7 +1194,7 @@ __device__ void recompute_partial(const StepParams& p, int u, int lo, int hi, in
           const int8_t* vb = reinterpret_cast<const int8_t*>(Vc) + at;
           const float sc = __ldcg(p.vs + (size_t)u * p.vs_stride + s);
 #pragma unroll
-          for (int e = 0; e < E; ++e) vx[r][e] = (float)__ldcg(vb + e) * sc;
+          for (int e = 0; e < E; ++e) vx[r][e] = vq_decode<VQ>((uint8_t)__ldcg(vb + e)) * sc;
         } else if constexpr (E == 4) {
           const uint2 vw = __ldcg(reinterpret_cast<const uint2*>(Vc + at));
           vx[r][0] = bf16_lo(vw.x);
@@ -1252,7 +1312,7 @@ __device__ __forceinline__ float take_part(float cm, float cl, const float4& ca,
 // MU: a CTA merges MT / (nq * GD4) units, one group of nq * GD4 threads each
 // (for steps with more units than SMs: the merge CTAs then run in one wave
 // instead of several); else one unit per CTA.
-template <int D, int G, bool VQ = false, bool CH = false, bool MU = false>
+template <int D, int G, int VQ = 0, bool CH = false, bool MU = false>
 __global__ void __launch_bounds__(kMergeMaxThreads)
     merge_kernel(const StepParams p, UnitOut* uo, int stream_ctas, int nq) {
   static_assert(!(CH && VQ), "chunk eviction keeps bf16 values");
@@ -1383,15 +1443,17 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
 
   float4 vs = make_float4(__uint_as_float(vs2.x << 16), __uint_as_float(vs2.x & 0xFFFF0000u),
                           __uint_as_float(vs2.y << 16), __uint_as_float(vs2.y & 0xFFFF0000u));
-  // int8 value cache: the evicted row as stored (q * s), and the new row's
-  // quantisation (s = max |v| / 127, q = v / s rounded half to even)
+  // quantised value cache: the evicted row as stored (decode(q) * s), and the
+  // new row's quantisation (s = max |v| / range, q = the code of v / s)
   float vnew = 0.0f;
   if constexpr (VQ) {
     if (full) {
-      const int32_t w4 = __ldcg(reinterpret_cast<const int32_t*>(uo[u].vqstar + d0));
+      const uint32_t w4 = __ldcg(reinterpret_cast<const uint32_t*>(uo[u].vqstar + d0));
       const float ss = __ldcg(&uo[u].vsstar);
-      vs = make_float4((float)(int8_t)(w4 & 0xFF) * ss, (float)(int8_t)((w4 >> 8) & 0xFF) * ss,
-                       (float)(int8_t)((w4 >> 16) & 0xFF) * ss, (float)(int8_t)(w4 >> 24) * ss);
+      vs = make_float4(vq_decode<VQ>((uint8_t)(w4 & 0xFF)) * ss,
+                       vq_decode<VQ>((uint8_t)((w4 >> 8) & 0xFF)) * ss,
+                       vq_decode<VQ>((uint8_t)((w4 >> 16) & 0xFF)) * ss,
+                       vq_decode<VQ>((uint8_t)(w4 >> 24)) * ss);
     }
     vnew = __uint_as_float((uint32_t)vt1 << 16);
     float m = tid < D ? fabsf(vnew) : 0.0f;
@@ -1405,12 +1467,9 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
   if constexpr (VQ) {
     float m = 0.0f;
     for (int w2 = 0; w2 < D / 32; ++w2) m = fmaxf(m, vqrow[D + w2]);
-    vscale = __fdiv_rn(m, 127.0f);
-    if (tid < D) {
-      float r = 0.0f;
-      if (vscale > 0.0f) r = fminf(fmaxf(rintf(__fdiv_rn(vnew, vscale)), -127.0f), 127.0f);
-      vqrow[tid] = r;
-    }
+    vscale = __fdiv_rn(m, vq_range<VQ>());
+    if (tid < D)  // the code's value (exact; the code is written from it below)
+      vqrow[tid] = vscale > 0.0f ? vq_decode<VQ>(vq_encode<VQ>(__fdiv_rn(vnew, vscale))) : 0.0f;
   }
 
   float mx = -1e30f, sum = 0.0f;
@@ -1632,8 +1691,8 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
   if (tid < D) {
     Kw[tid] = kt1;
     if constexpr (VQ)
-      reinterpret_cast<int8_t*>(p.V)[((size_t)u * p.budget + winner) * D + tid] =
-          (int8_t)(int)vqrow[tid];
+      reinterpret_cast<uint8_t*>(p.V)[((size_t)u * p.budget + winner) * D + tid] =
+          vq_encode<VQ>(vqrow[tid]);
     else
       reinterpret_cast<uint16_t*>(p.V)[((size_t)u * p.budget + wslot) * D + tid] = vt1;
   }

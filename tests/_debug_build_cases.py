@@ -54,7 +54,8 @@ def main():
         ("ragged budget, appends", base.with_(batch=2, budget=333, prompt=700), 300, 40, {}),
         ("units of many tiles", base.with_(batch=2, budget=3000, prompt=3100), 3000, 6, {}),
         ("chunk eviction", base.with_(batch=2, budget=480, prompt=960), 480, 40, {"chunk": 8}),
-        ("int8 values", base.with_(batch=2, budget=300, prompt=600), 300, 20, {"v_int8": True}),
+        ("int8 values", base.with_(batch=2, budget=300, prompt=600), 300, 20, {"v_format": "int8"}),
+        ("fp8 values", base.with_(batch=2, budget=300, prompt=600), 300, 20, {"v_format": "fp8"}),
         ("score memory", base.with_(batch=2, budget=333, prompt=700), 320, 30, {"decay": 0.5}),
         ("G = 8, D = 64", base.with_(batch=2, heads=64, head_dim=64, bits=16, budget=200,
                                      prompt=400), 200, 20, {}),

@@ -43,24 +43,24 @@ class GpuRun:
 
 
 def make_handle(w: synth.Workload, layer: int = 0, threshold: float = 0.0, decay: float = 0.0,
-                v_int8: bool = False, chunk: int = 1, engine: str = "pipeline"):
+                v_format: str = "elem", chunk: int = 1, engine: str = "pipeline"):
     from lsh_pre_attention_decode_b300 import HashEvict
     return HashEvict(w.batch, w.heads, w.kv_heads, w.head_dim, w.bits, w.budget, w.dtype,
                      seed=w.projection_seed(layer), threshold=threshold, decay=decay,
-                     v_int8=v_int8, chunk=chunk, engine=engine)
+                     v_format=v_format, chunk=chunk, engine=engine)
 
 
 def run_gpu(w: synth.Workload, fill_n: int, steps: int, out_steps=(), layer: int = 0,
             device_gen: bool = False, read_state: bool = False, batch_tokens: int = 256,
             profile: bool = False, threshold: float = 0.0, decay: float = 0.0,
-            v_int8: bool = False, chunk: int = 1, engine: str = "pipeline") -> GpuRun:
+            v_format: str = "elem", chunk: int = 1, engine: str = "pipeline") -> GpuRun:
     """Fill with prompt tokens [0, fill_n), then stream tokens fill_n .. fill_n+steps-1
     (generated batch_tokens at a time).  With decay > 0 the returned state also
-    holds the per-slot scores; with an int8 value cache, V is int8 and the value
-    scales follow; chunk > 1: chunk eviction (state rows budget + chunk - 1)."""
+    holds the per-slot scores; with a quantised value cache (v_format "int8" or
+    "fp8"), V holds the byte rows and the value scales follow; chunk > 1: chunk eviction (state rows budget + chunk - 1)."""
     import torch
     out_steps = set(out_steps)
-    he = make_handle(w, layer, threshold, decay, v_int8, chunk, engine)
+    he = make_handle(w, layer, threshold, decay, v_format, chunk, engine)
     try:
         if fill_n > 0:
             if device_gen:
@@ -98,7 +98,7 @@ def run_gpu(w: synth.Workload, fill_n: int, steps: int, out_steps=(), layer: int
         state = he.state() if read_state else None
         if read_state:
             state = state + (he.scores() if decay > 0.0 else None,
-                             he.vscales() if v_int8 else None)
+                             he.vscales() if v_format != "elem" else None)
         return GpuRun(evicted, outs, state, prof)
     finally:
         he.close()
@@ -113,13 +113,13 @@ class OracleRun:
     V: np.ndarray
     occupancy: int
     score: np.ndarray | None = None  # per-slot scores (score memory only)
-    Vq: np.ndarray | None = None     # int8 value cache: rows ...
+    Vq: np.ndarray | None = None     # quantised value cache: byte rows ...
     Vs: np.ndarray | None = None     # ... and scales
 
 
 def run_oracle_unit(w: synth.Workload, b: int, j: int, fill_n: int, steps: int, out_steps=(),
                     layer: int = 0, threshold: float = 0.0, decay: float = 0.0,
-                    v_int8: bool = False, chunk: int = 1) -> OracleRun:
+                    v_format: str = "elem", chunk: int = 1) -> OracleRun:
     o = oracle.load()
     W = o.projection(w.projection_seed(layer), w.head_dim, w.bits, w.dtype)
     Kin = synth.host_unit_kv(w, "key", b, j, 0, fill_n, layer)
@@ -127,7 +127,8 @@ def run_oracle_unit(w: synth.Workload, b: int, j: int, fill_n: int, steps: int, 
     if chunk > 1:
         st = o.unit_fill_chunk(W, w.budget, chunk, Kin, Vin, tau=threshold)
     else:
-        st = o.unit_fill(W, w.budget, Kin, Vin, tau=threshold, memory=decay > 0.0, vq=v_int8)
+        st = o.unit_fill(W, w.budget, Kin, Vin, tau=threshold, memory=decay > 0.0,
+                         vq=False if v_format == "elem" else v_format)
     q = synth.host_unit_queries(w, b, j, fill_n, steps, layer)
     k = synth.host_unit_kv(w, "key", b, j, fill_n, steps, layer)
     v = synth.host_unit_kv(w, "value", b, j, fill_n, steps, layer)
@@ -140,12 +141,12 @@ def run_oracle_unit(w: synth.Workload, b: int, j: int, fill_n: int, steps: int, 
 
 
 def run_oracle_units(w, units, fill_n, steps, out_steps=(), layer=0, threads=8,
-                     threshold: float = 0.0, decay: float = 0.0, v_int8: bool = False,
+                     threshold: float = 0.0, decay: float = 0.0, v_format: str = "elem",
                      chunk: int = 1):
     """Oracle over several (b, j) units in parallel threads (ctypes releases the GIL)."""
     with cf.ThreadPoolExecutor(max_workers=threads) as ex:
         futs = {u: ex.submit(run_oracle_unit, w, u[0], u[1], fill_n, steps, out_steps, layer,
-                             threshold, decay, v_int8, chunk)
+                             threshold, decay, v_format, chunk)
                 for u in units}
         return {u: f.result() for u, f in futs.items()}
 
@@ -171,8 +172,8 @@ def compare(w: synth.Workload, g: GpuRun, orc: dict, out_steps=(), check_state: 
             assert occ == r.occupancy
             assert np.array_equal(codes[b, j].astype(np.uint64), r.codes), f"codes ({b},{j})"
             assert np.array_equal(K[b, j], r.K), f"K ({b},{j})"
-            if r.Vq is not None:  # int8 value cache: rows and scales, exactly
-                assert np.array_equal(V[b, j], r.Vq), f"int8 V ({b},{j})"
+            if r.Vq is not None:  # quantised value cache: byte rows and scales, exactly
+                assert np.array_equal(V[b, j], r.Vq), f"V bytes ({b},{j})"
                 assert np.array_equal(g.state[5][b, j], r.Vs), f"value scales ({b},{j})"
             else:
                 assert np.array_equal(V[b, j], r.V), f"V ({b},{j})"
@@ -196,7 +197,7 @@ class B2BRun:
 
 def run_gpu_b2b(w: synth.Workload, fill_n: int, tokens: int, out_steps=(), layers: int = 1,
                 graph: bool = False, replays: int = 2, warm: int = 0, threshold: float = 0.0,
-                decay: float = 0.0, v_int8: bool = False, chunk: int = 1,
+                decay: float = 0.0, v_format: str = "elem", chunk: int = 1,
                 hold_ms: float = 20.0, engine: str = "pipeline") -> B2BRun:
     """Fill `layers` independent caches with prompt tokens [0, fill_n), then
     issue steps round robin over the layers (layer 0 token t, layer 1 token t,
@@ -228,7 +229,7 @@ def run_gpu_b2b(w: synth.Workload, fill_n: int, tokens: int, out_steps=(), layer
     he_step_raw = lib().he_step
     try:
         for layer in range(L):
-            he = make_handle(w, layer, threshold, decay, v_int8, chunk, engine)
+            he = make_handle(w, layer, threshold, decay, v_format, chunk, engine)
             handles.append(he)
             if fill_n > 0:
                 he.fill(synth.gpu_kv(w, "key", 0, fill_n, layer),
@@ -291,7 +292,7 @@ def run_gpu_b2b(w: synth.Workload, fill_n: int, tokens: int, out_steps=(), layer
                 res_outs[(layer, s)] = o.cpu().numpy()
             he = handles[layer]
             st = he.state()
-            states[layer] = st + (he.vscales() if v_int8 else None,
+            states[layer] = st + (he.vscales() if v_format != "elem" else None,
                                   he.scores() if decay > 0.0 else None)
         return B2BRun(evicted, res_outs, states, tok_of)
     finally:
@@ -300,7 +301,7 @@ def run_gpu_b2b(w: synth.Workload, fill_n: int, tokens: int, out_steps=(), layer
 
 
 def oracle_b2b(w: synth.Workload, units, fill_n: int, tok_of, out_steps=(), layer: int = 0,
-               threshold: float = 0.0, decay: float = 0.0, v_int8: bool = False,
+               threshold: float = 0.0, decay: float = 0.0, v_format: str = "elem",
                chunk: int = 1, threads: int = 8) -> dict:
     """The oracle over the token sequence tok_of (token indices, repeats
     allowed) for the given (b, j) units of one layer."""
@@ -320,7 +321,7 @@ def oracle_b2b(w: synth.Workload, units, fill_n: int, tok_of, out_steps=(), laye
             st = o.unit_fill_chunk(W, w.budget, chunk, Kin, Vin, tau=threshold)
         else:
             st = o.unit_fill(W, w.budget, Kin, Vin, tau=threshold, memory=decay > 0.0,
-                             vq=v_int8)
+                             vq=False if v_format == "elem" else v_format)
         q = synth.host_unit_queries(w, b, j, lo, hi - lo, layer)[sel]
         k = synth.host_unit_kv(w, "key", b, j, lo, hi - lo, layer)[sel]
         v = synth.host_unit_kv(w, "value", b, j, lo, hi - lo, layer)[sel]
@@ -350,7 +351,7 @@ def compare_b2b(w: synth.Workload, g: B2BRun, layer: int, orc: dict, out_steps=(
         assert np.array_equal(codes[b, j].astype(np.uint64), r.codes), f"codes ({b},{j})"
         assert np.array_equal(K[b, j], r.K), f"K ({b},{j})"
         if r.Vq is not None:
-            assert np.array_equal(V[b, j], r.Vq), f"int8 V ({b},{j})"
+            assert np.array_equal(V[b, j], r.Vq), f"V bytes ({b},{j})"
             assert np.array_equal(vs[b, j], r.Vs), f"value scales ({b},{j})"
         else:
             assert np.array_equal(V[b, j], r.V), f"V ({b},{j})"

@@ -59,15 +59,18 @@ def cfg(**kw):
 @pytest.mark.parametrize("bad", [dict(batch=0), dict(heads=30), dict(kv_heads=0), dict(bits=12),
                                  dict(bits=128), dict(budget=0), dict(budget=(1 << 24) + 1),
                                  dict(head_dim=96), dict(head_dim=256), dict(dtype=2),
-                                 dict(heads=64, kv_heads=4), dict(v_format=2),
-                                 dict(v_format=1, dtype=1),
+                                 dict(heads=64, kv_heads=4), dict(v_format=3),
+                                 dict(v_format=-1), dict(v_format=1, dtype=1),
+                                 dict(v_format=2, dtype=1),
                                  dict(batch=70000), dict(decay=-0.5), dict(decay=1.5),
                                  dict(decay=float("nan")), dict(threshold=float("inf")),
                                  dict(threshold=float("nan")), dict(chunk=-1), dict(chunk=17),
                                  dict(chunk=3), dict(chunk=2, dtype=1),
-                                 dict(chunk=2, v_format=1), dict(chunk=2, decay=0.5),
+                                 dict(chunk=2, v_format=1), dict(chunk=2, v_format=2),
+                                 dict(chunk=2, decay=0.5),
                                  dict(engine=2), dict(engine=-1), dict(engine=1, dtype=1),
                                  dict(engine=1, decay=0.5), dict(engine=1, v_format=1),
+                                 dict(engine=1, v_format=2),
                                  dict(engine=1, chunk=4, budget=256)])
 def test_create_rejects_bad_configs(L, bad):
     h = ctypes.c_void_p()

@@ -103,14 +103,15 @@ def test_chunk_eviction_back_to_back(graph):
         check(w, w.budget - 20, 100, all_units(w), chunk=16, out_steps=[0, 19, 20, 35, 36, 99])
 
 
+@pytest.mark.parametrize("fmt", ["int8", "fp8"])
 @pytest.mark.parametrize("graph", [False, True])
-def test_int8_values_back_to_back(graph):
+def test_quantised_values_back_to_back(graph, fmt):
     w = small(batch=2, budget=900, prompt=1900, decode=8)
     if graph:
-        check(w, w.budget, 64, all_units(w), graph=True, replays=2, v_int8=True,
+        check(w, w.budget, 64, all_units(w), graph=True, replays=2, v_format=fmt,
               out_steps=[64, 127])
     else:
-        check(w, w.budget - 10, 80, all_units(w), v_int8=True, out_steps=[0, 9, 10, 79])
+        check(w, w.budget - 10, 80, all_units(w), v_format=fmt, out_steps=[0, 9, 10, 79])
 
 
 @pytest.mark.parametrize("graph", [False, True])

@@ -106,7 +106,8 @@ def test_scores_bit_exact():
 @pytest.mark.parametrize("bits,budget,opt", [(32, 4096, {}), (8, 4096, {}), (64, 4096, {}),
                                               (16, 9000, {}), (32, 5000, {"decay": 0.5}),
                                               (32, 4096, {"threshold": 0.5}),
-                                              (32, 4096, {"v_int8": True})])
+                                              (32, 4096, {"v_format": "int8"}),
+                                              (32, 4096, {"v_format": "fp8"})])
 def test_step_distances_bit_exact(bits, budget, opt):
     """The group-summed Hamming distances that the step's own scan computes
     (method step 3, the codes/eviction kernel of every step), logged on the
@@ -116,9 +117,10 @@ def test_step_distances_bit_exact(bits, budget, opt):
     import torch
     from lsh_pre_attention_decode_b300 import he_set_dist_log
     w = small("llama8b_b8", batch=2, bits=bits, budget=budget, prompt=budget + 64)
-    decay, tau, vq = opt.get("decay", 0.0), opt.get("threshold", 0.0), opt.get("v_int8", False)
+    decay, tau = opt.get("decay", 0.0), opt.get("threshold", 0.0)
+    vq = opt.get("v_format", "elem")
     steps = 3
-    with make_handle(w, threshold=tau, decay=decay, v_int8=vq) as he:
+    with make_handle(w, threshold=tau, decay=decay, v_format=vq) as he:
         he.fill(synth.gpu_kv(w, "key", 0, w.budget), synth.gpu_kv(w, "value", 0, w.budget))
         q = synth.gpu_queries(w, w.budget, steps)
         k = synth.gpu_kv(w, "key", w.budget, steps, token_major=True)
