@@ -198,7 +198,9 @@ bool encode_cache_map(CUtensorMap* map, void* base, uint64_t rows, int D, int bo
 }
 
 // 2-D tensor map over a quantised value cache viewed as [rows][D] bytes; boxes of
-// one whole row (D bytes) x `box_rows` rows, no swizzle.
+// one whole row (D bytes) x `box_rows` rows, 16-byte chunks swizzled within the
+// row (128B swizzle for D = 128, 64B for D = 64; the stream kernel's
+// vq_tile_off reads that layout).
 bool encode_vq_map(CUtensorMap* map, void* base, uint64_t rows, int D, int box_rows) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
@@ -215,7 +217,8 @@ bool encode_vq_map(CUtensorMap* map, void* base, uint64_t rows, int D, int box_r
   const cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_INTERLEAVE_NONE,
+                D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

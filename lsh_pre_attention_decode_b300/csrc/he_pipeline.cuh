@@ -118,6 +118,48 @@ __device__ __forceinline__ void vq_widen4(uint32_t w, uint32_t& lo, uint32_t& hi
   }
 }
 
+// Byte words of two slots s (even) and s + 1 of one value-tile row position:
+// byte i of each word is the same column.  -> four f16 pairs (slot s in the
+// lower half), pair i from bytes i, exact (|int8| < 2^11; every E4M3 value is an
+// f16 normal).
+template <int VQ>
+__device__ __forceinline__ void vq_pairs_f16(uint32_t we, uint32_t wo, uint32_t (&pr)[4]) {
+  if constexpr (VQ == kVqFp8) {
+    const uint32_t x01 = __byte_perm(we, wo, 0x5140), x23 = __byte_perm(we, wo, 0x7362);
+    asm("{\n\t.reg .b16 a, b, c, d;\n\tmov.b32 {a, b}, %4;\n\tmov.b32 {c, d}, %5;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %2, c;\n\tcvt.rn.f16x2.e4m3x2 %3, d;\n\t}"
+        : "=r"(pr[0]), "=r"(pr[1]), "=r"(pr[2]), "=r"(pr[3])
+        : "r"(x01), "r"(x23));
+  } else {
+    // byte b ^ 0x80 as the low mantissa bits of f16 1024: 1024 + b + 128;
+    // minus 1152 gives b (both steps exact)
+    const uint32_t ue = we ^ 0x80808080u, uo = wo ^ 0x80808080u;
+    const __half2 off = __float2half2_rn(1152.0f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t t =
+          (__byte_perm(ue, uo, (uint32_t)(i | ((4 + i) << 8))) & 0x00FF00FFu) | 0x64006400u;
+      const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&t), off);
+      pr[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+  }
+}
+
+// Byte offset of (slot row s, byte b) in a value tile of D-byte rows as the
+// tensor copy lays it out: 16-byte chunks swizzled within 128-byte (D = 128)
+// or 64-byte (D = 64) rows, so that the four slot rows a thread reads per
+// column fall in different banks.
+template <int D>
+__device__ __forceinline__ int vq_tile_off(int s, int b) {
+  static_assert(D == 64 || D == 128, "value tile rows of 64 or 128 bytes");
+  const int x = D == 128 ? (s & 7) : ((s >> 1) & 3);
+  return s * D + ((((b >> 4) ^ x)) << 4) + (b & 15);
+}
+
+// Power-of-two exponent bound of the f16 value-MMA weights (see stream_kernel).
+constexpr int kVqExpMax = 100;
+
 // ---------------------------------------------------------------------------
 // prep
 // ---------------------------------------------------------------------------
@@ -488,8 +530,10 @@ constexpr int kDescLast = 2;   // last tile of a segment: write the partial
 constexpr int kDescEnd = 4;    // no more tiles
 
 // VQ: the value cache holds byte rows with one fp32 scale per slot (a stage is
-// the bf16 K tile, the byte V tile and the tile's scales; each consumer warp
-// widens its 16 value rows to bf16 in a buffer of its own for the value MMA).
+// the bf16 K tile, the swizzled byte V tile and the tile's scales).  The value
+// MMA runs in f16: each consumer warp converts its A fragments from the byte
+// tile in registers (an exact conversion), and the weights carry the slots'
+// scales times a power of two of the warp's.
 // FUSED: the whole step in this kernel (he_fused.cuh): a hash warp after the
 // producer warp, and the last CTA of each unit merges it.
 template <int D, int G, int NS, int VQ = 0, bool FUSED = false>
@@ -504,17 +548,15 @@ struct StreamShape {
   static constexpr int VQT = TS * D;         // VQ: bytes of the V tile
   static constexpr int SCB = TS * 4;         // VQ: bytes of the tile's scales
   static constexpr int STAGEB = VQ ? (TILEB + VQT + SCB + 1023) / 1024 * 1024 : 2 * TILEB;
-  static constexpr int VWB = 16 * D * 2;     // VQ: one warp's bf16 value rows
   static constexpr int QB = G * D * 2;       // the unit's query rows (bf16)
   static constexpr int KS = D / 16;          // k-steps of the logit MMA
   static constexpr int MT = D / 16;          // d blocks of the value MMA
-  static constexpr int PB = 8 * 16 * 2;      // bytes of one P^T block [8 heads][16 slots] bf16
+  static constexpr int PB = 8 * 16 * 2;      // bytes of one P^T block [8 heads][16 slots] bf16 (VQ: f16)
   // floats of the warp-merge area (FUSED: also the merge's recompute scratch)
   static constexpr int WACC = NCW * G * (D + (FUSED ? 2 : 0));
   static constexpr int OFF_STAGE = 0;        // 1024-byte aligned (128B swizzle)
   static constexpr int OFF_Q = NS * STAGEB;  // [NS][QB]
-  static constexpr int OFF_VW = (OFF_Q + NS * QB + 1023) / 1024 * 1024;  // VQ: [NCW][VWB]
-  static constexpr int OFF_WACC = OFF_VW + (VQ ? NCW * VWB : 0);
+  static constexpr int OFF_WACC = (OFF_Q + NS * QB + 15) / 16 * 16;
   static constexpr int OFF_P = OFF_WACC + WACC * 4;
   static constexpr int OFF_WM = OFF_P + NCW * 2 * PB;
   static constexpr int OFF_DESC = OFF_WM + 2 * NCW * G * 4;  // int4 [NS]
@@ -740,6 +782,7 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ, FUSED>::NT, 2)
   float mrun0 = -1e30f, mrun1 = -1e30f, lrun0 = 0.0f, lrun1 = 0.0f;
   float acc[S::MT][4];
   int wslot = -1;
+  int ew = kVqExpMax;  // VQ: the warp's weight exponent in this segment
   uint32_t sync_phase[3] = {0u, 0u, 0u};
   int seg = 0;     // FUSED: segments finished by this CTA
   int merges = 0;  // FUSED: units this CTA merged
@@ -773,6 +816,7 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ, FUSED>::NT, 2)
       lrun0 = lrun1 = 0.0f;
 #pragma unroll
       for (int mt = 0; mt < S::MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
+      ew = kVqExpMax;
       // the slot the previous step of this cache wrote in unit u (the evicted
       // slot, or the last appended one): stale in a tile fetched before the wait
       wslot = k < npre ? prew[k] : -1;
@@ -795,7 +839,7 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ, FUSED>::NT, 2)
         const int c = lane - CK;
         const uint4 x = __ldcg(reinterpret_cast<const uint4*>(
             reinterpret_cast<const uint8_t*>(p.V) + r * D + 16 * c));
-        *reinterpret_cast<uint4*>(Kd + S::TILEB + row * D + 16 * c) = x;
+        *reinterpret_cast<uint4*>(Kd + S::TILEB + vq_tile_off<D>(row, 16 * c)) = x;
       } else if (lane == CK + CV) {
         *reinterpret_cast<float*>(Kd + S::TILEB + S::VQT + 4 * row) =
             __ldcg(p.vs + (size_t)u * p.vs_stride + wslot);
@@ -854,70 +898,88 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ, FUSED>::NT, 2)
     const float p01 = exp2f(x01 - mn1), p11 = exp2f(x11 - mn1);
     lrun0 = lrun0 * sc0 + (p00 + p10);
     lrun1 = lrun1 * sc1 + (p01 + p11);
+    // VQ: the value MMA's weights are p * s * 2^ew in f16, ew the largest
+    // exponent (at most kVqExpMax) that keeps the warp's largest scale times
+    // 2^ew below 2^15 in every tile so far (weights p <= 1: no f16 overflow);
+    // the accumulator holds 2^ew times the values' sum, and shrinking ew
+    // rescales it (exact powers of two)
+    float sa = 0.0f, sb = 0.0f, fvq = 1.0f;
+    if constexpr (VQ) {
+      const float* scl = reinterpret_cast<const float*>(Ks + S::TILEB + S::VQT);
+      sa = sA < hi ? scl[row0 + g8] : 0.0f;
+      sb = sB < hi ? scl[row0 + g8 + 8] : 0.0f;
+      float smx = fmaxf(sa, sb);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) smx = fmaxf(smx, __shfl_xor_sync(kFull, smx, o));
+      // smx in [2^(E-127), 2^(E-126)) for its biased exponent E >= 1
+      const int en = smx > 0.0f ? min(141 - ((__float_as_int(smx) >> 23) & 0xFF), kVqExpMax)
+                                : kVqExpMax;
+      if (en < ew) {
+        fvq = en - ew >= -126 ? __int_as_float((127 + en - ew) << 23) : 0.0f;
+        ew = en;
+      }
+    }
+    const float ac0 = sc0 * fvq, ac1 = sc1 * fvq;
 #pragma unroll
     for (int mt = 0; mt < S::MT; ++mt) {
-      acc[mt][0] *= sc0;
-      acc[mt][2] *= sc0;
-      acc[mt][1] *= sc1;
-      acc[mt][3] *= sc1;
+      acc[mt][0] *= ac0;
+      acc[mt][2] *= ac0;
+      acc[mt][1] *= ac1;
+      acc[mt][3] *= ac1;
     }
 
     // P^T [8 heads][16 slots] in bf16 (hi, and the rounding remainder lo); with
-    // a quantised value cache each slot's weight carries the slot's value scale
-    {
-      float w00 = p00, w01 = p01, w10 = p10, w11 = p11;
-      if constexpr (VQ) {
-        const float* scl = reinterpret_cast<const float*>(Ks + S::TILEB + S::VQT);
-        const float sa = scl[row0 + g8], sb = scl[row0 + g8 + 8];
-        w00 *= sa;
-        w01 *= sa;
-        w10 *= sb;
-        w11 *= sb;
+    // a quantised value cache in f16, each slot's weight times its scale and 2^ew
+    if constexpr (VQ) {
+      const float pw = __int_as_float((127 + ew) << 23);
+      const float ea = sa * pw, eb = sb * pw;  // (exact)
+      const float w00 = p00 * ea, w01 = p01 * ea, w10 = p10 * eb, w11 = p11 * eb;
+      __half* Ph = reinterpret_cast<__half*>(Phi);
+      __half* Pl = reinterpret_cast<__half*>(Plo);
+      const __half a00 = __float2half_rn(w00), a01 = __float2half_rn(w01);
+      const __half a10 = __float2half_rn(w10), a11 = __float2half_rn(w11);
+      Ph[h0 * 16 + g8] = a00;
+      Ph[h1 * 16 + g8] = a01;
+      Ph[h0 * 16 + g8 + 8] = a10;
+      Ph[h1 * 16 + g8 + 8] = a11;
+      if (PSPLIT) {
+        Pl[h0 * 16 + g8] = __float2half_rn(w00 - __half2float(a00));
+        Pl[h1 * 16 + g8] = __float2half_rn(w01 - __half2float(a01));
+        Pl[h0 * 16 + g8 + 8] = __float2half_rn(w10 - __half2float(a10));
+        Pl[h1 * 16 + g8 + 8] = __float2half_rn(w11 - __half2float(a11));
       }
-      const __nv_bfloat16 a00 = __float2bfloat16_rn(w00), a01 = __float2bfloat16_rn(w01);
-      const __nv_bfloat16 a10 = __float2bfloat16_rn(w10), a11 = __float2bfloat16_rn(w11);
+    } else {
+      const __nv_bfloat16 a00 = __float2bfloat16_rn(p00), a01 = __float2bfloat16_rn(p01);
+      const __nv_bfloat16 a10 = __float2bfloat16_rn(p10), a11 = __float2bfloat16_rn(p11);
       Phi[h0 * 16 + g8] = a00;
       Phi[h1 * 16 + g8] = a01;
       Phi[h0 * 16 + g8 + 8] = a10;
       Phi[h1 * 16 + g8 + 8] = a11;
       if (PSPLIT) {
-        Plo[h0 * 16 + g8] = __float2bfloat16_rn(w00 - __bfloat162float(a00));
-        Plo[h1 * 16 + g8] = __float2bfloat16_rn(w01 - __bfloat162float(a01));
-        Plo[h0 * 16 + g8 + 8] = __float2bfloat16_rn(w10 - __bfloat162float(a10));
-        Plo[h1 * 16 + g8 + 8] = __float2bfloat16_rn(w11 - __bfloat162float(a11));
+        Plo[h0 * 16 + g8] = __float2bfloat16_rn(p00 - __bfloat162float(a00));
+        Plo[h1 * 16 + g8] = __float2bfloat16_rn(p01 - __bfloat162float(a01));
+        Plo[h0 * 16 + g8 + 8] = __float2bfloat16_rn(p10 - __bfloat162float(a10));
+        Plo[h1 * 16 + g8 + 8] = __float2bfloat16_rn(p11 - __bfloat162float(a11));
       }
     }
-    // VQ: this warp's 16 value rows (bytes) -> bf16 (exact), in the swizzled layout
-    // of a 16-row tile; the stage is then free
-    unsigned char* vw = smem + S::OFF_VW + cw * S::VWB;
+    // VQ: this thread's value words, the value MMA's A fragments before
+    // conversion.  Block mt = 4 q + i of the MMA takes row g8 + 8 h as
+    // d = 64 q + 32 h + 4 g8 + i, so one 32-bit word of a slot row holds a
+    // thread's four blocks; its slots are the fragment's columns 2 t4, 2 t4 + 1,
+    // 2 t4 + 8, 2 t4 + 9.  Then the stage is free.
+    uint32_t wv[VQ ? D / 64 : 1][2][4];
     if constexpr (VQ) {
-      // (each load of the warp covers 512 contiguous bytes of the unswizzled
-      // byte tile, lane l taking 16-byte piece i * 32 + l of the warp's rows:
-      // no two lanes of a load share a bank)
-      constexpr int CPR = D / 16;  // 16-byte pieces per value row
-      const int8_t* src = reinterpret_cast<const int8_t*>(Ks + S::TILEB) + row0 * D;
+      const unsigned char* vt = Ks + S::TILEB;
 #pragma unroll
-      for (int i = 0; i < D / 32; ++i) {
-        const int pc = i * 32 + lane, lr = pc / CPR, c16 = pc - lr * CPR;
-        const uint4 raw = *reinterpret_cast<const uint4*>(src + lr * D + 16 * c16);
-        const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
-        uint32_t o[8];
+      for (int q = 0; q < D / 64; ++q)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) vq_widen4<VQ>(wd[e], o[2 * e], o[2 * e + 1]);
-        const int cc = 2 * c16;  // first 8-column chunk of these 16 values
-        // (the lanes of a row's upper half store their two chunks in the other
-        // order, so that the eight lanes of each 128-bit store phase fall in
-        // eight different bank groups)
-        const bool swap = c16 >= CPR / 2;
-        const uint4 w0 = make_uint4(o[0], o[1], o[2], o[3]);
-        const uint4 w1 = make_uint4(o[4], o[5], o[6], o[7]);
-        const uint4 first = swap ? w1 : w0, second = swap ? w0 : w1;
-        const int ca = cc + (swap ? 1 : 0), cb = cc + (swap ? 0 : 1);
-        *reinterpret_cast<uint4*>(vw + (ca >> 3) * (16 * 128) + lr * 128 +
-                                  (((ca & 7) ^ (lr & 7)) << 4)) = first;
-        *reinterpret_cast<uint4*>(vw + (cb >> 3) * (16 * 128) + lr * 128 +
-                                  (((cb & 7) ^ (lr & 7)) << 4)) = second;
-      }
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int s = row0 + 2 * t4 + (j & 1) + 8 * (j >> 1);
+            wv[q][h][j] = *reinterpret_cast<const uint32_t*>(
+                vt + vq_tile_off<D>(s, 64 * q + 32 * h + 4 * g8));
+          }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[st]);  // stage free for refill
     }
@@ -929,18 +991,34 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ, FUSED>::NT, 2)
     const uint32_t bl1 = PSPLIT ? Plw[g8 * 8 + 4 + t4] : 0u;
 
     // values: O^T[d][head] += V^T[d][slots] P^T[slots][head]
+    if constexpr (VQ) {
 #pragma unroll
-    for (int mt = 0; mt < S::MT; ++mt) {
-      const int row = (VQ ? 0 : row0) + (lane & 7) + ((lane >> 4) << 3);
-      const int chunk = ((mt & 3) << 1) + ((lane >> 3) & 1);
-      uint32_t a[4];
-      const unsigned char* vbase = VQ ? vw + (mt >> 2) * (16 * 128) : Vs + (mt >> 2) * S::BOXB;
-      ldsm_x4_trans(a, smem_u32(vbase + row * 128 + ((chunk ^ (row & 7)) << 4)));
-      mma_bf16_16816(acc[mt], a, bh0, bh1);
-      if (PSPLIT) mma_bf16_16816(acc[mt], a, bl0, bl1);
+      for (int q = 0; q < D / 64; ++q) {
+        uint32_t r0[4], r1[4], r2[4], r3[4];
+        vq_pairs_f16<VQ>(wv[q][0][0], wv[q][0][1], r0);  // row g8, columns 2 t4, 2 t4 + 1
+        vq_pairs_f16<VQ>(wv[q][1][0], wv[q][1][1], r1);  // row g8 + 8
+        vq_pairs_f16<VQ>(wv[q][0][2], wv[q][0][3], r2);  // row g8, columns 2 t4 + 8, + 9
+        vq_pairs_f16<VQ>(wv[q][1][2], wv[q][1][3], r3);  // row g8 + 8
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t a[4] = {r0[i], r1[i], r2[i], r3[i]};
+          mma_f16_16816(acc[4 * q + i], a, bh0, bh1);
+          if (PSPLIT) mma_f16_16816(acc[4 * q + i], a, bl0, bl1);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int mt = 0; mt < S::MT; ++mt) {
+        const int row = row0 + (lane & 7) + ((lane >> 4) << 3);
+        const int chunk = ((mt & 3) << 1) + ((lane >> 3) & 1);
+        uint32_t a[4];
+        ldsm_x4_trans(a, smem_u32(Vs + (mt >> 2) * S::BOXB + row * 128 + ((chunk ^ (row & 7)) << 4)));
+        mma_bf16_16816(acc[mt], a, bh0, bh1);
+        if (PSPLIT) mma_bf16_16816(acc[mt], a, bl0, bl1);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[st]);  // stage free for refill
     }
-    __syncwarp();
-    if (!VQ && lane == 0) mbar_arrive(&empty_bar[st]);  // stage free for refill
 
     if (dsc.z & kDescLast) {
       // warp states -> shared memory -> the partial record of this segment
@@ -960,16 +1038,20 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ, FUSED>::NT, 2)
           wl[cw * G + h1] = l1;
         }
       }
+      // (VQ: the accumulator holds 2^ew times the sums, its rows in the value
+      // MMA's column order)
+      const float uvq = VQ ? __int_as_float((127 - ew) << 23) : 1.0f;
 #pragma unroll
       for (int mt = 0; mt < S::MT; ++mt) {
-        const int d = 16 * mt + g8;
+        const int d = VQ ? 64 * (mt >> 2) + 4 * g8 + (mt & 3) : 16 * mt + g8;
+        const int d8 = VQ ? d + 32 : d + 8;
         if (real0) {
-          wacc[(cw * G + h0) * D + d] = acc[mt][0];
-          wacc[(cw * G + h0) * D + d + 8] = acc[mt][2];
+          wacc[(cw * G + h0) * D + d] = acc[mt][0] * uvq;
+          wacc[(cw * G + h0) * D + d8] = acc[mt][2] * uvq;
         }
         if (real1) {
-          wacc[(cw * G + h1) * D + d] = acc[mt][1];
-          wacc[(cw * G + h1) * D + d + 8] = acc[mt][3];
+          wacc[(cw * G + h1) * D + d] = acc[mt][1] * uvq;
+          wacc[(cw * G + h1) * D + d8] = acc[mt][3] * uvq;
         }
       }
       if (!consumer_sync<S::NCW>(&sync_bar[0], sync_phase[0], lane)) {
