@@ -26,6 +26,8 @@ using he::StepParams;
 // Launch configuration of the two step engines.
 constexpr int kSimtStages = 4;    // CUDA-core engine (fp32 caches): 32-slot tiles
 constexpr int kTcStages = 2;      // tensor-core pipeline (bf16 caches): 64-slot tiles
+constexpr int kTcStagesVq = 3;    // the same with a quantised value cache (smaller stages),
+                                  // where two such CTAs and a prep CTA fit an SM
 constexpr bool kPSplit = true;    // attention weights as bf16 hi + lo parts
 // Stream CTAs that start behind the previous step's merge CTAs (a 512-thread
 // merge CTA leaves no room for a stream CTA on its SM) take this many tiles
@@ -63,6 +65,7 @@ struct Kernels {
   int fused_threads;
   int fused_rec_floats;
   int fused_stages;
+  int stages;  // ring stages of the step kernel
 };
 
 // Ring stages of the fused step: two (with the hash warp's copy of W, a third
@@ -70,6 +73,18 @@ struct Kernels {
 template <int D, int G>
 constexpr int fused_stages() {
   return 2 * (he::StreamShape<D, G, 3, false, true>::SMEM_ALLOC + 1024) <= 233472 ? 3 : 2;
+}
+
+// Ring stages of the stream kernel: kTcStagesVq for a quantised value cache
+// when two stream CTAs and one prep CTA still fit an SM's shared memory (each
+// CTA also reserves 1 KiB), else kTcStages.
+template <int D, int G, int VQ>
+constexpr int stream_stages() {
+  constexpr int kSmemPerSm = 233472;
+  return VQ && 2 * (he::StreamShape<D, G, kTcStagesVq, VQ>::SMEM_ALLOC + 1024) +
+                       he::PrepShape<D, G>::SMEM + 1024 <= kSmemPerSm
+             ? kTcStagesVq
+             : kTcStages;
 }
 
 template <int D, int G>
@@ -86,8 +101,10 @@ Kernels kernels_for() {
   k.score = reinterpret_cast<const void*>(&he::score_kernel<T, D, G>);
   k.code = reinterpret_cast<const void*>(&he::code_kernel<T, D>);
   if constexpr (std::is_same<T, bf16_t>::value) {
-    using S = he::StreamShape<D, G, kTcStages, VQ>;
-    k.step = reinterpret_cast<const void*>(&he::stream_kernel<D, G, kTcStages, kPSplit, VQ>);
+    constexpr int NS = stream_stages<D, G, VQ>();
+    using S = he::StreamShape<D, G, NS, VQ>;
+    k.step = reinterpret_cast<const void*>(&he::stream_kernel<D, G, NS, kPSplit, VQ>);
+    k.stages = NS;
     k.prep = reinterpret_cast<const void*>(&he::prep_kernel<D, G, false, VQ>);
     k.prep_mem = reinterpret_cast<const void*>(&he::prep_kernel<D, G, true, VQ>);
     k.merge = reinterpret_cast<const void*>(&he::merge_kernel<D, G, VQ>);
@@ -120,6 +137,7 @@ Kernels kernels_for() {
     k.step = reinterpret_cast<const void*>(&he::step_kernel_simt<T, D, G, kSimtStages>);
     k.step_smem = S::SMEM;
     k.step_threads = he::kThreads;
+    k.stages = kSimtStages;
     k.tile = he::kTile;
     k.rec_floats = he::Record<G, D>::FLOATS;
     k.tc = false;
@@ -743,7 +761,8 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
     const bool full = p.append_slot < 0;
     const bool ch = h->chunk > 1;
     // prep items: code slots of the budget per CTA (the chunk path: whole chunks)
-    const int item = ch ? he::chunk_item_slots(h->chunk) : he::kPrepItem;
+    const int item = ch ? he::chunk_item_slots(h->chunk, h->cfg.bits)
+                        : he::prep_item_slots(h->cfg.bits);
     int splits = full ? (h->cfg.budget + item - 1) / item : 1;
     if (splits < 1) splits = 1;
     he::UnitOut* uo = h->uo;
@@ -1066,7 +1085,7 @@ int he_launch_info(he_handle h, int32_t* ctas, int32_t* ctas_per_sm, int32_t* ti
   if (ctas) *ctas = T == 0 ? h->U : (T < h->max_ctas ? T : h->max_ctas);
   if (ctas_per_sm) *ctas_per_sm = h->ctas_per_sm;
   if (tiles) *tiles = T;
-  if (stages) *stages = h->fused ? h->kern.fused_stages : h->kern.tc ? kTcStages : kSimtStages;
+  if (stages) *stages = h->fused ? h->kern.fused_stages : h->kern.stages;
   return HE_OK;
 }
 

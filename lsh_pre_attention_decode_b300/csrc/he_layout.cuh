@@ -41,11 +41,17 @@ struct ChunkRec {
   static constexpr int FLOATS = A + 2 * G * D;
 };
 
+// Code slots a prep CTA scans per item: 16 KiB of codes at most (4096 slots
+// of up to 32 bits, 2048 of 64).
+__host__ __device__ __forceinline__ int prep_item_slots(int bits) {
+  return bits == 64 ? 2048 : 4096;
+}
+
 // Slots per prep item with chunks of c slots: a multiple of c and of 16 (so
 // that an item's codes start on a 16-byte boundary for the bulk copy).
-__host__ __device__ __forceinline__ int chunk_item_slots(int c) {
+__host__ __device__ __forceinline__ int chunk_item_slots(int c, int bits) {
   const int l = 16 * c / (c & -c);  // lcm(c, 16) for 1 <= c <= 16
-  return 4096 / l * l;
+  return prep_item_slots(bits) / l * l;
 }
 
 // Stream-K split of a step's TT tiles over NC stream CTAs, in two groups: the

@@ -164,14 +164,15 @@ constexpr int kVqExpMax = 100;
 // prep
 // ---------------------------------------------------------------------------
 constexpr int kPrepThreads = 128;  // one warp per SM sub-partition: fits beside two stream CTAs
-constexpr int kPrepItem = 4096;  // code slots scanned per CTA item
+constexpr int kPrepItem = 4096;  // code slots scanned per CTA item, at most (prep_item_slots)
+constexpr int kPrepCodeBytes = 16384;  // the item's codes in shared memory, at most
 
 template <int D, int G>
 struct PrepShape {
   static constexpr int OFF_W = 0;                         // [D][bits] bf16, <= 16 KiB
   static constexpr int OFF_X = OFF_W + D * 64 * 2;        // (G+1) vectors [D] bf16
   static constexpr int OFF_C = OFF_X + ((G + 1) * D * 2 + 15) / 16 * 16;  // the item's codes
-  static constexpr int OFF_BITS = OFF_C + kPrepItem * 8;
+  static constexpr int OFF_BITS = OFF_C + kPrepCodeBytes;
   static constexpr int OFF_RED = OFF_BITS + ((G + 1) * 64 / 32) * 4;
   static constexpr int OFF_BAR = (OFF_RED + 8 * 8 + 16 + 15) / 16 * 16;
   static constexpr int SMEM = OFF_BAR + 16;
@@ -219,7 +220,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
   uint32_t phase = 0;
   for (int it = blockIdx.x; it < nitems; it += gridDim.x, phase ^= 1u) {
     const int u = it / splits, split = it - u * splits;
-    const int item = CH ? chunk_item_slots(p.chunk) : kPrepItem;
+    const int item = CH ? chunk_item_slots(p.chunk, bits) : prep_item_slots(bits);
     const int s0 = split * item;
     const int s1 = full ? min(s0 + item, CH ? p.lbudget : p.occ) : s0;
     if (tid == 0) {
