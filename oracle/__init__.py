@@ -63,6 +63,16 @@ def _vfmt(fmt: str) -> int:
         raise ValueError(f"value format is 'int8' or 'fp8', got {fmt!r}") from None
 
 
+def _tauv(tau, bits: int):
+    """A per-bit threshold array (fp32 [bits]) from tau, or None for a scalar."""
+    if np.ndim(tau) == 0:
+        return None
+    tv = np.ascontiguousarray(tau, np.float32)
+    if tv.shape != (bits,):
+        raise ValueError(f"per-bit thresholds must have shape ({bits},), got {tv.shape}")
+    return tv
+
+
 def _ptr(a: np.ndarray | None):
     return None if a is None else a.ctypes.data_as(_vp)
 
@@ -71,7 +81,8 @@ def _ptr(a: np.ndarray | None):
 class UnitState:
     """Cache of one (batch, KV head) unit: K, V [budget][D], codes [budget]; with
     score memory, the per-slot scores A [budget] (fp32); tau: binarisation
-    threshold of every code of this unit."""
+    threshold of every code of this unit, or tauv [bits] (fp32): one threshold
+    per bit (e.g. the per-bit medians of the filled keys' projections)."""
     W: np.ndarray
     bits: int
     budget: int
@@ -86,6 +97,7 @@ class UnitState:
                                      # (then V is unused)
     chunk: int = 1                   # chunk eviction: K, V, codes hold budget + chunk - 1 rows
     chunked: bool = False            # filled by unit_fill_chunk: streams run the chunk routine
+    tauv: np.ndarray | None = None   # per-bit thresholds (then tau is unused)
 
 
 class Oracle:
@@ -97,15 +109,18 @@ class Oracle:
         lib.orc_code.restype = _u64
         lib.orc_code_many.argtypes = [_vp, _i32, _i32, _i32, _vp, _i32, _vp]
         lib.orc_code_many.restype = None
-        lib.orc_code_many_tau.argtypes = [_vp, _i32, _i32, _i32, _vp, _i32, ctypes.c_float, _vp]
+        lib.orc_code_many_tau.argtypes = [_vp, _i32, _i32, _i32, _vp, _i32, ctypes.c_float, _vp,
+                                          _vp]
+        lib.orc_median_thresholds.argtypes = [_vp, _i32, _i32, _i32, _vp, _i32, _vp]
+        lib.orc_median_thresholds.restype = None
         lib.orc_code_many_tau.restype = None
         lib.orc_most_dissimilar_score.argtypes = [_vp, _i32]
         lib.orc_most_dissimilar_score.restype = _i32
         lib.orc_unit_fill_tau.argtypes = [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _i32,
-                                          ctypes.c_float, _vp, _vp, _vp, _vp]
+                                          ctypes.c_float, _vp, _vp, _vp, _vp, _vp]
         lib.orc_unit_fill_tau.restype = None
         lib.orc_unit_stream_ext.argtypes = [_vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp,
-                                            _vp, _vp, _i32, _vp, _vp, _vp, ctypes.c_float,
+                                            _vp, _vp, _i32, _vp, _vp, _vp, ctypes.c_float, _vp,
                                             ctypes.c_float, _vp, _vp, _vp, _vp, _vp]
         lib.orc_unit_stream_ext.restype = None
         lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
@@ -117,14 +132,14 @@ class Oracle:
         lib.orc_attend_vq.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp]
         lib.orc_attend_vq.restype = None
         lib.orc_unit_fill_vq.argtypes = [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _i32,
-                                         ctypes.c_float, _i32, _vp, _vp, _vp, _vp, _vp]
+                                         ctypes.c_float, _vp, _i32, _vp, _vp, _vp, _vp, _vp]
         lib.orc_unit_fill_vq.restype = None
         lib.orc_unit_stream_vq.argtypes = [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp,
                                            _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp,
-                                           ctypes.c_float, ctypes.c_float, _vp, _vp, _vp, _vp]
+                                           ctypes.c_float, _vp, ctypes.c_float, _vp, _vp, _vp, _vp]
         lib.orc_unit_stream_vq.restype = None
         lib.orc_unit_stream_chunk.argtypes = [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp,
-                                              _vp, _vp, _i32, _vp, _vp, _vp, ctypes.c_float, _vp,
+                                              _vp, _vp, _i32, _vp, _vp, _vp, ctypes.c_float, _vp, _vp,
                                               _vp, _vp, _vp]
         lib.orc_unit_stream_chunk.restype = None
         lib.orc_group_distance.argtypes = [_vp, _i32, _u64]
@@ -148,21 +163,34 @@ class Oracle:
         self.lib.orc_projection(seed, head_dim, bits, _dtype_code(W), _ptr(W))
         return W
 
-    def code(self, x: np.ndarray, W: np.ndarray, tau: float = 0.0) -> np.ndarray:
+    def code(self, x: np.ndarray, W: np.ndarray, tau=0.0) -> np.ndarray:
         """Codes of the rows of x [n][D] (or one vector [D]) -> uint64 [n];
-        bit j = (projection > tau)."""
+        bit j = (projection > tau), or (projection_j > tau[j]) for an array of
+        one threshold per bit."""
         x2 = np.ascontiguousarray(x.reshape(-1, x.shape[-1]))
         Wc = np.ascontiguousarray(W)
         if _dtype_code(x2) != _dtype_code(Wc):
             raise TypeError("x and W must have the same element type")
         out = np.empty(x2.shape[0], np.uint64)
-        if tau == 0.0:
+        tv = _tauv(tau, Wc.shape[1])
+        if tv is None and float(tau) == 0.0:
             self.lib.orc_code_many(_ptr(x2), x2.shape[0], _dtype_code(x2), x2.shape[1], _ptr(Wc),
                                    Wc.shape[1], _ptr(out))
         else:
             self.lib.orc_code_many_tau(_ptr(x2), x2.shape[0], _dtype_code(x2), x2.shape[1],
-                                       _ptr(Wc), Wc.shape[1], float(tau), _ptr(out))
+                                       _ptr(Wc), Wc.shape[1], 0.0 if tv is not None else float(tau),
+                                       _ptr(tv), _ptr(out))
         return out
+
+    def median_thresholds(self, K: np.ndarray, W: np.ndarray) -> np.ndarray:
+        """Per-bit thresholds [bits] (fp32): the lower median of the rows'
+        projections onto each column of W (0 for no rows)."""
+        K2 = np.ascontiguousarray(K.reshape(-1, K.shape[-1]))
+        Wc = np.ascontiguousarray(W)
+        tau = np.empty(Wc.shape[1], np.float32)
+        self.lib.orc_median_thresholds(_ptr(K2), K2.shape[0], _dtype_code(K2), K2.shape[1],
+                                       _ptr(Wc), Wc.shape[1], _ptr(tau))
+        return tau
 
     # -- steps 3-4 -----------------------------------------------------------
     def group_distance(self, code_q: np.ndarray, code_slot: int) -> int:
@@ -234,25 +262,31 @@ class Oracle:
 
     # -- one (batch, KV head) unit -----------------------------------------
     def unit_fill_chunk(self, W: np.ndarray, budget: int, chunk: int, Kin: np.ndarray,
-                        Vin: np.ndarray, tau: float = 0.0) -> UnitState:
+                        Vin: np.ndarray, tau: float = 0.0, median: bool = False) -> UnitState:
         """A unit for chunk eviction: room for budget + chunk - 1 rows."""
         if budget % chunk:
             raise ValueError("the budget must be a whole number of chunks")
-        st = self.unit_fill(W, budget + chunk - 1, Kin, Vin, tau=tau)
+        st = self.unit_fill(W, budget + chunk - 1, Kin, Vin, tau=tau, median=median)
         st.budget = budget
         st.chunk = chunk
         st.chunked = True  # (c = 1 too: then the chunk routine must give the method)
         return st
 
     def unit_fill(self, W: np.ndarray, budget: int, Kin: np.ndarray, Vin: np.ndarray,
-                  tau: float = 0.0, memory: bool = False, vq=False) -> UnitState:
+                  tau: float = 0.0, memory: bool = False, vq=False,
+                  median: bool = False) -> UnitState:
         """A unit filled with the rows of Kin, Vin.  ``memory``: keep per-slot
         scores (zero after the fill) for streams with score memory.  ``vq``:
         a quantised value cache, one byte per value and one fp32 scale per row:
-        ``True`` or ``"int8"`` (int8 values), ``"fp8"`` (E4M3 codes)."""
+        ``True`` or ``"int8"`` (int8 values), ``"fp8"`` (E4M3 codes).
+        ``median``: one threshold per bit, the lower median of the filled
+        keys' projections (fixed for the unit's later steps; tau unused)."""
         n, D = Kin.shape
         if n > budget:
             raise ValueError("more fill tokens than the budget")
+        tv = self.median_thresholds(Kin, W) if median else None
+        if tv is not None:
+            tau = 0.0
         if vq:
             f = _vfmt("int8" if vq is True else vq)
             K = np.zeros((budget, D), Kin.dtype)
@@ -262,25 +296,26 @@ class Oracle:
             occ = np.zeros(1, np.int32)
             Kc, Vc, Wc = (np.ascontiguousarray(a) for a in (Kin, Vin, W))
             self.lib.orc_unit_fill_vq(_ptr(Wc), D, Wc.shape[1], _dtype_code(Kc), budget, _ptr(Kc),
-                                      _ptr(Vc), n, float(tau), f, _ptr(K), _ptr(Vq), _ptr(Vs),
-                                      _ptr(codes), _ptr(occ))
+                                      _ptr(Vc), n, float(tau), _ptr(tv), f, _ptr(K), _ptr(Vq),
+                                      _ptr(Vs), _ptr(codes), _ptr(occ))
             score = np.zeros(budget, np.float32) if memory else None
             return UnitState(Wc, Wc.shape[1], budget, K, None, codes, int(occ[0]), float(tau),
-                             score, Vq, Vs)
+                             score, Vq, Vs, tauv=tv)
         K = np.zeros((budget, D), Kin.dtype)
         V = np.zeros((budget, D), Kin.dtype)
         codes = np.zeros(budget, np.uint64)
         occ = np.zeros(1, np.int32)
         Kc, Vc, Wc = (np.ascontiguousarray(a) for a in (Kin, Vin, W))
-        if tau == 0.0:
+        if tau == 0.0 and tv is None:
             self.lib.orc_unit_fill(_ptr(Wc), D, Wc.shape[1], _dtype_code(Kc), budget, _ptr(Kc),
                                    _ptr(Vc), n, _ptr(K), _ptr(V), _ptr(codes), _ptr(occ))
         else:
             self.lib.orc_unit_fill_tau(_ptr(Wc), D, Wc.shape[1], _dtype_code(Kc), budget,
-                                       _ptr(Kc), _ptr(Vc), n, float(tau), _ptr(K), _ptr(V),
-                                       _ptr(codes), _ptr(occ))
+                                       _ptr(Kc), _ptr(Vc), n, float(tau), _ptr(tv), _ptr(K),
+                                       _ptr(V), _ptr(codes), _ptr(occ))
         score = np.zeros(budget, np.float32) if memory else None
-        return UnitState(Wc, Wc.shape[1], budget, K, V, codes, int(occ[0]), float(tau), score)
+        return UnitState(Wc, Wc.shape[1], budget, K, V, codes, int(occ[0]), float(tau), score,
+                         tauv=tv)
 
     def unit_stream(self, st: UnitState, q: np.ndarray, k: np.ndarray, v: np.ndarray,
                     want_out: np.ndarray | None = None, dist_log: bool = False,
@@ -309,19 +344,20 @@ class Oracle:
             self.lib.orc_unit_stream_chunk(_ptr(st.W), D, G, st.bits, _dtype_code(qc), st.budget,
                                            st.chunk, _ptr(st.K), _ptr(st.V), _ptr(st.codes),
                                            _ptr(occ), T, _ptr(qc), _ptr(kc), _ptr(vc),
-                                           float(st.tau), _ptr(evicted), _ptr(written), _ptr(wo),
-                                           _ptr(out))
+                                           float(st.tau), _ptr(st.tauv), _ptr(evicted),
+                                           _ptr(written), _ptr(wo), _ptr(out))
         elif st.Vq is not None:
             if st.score is None and decay != 0.0:
                 raise ValueError("score memory needs a unit filled with memory=True")
             self.lib.orc_unit_stream_vq(_ptr(st.W), D, G, st.bits, _dtype_code(qc), st.budget,
-                                        2 if st.Vq.dtype == np.uint8 else 1, _ptr(st.K), _ptr(st.Vq), _ptr(st.Vs), _ptr(st.codes),
+                                        2 if st.Vq.dtype == np.uint8 else 1, _ptr(st.K),
+                                        _ptr(st.Vq), _ptr(st.Vs), _ptr(st.codes),
                                         _ptr(st.score), _ptr(occ), T, _ptr(qc), _ptr(kc),
-                                        _ptr(vc), float(st.tau), float(decay), _ptr(evicted),
-                                        _ptr(written), _ptr(wo), _ptr(out))
+                                        _ptr(vc), float(st.tau), _ptr(st.tauv), float(decay),
+                                        _ptr(evicted), _ptr(written), _ptr(wo), _ptr(out))
             if dist_log:
                 raise ValueError("no distance log for the quantised value cache")
-        elif st.score is None and st.tau == 0.0:
+        elif st.score is None and st.tau == 0.0 and st.tauv is None:
             if decay != 0.0:
                 raise ValueError("score memory needs a unit filled with memory=True")
             self.lib.orc_unit_stream(_ptr(st.W), D, G, st.bits, _dtype_code(qc), st.budget,
@@ -334,8 +370,9 @@ class Oracle:
             self.lib.orc_unit_stream_ext(_ptr(st.W), D, G, st.bits, _dtype_code(qc), st.budget,
                                          _ptr(st.K), _ptr(st.V), _ptr(st.codes), _ptr(st.score),
                                          _ptr(occ), T, _ptr(qc), _ptr(kc), _ptr(vc),
-                                         float(st.tau), float(decay), _ptr(evicted),
-                                         _ptr(written), _ptr(wo), _ptr(out), _ptr(dl))
+                                         float(st.tau), _ptr(st.tauv), float(decay),
+                                         _ptr(evicted), _ptr(written), _ptr(wo), _ptr(out),
+                                         _ptr(dl))
         st.occupancy = int(occ[0])
         res = {"evicted": evicted, "written": written, "out": out}
         if dist_log:

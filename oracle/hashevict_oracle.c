@@ -28,7 +28,9 @@
  *   - "most dissimilar" = largest summed distance; ties go to the lowest slot;
  *   - scoring uses only the current step's distances (no accumulation);
  *     the extended stream below also takes the binarisation threshold tau
- *     (bit j = sum > tau; the method's design choices name the threshold) and a
+ *     (bit j = sum > tau; the method's design choices name the threshold; or
+ *     one threshold per bit, e.g. the per-bit medians of the filled keys'
+ *     projections, orc_median_thresholds) and a
  *     score memory gamma in [0, 1]: every resident slot s keeps a score
  *     A(s) = fmaf(gamma, A(s), d(s)) in fp32 at each scoring step, the largest
  *     A is evicted (ties: lowest slot) and a written slot starts at A = 0;
@@ -116,8 +118,11 @@ void orc_projection(uint64_t seed, int32_t D, int32_t bits, int32_t dtype, void*
 /* Steps 1-2: Gaussian projection and binarisation of one vector.             */
 /* ------------------------------------------------------------------------- */
 
-uint64_t orc_code_tau(const void* x, int32_t dtype, int32_t D, const void* W, int32_t bits,
-                      float tau) {
+/* Bit j of the code: the projection onto column j of W against the threshold
+ * of bit j, tauv[j] (one threshold per bit), or tau for every bit when tauv is
+ * NULL. */
+uint64_t orc_code_thr(const void* x, int32_t dtype, int32_t D, const void* W, int32_t bits,
+                      float tau, const float* tauv) {
   uint64_t code = 0;
   for (int32_t j = 0; j < bits; ++j) {
     float acc = 0.0f;
@@ -129,15 +134,24 @@ uint64_t orc_code_tau(const void* x, int32_t dtype, int32_t D, const void* W, in
 #endif
       acc = fmaf(xd, wdj, acc);
     }
+    float t = tauv ? tauv[j] : tau;
+#if ORACLE_MUTANT == 22 /* planted: bit j compared with the threshold of bit j + 1 */
+    if (tauv) t = tauv[(j + 1) % bits];
+#endif
 #if ORACLE_MUTANT == 2 /* planted: threshold >= instead of > */
-    if (acc >= tau) code |= (uint64_t)1 << j;
+    if (acc >= t) code |= (uint64_t)1 << j;
 #elif ORACLE_MUTANT == 11 /* planted: threshold with the wrong sign */
-    if (acc > -tau) code |= (uint64_t)1 << j;
+    if (acc > -t) code |= (uint64_t)1 << j;
 #else
-    if (acc > tau) code |= (uint64_t)1 << j;
+    if (acc > t) code |= (uint64_t)1 << j;
 #endif
   }
   return code;
+}
+
+uint64_t orc_code_tau(const void* x, int32_t dtype, int32_t D, const void* W, int32_t bits,
+                      float tau) {
+  return orc_code_thr(x, dtype, D, W, bits, tau, NULL);
 }
 
 /* The method's sign test: threshold 0. */
@@ -146,15 +160,48 @@ uint64_t orc_code(const void* x, int32_t dtype, int32_t D, const void* W, int32_
 }
 
 void orc_code_many_tau(const void* x, int32_t n, int32_t dtype, int32_t D, const void* W,
-                       int32_t bits, float tau, uint64_t* codes) {
+                       int32_t bits, float tau, const float* tauv, uint64_t* codes) {
   const char* p = (const char*)x;
   for (int32_t i = 0; i < n; ++i)
-    codes[i] = orc_code_tau(p + (size_t)i * (size_t)D * elem_bytes(dtype), dtype, D, W, bits, tau);
+    codes[i] = orc_code_thr(p + (size_t)i * (size_t)D * elem_bytes(dtype), dtype, D, W, bits,
+                            tau, tauv);
 }
 
 void orc_code_many(const void* x, int32_t n, int32_t dtype, int32_t D, const void* W,
                    int32_t bits, uint64_t* codes) {
-  orc_code_many_tau(x, n, dtype, D, W, bits, 0.0f, codes);
+  orc_code_many_tau(x, n, dtype, D, W, bits, 0.0f, NULL, codes);
+}
+
+/* Per-bit median thresholds (the method's "binarisation threshold" design
+ * choice, read as one threshold per bit that splits the cached keys in half):
+ * tau[j] = the lower median of the projections of the n keys onto column j of
+ * W (element (n - 1) / 2, counting from 0, of the ascending projections; the
+ * same fp32 fused multiply-add chain as the code), so that for distinct
+ * projections exactly floor(n / 2) keys have bit j set.  No keys: tau = 0. */
+static int cmp_float(const void* a, const void* b) {
+  const float x = *(const float*)a, y = *(const float*)b;
+  return (x > y) - (x < y);
+}
+
+void orc_median_thresholds(const void* K, int32_t n, int32_t dtype, int32_t D, const void* W,
+                           int32_t bits, float* tau) {
+  float* s = (float*)malloc(sizeof(float) * (size_t)(n > 0 ? n : 1));
+  for (int32_t j = 0; j < bits; ++j) {
+    for (int32_t i = 0; i < n; ++i) {
+      float acc = 0.0f;
+      for (int32_t d = 0; d < D; ++d)
+        acc = fmaf(elem(K, dtype, (size_t)i * (size_t)D + (size_t)d),
+                   elem(W, dtype, (size_t)d * (size_t)bits + (size_t)j), acc);
+      s[i] = acc;
+    }
+    qsort(s, (size_t)n, sizeof(float), cmp_float);
+#if ORACLE_MUTANT == 21 /* planted: the upper median */
+    tau[j] = n > 0 ? s[n / 2] : 0.0f;
+#else
+    tau[j] = n > 0 ? s[(n - 1) / 2] : 0.0f;
+#endif
+  }
+  free(s);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -254,21 +301,22 @@ void orc_attend(const void* q, const void* K, const void* V, int32_t n, int32_t 
 /* ------------------------------------------------------------------------- */
 
 void orc_unit_fill_tau(const void* W, int32_t D, int32_t bits, int32_t dtype, int32_t budget,
-                       const void* Kin, const void* Vin, int32_t n, float tau, void* K, void* V,
-                       uint64_t* codes, int32_t* occupancy) {
+                       const void* Kin, const void* Vin, int32_t n, float tau,
+                       const float* tauv, void* K, void* V, uint64_t* codes,
+                       int32_t* occupancy) {
   size_t row = (size_t)D * elem_bytes(dtype);
   (void)budget;
   memcpy(K, Kin, row * (size_t)n);
   memcpy(V, Vin, row * (size_t)n);
   for (int32_t s = 0; s < n; ++s)
-    codes[s] = orc_code_tau((const char*)Kin + (size_t)s * row, dtype, D, W, bits, tau);
+    codes[s] = orc_code_thr((const char*)Kin + (size_t)s * row, dtype, D, W, bits, tau, tauv);
   *occupancy = n;
 }
 
 void orc_unit_fill(const void* W, int32_t D, int32_t bits, int32_t dtype, int32_t budget,
                    const void* Kin, const void* Vin, int32_t n, void* K, void* V,
                    uint64_t* codes, int32_t* occupancy) {
-  orc_unit_fill_tau(W, D, bits, dtype, budget, Kin, Vin, n, 0.0f, K, V, codes, occupancy);
+  orc_unit_fill_tau(W, D, bits, dtype, budget, Kin, Vin, n, 0.0f, NULL, K, V, codes, occupancy);
 }
 
 /*
@@ -288,9 +336,9 @@ void orc_unit_fill(const void* W, int32_t D, int32_t bits, int32_t dtype, int32_
 void orc_unit_stream_ext(const void* W, int32_t D, int32_t G, int32_t bits, int32_t dtype,
                          int32_t budget, void* K, void* V, uint64_t* codes, float* score,
                          int32_t* occupancy, int32_t nsteps, const void* q, const void* k,
-                         const void* v, float tau, float decay, int32_t* evicted,
-                         int32_t* written, const uint8_t* want_out, double* out,
-                         int32_t* dist_log) {
+                         const void* v, float tau, const float* tauv, float decay,
+                         int32_t* evicted, int32_t* written, const uint8_t* want_out,
+                         double* out, int32_t* dist_log) {
   size_t row = (size_t)D * elem_bytes(dtype);
   int32_t* dist = (int32_t*)malloc(sizeof(int32_t) * (size_t)budget);
   uint64_t* code_q = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)G);
@@ -303,7 +351,7 @@ void orc_unit_stream_ext(const void* W, int32_t D, int32_t G, int32_t bits, int3
     if (*occupancy == budget) {
       /* steps 1-3: code the query heads of the group and score every slot */
       for (int32_t g = 0; g < G; ++g)
-        code_q[g] = orc_code_tau(qt + (size_t)g * row, dtype, D, W, bits, tau);
+        code_q[g] = orc_code_thr(qt + (size_t)g * row, dtype, D, W, bits, tau, tauv);
       for (int32_t s = 0; s < budget; ++s) dist[s] = orc_group_distance(code_q, G, codes[s]);
       /* step 4 */
       if (score) {
@@ -330,7 +378,7 @@ void orc_unit_stream_ext(const void* W, int32_t D, int32_t G, int32_t bits, int3
     /* step 5: the current token replaces the evicted one */
     memcpy((char*)K + (size_t)slot * row, kt, row);
     memcpy((char*)V + (size_t)slot * row, vt, row);
-    codes[slot] = orc_code_tau(kt, dtype, D, W, bits, tau);
+    codes[slot] = orc_code_thr(kt, dtype, D, W, bits, tau, tauv);
 #if ORACLE_MUTANT != 10 /* (planted when 10: the new token inherits the evicted score) */
     if (score) score[slot] = 0.0f; /* the new token has not been scored yet */
 #endif
@@ -491,15 +539,16 @@ void orc_attend_vq(const void* qv, const void* K, const uint8_t* Vq, const float
 /* Fill of a unit with a quantised value cache (format fmt): K copied, V
  * quantised row by row. */
 void orc_unit_fill_vq(const void* W, int32_t D, int32_t bits, int32_t dtype, int32_t budget,
-                      const void* Kin, const void* Vin, int32_t n, float tau, int32_t fmt,
-                      void* K, uint8_t* Vq, float* Vs, uint64_t* codes, int32_t* occupancy) {
+                      const void* Kin, const void* Vin, int32_t n, float tau,
+                      const float* tauv, int32_t fmt, void* K, uint8_t* Vq, float* Vs,
+                      uint64_t* codes, int32_t* occupancy) {
   size_t row = (size_t)D * elem_bytes(dtype);
   (void)budget;
   memcpy(K, Kin, row * (size_t)n);
   for (int32_t s = 0; s < n; ++s) {
     orc_quantize_row((const char*)Vin + (size_t)s * row, dtype, D, fmt, Vq + (size_t)s * D,
                      Vs + s);
-    codes[s] = orc_code_tau((const char*)Kin + (size_t)s * row, dtype, D, W, bits, tau);
+    codes[s] = orc_code_thr((const char*)Kin + (size_t)s * row, dtype, D, W, bits, tau, tauv);
   }
   *occupancy = n;
 }
@@ -509,9 +558,10 @@ void orc_unit_fill_vq(const void* W, int32_t D, int32_t bits, int32_t dtype, int
  * stored values decode(q) * scale. */
 void orc_unit_stream_vq(const void* W, int32_t D, int32_t G, int32_t bits, int32_t dtype,
                         int32_t budget, int32_t fmt, void* K, uint8_t* Vq, float* Vs,
-                        uint64_t* codes, float* score, int32_t* occupancy, int32_t nsteps, const void* q,
-                        const void* k, const void* v, float tau, float decay, int32_t* evicted,
-                        int32_t* written, const uint8_t* want_out, double* out) {
+                        uint64_t* codes, float* score, int32_t* occupancy, int32_t nsteps,
+                        const void* q, const void* k, const void* v, float tau,
+                        const float* tauv, float decay, int32_t* evicted, int32_t* written,
+                        const uint8_t* want_out, double* out) {
   size_t row = (size_t)D * elem_bytes(dtype);
   int32_t* dist = (int32_t*)malloc(sizeof(int32_t) * (size_t)budget);
   uint64_t* code_q = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)G);
@@ -523,7 +573,7 @@ void orc_unit_stream_vq(const void* W, int32_t D, int32_t G, int32_t bits, int32
     int32_t slot;
     if (*occupancy == budget) {
       for (int32_t g = 0; g < G; ++g)
-        code_q[g] = orc_code_tau(qt + (size_t)g * row, dtype, D, W, bits, tau);
+        code_q[g] = orc_code_thr(qt + (size_t)g * row, dtype, D, W, bits, tau, tauv);
       for (int32_t s = 0; s < budget; ++s) dist[s] = orc_group_distance(code_q, G, codes[s]);
       if (score) {
         for (int32_t s = 0; s < budget; ++s) score[s] = fmaf(decay, score[s], (float)dist[s]);
@@ -540,7 +590,7 @@ void orc_unit_stream_vq(const void* W, int32_t D, int32_t G, int32_t bits, int32
     written[t] = slot;
     memcpy((char*)K + (size_t)slot * row, kt, row);
     orc_quantize_row(vt, dtype, D, fmt, Vq + (size_t)slot * D, Vs + slot);
-    codes[slot] = orc_code_tau(kt, dtype, D, W, bits, tau);
+    codes[slot] = orc_code_thr(kt, dtype, D, W, bits, tau, tauv);
     if (score) score[slot] = 0.0f;
     if (!want_out || want_out[t])
       orc_attend_vq(qt, K, Vq, Vs, *occupancy, D, G, dtype, fmt,
@@ -565,8 +615,8 @@ void orc_unit_stream_vq(const void* W, int32_t D, int32_t G, int32_t bits, int32
 void orc_unit_stream_chunk(const void* W, int32_t D, int32_t G, int32_t bits, int32_t dtype,
                            int32_t budget, int32_t chunk, void* K, void* V, uint64_t* codes,
                            int32_t* occupancy, int32_t nsteps, const void* q, const void* k,
-                           const void* v, float tau, int32_t* evicted, int32_t* written,
-                           const uint8_t* want_out, double* out) {
+                           const void* v, float tau, const float* tauv, int32_t* evicted,
+                           int32_t* written, const uint8_t* want_out, double* out) {
   size_t row = (size_t)D * elem_bytes(dtype);
   const int32_t nch = budget / chunk;
   int32_t* dsum = (int32_t*)malloc(sizeof(int32_t) * (size_t)(nch > 0 ? nch : 1));
@@ -584,7 +634,7 @@ void orc_unit_stream_chunk(const void* W, int32_t D, int32_t G, int32_t bits, in
       evicted[t] = -1;
     } else {
       for (int32_t g = 0; g < G; ++g)
-        code_q[g] = orc_code_tau(qt + (size_t)g * row, dtype, D, W, bits, tau);
+        code_q[g] = orc_code_thr(qt + (size_t)g * row, dtype, D, W, bits, tau, tauv);
       for (int32_t i = 0; i < nch; ++i) {
         dsum[i] = 0;
         for (int32_t j = 0; j < chunk; ++j) {
@@ -617,7 +667,7 @@ void orc_unit_stream_chunk(const void* W, int32_t D, int32_t G, int32_t bits, in
     written[t] = slot;
     memcpy((char*)K + (size_t)slot * row, kt, row);
     memcpy((char*)V + (size_t)slot * row, vt, row);
-    codes[slot] = orc_code_tau(kt, dtype, D, W, bits, tau);
+    codes[slot] = orc_code_thr(kt, dtype, D, W, bits, tau, tauv);
     if (!want_out || want_out[t])
       orc_attend(qt, K, V, *occupancy, D, G, dtype, out + (n_out++) * (size_t)G * (size_t)D);
   }
@@ -632,5 +682,5 @@ void orc_unit_stream(const void* W, int32_t D, int32_t G, int32_t bits, int32_t 
                      int32_t* evicted, int32_t* written, const uint8_t* want_out, double* out,
                      int32_t* dist_log) {
   orc_unit_stream_ext(W, D, G, bits, dtype, budget, K, V, codes, NULL, occupancy, nsteps, q, k,
-                      v, 0.0f, 0.0f, evicted, written, want_out, out, dist_log);
+                      v, 0.0f, NULL, 0.0f, evicted, written, want_out, out, dist_log);
 }

@@ -134,6 +134,23 @@ def read_vquant_fp8_rows():
     return rows
 
 
+def read_median_case():
+    c = {"keys": []}
+    for tok in _lines("median_hand.txt"):
+        if tok[0] == "key":
+            c["keys"].append([float(t) for t in tok[1:]])
+        elif tok[0] in ("tau5", "tau4"):
+            c[tok[0]] = [float(t) for t in tok[1:]]
+        elif tok[0] == "codes5":
+            c["codes5"] = [int(t) for t in tok[1:]]
+        elif tok[0] == "step":
+            i_k, i_q, i_e, i_n = (tok.index(w) for w in ("k", "qcode", "evict", "newcode"))
+            c["step"] = {"q": [float(t) for t in tok[2:i_k]], "k": [float(t) for t in tok[i_k + 1:i_q]],
+                         "qcode": int(tok[i_q + 1]), "evict": int(tok[i_e + 1]),
+                         "newcode": int(tok[i_n + 1])}
+    return c
+
+
 def read_attention_cases():
     cases, cur = [], None
     for tok in _lines("attention_hand.txt"):
@@ -607,6 +624,48 @@ def check_vquant_stream(o):
             assert np.allclose(rb["out"][-1], last, rtol=0, atol=1e-5)
 
 
+def check_median_hand(o):
+    """Per-bit median thresholds (tests/golden/median_hand.txt): the lower
+    median of odd and even key counts, ties at the median, the codes under
+    them, and a step that codes its query and new key with the fill's
+    thresholds."""
+    c = read_median_case()
+    W = np.eye(4, dtype=np.float32)
+    K = f32(c["keys"])
+    assert o.median_thresholds(K, W).tolist() == c["tau5"]
+    assert o.median_thresholds(K[:4], W).tolist() == c["tau4"]
+    st = o.unit_fill(W, 5, K, K, median=True)
+    assert st.tauv.tolist() == c["tau5"]
+    assert st.codes.tolist() == c["codes5"]
+    s = c["step"]
+    assert int(o.code(f32(s["q"]), W, st.tauv)[0]) == s["qcode"]
+    r = o.unit_stream(st, f32([[s["q"]]]), f32([s["k"]]), f32([s["k"]]))
+    assert r["evicted"].tolist() == [s["evict"]]
+    assert int(st.codes[s["evict"]]) == s["newcode"]
+    assert st.tauv.tolist() == c["tau5"]  # (fixed after the fill)
+
+
+def check_median_balance(o):
+    """With distinct projections the lower-median threshold of each bit sets it
+    in exactly floor(n / 2) of the n filled keys' codes; the thresholds do not
+    depend on the keys' order; no keys gives thresholds 0."""
+    rng = np.random.default_rng(47)
+    for dtype in ("fp32", "bf16"):
+        cast = f32 if dtype == "fp32" else bf16_bits
+        for n, bits in ((1, 8), (2, 16), (7, 32), (64, 64), (65, 16)):
+            D = 16
+            W = o.projection(11 + n, D, bits, dtype)
+            K = cast(rng.standard_normal((n, D)))
+            tv = o.median_thresholds(K, W)
+            codes = o.code(K, W, tv)
+            for j in range(bits):
+                ones = int(sum((int(x) >> j) & 1 for x in codes))
+                assert ones == n // 2, (dtype, n, j, ones)
+            perm = rng.permutation(n)
+            assert np.array_equal(o.median_thresholds(K[perm], W), tv)
+    assert o.median_thresholds(f32(np.zeros((0, 4))), np.eye(4, dtype=np.float32)).tolist() == [0.0] * 4
+
+
 def check_chunk_hand(o):
     """Chunk eviction (tests/golden/chunk_hand.txt): staged appends, the chunk
     chosen, the slot written and the resident codes after every step, the rows
@@ -722,5 +781,6 @@ ALL_CHECKS = [
     check_attention_bf16_elements, check_codes_tau_hand, check_codes_tau_monotone,
     check_decay_hand, check_decay_zero_is_per_step, check_vquant_hand, check_vquant_fp8_hand,
     check_e4m3_table, check_e4m3_encode_brute, check_vquant_attention, check_vquant_stream, check_chunk_hand, check_chunk_one_is_method, check_chunk_whole_budget,
-    check_chunk_sums_brute, check_chunk_one_with_threshold_is_method,
+    check_chunk_sums_brute, check_chunk_one_with_threshold_is_method, check_median_hand,
+    check_median_balance,
 ]

@@ -27,6 +27,8 @@ MUTANTS = {
     18: "fp8 values: ties rounded away from zero",
     19: "fp8 value rows scaled by max / 256",
     20: "fp8 subnormals decoded with the implicit leading bit",
+    21: "median thresholds take the upper median",
+    22: "bit j compared with the threshold of bit j + 1",
 }
 
 
