@@ -65,9 +65,9 @@ extern "C" {
  * threshold finite; 0 <= decay <= 1; v_format HE_VFMT_*; 0 <= chunk <= 16
  * (chunk >= 2: bf16, budget % chunk == 0, decay 0, v_format HE_VFMT_ELEM);
  * engine HE_ENGINE_* (HE_ENGINE_FUSED: bf16, decay 0, v_format HE_VFMT_ELEM,
- * chunk <= 1).
- * A zero-initialised tail (threshold 0, decay 0, v_format 0, chunk 0) is the
- * method as the paper describes it.
+ * chunk <= 1); tau_mode HE_TAU_*.
+ * A zero-initialised tail (threshold 0, decay 0, v_format 0, chunk 0, engine 0,
+ * tau_mode 0) is the method as the paper describes it.
  * Rows per (batch, KV head): R = budget + chunk - 1 with chunk >= 2, else
  * R = budget; the state calls below return R rows per unit. */
 typedef struct {
@@ -111,7 +111,19 @@ typedef struct {
                         kernel (a hash warp per CTA, and the last CTA of each (batch,
                         KV head) merges it; the method only: threshold allowed, no
                         score memory, quantised values or chunks).  Same results. */
+  int32_t tau_mode;  /* HE_TAU_FIXED: every bit's threshold is `threshold`;
+                        HE_TAU_MEDIAN: one threshold per bit and (batch, KV head),
+                        the lower median of the projections of that unit's keys
+                        passed to he_fill onto column j of W (element (n - 1) / 2,
+                        counting from 0, of the ascending fp32 projections; n = 0
+                        gives 0), so that each bit splits the filled keys in half;
+                        fixed until the next he_fill.  `threshold` is then unused
+                        (the method section's binarisation-threshold design
+                        choice, read per bit) */
 } he_cfg;
+
+#define HE_TAU_FIXED 0
+#define HE_TAU_MEDIAN 1
 
 #define HE_ENGINE_PIPELINE 0
 #define HE_ENGINE_FUSED 1
@@ -126,9 +138,12 @@ typedef struct he_ctx* he_handle;
 int he_create(const he_cfg* cfg, he_handle* out);
 
 /* Fills the cache with n <= budget prompt tokens and codes their keys
- * (method steps 1-2 applied to the cached keys).  K, V: device
+ * (method steps 1-2 applied to the cached keys; with tau_mode HE_TAU_MEDIAN it
+ * first sets the per-bit thresholds from these keys, using stream-ordered
+ * scratch of up to 1 GiB, or one unit's bits * n floats if more).  K, V: device
  * [batch][kv_heads][n][head_dim].  n = 0 empties the cache (K, V may be NULL).
- * Errors: HE_EINVAL (NULL handle, n out of range, NULL or misaligned K/V), HE_ECUDA. */
+ * Errors: HE_EINVAL (NULL handle, n out of range, NULL or misaligned K/V),
+ * HE_ENOMEM (the threshold scratch), HE_ECUDA. */
 int he_fill(he_handle h, const void* K, const void* V, int32_t n, void* stream);
 
 /* One decode step (method steps 1-5, then attention).  bf16 handles launch
@@ -175,7 +190,8 @@ int he_get_projection(he_handle h, void* host_W);
 /* Codes of n vectors (method steps 1-2): x device [n][head_dim] (element type),
  * codes device [n] words of bits/8 bytes.  bit j = (sum_d x[d] W[d][j] > threshold),
  * the sum in fp32, fused multiply-add, d = 0..head_dim-1 in order from +0.
- * Errors: HE_EINVAL, HE_ECUDA. */
+ * Errors: HE_EINVAL (also for a handle with tau_mode HE_TAU_MEDIAN, whose
+ * thresholds belong to each (batch, KV head)), HE_ECUDA. */
 int he_codes(he_handle h, const void* x, int32_t n, void* codes, void* stream);
 
 /* Group-summed Hamming distances of every resident slot to the step's query
@@ -190,6 +206,12 @@ int he_scores(he_handle h, const void* q, int32_t* dist, void* stream);
  * values, or E4M3 codes).
  * Synchronises.  Errors: HE_EINVAL (NULL arguments, or another value format). */
 int he_read_vscales(he_handle h, float* host_scales);
+
+/* Binarisation thresholds, host fp32 [batch][kv_heads][bits]: the per-bit
+ * medians of a handle with tau_mode HE_TAU_MEDIAN (as of its last he_fill), else
+ * `threshold` in every entry.  Synchronises (median mode).
+ * Errors: HE_EINVAL (NULL arguments), HE_ECUDA, HE_EDEVICE. */
+int he_read_thresholds(he_handle h, float* host_tau);
 
 /* Per-slot eviction scores A of a handle with score memory (decay > 0), host
  * fp32 [batch][kv_heads][budget] (slots >= occupancy hold 0).  Synchronises.

@@ -13,6 +13,8 @@ HE_DTYPE_FP32 = 1
 HE_VFMT_ELEM = 0
 HE_VFMT_INT8 = 1
 HE_VFMT_FP8 = 2
+HE_TAU_FIXED = 0
+HE_TAU_MEDIAN = 1
 HE_ENGINE_PIPELINE = 0
 HE_ENGINE_FUSED = 1
 
@@ -24,7 +26,7 @@ class HeCfg(ctypes.Structure):
     _fields_ = [("batch", _i32), ("heads", _i32), ("kv_heads", _i32), ("head_dim", _i32),
                 ("bits", _i32), ("budget", _i32), ("dtype", _i32), ("threshold", ctypes.c_float),
                 ("seed", ctypes.c_uint64), ("decay", ctypes.c_float), ("v_format", _i32),
-                ("chunk", _i32), ("engine", _i32)]
+                ("chunk", _i32), ("engine", _i32), ("tau_mode", _i32)]
 
 
 class HashEvictError(RuntimeError):
@@ -66,6 +68,7 @@ def lib() -> ctypes.CDLL:
         L.he_attend_noalloc.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp]
         L.he_read_scores.argtypes = [_vp, _vp]
         L.he_read_vscales.argtypes = [_vp, _vp]
+        L.he_read_thresholds.argtypes = [_vp, _vp]
         L.he_set_alloc_limit.argtypes = [ctypes.c_uint64]
         L.he_wait_probe.argtypes = [_vp, ctypes.c_uint32, _vp]
         L.he_profile_start.argtypes = [_vp, _i32]
@@ -79,7 +82,7 @@ def lib() -> ctypes.CDLL:
                   "he_occupancy", "he_step_bytes", "he_launch_info", "he_recompute_count",
                   "he_attend_noalloc", "he_profile_start", "he_profile_stop", "he_read_scores",
                   "he_read_vscales", "he_set_alloc_limit", "he_wait_probe", "he_set_evict_log",
-                  "he_set_dist_log"):
+                  "he_set_dist_log", "he_read_thresholds"):
             getattr(L, n).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -178,6 +181,10 @@ def he_read_vscales(h: int, host_scales) -> None:
     _check("he_read_vscales", lib().he_read_vscales(h, _ptr(host_scales)))
 
 
+def he_read_thresholds(h: int, host_tau) -> None:
+    _check("he_read_thresholds", lib().he_read_thresholds(h, _ptr(host_tau)))
+
+
 def he_read_scores(h: int, host_scores) -> None:
     _check("he_read_scores", lib().he_read_scores(h, _ptr(host_scores)))
 
@@ -235,7 +242,7 @@ class HashEvict:
     def __init__(self, batch: int, heads: int, kv_heads: int, head_dim: int, bits: int,
                  budget: int, dtype: str = "bf16", seed: int = 0, threshold: float = 0.0,
                  decay: float = 0.0, v_format: str = "elem", chunk: int = 1,
-                 engine: str = "pipeline"):
+                 engine: str = "pipeline", tau_mode: str = "fixed"):
         self.cfg = HeCfg(batch=batch, heads=heads, kv_heads=kv_heads, head_dim=head_dim,
                          bits=bits, budget=budget,
                          dtype=HE_DTYPE_FP32 if dtype == "fp32" else HE_DTYPE_BF16,
@@ -243,7 +250,8 @@ class HashEvict:
                          v_format={"elem": HE_VFMT_ELEM, "int8": HE_VFMT_INT8,
                                    "fp8": HE_VFMT_FP8}[v_format], chunk=chunk,
                          engine={"pipeline": HE_ENGINE_PIPELINE,
-                                 "fused": HE_ENGINE_FUSED}[engine])
+                                 "fused": HE_ENGINE_FUSED}[engine],
+                         tau_mode={"fixed": HE_TAU_FIXED, "median": HE_TAU_MEDIAN}[tau_mode])
         self.v_format = v_format
         # rows per unit: the budget, plus chunk - 1 staging rows with chunk eviction
         self.rows = budget + max(chunk, 1) - 1
@@ -305,6 +313,15 @@ class HashEvict:
         occ = np.zeros(1, np.int32)
         he_read_state(self.h, K, V, codes, occ)
         return K, V, codes, int(occ[0])
+
+    def thresholds(self):
+        """Binarisation thresholds [batch][kv_heads][bits] (per-bit medians with
+        tau_mode "median", else the threshold in every entry)."""
+        import numpy as np
+        c = self.cfg
+        a = np.empty((c.batch, c.kv_heads, c.bits), np.float32)
+        he_read_thresholds(self.h, a)
+        return a
 
     def vscales(self):
         """Per-slot value scales [batch][kv_heads][budget] (quantised value cache only)."""

@@ -301,6 +301,7 @@ struct he_ctx {
   unsigned char* codes = nullptr;
   int32_t* evicted = nullptr;
   float* score = nullptr;  // per-slot scores with score memory (decay > 0), else null
+  float* tauv = nullptr;   // per-bit thresholds [U][bits] (tau_mode HE_TAU_MEDIAN), else null
   bool vq = false;         // quantised value cache: V holds byte rows (int8 or E4M3 codes),
                            // vs their scales
   float* vs = nullptr;     // [U][vs_stride]
@@ -372,7 +373,7 @@ void free_profile(he_ctx* h) {
 void free_all(he_ctx* h) {
   free_profile(h);
   void* ptrs[] = {h->K, h->V, h->W, h->codes, h->evicted, h->counters, h->err, h->partials,
-                  h->score, h->vs, h->cstar,
+                  h->score, h->vs, h->cstar, h->tauv,
                   h->uo, h->sq, h->sk, h->sv, h->sout};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -405,6 +406,7 @@ StepParams base_params(const he_ctx* h) {
   p.vs = h->vs;
   p.vs_stride = h->vs_stride;
   p.tau = h->cfg.threshold;
+  p.tauv = h->tauv;
   p.decay = h->cfg.decay;
   p.score = h->score;
   p.evlog = h->evlog;
@@ -414,8 +416,12 @@ StepParams base_params(const he_ctx* h) {
   return p;
 }
 
+// Codes (or, with proj, the projections) of rows of x; unit_tau: the rows are
+// the units' cache rows (per_unit each), coded with the handle's per-bit
+// thresholds when it has them.
 int launch_codes(he_ctx* h, const void* x, int64_t rows, int64_t per_unit, int64_t x_unit_rows,
-                 unsigned char* out, int64_t out_unit_bytes, cudaStream_t s) {
+                 unsigned char* out, int64_t out_unit_bytes, cudaStream_t s,
+                 bool unit_tau = true, float* proj = nullptr) {
   if (rows == 0) return HE_OK;
   const int vb = he::kAuxThreads / h->cfg.bits;
   int64_t blocks = (rows + vb - 1) / vb;
@@ -424,11 +430,48 @@ int launch_codes(he_ctx* h, const void* x, int64_t rows, int64_t per_unit, int64
   const void* W = h->W;
   int bits = h->cfg.bits;
   float tau = h->cfg.threshold;
-  void* args[] = {(void*)&x, (void*)&rows, (void*)&per_unit, (void*)&x_unit_rows, (void*)&W,
-                  (void*)&bits, (void*)&tau, (void*)&out, (void*)&out_unit_bytes};
+  const float* tauv = unit_tau ? h->tauv : nullptr;
+  void* args[] = {(void*)&x,    (void*)&rows, (void*)&per_unit, (void*)&x_unit_rows,
+                  (void*)&W,    (void*)&bits, (void*)&tau,      (void*)&tauv,
+                  (void*)&out,  (void*)&out_unit_bytes, (void*)&proj};
   HE_TRY(h, cudaLaunchKernel(h->kern.code, dim3((unsigned)blocks), dim3(he::kAuxThreads), args, 0,
                              s));
   return HE_OK;
+}
+
+// Scratch of the fill's key projections: at most this many bytes at a time
+// (or one unit's, if that is more).
+constexpr int64_t kMedianScratchBytes = (int64_t)1 << 30;
+
+// Per-bit lower-median thresholds of the n filled keys of every unit (n >= 1)
+// into h->tauv: the keys' projections (the code's arithmetic) into a scratch
+// buffer, a group of units at a time, then one radix select per (unit, bit).
+int fill_median_thresholds(he_ctx* h, int64_t n, cudaStream_t s) {
+  const int bits = h->cfg.bits;
+  const int64_t per_unit = (int64_t)bits * n * (int64_t)sizeof(float);
+  int64_t group = kMedianScratchBytes / per_unit;
+  if (group < 1) group = 1;
+  if (group > h->U) group = h->U;
+  float* proj = nullptr;
+  if (cudaMallocAsync((void**)&proj, (size_t)(group * per_unit), s) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return HE_ENOMEM;
+  }
+  int rc = HE_OK;
+  const size_t unit_bytes = (size_t)h->rows * h->cfg.head_dim * h->eb;
+  for (int64_t u0 = 0; u0 < h->U && rc == HE_OK; u0 += group) {
+    const int64_t g = group < h->U - u0 ? group : h->U - u0;
+    const void* x = reinterpret_cast<const unsigned char*>(h->K) + (size_t)u0 * unit_bytes;
+    rc = launch_codes(h, x, g * n, n, h->rows, nullptr, 0, s, false, proj);
+    if (rc != HE_OK) break;
+    float* tau = h->tauv + u0 * bits;
+    void* args[] = {(void*)&proj, (void*)&n, (void*)&tau};
+    if (cudaLaunchKernel((const void*)&he::median_select_kernel, dim3((unsigned)(g * bits)),
+                         dim3(he::kAuxThreads), args, 0, s) != cudaSuccess)
+      rc = fail_cuda(h, cudaGetLastError());
+  }
+  if (cudaFreeAsync(proj, s) != cudaSuccess && rc == HE_OK) rc = fail_cuda(h, cudaGetLastError());
+  return rc;
 }
 
 }  // namespace
@@ -459,6 +502,7 @@ int he_create(const he_cfg* cfg, he_handle* out) {
     return HE_EINVAL;
   if (!std::isfinite(c.threshold) || !(c.decay >= 0.0f && c.decay <= 1.0f)) return HE_EINVAL;
   if (c.chunk < 0 || c.chunk > he::kMaxChunk) return HE_EINVAL;
+  if (c.tau_mode != HE_TAU_FIXED && c.tau_mode != HE_TAU_MEDIAN) return HE_EINVAL;
   if (c.engine != HE_ENGINE_PIPELINE &&
       !(c.engine == HE_ENGINE_FUSED && c.dtype == HE_DTYPE_BF16 && c.decay == 0.0f &&
         c.v_format == HE_VFMT_ELEM && c.chunk <= 1))
@@ -581,6 +625,8 @@ int he_create(const he_cfg* cfg, he_handle* out) {
         {(void**)&h->uo, (size_t)U * sizeof(he::UnitOut)},
         {(void**)&h->score, c.decay > 0.0f ? (size_t)U * rows * sizeof(float) : 0},
         {(void**)&h->cstar, chunk > 1 ? (size_t)U * kern.chunk_floats * sizeof(float) : 0},
+        {(void**)&h->tauv,
+         c.tau_mode == HE_TAU_MEDIAN ? (size_t)U * c.bits * sizeof(float) : 0},
     };
     uint64_t total = 0;
     for (auto& a : allocs) total += a.bytes;
@@ -603,7 +649,8 @@ int he_create(const he_cfg* cfg, he_handle* out) {
         cudaMemset(h->counters, 0, (size_t)U * sizeof(int32_t)) != cudaSuccess ||
         cudaMemset(h->uo, 0, (size_t)U * sizeof(he::UnitOut)) != cudaSuccess ||
         cudaMemset(h->err, 0, sizeof(int32_t)) != cudaSuccess ||
-        cudaMemset(h->evicted, 0xFF, (size_t)U * sizeof(int32_t)) != cudaSuccess) {
+        cudaMemset(h->evicted, 0xFF, (size_t)U * sizeof(int32_t)) != cudaSuccess ||
+        (h->tauv && cudaMemset(h->tauv, 0, (size_t)U * c.bits * sizeof(float)) != cudaSuccess)) {
       rc = HE_ECUDA;
       break;
     }
@@ -667,9 +714,15 @@ int he_fill(he_handle h, const void* K, const void* V, int32_t n, void* stream) 
       HE_TRY(h, cudaMemcpy2DAsync(h->V, (size_t)h->rows * row, V, (size_t)n * row,
                                   (size_t)n * row, (size_t)h->U, cudaMemcpyDeviceToDevice, s));
     }
+    if (h->tauv) {
+      const int rc = fill_median_thresholds(h, n, s);
+      if (rc != HE_OK) return rc;
+    }
     const int rc = launch_codes(h, h->K, (int64_t)h->U * n, n, h->rows, h->codes,
                                 h->code_stride, s);
     if (rc != HE_OK) return rc;
+  } else if (h->tauv) {  // no keys: the sign test
+    HE_TRY(h, cudaMemsetAsync(h->tauv, 0, (size_t)h->U * h->cfg.bits * sizeof(float), s));
   }
   HE_TRY(h, cudaMemsetAsync(h->counters, 0, (size_t)h->U * sizeof(int32_t), s));
   if (h->uo) HE_TRY(h, cudaMemsetAsync(h->uo, 0, (size_t)h->U * sizeof(he::UnitOut), s));
@@ -915,12 +968,12 @@ int he_get_projection(he_handle h, void* host_W) {
 }
 
 int he_codes(he_handle h, const void* x, int32_t n, void* codes, void* stream) {
-  if (!h || n < 0) return HE_EINVAL;
+  if (!h || n < 0 || h->tauv) return HE_EINVAL;
   if (n > 0 && (!x || !codes || !aligned16(x) || !aligned16(codes))) return HE_EINVAL;
   if (h->sticky) return h->sticky;
   DeviceGuard g(h->device);
   return launch_codes(h, x, n, n > 0 ? n : 1, n, (unsigned char*)codes,
-                      (int64_t)n * h->code_bytes, (cudaStream_t)stream);
+                      (int64_t)n * h->code_bytes, (cudaStream_t)stream, false);
 }
 
 int he_scores(he_handle h, const void* q, int32_t* dist, void* stream) {
@@ -990,6 +1043,22 @@ int he_read_vscales(he_handle h, float* host_scales) {
   const size_t w = (size_t)h->rows * sizeof(float);
   HE_TRY(h, cudaMemcpy2D(host_scales, w, h->vs, (size_t)h->vs_stride * sizeof(float), w,
                          (size_t)h->U, cudaMemcpyDeviceToHost));
+  return HE_OK;
+}
+
+int he_read_thresholds(he_handle h, float* host_tau) {
+  if (!h || !host_tau) return HE_EINVAL;
+  const size_t n = (size_t)h->U * h->cfg.bits;
+  if (!h->tauv) {
+    for (size_t i = 0; i < n; ++i) host_tau[i] = h->cfg.threshold;
+    return HE_OK;
+  }
+  if (h->sticky) return h->sticky;
+  DeviceGuard g(h->device);
+  if (!g.ok) return fail_cuda(h, cudaErrorInvalidDevice);
+  const int rc = check_device_error(h);
+  if (rc != HE_OK) return rc;
+  HE_TRY(h, cudaMemcpy(host_tau, h->tauv, n * sizeof(float), cudaMemcpyDeviceToHost));
   return HE_OK;
 }
 

@@ -56,6 +56,7 @@ struct StepParams {
   int32_t append_slot;   // -1: cache full, evict; else the slot the token is appended to
   float qscale;          // log2(e) / sqrt(D): logits kept in base 2
   float tau;             // binarisation threshold: bit = (projection > tau)
+  const float* tauv;     // or one threshold per bit and unit [U][bits] (null: tau)
   float decay;           // score memory gamma (with score != nullptr)
   float* score;          // per-slot scores [U][budget] (null: evict by the step's distances)
   float* vs;             // int8 value cache: per-slot scales [U][vs_stride] (V holds int8 rows)
@@ -225,10 +226,12 @@ __device__ __forceinline__ uint64_t scan_codes(const unsigned char* row, int bit
 // staged in shared memory (s_q [G][D], s_k [D]) -> m.cq[], m.codek.  Bit tasks
 // are head-major (task = head * bits + j; head G is the key), packed by warp
 // ballots.  Run by the first NT threads; ends with a group barrier.
+// tauv: the unit's per-bit thresholds [bits], or null for tau on every bit.
 template <typename T, int D, int G, int NT, int BAR>
 __device__ __forceinline__ void code_queries_and_key(const float* s_q, const float* s_k,
                                                      const T* W, int bits, float tau,
-                                                     bool with_queries, Misc& m, int tid) {
+                                                     const float* tauv, bool with_queries,
+                                                     Misc& m, int tid) {
   const int lane = tid & 31, warp = tid >> 5;
   const int ntask = (G + 1) * bits;
   for (int t0 = warp * 32; t0 < ntask; t0 += NT) {
@@ -236,10 +239,11 @@ __device__ __forceinline__ void code_queries_and_key(const float* s_q, const flo
     uint32_t bit = 0;
     if (t < ntask) {
       const int h = t / bits, j = t - h * bits;
+      const float tj = tauv ? tauv[j] : tau;
       if (h == G)
-        bit = projection_bit<T, D>(s_k, W, bits, j, tau);
+        bit = projection_bit<T, D>(s_k, W, bits, j, tj);
       else if (with_queries)
-        bit = projection_bit<T, D>(s_q + h * D, W, bits, j, tau);
+        bit = projection_bit<T, D>(s_q + h * D, W, bits, j, tj);
     }
     const uint32_t word = __ballot_sync(kFull, bit);
     if (lane == 0) m.bits[t0 >> 5] = word;
@@ -273,7 +277,8 @@ __device__ __forceinline__ void unit_prologue(const StepParams& p, int u, float*
     if (lane == 0) m.lnew[g] = a * p.qscale;
   }
   code_queries_and_key<T, D, G, NT, BAR>(s_q, s_k, reinterpret_cast<const T*>(p.W), p.bits,
-                                         p.tau, p.append_slot < 0, m, tid);
+                                         p.tau, p.tauv ? p.tauv + (size_t)u * p.bits : nullptr,
+                                         p.append_slot < 0, m, tid);
 }
 
 // Local eviction candidate over slots [lo, hi) of unit u -> m.cand_slot/dist;
@@ -514,12 +519,16 @@ constexpr int kAuxThreads = 256;
 // Codes of rows of x (method steps 1-2).  Row r (r < rows) is vector
 // (r / per_unit, r % per_unit) at x + ((r / per_unit) * x_unit_rows + r % per_unit) * D;
 // its code goes to out + (r / per_unit) * out_unit_bytes + (r % per_unit) * bits/8.
+// Bit j's threshold: tauv[(r / per_unit) * bits + j], or tau with tauv null.
+// With proj non-null the kernel writes the projections instead of the codes:
+// proj[((r / per_unit) * bits + j) * per_unit + r % per_unit] (fp32).
 template <typename T, int D>
 __global__ void __launch_bounds__(kAuxThreads) code_kernel(const T* __restrict__ x, int64_t rows,
                                                            int64_t per_unit, int64_t x_unit_rows,
                                                            const T* __restrict__ W, int bits,
-                                                           float tau, unsigned char* out,
-                                                           int64_t out_unit_bytes) {
+                                                           float tau, const float* tauv,
+                                                           unsigned char* out,
+                                                           int64_t out_unit_bytes, float* proj) {
   __shared__ float xs[kAuxThreads / 8][D];  // up to 32 vectors (bits = 8)
   __shared__ uint32_t sbits[kAuxThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -537,18 +546,78 @@ __global__ void __launch_bounds__(kAuxThreads) code_kernel(const T* __restrict__
     }
     __syncthreads();
     const int vi = tid / bits, j = tid - vi * bits;
-    const uint32_t bit = (r0 + vi < rows) ? projection_bit<T, D>(xs[vi], W, bits, j, tau) : 0u;
-    const uint32_t word = __ballot_sync(kFull, bit);
-    if (lane == 0) sbits[warp] = word;
-    __syncthreads();
-    if (tid < vb && r0 + tid < rows) {
-      const int64_t r = r0 + tid;
-      const int64_t unit = r / per_unit, s = r - unit * per_unit;
-      store_code(out + unit * out_unit_bytes + s * (bits >> 3), bits,
-                 code_from_bits(sbits, bits, tid));
+    const int64_t r = r0 + vi;
+    if (proj != nullptr) {
+      if (r < rows) {
+        const int64_t unit = r / per_unit, s = r - unit * per_unit;
+        proj[(unit * bits + j) * per_unit + s] = projection_value<T, D>(xs[vi], W, bits, j);
+      }
+    } else {
+      float tj = tau;
+      if (tauv != nullptr && r < rows) tj = tauv[(r / per_unit) * bits + j];
+      const uint32_t bit = r < rows ? projection_bit<T, D>(xs[vi], W, bits, j, tj) : 0u;
+      const uint32_t word = __ballot_sync(kFull, bit);
+      if (lane == 0) sbits[warp] = word;
+      __syncthreads();
+      if (tid < vb && r0 + tid < rows) {
+        const int64_t r2 = r0 + tid;
+        const int64_t unit = r2 / per_unit, s = r2 - unit * per_unit;
+        store_code(out + unit * out_unit_bytes + s * (bits >> 3), bits,
+                   code_from_bits(sbits, bits, tid));
+      }
     }
     __syncthreads();
   }
+}
+
+// Order-preserving map of fp32 bit patterns to unsigned integers (a negative
+// value's bits are complemented, a non-negative one gets its sign bit set).
+__device__ __forceinline__ uint32_t float_order_key(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float float_from_order_key(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Per-bit lower-median thresholds: CTA c takes row c of proj ([rows][n] fp32,
+// the n keys' projections onto one column of W) and writes element (n - 1) / 2
+// of its ascending order to tau[c], by a radix select on the order-preserving
+// keys (four passes of 8 bits, a shared-memory histogram each).  n >= 1.
+static __global__ void __launch_bounds__(kAuxThreads)
+    median_select_kernel(const float* __restrict__ proj, int64_t n, float* tau) {
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t s_prefix, s_rank;
+  const int tid = threadIdx.x;
+  const float* row = proj + (size_t)blockIdx.x * n;
+  uint32_t prefix = 0, rank = (uint32_t)((n - 1) / 2);
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = tid; i < 256; i += kAuxThreads) hist[i] = 0;
+    __syncthreads();
+    for (int64_t i = tid; i < n; i += kAuxThreads) {
+      const uint32_t k = float_order_key(__ldcg(row + i));
+      // (keys that agree with the digits chosen so far)
+      if (pass == 0 || (k >> (shift + 8)) == (prefix >> (shift + 8)))
+        atomicAdd(&hist[(k >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t c = 0;
+      int b = 0;
+      for (; b < 255; ++b) {
+        if (c + hist[b] > rank) break;
+        c += hist[b];
+      }
+      s_rank = rank - c;
+      s_prefix = prefix | ((uint32_t)b << shift);
+    }
+    __syncthreads();
+    prefix = s_prefix;
+    rank = s_rank;
+    __syncthreads();
+  }
+  if (tid == 0) tau[blockIdx.x] = float_from_order_key(prefix);
 }
 
 // Group-summed distances of every resident slot to the step's query codes
@@ -566,7 +635,9 @@ __global__ void __launch_bounds__(kAuxThreads) score_kernel(const StepParams p, 
   for (int i = tid; i < D; i += kAuxThreads) s_k[i] = 0.0f;
   __syncthreads();
   code_queries_and_key<T, D, G, kAuxThreads, 0>(s_q, s_k, reinterpret_cast<const T*>(p.W),
-                                                p.bits, p.tau, true, m, tid);
+                                                p.bits, p.tau,
+                                                p.tauv ? p.tauv + (size_t)u * p.bits : nullptr,
+                                                true, m, tid);
   uint64_t cq[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) cq[g] = m.cq[g];

@@ -110,13 +110,19 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 // (exact copies of the stored elements).
 // ---------------------------------------------------------------------------
 template <typename T, int D>
-__device__ __forceinline__ uint32_t projection_bit(const float* __restrict__ x,
-                                                   const T* __restrict__ W, int bits, int j,
-                                                   float tau) {
+__device__ __forceinline__ float projection_value(const float* __restrict__ x,
+                                                  const T* __restrict__ W, int bits, int j) {
   float acc = 0.0f;
 #pragma unroll 16
   for (int d = 0; d < D; ++d) acc = __fmaf_rn(x[d], ldg_f32(W + (size_t)d * bits + j), acc);
-  return acc > tau ? 1u : 0u;
+  return acc;
+}
+
+template <typename T, int D>
+__device__ __forceinline__ uint32_t projection_bit(const float* __restrict__ x,
+                                                   const T* __restrict__ W, int bits, int j,
+                                                   float tau) {
+  return projection_value<T, D>(x, W, bits, j) > tau ? 1u : 0u;
 }
 
 // Extract the `bits`-bit code number `idx` from a packed bit string (32-bit words).

@@ -96,12 +96,15 @@ __device__ __forceinline__ float row_dot_s(const float* xs, const uint32_t (&b)[
 // are exact, so only that order matters).  Lane j owns bit j (and j + 32 for
 // 64-bit codes).  xs: the vectors as fp32 [NV][D] (exact copies of the bf16
 // elements) and Ws: W [D][bits] (bf16), both in shared memory.
+// tauv: per-bit thresholds [bits] (null: tau on every bit).
 template <int D, int NV>
 __device__ __forceinline__ void hash_codes(const float* xs, const uint16_t* Ws, int bits,
-                                           float tau, int lane, uint64_t (&code)[NV]) {
+                                           float tau, const float* tauv, int lane,
+                                           uint64_t (&code)[NV]) {
   const bool two = bits == 64;
   const bool ok0 = lane < bits;
   const int j0 = ok0 ? lane : 0, j1 = two ? lane + 32 : 0;
+  const float t0 = tauv ? __ldg(tauv + j0) : tau, t1 = tauv && two ? __ldg(tauv + j1) : tau;
   float a0[NV], a1[NV];
 #pragma unroll
   for (int v = 0; v < NV; ++v) a0[v] = a1[v] = 0.0f;
@@ -130,8 +133,8 @@ __device__ __forceinline__ void hash_codes(const float* xs, const uint16_t* Ws, 
   }
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
-    const uint32_t lo = __ballot_sync(kFull, ok0 && a0[v] > tau);
-    const uint32_t hi = __ballot_sync(kFull, two && a1[v] > tau);
+    const uint32_t lo = __ballot_sync(kFull, ok0 && a0[v] > t0);
+    const uint32_t hi = __ballot_sync(kFull, two && a1[v] > t1);
     code[v] = (uint64_t)lo | ((uint64_t)hi << 32);
   }
 }
@@ -232,7 +235,8 @@ __device__ void hash_warp(const StepParams& p, int sb, int se, volatile int32_t*
             make_float2(bf16_lo(w[i]), bf16_hi(w[i]));
     }
     __syncwarp();
-    hash_codes<D, G + 1>(xs, Ws, p.bits, p.tau, lane, code);
+    hash_codes<D, G + 1>(xs, Ws, p.bits, p.tau,
+                         p.tauv ? p.tauv + (size_t)u * p.bits : nullptr, lane, code);
     uint32_t kw[D / 64];
     load_row_words<D>(reinterpret_cast<const uint16_t*>(p.k) + (size_t)u * D, kw, lane);
 #pragma unroll

@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
         for (int d = 0; d < D; ++d)
           acc = __fmaf_rn(__uint_as_float((uint32_t)x[d] << 16),
                           __uint_as_float((uint32_t)Ws[d * bits + jj] << 16), acc);
-        bit = acc > p.tau ? 1u : 0u;
+        bit = acc > (p.tauv ? __ldg(p.tauv + (size_t)u * bits + jj) : p.tau) ? 1u : 0u;
       }
       const uint32_t word = __ballot_sync(kFull, bit);
       if (lane == 0) sbits[t0 >> 5] = word;

@@ -42,22 +42,27 @@ class GpuRun:
     prof: dict | None = None   # summed kernel times of the library's timing mode
 
 
-def make_handle(w: synth.Workload, layer: int = 0, threshold: float = 0.0, decay: float = 0.0,
+def make_handle(w: synth.Workload, layer: int = 0, threshold=0.0, decay: float = 0.0,
                 v_format: str = "elem", chunk: int = 1, engine: str = "pipeline"):
+    """threshold: a float, or "median" for the per-bit median thresholds."""
     from lsh_pre_attention_decode_b300 import HashEvict
+    median = threshold == "median"
     return HashEvict(w.batch, w.heads, w.kv_heads, w.head_dim, w.bits, w.budget, w.dtype,
-                     seed=w.projection_seed(layer), threshold=threshold, decay=decay,
-                     v_format=v_format, chunk=chunk, engine=engine)
+                     seed=w.projection_seed(layer), threshold=0.0 if median else threshold,
+                     decay=decay, v_format=v_format, chunk=chunk, engine=engine,
+                     tau_mode="median" if median else "fixed")
 
 
 def run_gpu(w: synth.Workload, fill_n: int, steps: int, out_steps=(), layer: int = 0,
             device_gen: bool = False, read_state: bool = False, batch_tokens: int = 256,
-            profile: bool = False, threshold: float = 0.0, decay: float = 0.0,
+            profile: bool = False, threshold=0.0, decay: float = 0.0,
             v_format: str = "elem", chunk: int = 1, engine: str = "pipeline") -> GpuRun:
     """Fill with prompt tokens [0, fill_n), then stream tokens fill_n .. fill_n+steps-1
     (generated batch_tokens at a time).  With decay > 0 the returned state also
     holds the per-slot scores; with a quantised value cache (v_format "int8" or
-    "fp8"), V holds the byte rows and the value scales follow; chunk > 1: chunk eviction (state rows budget + chunk - 1)."""
+    "fp8"), V holds the byte rows and the value scales follow; with threshold
+    "median" the per-bit thresholds follow; chunk > 1: chunk eviction (state
+    rows budget + chunk - 1)."""
     import torch
     out_steps = set(out_steps)
     he = make_handle(w, layer, threshold, decay, v_format, chunk, engine)
@@ -98,7 +103,8 @@ def run_gpu(w: synth.Workload, fill_n: int, steps: int, out_steps=(), layer: int
         state = he.state() if read_state else None
         if read_state:
             state = state + (he.scores() if decay > 0.0 else None,
-                             he.vscales() if v_format != "elem" else None)
+                             he.vscales() if v_format != "elem" else None,
+                             he.thresholds() if threshold == "median" else None)
         return GpuRun(evicted, outs, state, prof)
     finally:
         he.close()
@@ -115,20 +121,23 @@ class OracleRun:
     score: np.ndarray | None = None  # per-slot scores (score memory only)
     Vq: np.ndarray | None = None     # quantised value cache: byte rows ...
     Vs: np.ndarray | None = None     # ... and scales
+    tauv: np.ndarray | None = None   # per-bit median thresholds
 
 
 def run_oracle_unit(w: synth.Workload, b: int, j: int, fill_n: int, steps: int, out_steps=(),
-                    layer: int = 0, threshold: float = 0.0, decay: float = 0.0,
+                    layer: int = 0, threshold=0.0, decay: float = 0.0,
                     v_format: str = "elem", chunk: int = 1) -> OracleRun:
     o = oracle.load()
+    median = threshold == "median"
+    tau = 0.0 if median else threshold
     W = o.projection(w.projection_seed(layer), w.head_dim, w.bits, w.dtype)
     Kin = synth.host_unit_kv(w, "key", b, j, 0, fill_n, layer)
     Vin = synth.host_unit_kv(w, "value", b, j, 0, fill_n, layer)
     if chunk > 1:
-        st = o.unit_fill_chunk(W, w.budget, chunk, Kin, Vin, tau=threshold)
+        st = o.unit_fill_chunk(W, w.budget, chunk, Kin, Vin, tau=tau, median=median)
     else:
-        st = o.unit_fill(W, w.budget, Kin, Vin, tau=threshold, memory=decay > 0.0,
-                         vq=False if v_format == "elem" else v_format)
+        st = o.unit_fill(W, w.budget, Kin, Vin, tau=tau, memory=decay > 0.0,
+                         vq=False if v_format == "elem" else v_format, median=median)
     q = synth.host_unit_queries(w, b, j, fill_n, steps, layer)
     k = synth.host_unit_kv(w, "key", b, j, fill_n, steps, layer)
     v = synth.host_unit_kv(w, "value", b, j, fill_n, steps, layer)
@@ -137,11 +146,11 @@ def run_oracle_unit(w: synth.Workload, b: int, j: int, fill_n: int, steps: int, 
         want[s] = 1
     r = o.unit_stream(st, q, k, v, want_out=want, decay=decay)
     return OracleRun(r["evicted"], r["out"], st.codes, st.K, st.V, st.occupancy, st.score,
-                     st.Vq, st.Vs)
+                     st.Vq, st.Vs, st.tauv)
 
 
 def run_oracle_units(w, units, fill_n, steps, out_steps=(), layer=0, threads=8,
-                     threshold: float = 0.0, decay: float = 0.0, v_format: str = "elem",
+                     threshold=0.0, decay: float = 0.0, v_format: str = "elem",
                      chunk: int = 1):
     """Oracle over several (b, j) units in parallel threads (ctypes releases the GIL)."""
     with cf.ThreadPoolExecutor(max_workers=threads) as ex:
@@ -177,6 +186,8 @@ def compare(w: synth.Workload, g: GpuRun, orc: dict, out_steps=(), check_state: 
                 assert np.array_equal(g.state[5][b, j], r.Vs), f"value scales ({b},{j})"
             else:
                 assert np.array_equal(V[b, j], r.V), f"V ({b},{j})"
+            if r.tauv is not None:  # per-bit median thresholds, exactly
+                assert np.array_equal(g.state[6][b, j], r.tauv), f"thresholds ({b},{j})"
     assert worst_max <= MAX_ABS_TOL, f"max-abs error {worst_max}"
     assert worst_mean <= MEAN_ABS_TOL, f"mean-abs error {worst_mean}"
     return worst_max, worst_mean
@@ -191,12 +202,12 @@ def compare(w: synth.Workload, g: GpuRun, orc: dict, out_steps=(), check_state: 
 class B2BRun:
     evicted: dict   # layer -> [total steps][batch][kv_heads] from the device eviction log
     outs: dict      # (layer, step) -> out [batch][heads][D] float32
-    states: dict    # layer -> (K, V, codes, occupancy, vscales or None, scores or None)
+    states: dict    # layer -> (K, V, codes, occupancy, vscales, scores, thresholds or None)
     tokens: list    # per layer step -> token index (the stream each layer saw)
 
 
 def run_gpu_b2b(w: synth.Workload, fill_n: int, tokens: int, out_steps=(), layers: int = 1,
-                graph: bool = False, replays: int = 2, warm: int = 0, threshold: float = 0.0,
+                graph: bool = False, replays: int = 2, warm: int = 0, threshold=0.0,
                 decay: float = 0.0, v_format: str = "elem", chunk: int = 1,
                 hold_ms: float = 20.0, engine: str = "pipeline") -> B2BRun:
     """Fill `layers` independent caches with prompt tokens [0, fill_n), then
@@ -293,7 +304,8 @@ def run_gpu_b2b(w: synth.Workload, fill_n: int, tokens: int, out_steps=(), layer
             he = handles[layer]
             st = he.state()
             states[layer] = st + (he.vscales() if v_format != "elem" else None,
-                                  he.scores() if decay > 0.0 else None)
+                                  he.scores() if decay > 0.0 else None,
+                                  he.thresholds() if threshold == "median" else None)
         return B2BRun(evicted, res_outs, states, tok_of)
     finally:
         for he in handles:
@@ -301,12 +313,14 @@ def run_gpu_b2b(w: synth.Workload, fill_n: int, tokens: int, out_steps=(), layer
 
 
 def oracle_b2b(w: synth.Workload, units, fill_n: int, tok_of, out_steps=(), layer: int = 0,
-               threshold: float = 0.0, decay: float = 0.0, v_format: str = "elem",
+               threshold=0.0, decay: float = 0.0, v_format: str = "elem",
                chunk: int = 1, threads: int = 8) -> dict:
     """The oracle over the token sequence tok_of (token indices, repeats
     allowed) for the given (b, j) units of one layer."""
     o = oracle.load()
     W = o.projection(w.projection_seed(layer), w.head_dim, w.bits, w.dtype)
+    median = threshold == "median"
+    tau = 0.0 if median else threshold
     lo, hi = min(tok_of), max(tok_of) + 1
     sel = np.asarray(tok_of) - lo
     want = np.zeros(len(tok_of), np.uint8)
@@ -318,16 +332,16 @@ def oracle_b2b(w: synth.Workload, units, fill_n: int, tok_of, out_steps=(), laye
         Kin = synth.host_unit_kv(w, "key", b, j, 0, fill_n, layer)
         Vin = synth.host_unit_kv(w, "value", b, j, 0, fill_n, layer)
         if chunk > 1:
-            st = o.unit_fill_chunk(W, w.budget, chunk, Kin, Vin, tau=threshold)
+            st = o.unit_fill_chunk(W, w.budget, chunk, Kin, Vin, tau=tau, median=median)
         else:
-            st = o.unit_fill(W, w.budget, Kin, Vin, tau=threshold, memory=decay > 0.0,
-                             vq=False if v_format == "elem" else v_format)
+            st = o.unit_fill(W, w.budget, Kin, Vin, tau=tau, memory=decay > 0.0,
+                             vq=False if v_format == "elem" else v_format, median=median)
         q = synth.host_unit_queries(w, b, j, lo, hi - lo, layer)[sel]
         k = synth.host_unit_kv(w, "key", b, j, lo, hi - lo, layer)[sel]
         v = synth.host_unit_kv(w, "value", b, j, lo, hi - lo, layer)[sel]
         r = o.unit_stream(st, q, k, v, want_out=want, decay=decay)
         return OracleRun(r["evicted"], r["out"], st.codes, st.K, st.V, st.occupancy, st.score,
-                         st.Vq, st.Vs)
+                         st.Vq, st.Vs, st.tauv)
 
     with cf.ThreadPoolExecutor(max_workers=threads) as ex:
         futs = {u: ex.submit(one, u) for u in units}
@@ -338,7 +352,7 @@ def compare_b2b(w: synth.Workload, g: B2BRun, layer: int, orc: dict, out_steps=(
     """Every logged eviction bit-exact, the final cache state of each unit
     byte-exact, kept outputs within the tolerance."""
     out_steps = sorted(out_steps)
-    K, V, codes, occ, vs, sc = g.states[layer]
+    K, V, codes, occ, vs, sc, tv = g.states[layer]
     worst_max = worst_mean = 0.0
     for (b, j), r in orc.items():
         ge = g.evicted[layer][:, b, j]
@@ -357,6 +371,8 @@ def compare_b2b(w: synth.Workload, g: B2BRun, layer: int, orc: dict, out_steps=(
             assert np.array_equal(V[b, j], r.V), f"V ({b},{j})"
         if r.score is not None:
             assert np.array_equal(sc[b, j], r.score), f"scores ({b},{j})"
+        if r.tauv is not None:
+            assert np.array_equal(tv[b, j], r.tauv), f"thresholds ({b},{j})"
         for i, s in enumerate(out_steps):
             got = g.outs[(layer, s)][b, j * w.group:(j + 1) * w.group].astype(np.float64)
             err = np.abs(got - r.outs[i])

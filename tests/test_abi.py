@@ -71,7 +71,8 @@ def cfg(**kw):
                                  dict(engine=2), dict(engine=-1), dict(engine=1, dtype=1),
                                  dict(engine=1, decay=0.5), dict(engine=1, v_format=1),
                                  dict(engine=1, v_format=2),
-                                 dict(engine=1, chunk=4, budget=256)])
+                                 dict(engine=1, chunk=4, budget=256), dict(tau_mode=2),
+                                 dict(tau_mode=-1)])
 def test_create_rejects_bad_configs(L, bad):
     h = ctypes.c_void_p()
     assert L.he_create(ctypes.byref(cfg(**bad)), ctypes.byref(h)) == -1

@@ -125,6 +125,16 @@ def test_score_memory_back_to_back(graph):
               out_steps=[0, 8, 79])
 
 
+@pytest.mark.parametrize("graph", [False, True])
+def test_median_thresholds_back_to_back(graph):
+    w = small(batch=2, budget=700, prompt=1500, decode=8)
+    if graph:
+        check(w, w.budget, 64, all_units(w), graph=True, replays=2, threshold="median",
+              out_steps=[64, 127])
+    else:
+        check(w, w.budget - 8, 80, all_units(w), threshold="median", out_steps=[0, 8, 79])
+
+
 def test_other_shapes_back_to_back():
     """G = 8 with D = 64 and 16-bit codes, G = 1; two caches in turn."""
     w = small(batch=2, heads=64, head_dim=64, bits=16, budget=500, prompt=1100, decode=8)

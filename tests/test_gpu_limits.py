@@ -45,3 +45,21 @@ def test_long_unit():
     g = run_gpu(w, w.budget, steps, out_steps, device_gen=True)
     orc = run_oracle_units(w, [(0, 0)], w.budget, steps, out_steps)
     compare(w, g, orc, out_steps)
+
+
+def test_median_thresholds_in_several_scratch_groups():
+    """Per-bit medians of 17 units of 2^18 filled keys at 64-bit codes: the
+    fill's projection scratch (64 x 2^18 floats per unit, 1 GiB at most at a
+    time) takes two groups of units.  The thresholds of a unit of each group
+    and its codes against the oracle."""
+    import oracle
+    w = synth.WORKLOADS["llama8b_b8"].with_(batch=17, heads=4, kv_heads=1, bits=64,
+                                            budget=1 << 18, prompt=(1 << 18) + 8)
+    g = run_gpu(w, w.budget, 0, (), read_state=True, device_gen=True, threshold="median")
+    o = oracle.load()
+    W = o.projection(w.projection_seed(), w.head_dim, w.bits, w.dtype)
+    for b in (0, 16):
+        K = synth.host_unit_kv(w, "key", b, 0, 0, w.budget)
+        tv = o.median_thresholds(K, W)
+        assert np.array_equal(g.state[6][b, 0], tv), b
+        assert np.array_equal(g.state[2][b, 0, :4096].astype(np.uint64), o.code(K[:4096], W, tv))

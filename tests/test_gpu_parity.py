@@ -107,7 +107,9 @@ def test_scores_bit_exact():
                                               (16, 9000, {}), (32, 5000, {"decay": 0.5}),
                                               (32, 4096, {"threshold": 0.5}),
                                               (32, 4096, {"v_format": "int8"}),
-                                              (32, 4096, {"v_format": "fp8"})])
+                                              (32, 4096, {"v_format": "fp8"}),
+                                              (32, 4096, {"threshold": "median"}),
+                                              (64, 9000, {"threshold": "median"})])
 def test_step_distances_bit_exact(bits, budget, opt):
     """The group-summed Hamming distances that the step's own scan computes
     (method step 3, the codes/eviction kernel of every step), logged on the
@@ -138,8 +140,9 @@ def test_step_distances_bit_exact(bits, budget, opt):
     for b in range(w.batch):
         for j in range(w.kv_heads):
             st = o.unit_fill(W, w.budget, synth.host_unit_kv(w, "key", b, j, 0, w.budget),
-                             synth.host_unit_kv(w, "value", b, j, 0, w.budget), tau=tau,
-                             memory=decay > 0.0)
+                             synth.host_unit_kv(w, "value", b, j, 0, w.budget),
+                             tau=0.0 if tau == "median" else tau, memory=decay > 0.0,
+                             median=tau == "median")
             r = o.unit_stream(st, synth.host_unit_queries(w, b, j, w.budget, steps),
                               synth.host_unit_kv(w, "key", b, j, w.budget, steps),
                               synth.host_unit_kv(w, "value", b, j, w.budget, steps),
