@@ -74,6 +74,9 @@ def parse_args(argv=None):
                     help="shortest timed region of each per_config workload")
     ap.add_argument("--threshold", type=float, default=0.0,
                     help="binarisation threshold tau (0: the sign test of the method)")
+    ap.add_argument("--tau-mode", choices=["fixed", "median"], default="fixed",
+                    help="median: one threshold per bit and (batch, KV head), the lower "
+                         "median of the filled keys' projections (--threshold unused)")
     ap.add_argument("--decay", type=float, default=0.0,
                     help="score memory gamma (0: the step's own distances, the method)")
     ap.add_argument("--v-format", choices=["elem", "int8", "fp8"], default="elem",
@@ -213,6 +216,7 @@ def config_of(w: synth.Workload, opts: dict, extra=None):
     c = {"workload": f"{w.name}: {w.description}" + (
             f"; threshold {opts.get('threshold')}, score memory {opts.get('decay')}"
             if (opts.get("threshold") or opts.get("decay")) else "") + (
+            "; per-bit median thresholds" if opts.get("tau_mode") == "median" else "") + (
             f"; {opts.get('v_format')} value cache"
             if opts.get("v_format", "elem") != "elem" else "") + (
             f"; chunk eviction, chunks of {chunk} slots" if chunk > 1 else "") + (
@@ -236,6 +240,7 @@ def config_of(w: synth.Workload, opts: dict, extra=None):
 
 def run_cpu_baseline(w: synth.Workload, target_s: float, steps: int | None = None,
                      threads: int | None = None, threshold: float = 0.0, decay: float = 0.0,
+                     tau_mode: str = "fixed",
                      v_format: str = "elem", chunk: int = 1):
     """Times the CPU oracle, as it stands, on a bounded sample of the workload.
 
@@ -262,10 +267,11 @@ def run_cpu_baseline(w: synth.Workload, target_s: float, steps: int | None = Non
         b, j = u
         K0 = synth.host_unit_kv(w, "key", b, j, 0, w.budget)
         V0 = synth.host_unit_kv(w, "value", b, j, 0, w.budget)
+        median = tau_mode == "median"
         if chunk > 1:
-            return o.unit_fill_chunk(W, w.budget, chunk, K0, V0, tau=threshold)
+            return o.unit_fill_chunk(W, w.budget, chunk, K0, V0, tau=threshold, median=median)
         return o.unit_fill(W, w.budget, K0, V0, tau=threshold, memory=decay > 0.0,
-                           vq=False if v_format == "elem" else v_format)
+                           vq=False if v_format == "elem" else v_format, median=median)
 
     def run(u, st, t0, n):
         b, j = u
@@ -354,7 +360,8 @@ def measure(w: synth.Workload, opts: dict, L: int, min_s: float, min_steps: int,
         he = HashEvict(w.batch, w.heads, w.kv_heads, w.head_dim, w.bits, w.budget, w.dtype,
                        seed=w.projection_seed(layer), threshold=opts.get("threshold", 0.0),
                        decay=opts.get("decay", 0.0), v_format=opts.get("v_format", "elem"),
-                       chunk=chunk, engine=opts.get("engine", "pipeline"))
+                       chunk=chunk, engine=opts.get("engine", "pipeline"),
+                       tau_mode=opts.get("tau_mode", "fixed"))
         K = synth.gpu_kv(w, "key", 0, w.budget, layer)
         V = synth.gpu_kv(w, "value", 0, w.budget, layer)
         he.fill(K, V)
@@ -571,8 +578,7 @@ def measure(w: synth.Workload, opts: dict, L: int, min_s: float, min_steps: int,
             "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
             # (the committed summaries are of the method's three-kernel stream kernel)
             "traffic": profiled_traffic(w.name) if w.bits == synth.WORKLOADS[w.name].bits
-            and not vq and chunk <= 1 and not opts.get("decay")
-            and opts.get("engine", "pipeline") == "pipeline" else None,
+            and is_method(opts) and opts.get("engine", "pipeline") == "pipeline" else None,
             "kernel": "he::stream_kernel (cache-streaming attention partials)",
             "algorithmic_bytes_per_launch": stream_bytes,
             "kernel_ms": stream_ms,
@@ -597,12 +603,14 @@ def measure(w: synth.Workload, opts: dict, L: int, min_s: float, min_steps: int,
 def is_method(opts: dict) -> bool:
     """The options are those of the method as the pages describe it."""
     return (not opts.get("threshold") and not opts.get("decay") and opts.get("chunk", 1) <= 1
+            and opts.get("tau_mode", "fixed") == "fixed"
             and opts.get("v_format", "elem") == "elem")
 
 
 def run_ours(args, rank: int, world: int, dist_on: bool):
     w = make_workload(args.workload, args.bits, args.budget)
     opts = {"threshold": args.threshold, "decay": args.decay, "v_format": args.v_format,
+            "tau_mode": args.tau_mode,
             "chunk": args.chunk, "engine": args.engine}
     L = args.layers if args.layers else (w.layers if w.layers > 1 else 4)
     if w.layers > 1 and L != w.layers:
@@ -650,6 +658,7 @@ def main(argv=None):
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     opts = {"threshold": args.threshold, "decay": args.decay, "v_format": args.v_format,
+            "tau_mode": args.tau_mode,
             "chunk": args.chunk}
 
     if args.impl == "reference":
