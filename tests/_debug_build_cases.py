@@ -57,6 +57,8 @@ def main():
         ("int8 values", base.with_(batch=2, budget=300, prompt=600), 300, 20, {"v_format": "int8"}),
         ("fp8 values", base.with_(batch=2, budget=300, prompt=600), 300, 20, {"v_format": "fp8"}),
         ("score memory", base.with_(batch=2, budget=333, prompt=700), 320, 30, {"decay": 0.5}),
+        ("median thresholds", base.with_(batch=2, budget=333, prompt=700), 320, 30,
+         {"threshold": "median"}),
         ("G = 8, D = 64", base.with_(batch=2, heads=64, head_dim=64, bits=16, budget=200,
                                      prompt=400), 200, 20, {}),
         ("single-kernel engine", base.with_(batch=2, budget=3000, prompt=3100), 2990, 20,

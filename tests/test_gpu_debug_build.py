@@ -24,4 +24,4 @@ def test_debug_build_runs_clean():
     r = subprocess.run([sys.executable, os.path.join(HERE, "_debug_build_cases.py")], cwd=ROOT,
                        env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
-    assert r.stdout.count("ok ") == 9, r.stdout
+    assert r.stdout.count("ok ") == 10, r.stdout
