@@ -281,6 +281,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
       }
     }
     __syncthreads();
+    HE_STAMP(0, 6);
     if (split == 0 && tid == 0) uo[u].codek = code_from_bits(sbits, bits, G);
 
     if (full) {
@@ -348,22 +349,36 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
           }
         }
       }
+      HE_STAMP(0, 7);
       best = warp_max_u64(best);
       if (lane == 0) red[warp] = best;
       __syncthreads();
+      HE_STAMP(0, 4);
+      // a unit of one item decides here: its key is this CTA's best (a plain
+      // store; the key was zeroed by the previous step's merge); else the
+      // items fold their bests with atomicMax and the last one decides
+      uint64_t* s_key = red + kPrepThreads / 32 + 1;  // (after the flag `last`)
       if (tid == 0) {
         uint64_t b2 = 0;
         for (int w2 = 0; w2 < kPrepThreads / 32; ++w2) b2 = red[w2] > b2 ? red[w2] : b2;
-        if (b2) atomicMax(&uo[u].key[p.kpar], (unsigned long long)b2);
-        __threadfence();
-        *last = atomicAdd(&uo[u].arrived, 1) == splits - 1;
-        __threadfence();
+        if (splits == 1) {
+          uo[u].key[p.kpar] = b2;
+          *s_key = b2;
+          *last = 1;
+        } else {
+          if (b2) atomicMax(&uo[u].key[p.kpar], (unsigned long long)b2);
+          __threadfence();
+          *last = atomicAdd(&uo[u].arrived, 1) == splits - 1;
+          __threadfence();
+          if (*last) *s_key = __ldcg(&uo[u].key[p.kpar]);
+        }
       }
       __syncthreads();
+      HE_STAMP(0, 5);
       if (*last) {
         // the unit's eviction is decided: hand merge the evicted slot's logits
         // and value row, so that merge needs no dependent load
-        const int winner = (int)evict_key_slot(__ldcg(&uo[u].key[p.kpar]));
+        const int winner = (int)evict_key_slot(*s_key);
         if constexpr (CH) {
           // the chunk's softmax parts (see ChunkRec): every key and value row
           // of the chunk loaded at once (rows i = warp, warp + 4, ...), the
@@ -454,22 +469,39 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
               reinterpret_cast<const uint16_t*>(p.K) + ((size_t)u * p.budget + winner) * D;
           const uint16_t* Vrow =
               reinterpret_cast<const uint16_t*>(p.V) + ((size_t)u * p.budget + winner) * D;
+          // the value row (and scale) and the key row are loaded together: one
+          // memory round trip (D <= kPrepThreads: one value element per thread)
+          static_assert(D <= kPrepThreads, "one value element per thread");
+          uint16_t vh = 0;
+          uint8_t vb = 0;
+          float vsc = 0.0f;
+          if constexpr (VQ) {
+            if (tid < D) vb = __ldcg(reinterpret_cast<const uint8_t*>(p.V) +
+                                     ((size_t)u * p.budget + winner) * D + tid);
+            if (tid == 0) vsc = __ldcg(p.vs + (size_t)u * p.vs_stride + winner);
+          } else {
+            if (tid < D) vh = __ldcg(Vrow + tid);
+          }
+          constexpr int KE = D / 32;  // key elements per lane
+          uint16_t kv[KE];
+#pragma unroll
+          for (int e = 0; e < KE; ++e) kv[e] = __ldcg(Krow + lane + 32 * e);
           for (int g = warp; g < G; g += kPrepThreads / 32) {
             float a = 0.0f;
-            for (int d = lane; d < D; d += 32)
-              a = fmaf(__uint_as_float((uint32_t)xs[g * D + d] << 16),
-                       __uint_as_float((uint32_t)__ldcg(Krow + d) << 16), a);
+#pragma unroll
+            for (int e = 0; e < KE; ++e)
+              a = fmaf(__uint_as_float((uint32_t)xs[g * D + lane + 32 * e] << 16),
+                       __uint_as_float((uint32_t)kv[e] << 16), a);
             a = warp_sum(a);
             if (lane == 0) uo[u].lstar[g] = a * p.qscale;
           }
           if constexpr (VQ) {
-            const uint8_t* Vq = reinterpret_cast<const uint8_t*>(p.V) + ((size_t)u * p.budget + winner) * D;
-            for (int d = tid; d < D; d += kPrepThreads) uo[u].vqstar[d] = __ldcg(Vq + d);
-            if (tid == 0) uo[u].vsstar = __ldcg(p.vs + (size_t)u * p.vs_stride + winner);
+            if (tid < D) uo[u].vqstar[tid] = vb;
+            if (tid == 0) uo[u].vsstar = vsc;
           } else {
-            for (int d = tid; d < D; d += kPrepThreads) uo[u].vstar[d] = __ldcg(Vrow + d);
+            if (tid < D) uo[u].vstar[tid] = vh;
           }
-          if (tid == 0) uo[u].arrived = 0;
+          if (tid == 0 && splits > 1) uo[u].arrived = 0;
         }
       }
     }
