@@ -23,6 +23,8 @@ struct UnitOut {
   uint16_t vstar[128];     // the evicted slot's value row (bf16)
   uint8_t vqstar[128];     // quantised value cache: the evicted slot's byte row ...
   float vsstar;            // ... and its scale
+  uint8_t vqnew[128];      // quantised value cache: the new token's byte row ...
+  float vsnew;             // ... and its scale (prep quantises, merge writes them)
   int32_t cready[2];       // fused step: cq[parity] published (1), reset by the unit's merge
   int32_t pad2;
   unsigned long long cq[2][8];  // fused step: the query codes, per key parity

@@ -269,7 +269,17 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
       const uint32_t word = __ballot_sync(kFull, bit);
       if (lane == 0) sbits[t0 >> 5] = word;
     }
-    // the new token's logits (only the unit's first item publishes them)
+    // the new token's logits (only the unit's first item publishes them);
+    // with a quantised value cache also its value row, quantised as merge
+    // will store it (s = max |v| / range, codes of v / s, both fp32 divisions)
+    float vnew = 0.0f;
+    if constexpr (VQ) {
+      static_assert(D <= kPrepThreads, "one value element per thread");
+      if (split == 0 && tid < D)
+        vnew = __uint_as_float((uint32_t)__ldcg(reinterpret_cast<const uint16_t*>(p.v) +
+                                                (size_t)u * D + tid)
+                               << 16);
+    }
     if (split == 0) {
       for (int g = warp; g < G; g += kPrepThreads / 32) {
         float a = 0.0f;
@@ -278,6 +288,19 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
                    __uint_as_float((uint32_t)xs[G * D + d] << 16), a);
         a = warp_sum(a);
         if (lane == 0) uo[u].lnew[g] = a * p.qscale;
+      }
+      if constexpr (VQ) {
+        float m = fabsf(vnew);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+        float* wmax = reinterpret_cast<float*>(red + kPrepThreads / 32 + 2);  // [4]
+        if (lane == 0) wmax[warp] = m;
+        __syncthreads();
+        m = 0.0f;
+        for (int w2 = 0; w2 < D / 32; ++w2) m = fmaxf(m, wmax[w2]);
+        const float sc = __fdiv_rn(m, vq_range<VQ>());
+        if (tid < D) uo[u].vqnew[tid] = sc > 0.0f ? vq_encode<VQ>(__fdiv_rn(vnew, sc)) : 0;
+        if (tid == 0) uo[u].vsnew = sc;
       }
     }
     __syncthreads();
@@ -1486,6 +1509,13 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
   const unsigned long long codek = __ldcg(&uo[u].codek);
   const uint16_t* kt = reinterpret_cast<const uint16_t*>(p.k) + (size_t)u * D;
   const uint16_t* vtp = reinterpret_cast<const uint16_t*>(p.v) + (size_t)u * D;
+  // (quantised value cache: the evicted slot's codes and scale, and the new
+  // token's codes and scale, as prep staged them)
+  const uint32_t w4 = (VQ && full) ? __ldcg(reinterpret_cast<const uint32_t*>(uo[u].vqstar + d0))
+                                   : 0u;
+  const float ss = (VQ && full) ? __ldcg(&uo[u].vsstar) : 0.0f;
+  const uint8_t vqn = (VQ && tid < D) ? __ldcg(&uo[u].vqnew[tid]) : (uint8_t)0;
+  const float vsn = VQ ? __ldcg(&uo[u].vsnew) : 0.0f;
   const uint16_t kt1 = tid < D ? __ldcg(kt + tid) : (uint16_t)0;
   const uint16_t vt1 = tid < D ? __ldcg(vtp + tid) : (uint16_t)0;
   const uint2 vt2 = __ldcg(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(p.v) +
@@ -1534,6 +1564,7 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
     }
   }
 
+  HE_STAMP(2, 3);  // (the loads are issued; the key is the first to be used)
   int winner = full ? (key ? (int)evict_key_slot(key) : -1) : p.append_slot;
   // slots evicted, and the end of the slots eviction may choose from
   const int nev = (CH && full) ? p.chunk : 1;
@@ -1559,33 +1590,20 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
   float4 vs = make_float4(__uint_as_float(vs2.x << 16), __uint_as_float(vs2.x & 0xFFFF0000u),
                           __uint_as_float(vs2.y << 16), __uint_as_float(vs2.y & 0xFFFF0000u));
   // quantised value cache: the evicted row as stored (decode(q) * s), and the
-  // new row's quantisation (s = max |v| / range, q = the code of v / s)
-  float vnew = 0.0f;
+  // new row's codes and scale from prep
   if constexpr (VQ) {
     if (full) {
-      const uint32_t w4 = __ldcg(reinterpret_cast<const uint32_t*>(uo[u].vqstar + d0));
-      const float ss = __ldcg(&uo[u].vsstar);
       vs = make_float4(vq_decode<VQ>((uint8_t)(w4 & 0xFF)) * ss,
                        vq_decode<VQ>((uint8_t)((w4 >> 8) & 0xFF)) * ss,
                        vq_decode<VQ>((uint8_t)((w4 >> 16) & 0xFF)) * ss,
                        vq_decode<VQ>((uint8_t)(w4 >> 24)) * ss);
     }
-    vnew = __uint_as_float((uint32_t)vt1 << 16);
-    float m = tid < D ? fabsf(vnew) : 0.0f;
-#pragma unroll
-    for (int o2 = 16; o2 > 0; o2 >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o2));
-    if ((tid & 31) == 0 && tid < D) vqrow[D + (tid >> 5)] = m;
+    // the new token's row as stored (prep quantised it): its codes' values
+    if (tid < D) vqrow[tid] = vq_decode<VQ>(vqn);
   }
   if (tid == 0) sflag[grp] = 0;
   __syncthreads();
-  float vscale = 0.0f;
-  if constexpr (VQ) {
-    float m = 0.0f;
-    for (int w2 = 0; w2 < D / 32; ++w2) m = fmaxf(m, vqrow[D + w2]);
-    vscale = __fdiv_rn(m, vq_range<VQ>());
-    if (tid < D)  // the code's value (exact; the code is written from it below)
-      vqrow[tid] = vscale > 0.0f ? vq_decode<VQ>(vq_encode<VQ>(__fdiv_rn(vnew, vscale))) : 0.0f;
-  }
+  const float vscale = VQ ? vsn : 0.0f;
 
   float mx = -1e30f, sum = 0.0f;
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1650,6 +1668,7 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
       }
     }
   }
+  HE_STAMP(2, 4);
   bool recomputed;
   if constexpr (!MU) {
     __syncthreads();
@@ -1796,6 +1815,7 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
       wslot = winner + c - 1;
     }
   }
+  HE_STAMP(2, 5);
   // method step 5: the current token's key, value and code replace the slot
   if (bad) return;
   if (!HE_CHECK(wslot >= 0 && wslot < p.budget &&
@@ -1806,8 +1826,7 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
   if (tid < D) {
     Kw[tid] = kt1;
     if constexpr (VQ)
-      reinterpret_cast<uint8_t*>(p.V)[((size_t)u * p.budget + winner) * D + tid] =
-          vq_encode<VQ>(vqrow[tid]);
+      reinterpret_cast<uint8_t*>(p.V)[((size_t)u * p.budget + winner) * D + tid] = vqn;
     else
       reinterpret_cast<uint16_t*>(p.V)[((size_t)u * p.budget + wslot) * D + tid] = vt1;
   }
