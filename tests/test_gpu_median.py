@@ -115,3 +115,19 @@ def test_refill_recomputes_thresholds():
             he.fill(torch_from_host(K), torch_from_host(synth.host_kv(w, "value", t0, 128)))
             for j in range(w.kv_heads):
                 assert np.array_equal(he.thresholds()[0, j], o.median_thresholds(K[0, j], W))
+
+
+@pytest.mark.slow
+def test_full_llama8b_b8_sampled():
+    """Per-bit median thresholds on the Llama-3-8B-shaped layer at full size
+    (batch 8, budget 4096, the benchmark's launch configuration): the
+    thresholds, 48 steps' evictions and outputs, and the final cache of
+    sampled units."""
+    w = synth.WORKLOADS["llama8b_b8"]
+    steps = 48
+    out_steps = [0, 23, 47]
+    g = run_gpu(w, w.budget, steps, out_steps, read_state=True, device_gen=True,
+                threshold="median")
+    units = [(0, 0), (3, 5), (7, 7)]
+    orc = run_oracle_units(w, units, w.budget, steps, out_steps, threshold="median")
+    compare(w, g, orc, out_steps, check_state=True)

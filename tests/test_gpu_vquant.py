@@ -178,3 +178,34 @@ def test_more_units_than_sms(fmt):
     each; every unit's rows, scales and evictions are checked."""
     w = small("serving_b64", batch=40, budget=96, prompt=300, decode=8)
     _stream(w, 90, 40, 13, fmt)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_full_llama8b_b8_sampled(fmt):
+    """The Llama-3-8B-shaped layer at full size (batch 8, 32/8 heads, budget
+    4096) in the launch configuration the benchmark times (296 stream CTAs,
+    three ring stages, the two-group split): 48 streamed steps; sampled units'
+    evictions, outputs and final byte rows and scales against the oracle."""
+    w = synth.WORKLOADS["llama8b_b8"]
+    steps = 48
+    out_steps = [0, 23, 47]
+    g = run_gpu(w, w.budget, steps, out_steps, read_state=True, device_gen=True, v_format=fmt)
+    units = [(0, 0), (3, 5), (7, 7)]
+    orc = run_oracle_units(w, units, w.budget, steps, out_steps, v_format=fmt)
+    compare(w, g, orc, out_steps, check_state=True)
+
+
+@pytest.mark.slow
+def test_full_32layer_fp8_sampled_layers():
+    """The 32-layer workload's layer shape (batch 16, budget 9728) with fp8
+    values: 40 steps of layers 0 and 31 on sampled units."""
+    w = synth.WORKLOADS["llama8b_32layer"]
+    steps = 40
+    out_steps = [0, 39]
+    for layer in (0, 31):
+        g = run_gpu(w, w.budget, steps, out_steps, layer=layer, device_gen=True,
+                    v_format="fp8")
+        orc = run_oracle_units(w, [(0, 0), (15, 7)], w.budget, steps, out_steps, layer=layer,
+                               v_format="fp8")
+        compare(w, g, orc, out_steps)
