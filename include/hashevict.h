@@ -143,7 +143,9 @@ int he_create(const he_cfg* cfg, he_handle* out);
  * scratch of up to 1 GiB, or one unit's bits * n floats if more).  K, V: device
  * [batch][kv_heads][n][head_dim].  n = 0 empties the cache (K, V may be NULL).
  * Errors: HE_EINVAL (NULL handle, n out of range, NULL or misaligned K/V),
- * HE_ENOMEM (the threshold scratch), HE_ECUDA. */
+ * HE_ENOMEM (the threshold scratch), HE_ECUDA.  A fill that fails after its
+ * checks leaves the handle unfilled: he_step returns HE_ENOTFILLED until a
+ * fill succeeds. */
 int he_fill(he_handle h, const void* K, const void* V, int32_t n, void* stream);
 
 /* One decode step (method steps 1-5, then attention).  bf16 handles launch
@@ -279,9 +281,11 @@ int he_set_dist_log(he_handle h, int32_t* dist);
 
 /* Checks of the failure paths.
  * he_set_alloc_limit: a process-wide cap, in bytes, on the device memory one
- * he_create may allocate (0 = no cap, the default).  A handle that would need
- * more fails with HE_ENOMEM before allocating anything, as on an exhausted
- * device.  Always returns HE_OK.
+ * he_create may allocate, and on the scratch of one he_fill with per-bit
+ * median thresholds (0 = no cap, the default).  A handle that would need more
+ * fails with HE_ENOMEM before allocating anything, and such a fill with
+ * HE_ENOMEM (leaving the handle unfilled), as on an exhausted device.  Always
+ * returns HE_OK.
  * he_wait_probe: launches on `stream` one kernel that waits on a barrier that
  * nothing completes, through the same bounded wait as every kernel of the
  * library, giving up after limit_us microseconds (1 .. 1,000,000).  On giving

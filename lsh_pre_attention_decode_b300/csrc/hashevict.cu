@@ -453,6 +453,7 @@ int fill_median_thresholds(he_ctx* h, int64_t n, cudaStream_t s) {
   if (group < 1) group = 1;
   if (group > h->U) group = h->U;
   float* proj = nullptr;
+  if (g_alloc_limit != 0 && (uint64_t)(group * per_unit) > g_alloc_limit) return HE_ENOMEM;
   if (cudaMallocAsync((void**)&proj, (size_t)(group * per_unit), s) != cudaSuccess) {
     (void)cudaGetLastError();
     return HE_ENOMEM;
@@ -697,6 +698,9 @@ int he_fill(he_handle h, const void* K, const void* V, int32_t n, void* stream) 
   if (!g.ok) return fail_cuda(h, cudaErrorInvalidDevice);
   cudaStream_t s = (cudaStream_t)stream;
   const size_t row = (size_t)h->cfg.head_dim * h->eb;
+  // a fill that fails part-way (the threshold scratch) leaves the handle
+  // unfilled rather than mixing the new rows with the old codes
+  h->filled = false;
   if (n > 0) {
     HE_TRY(h, cudaMemcpy2DAsync(h->K, (size_t)h->rows * row, K, (size_t)n * row,
                                 (size_t)n * row, (size_t)h->U, cudaMemcpyDeviceToDevice, s));

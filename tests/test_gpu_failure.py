@@ -37,6 +37,40 @@ def test_allocation_cap_fails_cleanly():
     compare(w, g, orc, range(6), check_state=True)
 
 
+def test_median_fill_scratch_cap_leaves_the_handle_unfilled():
+    """A refill whose threshold scratch does not fit the cap fails with
+    HE_ENOMEM and leaves the handle unfilled (the step is refused, not run on
+    new rows with old codes); the next fill that fits restores it, with the
+    oracle's thresholds and codes."""
+    import torch
+    import oracle
+    w = W_SMALL
+    K = synth.host_kv(w, "key", 0, w.budget)
+    V = synth.host_kv(w, "value", 0, w.budget)
+    q = torch_from_host(synth.host_queries(w, w.budget, 1)[0])
+    k = torch_from_host(synth.host_kv(w, "key", w.budget, 1, token_major=True)[0])
+    v = torch_from_host(synth.host_kv(w, "value", w.budget, 1, token_major=True)[0])
+    with make_handle(w, threshold="median") as he:
+        he.fill(torch_from_host(K), torch_from_host(V))
+        pkg.he_set_alloc_limit(1024)  # (the scratch: bits x budget floats per unit)
+        try:
+            with pytest.raises(pkg.HashEvictError) as e:
+                he.fill(torch_from_host(K), torch_from_host(V))
+            assert e.value.code == -4  # HE_ENOMEM
+        finally:
+            pkg.he_set_alloc_limit(0)
+        with pytest.raises(pkg.HashEvictError) as e:
+            he.step(q, k, v)
+        assert e.value.code == -2  # HE_ENOTFILLED
+        he.fill(torch_from_host(K), torch_from_host(V))
+        he.step(q, k, v)
+        o = oracle.load()
+        W = o.projection(w.projection_seed(), w.head_dim, w.bits, w.dtype)
+        tv = he.thresholds()
+        for j in range(w.kv_heads):
+            assert np.array_equal(tv[0, j], o.median_thresholds(K[0, j], W))
+
+
 def test_bounded_wait_gives_up_and_reports():
     import torch
     w = W_SMALL
