@@ -59,7 +59,7 @@ struct StepParams {
   const float* tauv;     // or one threshold per bit and unit [U][bits] (null: tau)
   float decay;           // score memory gamma (with score != nullptr)
   float* score;          // per-slot scores [U][budget] (null: evict by the step's distances)
-  float* vs;             // int8 value cache: per-slot scales [U][vs_stride] (V holds int8 rows)
+  float* vs;             // quantised value cache: per-slot scales [U][vs_stride] (V holds byte rows)
   int32_t vs_stride;
   // bf16 pipeline: per-unit results, the parity of this step's eviction key,
   // and the slot the previous step of this cache wrote: 0 none (or not

@@ -85,39 +85,6 @@ __device__ __forceinline__ float vq_decode(uint8_t c) {
   }
 }
 
-// Four stored bytes (byte i = element i) -> bf16 pairs, exact: lo holds
-// elements 0 and 1, hi elements 2 and 3 (the lower element in the lower half).
-template <int VQ>
-__device__ __forceinline__ void vq_widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  if constexpr (VQ == kVqFp8) {
-    // E4M3 -> f16 is exact (every E4M3 value is an f16 normal), f16 -> fp32
-    // exact, and the fp32 values have at most 4 significant bits: exact in bf16
-    uint32_t h01, h23;
-    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
-        : "=r"(h01), "=r"(h23)
-        : "r"(w));
-    const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-    const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-    const __nv_bfloat162 b01 = __floats2bfloat162_rn(f01.x, f01.y);
-    const __nv_bfloat162 b23 = __floats2bfloat162_rn(f23.x, f23.y);
-    lo = *reinterpret_cast<const uint32_t*>(&b01);
-    hi = *reinterpret_cast<const uint32_t*>(&b23);
-  } else {
-    // byte b -> fp32 with exponent 2^23 holding b + 128 in its low mantissa
-    // bits (a byte permute), minus 2^23 + 128: b exactly; two at a time to bf16
-    const uint32_t u4 = w ^ 0x80808080u;
-    float f[4];
-#pragma unroll
-    for (int i2 = 0; i2 < 4; ++i2)
-      f[i2] = __uint_as_float(__byte_perm(u4, 0x4B000000u, 0x7540u + i2)) - 8388736.0f;
-    const __nv_bfloat162 b01 = __floats2bfloat162_rn(f[0], f[1]);
-    const __nv_bfloat162 b23 = __floats2bfloat162_rn(f[2], f[3]);
-    lo = *reinterpret_cast<const uint32_t*>(&b01);
-    hi = *reinterpret_cast<const uint32_t*>(&b23);
-  }
-}
-
 // Byte words of two slots s (even) and s + 1 of one value-tile row position:
 // byte i of each word is the same column.  -> four f16 pairs (slot s in the
 // lower half), pair i from bytes i, exact (|int8| < 2^11; every E4M3 value is an
