@@ -207,6 +207,16 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
         bulk_g2s(smem + S::OFF_C, p.codes + (size_t)u * p.code_stride + (size_t)s0 * wb, cbytes,
                  bar);
     }
+    // (quantised value cache: the new token's value row, for the first item,
+    // loaded while the copies are in flight)
+    float vnew = 0.0f;
+    if constexpr (VQ) {
+      static_assert(D <= kPrepThreads, "one value element per thread");
+      if (split == 0 && tid < D)
+        vnew = __uint_as_float((uint32_t)__ldcg(reinterpret_cast<const uint16_t*>(p.v) +
+                                                (size_t)u * D + tid)
+                               << 16);
+    }
     if (!__syncthreads_and(mbar_wait_bounded(bar, phase))) {
       // gave up: record it and leave once the copies have landed
       if (tid == 0) {
@@ -239,14 +249,6 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const StepParams p, 
     // the new token's logits (only the unit's first item publishes them);
     // with a quantised value cache also its value row, quantised as merge
     // will store it (s = max |v| / range, codes of v / s, both fp32 divisions)
-    float vnew = 0.0f;
-    if constexpr (VQ) {
-      static_assert(D <= kPrepThreads, "one value element per thread");
-      if (split == 0 && tid < D)
-        vnew = __uint_as_float((uint32_t)__ldcg(reinterpret_cast<const uint16_t*>(p.v) +
-                                                (size_t)u * D + tid)
-                               << 16);
-    }
     if (split == 0) {
       for (int g = warp; g < G; g += kPrepThreads / 32) {
         float a = 0.0f;
