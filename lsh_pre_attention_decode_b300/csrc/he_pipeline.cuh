@@ -1203,8 +1203,11 @@ __global__ void __launch_bounds__(StreamShape<D, G, NS, VQ, FUSED>::NT, 2)
 // ---------------------------------------------------------------------------
 // A merge CTA has GD4 * NQ threads: NQ contributor groups of GD4 = G * D / 4
 // threads (one float4 of the unit's output each).  Every shape runs 512
-// threads: smaller CTAs (which could sit beside two stream CTAs) made the
-// merge itself slower by more than their earlier start gained.
+// threads.  A merge CTA fits beside two stream CTAs only with at most four
+// warps of at most 64 registers (an SM's registers are four sub-partitions of
+// 16384, and two stream CTAs put three warps of 136 registers on two of them);
+// such CTAs, with the partial records staged in shared memory, let all the next
+// step's stream CTAs start together but did not shorten the step.
 constexpr int kMergeMaxThreads = 512;
 constexpr int kMergeMinThreads = 512;
 constexpr int kMergeRegs = 12;  // partials held in registers per thread (more are looped)
