@@ -93,3 +93,24 @@ def test_memory_zero_equals_the_method():
     assert np.array_equal(a.evicted, b.evicted)
     for s in (0, 39):
         assert np.array_equal(a.outs[s], b.outs[s])
+
+
+@pytest.mark.slow
+def test_score_memory_full_llama8b_b8_sampled():
+    """Score memory (gamma 0.5, the benchmark's option) on the Llama-3-8B-shaped
+    layer at full size (batch 8, budget 4096, the benchmark's launch
+    configuration): 48 steps' evictions and outputs, the final cache and every
+    slot's score of sampled units."""
+    w = synth.WORKLOADS["llama8b_b8"]
+    steps = 48
+    out_steps = [0, 23, 47]
+    g = run_gpu(w, w.budget, steps, out_steps, read_state=True, device_gen=True, decay=0.5)
+    units = [(0, 0), (3, 5), (7, 7)]
+    orc = run_oracle_units(w, units, w.budget, steps, out_steps, decay=0.5)
+    compare(w, g, orc, out_steps, check_state=True)
+    scores = g.state[4]
+    for (b, j), r in orc.items():
+        assert np.array_equal(scores[b, j], r.score), f"scores of unit ({b},{j})"
+    # the memory changes the evictions (the case is not vacuous)
+    ref = run_oracle_units(w, [(0, 0)], w.budget, steps)
+    assert not np.array_equal(ref[(0, 0)].evicted, orc[(0, 0)].evicted)
