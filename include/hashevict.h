@@ -313,8 +313,8 @@ int he_wait_probe(he_handle h, uint32_t limit_us, void* stream);
  * ceil(2G / 4) + G * head_dim) bytes per partial record (G = heads / kv_heads),
  * (C + batch * kv_heads) * R + 256 <= HE_NOALLOC_SCRATCH_BYTES, else HE_EINVAL.
  * The first call on each device does a one-off set-up (the array's device
- * address, kernel attributes) on the current device; make that first call
- * before any stream capture.  Not thread-safe on a device's first call.  Every
+ * address, kernel attributes) on the current device.  Not thread-safe on a
+ * device's first call.  Every
  * call uses the same array, so calls that overlap on the GPU race: order them
  * (one stream, or events).  Each call clears the array's error word itself
  * (an asynchronous memset on `stream`); nothing else in the array needs to
