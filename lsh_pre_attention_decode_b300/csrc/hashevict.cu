@@ -844,6 +844,19 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
         p.split_t1 = (int32_t)T1;
       }
     }
+    // partials per unit: at most ceil(tiles per unit / fewest tiles of a CTA) + 1
+    int nmax = 0;
+    if (TT > 0 && stream_ctas > 0) {
+      const he::TileSplit sp{TT, stream_ctas, p.split_e, p.split_t1};
+      int64_t fewest = TT;
+      for (int64_t c : {(int64_t)0, (int64_t)stream_ctas - 1})
+        fewest = std::min(fewest, sp.begin(c + 1) - sp.begin(c));
+      if (p.split_e > 0) fewest = std::min(fewest, sp.begin(p.split_e) - sp.begin(p.split_e - 1));
+      nmax = (int)((p.tpu + fewest - 1) / fewest) + 1;
+    }
+    // more partials than merge holds in registers: its loads take longest, so
+    // it releases the next step only once they are issued
+    p.late_release = nmax > he::kMergeRegs ? 1 : 0;
     if (stream_ctas > 0) {
       void* sa[] = {(void*)&p, (void*)&h->tmK, (void*)&h->tmV};
       HE_TRY(h, launch_pdl(h->kern.step, dim3(stream_ctas), dim3(h->kern.step_threads),
@@ -859,16 +872,6 @@ int he_step(he_handle h, const void* q, const void* k, const void* v, float* out
                          (size_t)h->kern.prep_smem, s, pa));
     if (ev) HE_TRY(h, cudaEventRecord(ev[2], s));
     int sc = stream_ctas;
-    // partials per unit: at most ceil(tiles per unit / fewest tiles of a CTA) + 1
-    int nmax = 0;
-    if (TT > 0 && stream_ctas > 0) {
-      const he::TileSplit sp{TT, stream_ctas, p.split_e, p.split_t1};
-      int64_t fewest = TT;
-      for (int64_t c : {(int64_t)0, (int64_t)stream_ctas - 1})
-        fewest = std::min(fewest, sp.begin(c + 1) - sp.begin(c));
-      if (p.split_e > 0) fewest = std::min(fewest, sp.begin(p.split_e) - sp.begin(p.split_e - 1));
-      nmax = (int)((p.tpu + fewest - 1) / fewest) + 1;
-    }
     // several units per merge CTA only when the units outnumber the SMs (one
     // wave of merge CTAs instead of several); else one unit per CTA
     int msmem = 0, nq = 1, upc = 1;

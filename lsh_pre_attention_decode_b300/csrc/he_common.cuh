@@ -80,6 +80,9 @@ struct StepParams {
   // split_e = split_t1 = 0 is the even split
   int32_t split_e;
   int32_t split_t1;
+  // bf16 pipeline: merge lets the next step launch only once its loads are
+  // issued (1; units of many partials), else as soon as its wait returns (0)
+  int32_t late_release;
   // fused step: the split of this cache's previous step (prev_tpu tiles per
   // unit over prev_nc CTAs, prev_e / prev_t1 as split_e / split_t1; prev_nc = 0:
   // no CTA), which fixes how many hash warps fold that step's eviction key

@@ -1449,8 +1449,12 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
   const bool full = p.append_slot < 0;
 
   HE_STAMP(2, 0);
-  pdl_wait();     // stream (and so prep) is complete and visible
-  pdl_trigger();  // the next step's prep may launch; it waits for this grid
+  pdl_wait();  // stream (and so prep) is complete and visible
+  // the next step's stream kernel may launch (it waits for this grid): at once,
+  // so that its first tiles load while this grid works, unless the units have
+  // many partials each: then after this CTA's loads are issued, which go ahead
+  // of that flood of tile loads (the loads of such units take longest)
+  if (!p.late_release) pdl_trigger();
   HE_STAMP(2, 1);
 
   // contributors: the CTAs whose ranges cover the unit's tiles (records first+u ..)
@@ -1537,6 +1541,7 @@ __global__ void __launch_bounds__(kMergeMaxThreads)
   }
 
   HE_STAMP(2, 3);  // (the loads are issued; the key is the first to be used)
+  if (p.late_release) pdl_trigger();
   int winner = full ? (key ? (int)evict_key_slot(key) : -1) : p.append_slot;
   // slots evicted, and the end of the slots eviction may choose from
   const int nev = (CH && full) ? p.chunk : 1;
