@@ -3,7 +3,8 @@ benchmark issue steps: back to back on one stream with no host synchronisation,
 over one to three caches in turn, eagerly or as a captured CUDA graph replayed
 twice.  Shapes, code lengths, budgets and the options in the combinations the
 library accepts (int8 and fp8 value rows, chunk eviction, score memory, a
-scalar or per-bit median threshold).
+scalar or per-bit median threshold), with the three-kernel pipeline or the
+single-kernel engine.
 
 A graph starts right after a full fill and holds whole eviction cycles (an even
 number of steps, a multiple of the chunk), so that each replay runs on the
@@ -65,6 +66,11 @@ def config(i: int) -> dict:
         c["fill"] = int(rng.choice([budget, budget - int(rng.integers(1, 40))]))
         c["tokens"] = budget - c["fill"] + max(40, 3 * c["chunk"]) + (c["chunk"] - 1)
     c["seed"] = int(rng.integers(1, 1 << 30))
+    # the single-kernel engine where it applies (bf16 values, no chunks, no memory)
+    c["engine"] = "pipeline"
+    if (c["dtype"] == "bf16" and c["v_format"] == "elem" and c["chunk"] == 1 and
+            c["decay"] == 0.0 and rng.random() < 0.35):
+        c["engine"] = "fused"
     return c
 
 
@@ -81,6 +87,8 @@ def case_id(i: int) -> str:
         opts.append(f"decay{c['decay']}")
     if c["threshold"] != 0.0:
         opts.append("median" if c["threshold"] == "median" else f"tau{c['threshold']}")
+    if c["engine"] != "pipeline":
+        opts.append(c["engine"])
     return f"{i}-" + "-".join(opts)
 
 
@@ -97,7 +105,7 @@ def test_random_config_back_to_back(i):
     opts = dict(threshold=c["threshold"], decay=c["decay"], v_format=c["v_format"],
                 chunk=c["chunk"])
     g = run_gpu_b2b(w, c["fill"], n, out_steps, layers=c["layers"], graph=c["graph"],
-                    replays=2, **opts)
+                    replays=2, engine=c["engine"], **opts)
     units = [(b, j) for b in range(w.batch) for j in range(w.kv_heads)]
     for layer in range(c["layers"]):
         orc = oracle_b2b(w, units, c["fill"], g.tokens, out_steps, layer=layer, **opts)

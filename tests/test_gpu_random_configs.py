@@ -2,7 +2,8 @@
 CPU oracle: shapes (batch, query and KV heads, head_dim 64 and 128), code
 lengths, ragged budgets, fills from empty to full, and the options in the
 combinations the library accepts (int8 and fp8 value rows, chunk eviction,
-score memory, a scalar threshold or per-bit median thresholds), bf16 and fp32.
+score memory, a scalar threshold or per-bit median thresholds), bf16 and fp32,
+the three-kernel pipeline and the single-kernel engine.
 
 Every case streams enough tokens to fill the cache and then evict for at least
 40 steps (three chunk cycles with chunks).  A fifth of the cases have budgets
@@ -55,6 +56,11 @@ def config(i: int) -> dict:
     # appends up to the budget (and through the stage with chunks), then evictions
     c["steps"] = budget - c["fill"] + max(40, 3 * c["chunk"]) + (c["chunk"] - 1)
     c["seed"] = int(rng.integers(1, 1 << 30))
+    # the single-kernel engine where it applies (bf16 values, no chunks, no memory)
+    c["engine"] = "pipeline"
+    if (c["dtype"] == "bf16" and c["v_format"] == "elem" and c["chunk"] == 1 and
+            c["decay"] == 0.0 and rng.random() < 0.35):
+        c["engine"] = "fused"
     return c
 
 
@@ -70,6 +76,8 @@ def case_id(i: int) -> str:
         opts.append(f"decay{c['decay']}")
     if c["threshold"] != 0.0:
         opts.append("median" if c["threshold"] == "median" else f"tau{c['threshold']}")
+    if c["engine"] != "pipeline":
+        opts.append(c["engine"])
     return f"{i}-" + "-".join(opts)
 
 
@@ -84,7 +92,7 @@ def test_random_config(i):
     out_steps = sorted({0, steps // 3, steps // 2, steps - 2, steps - 1})
     opts = dict(threshold=c["threshold"], decay=c["decay"], v_format=c["v_format"],
                 chunk=c["chunk"])
-    g = run_gpu(w, c["fill"], steps, out_steps, read_state=True, **opts)
+    g = run_gpu(w, c["fill"], steps, out_steps, read_state=True, engine=c["engine"], **opts)
     units = [(b, j) for b in range(w.batch) for j in range(w.kv_heads)]
     orc = run_oracle_units(w, units, c["fill"], steps, out_steps, **opts)
     compare(w, g, orc, out_steps, check_state=True)
