@@ -7,8 +7,9 @@ with its scratch in a static device array that every call shares.
 
 Checked here: against the CPU oracle's fp64 attention on the identical cache
 (stream CTAs that hold several tiles of several units, n below the budget,
-head_dim 64 and 128, G = 1, 2, 4 and 8), two calls in a row each time; and
-against he_step's own output on the cache the step leaves.  This file is
+head_dim 64 and 128, G = 1, 2, 4 and 8), two calls in a row each time, and on
+a seeded sweep of random shapes; and against he_step's own output on the cache
+the step leaves.  This file is
 collected last on purpose.
 """
 import numpy as np
@@ -69,6 +70,51 @@ def test_matches_the_oracle_on_two_calls_in_a_row(batch, heads, kv, D, budget, n
                 worst_mean = max(worst_mean, float(err.mean()))
         assert worst_max <= MAX_ABS_TOL and worst_mean <= MEAN_ABS_TOL, (call, worst_max,
                                                                           worst_mean)
+
+
+def _random_shape(i):
+    rng = np.random.default_rng(6300 + i)
+    G = int(rng.choice([1, 2, 4, 8]))
+    kv = int(rng.integers(1, 9))
+    budget = int(rng.integers(16, 6000))
+    return dict(batch=int(rng.integers(1, 9)), heads=G * kv, kv=kv,
+                D=int(rng.choice([64, 128])), budget=budget,
+                n=int(rng.choice([budget, int(rng.integers(1, budget + 1))])),
+                seed=int(rng.integers(1, 1 << 30)))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("i", range(16), ids=[
+    "{i}-b{batch}-h{heads}-kv{kv}-D{D}-B{budget}-n{n}".format(i=i, **_random_shape(i))
+    for i in range(16)])
+def test_random_shapes_match_the_oracle(i):
+    """A seeded sweep of random shapes (batch, query and KV heads, head_dim,
+    budget, n from 1 to the budget) against the oracle's fp64 attention."""
+    import torch
+    _cuda()
+    c = _random_shape(i)
+    batch, heads, kv, D, budget, n = (c["batch"], c["heads"], c["kv"], c["D"], c["budget"],
+                                      c["n"])
+    w = synth.WORKLOADS["llama8b_b8"].with_(batch=batch, heads=heads, kv_heads=kv, head_dim=D,
+                                            budget=budget, prompt=budget + 8, seed=c["seed"])
+    K = synth.host_kv(w, "key", 0, budget)
+    V = synth.host_kv(w, "value", 0, budget)
+    Q = synth.host_queries(w, budget, 1)[0]
+    out = torch.full((batch, heads, D), float("nan"), dtype=torch.float32, device="cuda")
+    pkg.he_attend_noalloc(batch, heads, kv, D, budget, n, torch_from_host(K), torch_from_host(V),
+                          torch_from_host(Q), out)
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all()
+    o = oracle.load()
+    G = heads // kv
+    worst_max = worst_mean = 0.0
+    for b in range(batch):
+        for j in range(kv):
+            want = o.attend(Q[b, j * G:(j + 1) * G], K[b, j, :n], V[b, j, :n])
+            err = np.abs(got[b, j * G:(j + 1) * G] - want)
+            worst_max = max(worst_max, float(err.max()))
+            worst_mean = max(worst_mean, float(err.mean()))
+    assert worst_max <= MAX_ABS_TOL and worst_mean <= MEAN_ABS_TOL, (worst_max, worst_mean)
 
 
 @pytest.mark.gpu
