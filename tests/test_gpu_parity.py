@@ -268,13 +268,21 @@ def test_all_keys_equal_tie_goes_to_slot_zero():
         he.close()
 
 
-def test_host_entry_point_matches_device_entry_point():
+@pytest.mark.parametrize("opt", [
+    {}, {"v_format": "int8"}, {"v_format": "fp8"}, {"chunk": 4}, {"decay": 0.5},
+    {"threshold": "median"}, {"engine": "fused"}, {"dtype": "fp32"}],
+    ids=["method", "int8", "fp8", "chunk4", "decay", "median", "fused", "fp32"])
+def test_host_entry_point_matches_device_entry_point(opt):
+    """he_step_host (host buffers, copies inside the call) gives the device
+    entry point's results bit for bit, with each option."""
     import torch
     from lsh_pre_attention_decode_b300 import he_step_host
-    w = small("llama8b_b8", batch=2, budget=128, prompt=256, decode=4)
+    opt = dict(opt)
+    w = small("llama8b_b8", batch=2, budget=128, prompt=256, decode=4,
+              dtype=opt.pop("dtype", "bf16"))
     outs = []
     for host in (False, True):
-        he = make_handle(w)
+        he = make_handle(w, **opt)
         try:
             he.fill(torch_from_host(synth.host_kv(w, "key", 0, w.budget)),
                     torch_from_host(synth.host_kv(w, "value", 0, w.budget)))
